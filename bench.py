@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark of one draft-tree verification step on a GB300.
+
+A step is one pass of the whole path over one batch: tree mask and positions
+(tv_tree_mask), depth-indexed RoPE of the tree queries and keys
+(tv_rope_apply), tree attention over the paged KV cache (tv_tree_attn_verify:
+plan, split kernel, combine) and tree acceptance (tv_tree_accept_greedy from
+the target logits, or tv_tree_accept_sample).  The static tree's rank paths
+are built once with tv_tree_build, as a static tree is in serving.
+
+Reported (one JSON line on rank 0):
+  value       tree-verify nodes/s (B * N per step) over the timed steps with
+              every input resident in HBM, max over ranks;
+  roofline    the tree-attention call: algorithmic bytes (prefix K+V + tree
+              K+V + Q + O) / its CUDA-event time, against the measured HBM peak;
+  e2e         the same metric through the public API with the step's inputs
+              copied from pinned host memory and the accepted tokens read back;
+  cpu_baseline the CPU oracle timed on a bounded sample of the same workload.
+With --impl reference the CPU oracle itself is timed (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_tree_attn_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "b64_l1k_8k_n64_greedy"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+ATTN_SOURCES = ["attn.cu", "attn_tc.cu", "attn_common.cuh", "attn_tc.h"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--flags", type=int, default=0, help="tree attention kernel selection (0 auto, 1 CUDA-core, 2 tcgen05)")
+    ap.add_argument("--num-ctas", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available() and args.impl == "ours":
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_source_hash():
+    h = hashlib.sha256()
+    for f in ATTN_SOURCES:
+        p = os.path.join(ROOT, "speculative_decoding_tree_attn_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current attention sources for this workload (else None)."""
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    for r in rec if isinstance(rec, list) else [rec]:
+        if r.get("workload") == workload and r.get("source_sha") == attn_source_hash():
+            return r.get("dram_bytes_per_call")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = str(device_index)
+        self.cmd = ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "100"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for r in csv.reader(f):
+                if len(r) >= 7:
+                    rows.append([x.strip() for x in r])
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[3 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def attention_bytes(w, lens, N, esize):
+    kv = int(np.sum(lens)) * w.Hkv * w.D * 2 * esize
+    tree = w.B * N * w.Hkv * w.D * 2 * esize
+    qo = 2 * w.B * N * w.Hq * w.D * esize
+    return kv + tree + qo
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_run(w, inp_cpu, paths, greedy, sample, requests):
+    """The oracle on a list of requests (all nodes, all heads) plus acceptance."""
+    from oracle import accept as OA
+    from oracle import attention as OAt
+    from oracle import tree as OT
+
+    parent, depth, rows, _ = OT.build_tree(paths)
+    OT.tree_mask_batch(np.broadcast_to(parent, (len(requests), parent.size)), inp_cpu["seq_lens"][requests])
+    for b in requests:
+        sl = slice(b, b + 1)
+        OAt.tree_attention(inp_cpu["q"][sl], inp_cpu["k_cache"], inp_cpu["v_cache"], inp_cpu["block_table"][sl],
+                           inp_cpu["seq_lens"][sl], inp_cpu["k_tree"][sl], inp_cpu["v_tree"][sl], parent)
+        if greedy is not None:
+            am = OA.argmax_rows(greedy["logits"][b])
+            OA.tree_accept_greedy(am[None], greedy["tokens"][sl], parent)
+        if sample is not None:
+            OA.tree_accept_sample(sample["p"][sl], sample["q"][sl], sample["tokens"][sl], sample["parent"],
+                                  sample["n_nodes"][sl], sample["u_accept"][sl], sample["u_final"][sl])
+
+
+def cpu_inputs(w, device_inp, greedy, sample):
+    def c(t):
+        return (t.float() if t.dtype == torch.bfloat16 else t).cpu().numpy()
+    inp = {k: c(v) for k, v in device_inp.items()}
+    g = {k: c(v) for k, v in greedy.items()} if greedy else None
+    s = {k: c(v) for k, v in sample.items()} if sample else None
+    return inp, g, s
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def time_oracle(w, inp_cpu, paths, greedy, sample, seconds, order):
+    """Times the oracle request by request until `seconds` elapse; returns
+    (nodes/s, requests used, elapsed)."""
+    done, t0 = [], time.perf_counter()
+    for b in order:
+        oracle_sample_run(w, inp_cpu, paths, greedy, sample, [b])
+        done.append(int(b))
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return len(done) * w.n_nodes / el, done, el
+
+
+def sample_order(lens, seed=0):
+    rng = np.random.default_rng(seed)
+    first = [int(np.argmin(lens)), int(np.argmax(lens))]
+    rest = [int(b) for b in rng.permutation(len(lens)) if b not in first]
+    return first + rest
+
+
+# --------------------------------------------------------------------------- GPU step
+
+class Step:
+    def __init__(self, w, dev, flags, num_ctas):
+        from speculative_decoding_tree_attn_gb300 import capi
+        self.capi, self.w, self.dev = capi, w, dev
+        self.paths = w.paths()
+        self.inp = W.attention_inputs(w, device=dev)
+        parent, depth, rows, _, n = capi.tv_tree_build(self.paths)
+        self.N = n
+        self.parent = torch.from_numpy(parent).to(dev)
+        B = w.B
+        self.seq_lens = self.inp["seq_lens"]
+        self.lens = self.seq_lens.cpu().numpy()
+        self.mask = torch.empty(B, n, dtype=torch.int64, device=dev)
+        self.depth = torch.empty(B, n, dtype=torch.int32, device=dev)
+        self.pos = torch.empty(B, n, dtype=torch.int32, device=dev)
+        self.table = capi.tv_rope_table(int(self.lens.max()) + n + 1, w.D, device=dev)
+        self.out = torch.empty_like(self.inp["q"])
+        dt = self.inp["q"].dtype
+        self.flags, self.num_ctas = flags, num_ctas
+        self.ws = capi.alloc_workspace(capi.tv_tree_attn_workspace_size(B, n, w.Hq, w.Hkv, w.D, dt, w.block_size,
+                                                                         num_ctas, flags), dev)
+        self.greedy = self.sample = None
+        if w.accept == "greedy":
+            self.greedy = W.greedy_inputs(w, parent, device=dev)
+        elif w.accept == "sample":
+            self.sample = W.sample_chain_inputs(w, device=dev)
+        cols = n if self.sample is None else self.sample["p"].shape[1]
+        self.acc_out = torch.empty(B, cols, dtype=torch.int32, device=dev)
+        self.acc_n = torch.empty(B, dtype=torch.int32, device=dev)
+        self.acc_path = torch.empty(B, cols, dtype=torch.int32, device=dev)
+        self.esize = 2 if dt == torch.bfloat16 else 4
+        self.attn_bytes = attention_bytes(w, self.lens, n, self.esize)
+        self.launches = 5 + (1 if w.accept != "none" else 0)
+
+    def run(self, ev_attn=None):
+        c, i = self.capi, self.inp
+        c.tv_tree_mask(self.parent, self.seq_lens, mask=self.mask, depth=self.depth, pos=self.pos)
+        c.tv_rope_apply(i["q"], i["k_tree"], self.pos, self.table)
+        if ev_attn:
+            ev_attn[0].record()
+        c.tv_tree_attn_verify(i["q"], i["k_cache"], i["v_cache"], i["block_table"], self.seq_lens, i["k_tree"],
+                              i["v_tree"], self.mask, out=self.out, workspace=self.ws, num_ctas=self.num_ctas,
+                              flags=self.flags)
+        if ev_attn:
+            ev_attn[1].record()
+        if self.greedy is not None:
+            c.tv_tree_accept_greedy(self.greedy["tokens"], self.parent, logits=self.greedy["logits"], out=self.acc_out,
+                                    n_out=self.acc_n, path=self.acc_path)
+        elif self.sample is not None:
+            s = self.sample
+            c.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
+                                    n_nodes=s["n_nodes"], out=self.acc_out, n_out=self.acc_n, path=self.acc_path)
+
+    def per_step_inputs(self):
+        """Tensors a caller supplies fresh every step (the KV cache is resident state)."""
+        t = {"q": self.inp["q"], "k_tree": self.inp["k_tree"], "v_tree": self.inp["v_tree"],
+             "block_table": self.inp["block_table"], "seq_lens": self.seq_lens, "parent": self.parent}
+        if self.greedy is not None:
+            t.update(tokens=self.greedy["tokens"], logits=self.greedy["logits"])
+        if self.sample is not None:
+            t.update({f"s_{k}": v for k, v in self.sample.items()})
+        return t
+
+
+def run_ours(args, world, rank, local):
+    w = W.WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = Step(w, dev, args.flags, args.num_ctas)
+    ws_bytes = st.attn_bytes + sum(t.numel() * t.element_size() for t in st.per_step_inputs().values())
+    flush = None
+    if ws_bytes < 2 * L2_BYTES:
+        flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:
+        for k in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            evs[k][0].record()
+            st.run(eva[k])
+            evs[k][1].record()
+        torch.cuda.synchronize()
+    clocks = sampler.summary()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_ms = [a.elapsed_time(b) for a, b in eva]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    nodes = w.B * st.N
+    value = world * nodes * args.steps / (total_ms / 1e3)
+
+    # end to end through the public API: pinned host inputs in, accepted tokens out
+    e2e = None
+    if not args.no_e2e:
+        dev_t = st.per_step_inputs()
+        host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) for k, v in dev_t.items()}
+        h_out = torch.empty(st.acc_out.shape, dtype=torch.int32, pin_memory=True)
+        h_n = torch.empty(st.acc_n.shape, dtype=torch.int32, pin_memory=True)
+        bi = sum(v.numel() * v.element_size() for v in host.values())
+        bo = h_out.numel() * 4 + h_n.numel() * 4
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            for k, v in host.items():
+                dev_t[k].copy_(v, non_blocking=True)
+            st.run()
+            h_out.copy_(st.acc_out, non_blocking=True)
+            h_n.copy_(st.acc_n, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * nodes * args.steps / (e_ms / 1e3), "unit": "nodes/s",
+               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+
+    peak, peak_kind = measured_hbm_peak()
+    attn_mean_ms = statistics.mean(attn_ms)
+    achieved = st.attn_bytes / (attn_mean_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+                "kernel": "tv_tree_attn_verify (plan + split kernel + combine)",
+                "algorithmic_bytes_per_call": int(st.attn_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
+                "attn_ms_mean": round(attn_mean_ms, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_cpu, g, s = cpu_inputs(w, st.inp, st.greedy, st.sample)
+        nps, used, el = time_oracle(w, inp_cpu, st.paths, g, s, args.cpu_seconds, sample_order(st.lens))
+        cpu = {"value": nps, "unit": "nodes/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{len(used)} of {w.B} requests (all {st.N} nodes, all {w.Hq} heads, acceptance incl.), "
+                         f"prefix lengths {[int(st.lens[b]) for b in used][:6]}..., {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "tree-verify nodes/s and KV-read HBM GB/s (% of GB300 peak), 1 GPU",
+            "value": value, "unit": "nodes/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if st.esize == 2 else "f32",
+            "data": "synthetic (seeded; no model weights)",
+            "config": {"workload": w.name, "B": w.B, "N": st.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                       "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab,
+                       "l2": ("L2 flushed between steps" if flush is not None
+                              else f"inputs larger than L2 ({ws_bytes / 2**30:.2f} GiB per step)"),
+                       "kernel_flags": args.flags, "parallelism": f"replicas x{world} (requests sharded)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": st.launches * args.steps,
+            "kv_read_gbs": round(achieved, 1), "kv_read_frac_of_peak": round(achieved / peak, 4),
+        }
+        print(json.dumps(line))
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    inp = W.attention_inputs(w, device="cpu")
+    parent = None
+    from oracle import tree as OT
+    parent = OT.build_tree(w.paths())[0]
+    greedy = W.greedy_inputs(w, parent, device="cpu") if w.accept == "greedy" else None
+    sample = W.sample_chain_inputs(w, device="cpu") if w.accept == "sample" else None
+    inp_cpu, g, s = cpu_inputs(w, inp, greedy, sample)
+    lens = inp_cpu["seq_lens"]
+    order = sample_order(lens)
+    for k in range(args.warmup):
+        oracle_sample_run(w, inp_cpu, w.paths(), g, s, [order[k % len(order)]])
+    t0 = time.perf_counter()
+    used = []
+    for k in range(args.steps):
+        b = order[k % len(order)]
+        oracle_sample_run(w, inp_cpu, w.paths(), g, s, [b])
+        used.append(b)
+    el = time.perf_counter() - t0
+    value = args.steps * w.n_nodes / el
+    cores = blas_threads()
+    line = {
+        "impl": "reference",
+        "metric": "tree-verify nodes/s and KV-read HBM GB/s (% of GB300 peak), 1 GPU",
+        "value": value, "unit": "nodes/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded; no model weights)",
+        "config": {"workload": w.name, "B": w.B, "N": w.n_nodes, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab},
+        "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one request per step (all {w.n_nodes} nodes, all heads, acceptance incl.), "
+                                   f"requests {used[:6]}..."},
+        "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

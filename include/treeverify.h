@@ -1,0 +1,274 @@
+/*
+ * treeverify.h -- C ABI of libtreeverify: one-pass verification of a
+ * speculative draft tree on an sm_103a GPU (tree structure, depth-indexed
+ * RoPE, tree attention over a paged KV cache, tree acceptance).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every function returns an int status: TV_OK (0) or a negative TV_ERR_*
+ *   code; tv_last_error() then describes the failure (thread-local string).
+ * - "device" pointers are CUDA global memory of the current device; "host"
+ *   pointers are ordinary CPU memory.  The caller owns every buffer; the
+ *   library allocates no device memory anywhere and keeps no state between
+ *   calls apart from per-device property caches.
+ * - Device entry points only enqueue work on the caller's stream (a
+ *   cudaStream_t passed as void*, NULL = legacy default stream); they never
+ *   synchronise and never read device data on the host.  Device-side input
+ *   problems (a bad parent array, an out-of-vocabulary token, a negative
+ *   prefix length) are not errors of the call: kernels OR TV_DEV_* bits into
+ *   the caller's int32 status word (device memory, may be NULL when the
+ *   caller does not want it) and skip the offending item, never trapping.
+ * - B == 0 is legal everywhere: nothing is launched and TV_OK is returned.
+ * - Node 0 of a tree is the root (the last accepted token); N <= 64 nodes,
+ *   parent-before-child order (parent[i] < i).
+ *
+ * Pages cited ("Build the tree attention mask that verifies a draft tree in
+ * one pass"; "Implement the lossless speculative sampling verifier for a
+ * batch with ragged draft lengths"; "Tree Verification"; "Encode branch
+ * histories in masks and positions") are the sources the operations follow.
+ */
+#ifndef TREEVERIFY_H
+#define TREEVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) ------------------------------------ */
+#define TV_OK 0
+#define TV_ERR_INVALID_ARG (-1)     /* null pointer, bad size or stride     */
+#define TV_ERR_MISSING_PARENT (-2)  /* a rank path whose prefix is absent   */
+#define TV_ERR_TOO_MANY_NODES (-3)  /* more than max_nodes / 64 tree nodes  */
+#define TV_ERR_UNSUPPORTED (-4)     /* shape or dtype this build cannot run */
+#define TV_ERR_WORKSPACE (-5)       /* workspace missing or too small       */
+#define TV_ERR_CUDA (-6)            /* a CUDA runtime / driver call failed  */
+
+/* ---- device status bits (OR-ed into the caller's int32 status word) ---- */
+#define TV_DEV_BAD_TOPOLOGY 1   /* parent[0] != -1 or parent[i] not in [0, i) */
+#define TV_DEV_BAD_TOKEN 2      /* draft token outside [0, V): child skipped  */
+#define TV_DEV_OUT_OVERFLOW 4   /* walk longer than out_cols: truncated       */
+#define TV_DEV_BAD_POSITION 8   /* prefix length < 0 or position >= max_pos   */
+
+/* ---- element types ------------------------------------------------------ */
+#define TV_F32 0
+#define TV_BF16 1
+
+#define TV_MAX_NODES 64
+
+/* Kernel selection for tv_tree_attn_verify (flags & 3). */
+#define TV_ATTN_AUTO 0      /* tensor-core kernel when the shape allows it */
+#define TV_ATTN_SIMT 1      /* CUDA-core FP32 kernel (any supported shape)  */
+#define TV_ATTN_TCGEN05 2   /* tcgen05/TMEM/TMA kernel; TV_ERR_UNSUPPORTED
+                               if the shape or device does not allow it   */
+
+/* Description of the last failure on this thread ("" if none). */
+const char* tv_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int tv_version(void);
+
+/*
+ * tv_tree_build -- host, synchronous.
+ * "Build the tree attention mask ...", sections "The tree." and "The mask.":
+ * candidates are rank paths ((0,) = top guess, (0,1) = second guess after
+ * the top guess); duplicates are removed; paths are ordered by length, then
+ * lexicographically; candidate k of that order becomes node k + 1 (node 0 is
+ * the root); parent = node of the path without its last rank; depth = path
+ * length; a path whose prefix is not a candidate is rejected; a node attends
+ * to itself and its ancestors.
+ *
+ * ranks     host int32 [offsets[n_paths]]: all paths' ranks concatenated.
+ * offsets   host int32 [n_paths + 1]: path k is ranks[offsets[k] .. offsets[k+1]);
+ *           an empty path denotes the root and is ignored.
+ * max_nodes capacity of the outputs (1..64).
+ * parent    host int32 [max_nodes] out: parent[0] = -1.
+ * depth     host int32 [max_nodes] out.
+ * mask      host uint64 [max_nodes] out: bit j of mask[i] <=> j is i or an
+ *           ancestor of i.
+ * path_to_node host int32 [n_paths] out (may be NULL): node of each input path.
+ * n_nodes   host int32 out: N = 1 + number of distinct non-empty paths.
+ * Errors: TV_ERR_INVALID_ARG (null / negative rank / bad offsets),
+ * TV_ERR_MISSING_PARENT, TV_ERR_TOO_MANY_NODES.  Zero paths give N = 1.
+ */
+int tv_tree_build(const int32_t* ranks, const int32_t* offsets, int32_t n_paths,
+                  int32_t max_nodes, int32_t* parent, int32_t* depth,
+                  uint64_t* mask, int32_t* path_to_node, int32_t* n_nodes);
+
+/*
+ * tv_tree_mask -- device, asynchronous.  Batched ancestor rows and positions.
+ * "Build the tree attention mask ...", "The mask." (position = prefix length
+ * + depth, siblings share a position) and "Tree Verification", "Tree
+ * Attention" (parent-before-child flattening).
+ *
+ * parent    device int32 [B, N] with row stride parent_bstride elements
+ *           (0 = one tree shared by all requests).
+ * seq_lens  device int32 [B]: prefix length L_b (tokens already cached).
+ * mask      device uint64 [B, N] out; depth, pos device int32 [B, N] out
+ *           (pos = L_b + depth).  A request whose parent row is not a
+ *           parent-before-child tree gets zero rows and TV_DEV_BAD_TOPOLOGY.
+ * status    device int32 (nullable), see TV_DEV_*.
+ */
+int tv_tree_mask(const int32_t* parent, int64_t parent_bstride, const int32_t* seq_lens,
+                 int32_t B, int32_t N, uint64_t* mask, int32_t* depth, int32_t* pos,
+                 int32_t* status, void* stream);
+
+/*
+ * tv_rope_table -- device, asynchronous.  Fills the rotary table used by
+ * tv_rope_apply: cos_sin float32 [max_pos, 2, D/2]; row p holds
+ * cos(p * base^(-2k/D)) for k < D/2 followed by the matching sines, each
+ * evaluated in float64 and rounded once to float32.
+ */
+int tv_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base, void* stream);
+
+/*
+ * tv_rope_apply -- device, asynchronous, in place.
+ * "Build the tree attention mask ...", "What interviewers probe next" and
+ * "Common mistakes" (RoPE must rotate a node at its depth, not at its
+ * flattened index); "Encode branch histories ..." (positional features
+ * follow the model's position semantics).  Rotate-half convention: for each
+ * row x of length D, (x1, x2) = (x[:D/2], x[D/2:]) becomes
+ * (x1 cos - x2 sin, x2 cos + x1 sin) at position pos[b, i], math in float32.
+ *
+ * q       device [B, N, Hq, D] (dtype), rotated in place.
+ * k_tree  device [B, N, Hkv, D] (dtype), rotated in place (may be NULL).
+ * pos     device int32 [B, N] (from tv_tree_mask).
+ * cos_sin device float32 [max_pos, 2, D/2] from tv_rope_table.
+ * A position outside [0, max_pos) leaves the row untouched and sets
+ * TV_DEV_BAD_POSITION.  D must be even and a multiple of 16.
+ */
+int tv_rope_apply(void* q, void* k_tree, const int32_t* pos, const float* cos_sin,
+                  int32_t max_pos, int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
+                  int32_t head_dim, int32_t dtype, int32_t* status, void* stream);
+
+/*
+ * tv_tree_attn_workspace_size -- host.  Bytes of device workspace that
+ * tv_tree_attn_verify needs for this shape, kernel choice (flags) and grid
+ * (num_ctas, 0 = one wave of the current device).  Does not depend on the
+ * prefix lengths.
+ */
+int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
+                                int32_t head_dim, int32_t dtype, int32_t block_size,
+                                int32_t num_ctas, int32_t flags, size_t* bytes);
+
+/*
+ * tv_tree_attn_verify -- device, asynchronous.  One-pass tree attention.
+ * "Tree Verification", "Tree Attention": every node attends to the whole
+ * cached prefix, to its root-path ancestors and to itself, nothing else;
+ * "Build the tree attention mask ...", "The mask.": the step mask is
+ * [prefix all true | tree mask] and a kernel may take the tree part as
+ * per-node ancestor rows.  Output row (b, i, h) is
+ *   softmax(scale * q . K^T) V  over keys = prefix 0..L_b-1 of request b
+ *   (KV head h / (Hq/Hkv)) followed by the tree nodes j with bit j of
+ *   mask[b, i] set.
+ * q and k_tree must already be rotated (tv_rope_apply); the cached prefix
+ * keys are stored rotated.
+ *
+ * q          device [B, N, Hq, D] (dtype).
+ * k_cache,   device [num_blocks, Hkv, block_size, D] (dtype): position t of
+ * v_cache    request b is block block_table[b, t / block_size], slot
+ *            t % block_size.  Slots >= L_b of a used block must hold finite
+ *            values (they are read and weighted by exactly zero).
+ * block_table device int32 [B, max_blocks]; entries >= ceil(L_b/block_size)
+ *            are never read.
+ * seq_lens   device int32 [B], 0 <= L_b <= max_blocks * block_size.
+ * k_tree,    device [B, N, Hkv, D] (dtype): node K/V (node 0 = root).
+ * v_tree
+ * mask       device uint64 [B, N] with row stride mask_bstride elements
+ *            (0 = shared); bit j of mask[b, i] <=> node i may see node j.
+ * scale      softmax scale (e.g. 1/sqrt(D)).
+ * out        device [B, N, Hq, D] (dtype) out.
+ * lse        device float32 [B, N, Hq] out (nullable): natural-log softmax
+ *            normaliser of each row.
+ * workspace  device buffer of at least tv_tree_attn_workspace_size bytes,
+ *            256-byte aligned; its contents on entry are irrelevant.
+ * flags      TV_ATTN_* kernel selection.
+ * num_ctas   persistent grid size (0 = one wave of the current device);
+ *            must equal the value given to tv_tree_attn_workspace_size.
+ * Supported: N <= 64, D in {64, 128, 256}, dtype TV_F32 or TV_BF16,
+ * Hq % Hkv == 0.  The tensor-core kernel needs bf16, D = 128, Hq/Hkv * N <= 256
+ * and block_size a multiple of 16; TV_ATTN_AUTO falls back to the CUDA-core
+ * kernel otherwise.
+ */
+int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
+                        int64_t num_blocks, int32_t block_size,
+                        const int32_t* block_table, int32_t max_blocks,
+                        const int32_t* seq_lens, const void* k_tree, const void* v_tree,
+                        const uint64_t* mask, int64_t mask_bstride,
+                        int32_t B, int32_t N, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                        int32_t dtype, float scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, int32_t num_ctas,
+                        int32_t flags, void* stream);
+
+/*
+ * tv_tree_accept_greedy -- device, asynchronous.
+ * "Build the tree attention mask ...", "The mask." (walk from the root while
+ * some child's draft token equals the target's choice after the current
+ * node; every visited node emits the target's choice) and "Encode branch
+ * histories ..." (node i's logits predict its children).  Children are tried
+ * in ascending node index; the target's choice is the largest logit, ties to
+ * the lowest vocabulary index.
+ *
+ * logits        device float32 [B, N, V] (row stride V) or NULL; then
+ * target_argmax device int32 [B, N] gives the choices directly.
+ * tokens        device int32 [B, N]: draft token of node i (column 0 unused).
+ * parent        device int32 [B, N], row stride parent_bstride (0 = shared).
+ * n_nodes       device int32 [B] (nullable = N): nodes >= n_nodes[b] absent.
+ * out           device int32 [B, out_cols] out: emitted tokens, -1 padded.
+ * n_out         device int32 [B] out: accepted drafts + 1.
+ * path          device int32 [B, out_cols] out (nullable): node at which
+ *               each token was emitted (root first), -1 padded.
+ * status        device int32 (nullable), TV_DEV_OUT_OVERFLOW if a walk does
+ *               not fit in out_cols (out_cols >= max depth + 1 avoids it).
+ */
+int tv_tree_accept_greedy(const float* logits, const int32_t* target_argmax,
+                          const int32_t* tokens, const int32_t* parent,
+                          int64_t parent_bstride, const int32_t* n_nodes,
+                          int32_t B, int32_t N, int32_t V, int32_t* out,
+                          int32_t* n_out, int32_t* path, int32_t out_cols,
+                          int32_t* status, void* stream);
+
+/*
+ * tv_tree_accept_sample -- device, asynchronous.  Lossless stochastic walk.
+ * "Implement the lossless speculative sampling verifier ...", "A strong
+ * answer" (accept x iff u * q(x) < p(x), no division; first rejection stops
+ * the chain; replacement from the normalised residual max(0, p - q); bonus
+ * from p after the last accepted node; p = q guard) and "What interviewers
+ * probe next" (on a tree: after a rejection the target at that node becomes
+ * the normalised residual and the next sibling is tested against it);
+ * "Tree Verification", "Accepting on a Tree" (top-down walk, a leaf earns the
+ * bonus).
+ *
+ * Exact arithmetic (both this kernel and any checker follow it bit for bit):
+ *  - level 0 at a node: accept child x iff (double)u * (double)q(x) < (double)p(x);
+ *  - integer images P = rint(p * 2^40), Q = rint(q * 2^40) (half to even);
+ *    after a rejection at level m (scale S_0 = 2^40, S_m = W_m for m >= 1):
+ *    w_{m+1} = max(0, w_m - floor((S_m * Q + 2^39) / 2^40)), w_0 = P,
+ *    W_{m+1} = sum w_{m+1}; if W_{m+1} == 0 the level is not advanced;
+ *  - level m >= 1: accept iff fl64(fl64(u * q(x)) * W_m) < w_m(x);
+ *  - the final draw (replacement, or bonus from p at level 0 with W = sum P)
+ *    returns min(#{x : prefix_sum_w(x) < ceil(fl64(u_final * W))}, V - 1).
+ * Contract: every p and q row sums to at most 2 (probability rows).
+ *
+ * p, q      device float32 [B, N, V]: target distribution after node i and the
+ *           draft distribution node i's children were drawn from.
+ * tokens    device int32 [B, N]; parent as in greedy; n_nodes [B] (nullable).
+ * u_accept  device float32 [B, N]: uniform used when node i is tested.
+ * u_final   device float32 [B]: uniform of the replacement / bonus draw.
+ * out, n_out, path, out_cols, status: as in tv_tree_accept_greedy.  Tokens
+ * outside [0, V) are skipped and flagged TV_DEV_BAD_TOKEN.
+ */
+int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,
+                          const int32_t* parent, int64_t parent_bstride,
+                          const int32_t* n_nodes, const float* u_accept,
+                          const float* u_final, int32_t B, int32_t N, int32_t V,
+                          int32_t* out, int32_t* n_out, int32_t* path, int32_t out_cols,
+                          int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEVERIFY_H */

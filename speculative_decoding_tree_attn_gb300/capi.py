@@ -1,0 +1,253 @@
+"""Thin Python binding of libtreeverify (ctypes).
+
+Each function carries the name of the C entry point it calls and only
+marshals arguments: it checks tensor placement/dtype/contiguity, passes raw
+pointers, sizes and the current CUDA stream, and raises :class:`TVError` on a
+non-zero status.  Every step of the computation runs in the library's
+kernels; there is no Python or CPU fallback, and a missing library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtreeverify.so")
+
+TV_F32, TV_BF16 = 0, 1
+TV_ATTN_AUTO, TV_ATTN_SIMT, TV_ATTN_TCGEN05 = 0, 1, 2
+TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION = 1, 2, 4, 8
+STATUS_NAMES = {0: "TV_OK", -1: "TV_ERR_INVALID_ARG", -2: "TV_ERR_MISSING_PARENT", -3: "TV_ERR_TOO_MANY_NODES",
+                -4: "TV_ERR_UNSUPPORTED", -5: "TV_ERR_WORKSPACE", -6: "TV_ERR_CUDA"}
+
+# exported symbol -> (restype, argtypes)
+_I32, _I64, _P, _SZ, _F, _D = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float, ctypes.c_double
+SIGNATURES = {
+    "tv_last_error": (ctypes.c_char_p, []),
+    "tv_version": (ctypes.c_int, []),
+    "tv_tree_build": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P, _P, _P]),
+    "tv_tree_mask": (ctypes.c_int, [_P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P]),
+    "tv_rope_table": (ctypes.c_int, [_P, _I32, _I32, _D, _P]),
+    "tv_rope_apply": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P]),
+    "tv_tree_attn_workspace_size": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
+    "tv_tree_attn_verify": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32,
+                                           _I32, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _I32, _I32, _P]),
+    "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
+    "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
+                                             _P, _P]),
+}
+
+
+class TVError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with speculative_decoding_tree_attn_gb300.build")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(h, name)
+            f.restype, f.argtypes = res, args
+        _lib = h
+    return _lib
+
+
+def _check(fn, code):
+    if code != 0:
+        raise TVError(fn, code, lib().tv_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev(t, name, dtypes):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _code(dtype):
+    if dtype == torch.float32:
+        return TV_F32
+    if dtype == torch.bfloat16:
+        return TV_BF16
+    raise ValueError(f"unsupported dtype {dtype}")
+
+
+def tv_version():
+    return lib().tv_version()
+
+
+def tv_tree_build(paths, max_nodes=64):
+    """Rank paths -> (parent, depth, mask (uint64), path_to_node, n_nodes) on the host."""
+    ranks = np.array([r for p in paths for r in p], dtype=np.int32)
+    offsets = np.zeros(len(paths) + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum([len(p) for p in paths])
+    parent = np.zeros(max_nodes, dtype=np.int32)
+    depth = np.zeros(max_nodes, dtype=np.int32)
+    mask = np.zeros(max_nodes, dtype=np.uint64)
+    p2n = np.zeros(max(len(paths), 1), dtype=np.int32)
+    n = np.zeros(1, dtype=np.int32)
+    _check("tv_tree_build", lib().tv_tree_build(_ptr(ranks) if ranks.size else None, _ptr(offsets), len(paths),
+                                                max_nodes, _ptr(parent), _ptr(depth), _ptr(mask), _ptr(p2n), _ptr(n)))
+    k = int(n[0])
+    return parent[:k].copy(), depth[:k].copy(), mask[:k].copy(), p2n[:len(paths)].copy(), k
+
+
+def tv_tree_mask(parent, seq_lens, status=None, mask=None, depth=None, pos=None, stream=None):
+    """parent int32 [N] (shared) or [B, N]; seq_lens int32 [B] -> (mask int64 [B, N]
+    holding the uint64 rows, depth int32 [B, N], pos int32 [B, N])."""
+    _dev(parent, "parent", (torch.int32,))
+    _dev(seq_lens, "seq_lens", (torch.int32,))
+    B = seq_lens.numel()
+    N = parent.shape[-1]
+    bstride = 0 if parent.dim() == 1 else parent.stride(0)
+    dev = seq_lens.device
+    mask = torch.empty(B, N, dtype=torch.int64, device=dev) if mask is None else mask
+    depth = torch.empty(B, N, dtype=torch.int32, device=dev) if depth is None else depth
+    pos = torch.empty(B, N, dtype=torch.int32, device=dev) if pos is None else pos
+    _check("tv_tree_mask", lib().tv_tree_mask(_ptr(parent), bstride, _ptr(seq_lens), B, N, _ptr(mask), _ptr(depth),
+                                              _ptr(pos), _ptr(status), _stream(stream)))
+    return mask, depth, pos
+
+
+def tv_rope_table(max_pos, head_dim, base=10000.0, device="cuda", stream=None):
+    cs = torch.empty(max_pos, 2, head_dim // 2, dtype=torch.float32, device=device)
+    _check("tv_rope_table", lib().tv_rope_table(_ptr(cs), max_pos, head_dim, float(base), _stream(stream)))
+    return cs
+
+
+def tv_rope_apply(q, k_tree, pos, cos_sin, status=None, stream=None):
+    """Rotates q [B, N, Hq, D] and k_tree [B, N, Hkv, D] in place at pos [B, N]."""
+    _dev(q, "q", (torch.float32, torch.bfloat16))
+    if k_tree is not None:
+        _dev(k_tree, "k_tree", (q.dtype,))
+    _dev(pos, "pos", (torch.int32,))
+    _dev(cos_sin, "cos_sin", (torch.float32,))
+    B, N, Hq, D = q.shape
+    Hkv = k_tree.shape[2] if k_tree is not None else 1
+    _check("tv_rope_apply", lib().tv_rope_apply(_ptr(q), _ptr(k_tree), _ptr(pos), _ptr(cos_sin), cos_sin.shape[0],
+                                                B, N, Hq, Hkv, D, _code(q.dtype), _ptr(status), _stream(stream)))
+
+
+def tv_tree_attn_workspace_size(B, N, Hq, Hkv, head_dim, dtype, block_size, num_ctas=0, flags=0):
+    out = ctypes.c_size_t(0)
+    _check("tv_tree_attn_workspace_size",
+           lib().tv_tree_attn_workspace_size(B, N, Hq, Hkv, head_dim, _code(dtype), block_size, num_ctas, flags,
+                                             ctypes.addressof(out)))
+    return out.value
+
+
+def alloc_workspace(nbytes, device="cuda"):
+    """A 256-byte aligned workspace tensor of at least nbytes."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def tv_tree_attn_verify(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, mask, *, scale=None,
+                        out=None, lse=None, workspace=None, num_ctas=0, flags=0, stream=None):
+    """Tree attention; returns out [B, N, Hq, D].  mask is int64 [B, N] (uint64 rows)
+    or [N] (shared)."""
+    dts = (torch.float32, torch.bfloat16)
+    _dev(q, "q", dts)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_tree", k_tree), ("v_tree", v_tree)):
+        _dev(t, name, (q.dtype,))
+    _dev(block_table, "block_table", (torch.int32,))
+    _dev(seq_lens, "seq_lens", (torch.int32,))
+    _dev(mask, "mask", (torch.int64,))
+    B, N, Hq, D = q.shape
+    Hkv = k_tree.shape[2]
+    num_blocks, _, block_size, _ = k_cache.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(tv_tree_attn_workspace_size(B, N, Hq, Hkv, D, q.dtype, block_size, num_ctas,
+                                                                flags), q.device)
+    mstride = 0 if mask.dim() == 1 else mask.stride(0)
+    _check("tv_tree_attn_verify",
+           lib().tv_tree_attn_verify(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, block_size, _ptr(block_table),
+                                     block_table.shape[1], _ptr(seq_lens), _ptr(k_tree), _ptr(v_tree), _ptr(mask),
+                                     mstride, B, N, Hq, Hkv, D, _code(q.dtype), scale, _ptr(out), _ptr(lse),
+                                     _ptr(workspace), workspace.numel(), num_ctas, flags, _stream(stream)))
+    return out
+
+
+def _accept_outputs(B, out_cols, device, out, n_out, path):
+    if out is None:
+        out = torch.empty(B, out_cols, dtype=torch.int32, device=device)
+    if n_out is None:
+        n_out = torch.empty(B, dtype=torch.int32, device=device)
+    if path is None:
+        path = torch.empty(B, out_cols, dtype=torch.int32, device=device)
+    return out, n_out, path
+
+
+def tv_tree_accept_greedy(tokens, parent, *, logits=None, target_argmax=None, n_nodes=None, out_cols=None,
+                          out=None, n_out=None, path=None, status=None, stream=None):
+    """Greedy walk; returns (out [B, out_cols], n_out [B], path [B, out_cols])."""
+    _dev(tokens, "tokens", (torch.int32,))
+    _dev(parent, "parent", (torch.int32,))
+    B, N = tokens.shape
+    if logits is not None:
+        _dev(logits, "logits", (torch.float32,))
+        V = logits.shape[-1]
+    else:
+        _dev(target_argmax, "target_argmax", (torch.int32,))
+        V = 1
+    out_cols = N if out_cols is None else out_cols
+    out, n_out, path = _accept_outputs(B, out_cols, tokens.device, out, n_out, path)
+    bstride = 0 if parent.dim() == 1 else parent.stride(0)
+    _check("tv_tree_accept_greedy",
+           lib().tv_tree_accept_greedy(_ptr(logits), _ptr(target_argmax), _ptr(tokens), _ptr(parent), bstride,
+                                       _ptr(n_nodes), B, N, V, _ptr(out), _ptr(n_out), _ptr(path), out_cols,
+                                       _ptr(status), _stream(stream)))
+    return out, n_out, path
+
+
+def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=None, out_cols=None, out=None,
+                          n_out=None, path=None, status=None, stream=None):
+    """Stochastic walk; returns (out [B, out_cols], n_out [B], path [B, out_cols])."""
+    _dev(p, "p", (torch.float32,))
+    _dev(q, "q", (torch.float32,))
+    _dev(tokens, "tokens", (torch.int32,))
+    _dev(parent, "parent", (torch.int32,))
+    _dev(u_accept, "u_accept", (torch.float32,))
+    _dev(u_final, "u_final", (torch.float32,))
+    B, N, V = p.shape
+    out_cols = N if out_cols is None else out_cols
+    out, n_out, path = _accept_outputs(B, out_cols, p.device, out, n_out, path)
+    bstride = 0 if parent.dim() == 1 else parent.stride(0)
+    _check("tv_tree_accept_sample",
+           lib().tv_tree_accept_sample(_ptr(p), _ptr(q), _ptr(tokens), _ptr(parent), bstride, _ptr(n_nodes),
+                                       _ptr(u_accept), _ptr(u_final), B, N, V, _ptr(out), _ptr(n_out), _ptr(path),
+                                       out_cols, _ptr(status), _stream(stream)))
+    return out, n_out, path

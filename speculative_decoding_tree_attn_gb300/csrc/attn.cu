@@ -1,0 +1,450 @@
+// Tree attention: the plan and combine kernels, the CUDA-core (FP32 FFMA)
+// kernel, and the tv_tree_attn_verify entry point that dispatches between the
+// CUDA-core kernel and the tcgen05 kernel of attn_tc.cu.
+//
+// What is computed ("Tree Verification", "Tree Attention"; "Build the tree
+// attention mask that verifies a draft tree in one pass", "The mask."): each
+// row (request b, node i, query head h) attends to the whole cached prefix of
+// b with no mask, then to the tree nodes whose bit is set in the node's
+// ancestor row (itself and its ancestors) -- the [prefix all true | tree
+// mask] step mask, with the tree part taken as per-node bit rows.  Online
+// softmax in the log2 domain with float32 accumulation.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "attn_common.cuh"
+#include "attn_tc.h"
+
+namespace tv {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// plan: tile_start[u] = sum of tile counts of units < u
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  for (int base = 0; base < p.U; base += blockDim.x) {
+    const int u = base + threadIdx.x;
+    int n = 0;
+    if (u < p.U) {
+      int b, kvh, rg;
+      unit_coords(p, u, b, kvh, rg);
+      n = (clamp_len(p, b) + p.BLK - 1) / p.BLK + 1;
+    }
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = (lane < (int)(blockDim.x / 32)) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = carry + (warp ? warp_sums[warp - 1] : 0) + incl - n;
+    if (u < p.U) p.tile_start[u] = before;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = before + n;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.tile_start[p.U] = carry;
+}
+
+// ---------------------------------------------------------------------------
+// element helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core kernel: 8 warps, 32 rows per unit (4 per warp), 64-key tiles in
+// shared memory as float32.  Lane j scores keys j and j + 32 of the tile and
+// owns output dimensions lane + 32 e.
+// ---------------------------------------------------------------------------
+constexpr int kSimtBlk = 64;
+constexpr int kSimtRows = 32;
+constexpr int kSimtWarps = 8;
+
+template <int D>
+constexpr size_t simt_smem_bytes() {
+  return sizeof(float) * ((size_t)kSimtBlk * (D + 1) + (size_t)kSimtBlk * D + (size_t)kSimtRows * D);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(AttnParams p) {
+  constexpr int RPW = kSimtRows / kSimtWarps;
+  constexpr int DPL = D / 32;
+  extern __shared__ float smem[];
+  float* Ks = smem;                          // [BLK][D + 1]
+  float* Vs = Ks + kSimtBlk * (D + 1);       // [BLK][D]
+  float* Qs = Vs + kSimtBlk * D;             // [RPG][D]
+  __shared__ uint64_t s_rowmask[kSimtRows];
+
+  const T* __restrict__ q = static_cast<const T*>(p.q);
+  const T* __restrict__ kc = static_cast<const T*>(p.k_cache);
+  const T* __restrict__ vc = static_cast<const T*>(p.v_cache);
+  const T* __restrict__ kt = static_cast<const T*>(p.k_tree);
+  const T* __restrict__ vt = static_cast<const T*>(p.v_tree);
+  T* __restrict__ out = static_cast<T*>(p.out);
+
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int64_t T_total = p.tile_start[p.U];
+  const int64_t c = blockIdx.x;
+  const int64_t t0 = cta_start(c, T_total, p.P), t1 = cta_start(c + 1, T_total, p.P);
+  if (t0 >= t1) return;
+
+  for (int u = find_unit(p.tile_start, p.U, t0); u < p.U && p.tile_start[u] < t1; ++u) {
+    const int64_t us = p.tile_start[u], ue = p.tile_start[u + 1];
+    const int a = (int)(max(t0, us) - us), e = (int)(min(t1, ue) - us), n_u = (int)(ue - us);
+    int b, kvh, rg;
+    unit_coords(p, u, b, kvh, rg);
+    const int L = clamp_len(p, b);
+
+    for (int idx = tid; idx < kSimtRows * D; idx += blockDim.x) {
+      const int r = idx / D, d = idx % D, gr = rg * kSimtRows + r;
+      float v = 0.f;
+      if (gr < p.R) {
+        const int i = gr / p.G, h = kvh * p.G + gr % p.G;
+        v = to_f32(q[(((int64_t)b * p.N + i) * p.Hq + h) * D + d]);
+      }
+      Qs[idx] = v;
+    }
+    for (int r = tid; r < kSimtRows; r += blockDim.x) {
+      const int gr = rg * kSimtRows + r;
+      s_rowmask[r] = gr < p.R ? p.mask[(int64_t)b * p.mask_bstride + gr / p.G] : 0ull;
+    }
+    float m[RPW], l[RPW], acc[RPW][DPL];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+      m[rr] = -INFINITY;
+      l[rr] = 0.f;
+#pragma unroll
+      for (int x = 0; x < DPL; ++x) acc[rr][x] = 0.f;
+    }
+    __syncthreads();
+
+    for (int k = a; k < e; ++k) {
+      const bool tree_tile = (k == n_u - 1);
+      for (int idx = tid; idx < kSimtBlk * D; idx += blockDim.x) {
+        const int j = idx / D, d = idx % D;
+        float kv = 0.f, vv = 0.f;
+        if (tree_tile) {
+          if (j < p.N) {
+            const int64_t o = (((int64_t)b * p.N + j) * p.Hkv + kvh) * D + d;
+            kv = to_f32(kt[o]);
+            vv = to_f32(vt[o]);
+          }
+        } else {
+          const int t = k * kSimtBlk + j;
+          if (t < L) {
+            const int64_t blk = p.block_table[(int64_t)b * p.max_blocks + t / p.block_size];
+            if (blk >= 0 && blk < p.num_blocks) {  // a bad table entry reads as zeros
+              const int64_t o = ((blk * p.Hkv + kvh) * p.block_size + t % p.block_size) * D + d;
+              kv = to_f32(kc[o]);
+              vv = to_f32(vc[o]);
+            }
+          }
+        }
+        Ks[j * (D + 1) + d] = kv;
+        Vs[j * D + d] = vv;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int rr = 0; rr < RPW; ++rr) {
+        const int r = warp * RPW + rr;
+        if (rg * kSimtRows + r >= p.R) continue;
+        float s0 = 0.f, s1 = 0.f;
+        const float* qr = Qs + r * D;
+        const float* k0 = Ks + lane * (D + 1);
+        const float* k1 = Ks + (lane + 32) * (D + 1);
+#pragma unroll 8
+        for (int d = 0; d < D; ++d) {
+          const float qd = qr[d];
+          s0 = fmaf(qd, k0[d], s0);
+          s1 = fmaf(qd, k1[d], s1);
+        }
+        bool ok0, ok1;
+        if (tree_tile) {
+          const uint64_t row = s_rowmask[r];
+          ok0 = lane < p.N && ((row >> lane) & 1ull);
+          ok1 = lane + 32 < p.N && ((row >> (lane + 32)) & 1ull);
+        } else {
+          ok0 = k * kSimtBlk + lane < L;
+          ok1 = k * kSimtBlk + lane + 32 < L;
+        }
+        const float x0 = ok0 ? s0 * p.scale_log2 : -INFINITY;
+        const float x1 = ok1 ? s1 * p.scale_log2 : -INFINITY;
+        const float m_new = fmaxf(m[rr], warp_max(fmaxf(x0, x1)));
+        if (m_new == -INFINITY) continue;
+        const float alpha = exp2f(m[rr] - m_new);
+        const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
+        l[rr] = l[rr] * alpha + warp_sum(p0 + p1);
+#pragma unroll
+        for (int x = 0; x < DPL; ++x) acc[rr][x] *= alpha;
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+          const float pa = __shfl_sync(0xffffffffu, p0, j);
+          const float pb = __shfl_sync(0xffffffffu, p1, j);
+#pragma unroll
+          for (int x = 0; x < DPL; ++x)
+            acc[rr][x] = fmaf(pa, Vs[j * D + lane + 32 * x], fmaf(pb, Vs[(j + 32) * D + lane + 32 * x], acc[rr][x]));
+        }
+        m[rr] = m_new;
+      }
+      __syncthreads();
+    }
+
+    const bool complete = (a == 0 && e == n_u);
+    const int slot = (t0 < us) ? 1 : 0;  // 0: the CTA's first unit, 1: its last
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+      const int r = warp * RPW + rr, gr = rg * kSimtRows + r;
+      if (gr >= p.R) continue;
+      const float inv = 1.f / l[rr];
+      const float lse2 = m[rr] + log2f(l[rr]);
+      if (complete) {
+        const int i = gr / p.G, h = kvh * p.G + gr % p.G;
+        const int64_t row = ((int64_t)b * p.N + i) * p.Hq + h;
+#pragma unroll
+        for (int x = 0; x < DPL; ++x) out[row * D + lane + 32 * x] = from_f32<T>(acc[rr][x] * inv);
+        if (p.lse && lane == 0) p.lse[row] = lse2 * 0.69314718055994530942f;
+      } else {
+        const int64_t srow = (c * 2 + slot) * p.RPG + r;
+#pragma unroll
+        for (int x = 0; x < DPL; ++x) p.part_o[srow * D + lane + 32 * x] = acc[rr][x] * inv;
+        if (lane == 0) p.part_lse[srow] = lse2;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine: O = sum_k 2^(lse_k - lse*) O_k over the pieces of a split unit
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
+  const int u = blockIdx.x;
+  const int64_t T_total = p.tile_start[p.U];
+  const int64_t us = p.tile_start[u], ue = p.tile_start[u + 1];
+  const int64_t c0 = cta_of(us, T_total, p.P), c1 = cta_of(ue - 1, T_total, p.P);
+  if (c0 == c1) return;
+  int b, kvh, rg;
+  unit_coords(p, u, b, kvh, rg);
+  T* __restrict__ out = static_cast<T*>(p.out);
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32, nwarps = blockDim.x / 32;
+  for (int r = warp; r < p.RPG; r += nwarps) {
+    const int gr = rg * p.RPG + r;
+    if (gr >= p.R) break;
+    float mx = -INFINITY;
+    for (int64_t c = c0; c <= c1; ++c) {
+      const int64_t s0 = cta_start(c, T_total, p.P);
+      if (s0 == cta_start(c + 1, T_total, p.P)) continue;
+      const int slot = s0 < us ? 1 : 0;
+      mx = fmaxf(mx, p.part_lse[(c * 2 + slot) * p.RPG + r]);
+    }
+    float z = 0.f;
+    for (int64_t c = c0; c <= c1; ++c) {
+      const int64_t s0 = cta_start(c, T_total, p.P);
+      if (s0 == cta_start(c + 1, T_total, p.P)) continue;
+      const int slot = s0 < us ? 1 : 0;
+      z += exp2f(p.part_lse[(c * 2 + slot) * p.RPG + r] - mx);
+    }
+    const float lse2 = mx + log2f(z);
+    const int i = gr / p.G, h = kvh * p.G + gr % p.G;
+    const int64_t row = ((int64_t)b * p.N + i) * p.Hq + h;
+    for (int d = lane; d < p.D; d += 32) {
+      float o = 0.f;
+      for (int64_t c = c0; c <= c1; ++c) {
+        const int64_t s0 = cta_start(c, T_total, p.P);
+        if (s0 == cta_start(c + 1, T_total, p.P)) continue;
+        const int slot = s0 < us ? 1 : 0;
+        const int64_t srow = (c * 2 + slot) * p.RPG + r;
+        o = fmaf(exp2f(p.part_lse[srow] - lse2), p.part_o[srow * p.D + d], o);
+      }
+      out[row * p.D + d] = from_f32<T>(o);
+    }
+    if (p.lse && lane == 0) p.lse[row] = lse2 * 0.69314718055994530942f;
+  }
+}
+
+template <typename T, int D>
+int launch_simt_t(const AttnParams& p, cudaStream_t stream) {
+  const size_t smem = simt_smem_bytes<D>();
+  cudaError_t err = cudaFuncSetAttribute(attn_simt_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(attn_simt_kernel)");
+  attn_simt_kernel<T, D><<<p.P, kSimtWarps * 32, smem, stream>>>(p);
+  TV_LAUNCH_CHECK("attn_simt_kernel");
+  return TV_OK;
+}
+
+template <typename T, int D>
+int simt_blocks_per_sm(int* n) {
+  const size_t smem = simt_smem_bytes<D>();
+  cudaError_t err = cudaFuncSetAttribute(attn_simt_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(attn_simt_kernel)");
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, attn_simt_kernel<T, D>, kSimtWarps * 32, smem);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (*n < 1) *n = 1;
+  return TV_OK;
+}
+
+int simt_dispatch(const AttnParams& p, int dtype, cudaStream_t stream, int* blocks_per_sm) {
+#define TV_SIMT_CASE(TT, DD)                                                   \
+  if (p.D == DD) return blocks_per_sm ? simt_blocks_per_sm<TT, DD>(blocks_per_sm) \
+                                      : launch_simt_t<TT, DD>(p, stream);
+  if (dtype == TV_F32) {
+    TV_SIMT_CASE(float, 64) TV_SIMT_CASE(float, 128) TV_SIMT_CASE(float, 256)
+  } else {
+    TV_SIMT_CASE(__nv_bfloat16, 64) TV_SIMT_CASE(__nv_bfloat16, 128) TV_SIMT_CASE(__nv_bfloat16, 256)
+  }
+#undef TV_SIMT_CASE
+  return fail(TV_ERR_UNSUPPORTED, "tree attention: head_dim %d not in {64, 128, 256}", p.D);
+}
+
+// Shape decisions shared by the workspace query and the launch.
+struct AttnConfig {
+  bool tc;
+  int RPG, RG, U, BLK, P;
+  int64_t off_part_o, off_part_lse, bytes;
+};
+
+int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size, int num_ctas, int flags,
+                AttnConfig* cfg) {
+  if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Hq % Hkv)
+    return fail(TV_ERR_INVALID_ARG, "tree attention: bad sizes B=%d N=%d Hq=%d Hkv=%d", B, N, Hq, Hkv);
+  if (D != 64 && D != 128 && D != 256)
+    return fail(TV_ERR_UNSUPPORTED, "tree attention: head_dim %d not in {64, 128, 256}", D);
+  if (dtype != TV_F32 && dtype != TV_BF16) return fail(TV_ERR_UNSUPPORTED, "tree attention: dtype %d", dtype);
+  if (block_size < 1) return fail(TV_ERR_INVALID_ARG, "tree attention: block_size %d", block_size);
+  if (num_ctas < 0) return fail(TV_ERR_INVALID_ARG, "tree attention: num_ctas %d", num_ctas);
+  const int sel = flags & 3;
+  if (sel == 3) return fail(TV_ERR_INVALID_ARG, "tree attention: bad kernel selection flags %d", flags);
+  DeviceInfo dev;
+  int st = current_device_info(&dev);
+  if (st) return st;
+  const int G = Hq / Hkv, R = G * N;
+  const bool tc_ok = tc_supported(dev, dtype, D, R, block_size);
+  if (sel == TV_ATTN_TCGEN05 && !tc_ok)
+    return fail(TV_ERR_UNSUPPORTED, "tcgen05 tree attention needs sm_10x, bf16, head_dim 128, "
+                "(Hq/Hkv)*N <= %d and block_size %% 16 == 0", kTcMaxRows);
+  cfg->tc = (sel == TV_ATTN_TCGEN05) || (sel == TV_ATTN_AUTO && tc_ok);
+  int per_sm = 1;
+  if (cfg->tc) {
+    cfg->RPG = tc_rows_per_unit(R);
+    cfg->BLK = kTcBlk;
+  } else {
+    cfg->RPG = kSimtRows;
+    cfg->BLK = kSimtBlk;
+    AttnParams dummy{};
+    dummy.D = D;
+    st = simt_dispatch(dummy, dtype, nullptr, &per_sm);
+    if (st) return st;
+  }
+  cfg->RG = (int)ceil_div(R, cfg->RPG);
+  cfg->U = B * Hkv * cfg->RG;
+  cfg->P = num_ctas > 0 ? num_ctas : dev.sm_count * per_sm;
+  const int64_t plan = align256((int64_t)(cfg->U + 1) * 4);
+  const int64_t po = align256((int64_t)cfg->P * 2 * cfg->RPG * D * 4);
+  const int64_t pl = align256((int64_t)cfg->P * 2 * cfg->RPG * 4);
+  cfg->off_part_o = plan;
+  cfg->off_part_lse = plan + po;
+  cfg->bytes = plan + po + pl;
+  return TV_OK;
+}
+
+}  // namespace
+
+int launch_plan(const AttnParams& p, cudaStream_t stream) {
+  plan_kernel<<<1, 1024, 0, stream>>>(p);
+  TV_LAUNCH_CHECK("plan_kernel");
+  return TV_OK;
+}
+
+int launch_combine(const AttnParams& p, int dtype, cudaStream_t stream) {
+  if (p.P <= 1) return TV_OK;
+  if (dtype == TV_F32) combine_kernel<float><<<p.U, 256, 0, stream>>>(p);
+  else combine_kernel<__nv_bfloat16><<<p.U, 256, 0, stream>>>(p);
+  TV_LAUNCH_CHECK("combine_kernel");
+  return TV_OK;
+}
+
+}  // namespace tv
+
+extern "C" int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                           int32_t dtype, int32_t block_size, int32_t num_ctas, int32_t flags,
+                                           size_t* bytes) {
+  tv::clear_error();
+  if (!bytes) return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_attn_workspace_size: null output");
+  tv::AttnConfig cfg;
+  int st = tv::attn_config(B, N, Hq, Hkv, head_dim, dtype, block_size, num_ctas, flags, &cfg);
+  if (st) return st;
+  *bytes = (size_t)cfg.bytes;
+  return TV_OK;
+}
+
+extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                                   int32_t block_size, const int32_t* block_table, int32_t max_blocks,
+                                   const int32_t* seq_lens, const void* k_tree, const void* v_tree,
+                                   const uint64_t* mask, int64_t mask_bstride, int32_t B, int32_t N, int32_t Hq,
+                                   int32_t Hkv, int32_t head_dim, int32_t dtype, float scale, void* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, int32_t num_ctas, int32_t flags,
+                                   void* stream) {
+  using namespace tv;
+  clear_error();
+  AttnConfig cfg;
+  int st = attn_config(B, N, Hq, Hkv, head_dim, dtype, block_size, num_ctas, flags, &cfg);
+  if (st) return st;
+  if (B == 0) return TV_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !k_tree || !v_tree || !mask || !out)
+    return fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify: null pointer");
+  if (num_blocks < 1 || max_blocks < 1 || mask_bstride < 0)
+    return fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify: bad num_blocks/max_blocks/mask stride");
+  if (!workspace || workspace_bytes < (size_t)cfg.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return fail(TV_ERR_WORKSPACE, "tv_tree_attn_verify: workspace needs %lld bytes, 256-byte aligned",
+                (long long)cfg.bytes);
+  AttnParams p{};
+  p.q = q; p.k_cache = k_cache; p.v_cache = v_cache; p.block_table = block_table; p.seq_lens = seq_lens;
+  p.k_tree = k_tree; p.v_tree = v_tree; p.mask = mask; p.mask_bstride = mask_bstride; p.out = out; p.lse = lse;
+  char* ws = static_cast<char*>(workspace);
+  p.tile_start = reinterpret_cast<int32_t*>(ws);
+  p.part_o = reinterpret_cast<float*>(ws + cfg.off_part_o);
+  p.part_lse = reinterpret_cast<float*>(ws + cfg.off_part_lse);
+  p.num_blocks = num_blocks; p.block_size = block_size; p.max_blocks = max_blocks;
+  p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.D = head_dim; p.G = Hq / Hkv;
+  p.R = p.G * N; p.RPG = cfg.RPG; p.RG = cfg.RG; p.U = cfg.U; p.BLK = cfg.BLK; p.P = cfg.P;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((st = launch_plan(p, s))) return st;
+  st = cfg.tc ? launch_attn_tc(p, s) : simt_dispatch(p, dtype, s, nullptr);
+  if (st) return st;
+  return launch_combine(p, dtype, s);
+}

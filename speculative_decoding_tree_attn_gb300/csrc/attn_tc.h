@@ -1,0 +1,21 @@
+// Interface of the tcgen05 tree-attention kernel (attn_tc.cu) used by the
+// dispatcher in attn.cu.
+#pragma once
+
+#include "attn_common.cuh"
+
+namespace tv {
+
+constexpr int kTcBlk = 128;      // KV positions per tile (one MMA N / K extent)
+constexpr int kTcMaxRows = 256;  // two 128-row M tiles per CTA
+
+// True when the tensor-core kernel can run this shape on this device.
+bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int block_size);
+
+// Rows per unit for `rows` = G * N query rows per KV head (128 or 256).
+int tc_rows_per_unit(int rows);
+
+// Launches the persistent tensor-core kernel (plan already enqueued).
+int launch_attn_tc(const AttnParams& p, cudaStream_t stream);
+
+}  // namespace tv

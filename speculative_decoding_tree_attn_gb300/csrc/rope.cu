@@ -1,0 +1,148 @@
+// Depth-indexed rotary embedding of the tree queries and tree keys.
+//
+// "Build the tree attention mask that verifies a draft tree in one pass",
+// "What interviewers probe next" / "Common mistakes": siblings share a
+// position and rotating a node at its flattened index scores it in the wrong
+// place; "Encode branch histories in masks and positions": rotary features
+// follow the model's position semantics.  The positions come from
+// tv_tree_mask (prefix length + depth); the cached prefix keys were rotated
+// when they were written.
+//
+// Layout of the table: cos_sin[p][0][k] = cos(p * base^(-2k/D)),
+// cos_sin[p][1][k] = sin(...), k < D/2, computed in float64 and rounded once.
+// Rotate-half pairing: element k is paired with element k + D/2.
+#include <algorithm>
+
+#include <cuda_bf16.h>
+
+#include "common.h"
+
+namespace {
+
+__global__ void rope_table_kernel(float* __restrict__ cs, int max_pos, int D, double base) {
+  const int half = D / 2;
+  const int64_t n = (int64_t)max_pos * half;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int p = (int)(t / half);
+    const int k = (int)(t % half);
+    const double inv_freq = pow(base, -2.0 * (double)k / (double)D);
+    double s, c;
+    sincos((double)p * inv_freq, &s, &c);
+    cs[(int64_t)p * D + k] = (float)c;
+    cs[(int64_t)p * D + half + k] = (float)s;
+  }
+}
+
+template <typename T>
+struct Vec8;  // eight consecutive elements, one 16- or 32-byte access
+
+template <>
+struct Vec8<__nv_bfloat16> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
+    uint4 raw = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[8]) {
+    uint4 raw;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = raw;
+  }
+};
+
+template <>
+struct Vec8<float> {
+  static __device__ __forceinline__ void load(const float* p, float (&v)[8]) {
+    float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float (&v)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+};
+
+// One thread rotates 8 pairs (elements k..k+7 and k+D/2..k+D/2+7) of one row.
+// Rows are enumerated as (b, i, head) with the Hq query heads first, then the
+// Hkv tree-key heads of the same node.
+template <typename T>
+__global__ void rope_apply_kernel(T* __restrict__ q, T* __restrict__ kt, const int32_t* __restrict__ pos,
+                                  const float* __restrict__ cs, int max_pos, int64_t BN, int Hq, int Hkv,
+                                  int D, int32_t* __restrict__ status) {
+  const int half = D / 2;
+  const int chunks = half / 8;
+  const int heads = Hq + (kt ? Hkv : 0);
+  const int64_t total = BN * heads * chunks;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(t % chunks);
+    const int64_t r = t / chunks;
+    const int h = (int)(r % heads);
+    const int64_t bi = r / heads;
+    const int32_t p = pos[bi];
+    if (p < 0 || p >= max_pos) {
+      if (status && c == 0) atomicOr(status, TV_DEV_BAD_POSITION);
+      continue;
+    }
+    T* row = (h < Hq) ? q + (bi * Hq + h) * D : kt + (bi * Hkv + (h - Hq)) * D;
+    const float* cosr = cs + (int64_t)p * D + c * 8;
+    const float* sinr = cosr + half;
+    float x1[8], x2[8], co[8], si[8];
+    Vec8<T>::load(row + c * 8, x1);
+    Vec8<T>::load(row + half + c * 8, x2);
+    Vec8<float>::load(cosr, co);
+    Vec8<float>::load(sinr, si);
+    float y1[8], y2[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      y1[e] = x1[e] * co[e] - x2[e] * si[e];
+      y2[e] = x2[e] * co[e] + x1[e] * si[e];
+    }
+    Vec8<T>::store(row + c * 8, y1);
+    Vec8<T>::store(row + half + c * 8, y2);
+  }
+}
+
+}  // namespace
+
+extern "C" int tv_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base, void* stream) {
+  tv::clear_error();
+  if (!cos_sin || max_pos < 1 || head_dim < 2 || head_dim % 2 || !(base > 0.0))
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_rope_table: bad arguments");
+  const int64_t n = (int64_t)max_pos * (head_dim / 2);
+  const int blocks = (int)std::min<int64_t>(tv::ceil_div(n, 256), 4096);
+  rope_table_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(cos_sin, max_pos, head_dim, base);
+  TV_LAUNCH_CHECK("rope_table_kernel");
+  return TV_OK;
+}
+
+extern "C" int tv_rope_apply(void* q, void* k_tree, const int32_t* pos, const float* cos_sin, int32_t max_pos,
+                             int32_t B, int32_t N, int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t dtype,
+                             int32_t* status, void* stream) {
+  tv::clear_error();
+  if (B < 0 || N < 1 || Hq < 1 || Hkv < 1 || head_dim % 16 || head_dim < 16 || max_pos < 1)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_rope_apply: bad sizes");
+  if (dtype != TV_F32 && dtype != TV_BF16) return tv::fail(TV_ERR_UNSUPPORTED, "tv_rope_apply: dtype %d", dtype);
+  if (B == 0) return TV_OK;
+  if (!q || !pos || !cos_sin) return tv::fail(TV_ERR_INVALID_ARG, "tv_rope_apply: null pointer");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_tree) |
+       reinterpret_cast<uintptr_t>(cos_sin)) & 15)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_rope_apply: buffers must be 16-byte aligned");
+  const int64_t BN = (int64_t)B * N;
+  const int64_t total = BN * (Hq + (k_tree ? Hkv : 0)) * (head_dim / 16);
+  const int blocks = (int)std::min<int64_t>(tv::ceil_div(total, 256), 152 * 16);
+  if (dtype == TV_BF16)
+    rope_apply_kernel<__nv_bfloat16><<<blocks, 256, 0, (cudaStream_t)stream>>>(
+        (__nv_bfloat16*)q, (__nv_bfloat16*)k_tree, pos, cos_sin, max_pos, BN, Hq, Hkv, head_dim, status);
+  else
+    rope_apply_kernel<float><<<blocks, 256, 0, (cudaStream_t)stream>>>(
+        (float*)q, (float*)k_tree, pos, cos_sin, max_pos, BN, Hq, Hkv, head_dim, status);
+  TV_LAUNCH_CHECK("rope_apply_kernel");
+  return TV_OK;
+}

@@ -1,0 +1,153 @@
+"""GPU parity of tree acceptance against the oracle: bit-exact tokens, n_out
+and paths for greedy (from logits or from target choices) and for the
+stochastic walk given the same uniforms; plus the sampling page's
+losslessness chi-square run end to end through the GPU kernel."""
+
+import numpy as np
+import pytest
+import torch
+
+from markov_harness import chi_square, generate
+from oracle import accept as OA
+from oracle import tree as OT
+from speculative_decoding_tree_attn_gb300 import capi
+from speculative_decoding_tree_attn_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _cmp(gpu, ref_out, ref_n, ref_path, out_cols=None):
+    out, n_out, path = (t.cpu().numpy() for t in gpu)
+    np.testing.assert_array_equal(n_out, ref_n)
+    k = ref_out.shape[1] if out_cols is None else out_cols
+    np.testing.assert_array_equal(out[:, :k], ref_out[:, :k])
+    np.testing.assert_array_equal(path[:, :k], ref_path[:, :k])
+
+
+@pytest.mark.parametrize("name", ["tiny_b1_f32", "gqa_b8_l512_2048_n26", "b64_l1k_8k_n64_greedy"])
+def test_greedy_from_logits_bit_exact(name):
+    w = W.WORKLOADS[name]
+    parent, *_ = OT.build_tree(w.paths())
+    g = W.greedy_inputs(w, parent, device="cuda")
+    par = torch.from_numpy(parent.astype(np.int32)).cuda()
+    res = capi.tv_tree_accept_greedy(g["tokens"], par, logits=g["logits"])
+    am = OA.argmax_rows(g["logits"].cpu().numpy())
+    ref = OA.tree_accept_greedy(am, g["tokens"].cpu().numpy(), parent)
+    _cmp(res, *ref)
+    assert res[1].float().mean().item() > 1.0
+
+
+def test_greedy_ties_and_target_choices():
+    V, N = 1000, 10
+    parent, *_ = OT.build_tree(W.PAGE_TREE_PATHS)
+    rng = np.random.default_rng(110)
+    B = 300
+    tokens = rng.integers(0, 5, size=(B, N)).astype(np.int32)
+    logits = rng.integers(0, 4, size=(B, N, V)).astype(np.float32)      # many ties
+    par = torch.from_numpy(parent.astype(np.int32)).cuda()
+    res = capi.tv_tree_accept_greedy(torch.from_numpy(tokens).cuda(), par, logits=torch.from_numpy(logits).cuda())
+    am = OA.argmax_rows(logits)
+    _cmp(res, *OA.tree_accept_greedy(am, tokens, parent))
+    am2 = rng.integers(0, 5, size=(B, N)).astype(np.int32)
+    n_nodes = rng.integers(1, N + 1, size=B).astype(np.int32)
+    res = capi.tv_tree_accept_greedy(torch.from_numpy(tokens).cuda(), par, target_argmax=torch.from_numpy(am2).cuda(),
+                                     n_nodes=torch.from_numpy(n_nodes).cuda())
+    _cmp(res, *OA.tree_accept_greedy(am2, tokens, parent, n_nodes))
+
+
+def test_greedy_odd_vocab_and_per_request_parents():
+    rng = np.random.default_rng(111)
+    B, N, V = 40, 20, 997
+    parents = np.stack([OT.build_tree(W.random_rank_paths(N, 5, rng))[0] for _ in range(B)]).astype(np.int32)
+    tokens = rng.integers(0, 3, size=(B, N)).astype(np.int32)
+    logits = rng.standard_normal((B, N, V)).astype(np.float32)
+    logits[..., :3] += 2.5
+    res = capi.tv_tree_accept_greedy(torch.from_numpy(tokens).cuda(), torch.from_numpy(parents).cuda(),
+                                     logits=torch.from_numpy(logits).cuda())
+    _cmp(res, *OA.tree_accept_greedy(OA.argmax_rows(logits), tokens, parents))
+
+
+def test_greedy_overflow_flag():
+    parent = np.arange(-1, 7).astype(np.int32)
+    tokens = np.full((1, 8), 5, dtype=np.int32)
+    am = np.full((1, 8), 5, dtype=np.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, n_out, path = capi.tv_tree_accept_greedy(torch.from_numpy(tokens).cuda(), torch.from_numpy(parent).cuda(),
+                                                  target_argmax=torch.from_numpy(am).cuda(), out_cols=3,
+                                                  status=status)
+    assert status.item() == capi.TV_DEV_OUT_OVERFLOW and n_out.item() == 3
+
+
+def test_sample_full_workload_bit_exact():
+    """B=256 chains over a 128000-token vocabulary, ragged num_draft ~ U{0..4}."""
+    w = W.WORKLOADS["b256_l2k_4k_n10_sample"]
+    s = W.sample_chain_inputs(w, device="cuda")
+    res = capi.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
+                                     n_nodes=s["n_nodes"])
+    c = {k: v.cpu().numpy() for k, v in s.items()}
+    ref = OA.tree_accept_sample(c["p"], c["q"], c["tokens"], c["parent"], c["n_nodes"], c["u_accept"], c["u_final"])
+    _cmp(res, *ref)
+    K = c["p"].shape[1] - 1
+    out_c, n_c = OA.verify_chain(c["tokens"][:, 1:], c["q"][:, :K], c["p"], c["n_nodes"] - 1, c["u_accept"][:, 1:],
+                                 c["u_final"])
+    np.testing.assert_array_equal(res[1].cpu().numpy(), n_c)
+
+
+@pytest.mark.parametrize("V", [4, 33, 1000, 4096])
+def test_sample_trees_with_sibling_levels(V):
+    """Trees with up to 5 siblings per node: several residual levels per node."""
+    rng = np.random.default_rng(120 + V)
+    B, N = 200, 16
+    paths = [(0,), (1,), (2,), (3,), (4,), (0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (4, 0), (0, 0, 0), (0, 0, 1),
+             (0, 1, 0), (1, 0, 0)]
+    parent, *_ = OT.build_tree(paths)
+    p = rng.dirichlet(np.ones(V) * 0.3, size=(B, N)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.3, size=(B, N)).astype(np.float32)
+    q[:20] = p[:20]
+    tokens = np.zeros((B, N), dtype=np.int32)
+    for b in range(B):
+        for c in range(1, N):
+            row = q[b, parent[c]].astype(np.float64)
+            tokens[b, c] = rng.choice(V, p=row / row.sum())
+    n_nodes = rng.integers(1, N + 1, size=B).astype(np.int32)
+    ua = rng.random((B, N), dtype=np.float32)
+    uf = rng.random(B, dtype=np.float32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    res = capi.tv_tree_accept_sample(t(p), t(q), t(tokens), t(parent.astype(np.int32)), t(ua), t(uf),
+                                     n_nodes=t(n_nodes))
+    _cmp(res, *OA.tree_accept_sample(p, q, tokens, parent, n_nodes, ua, uf))
+
+
+def test_sample_bad_token_flag():
+    p = torch.full((1, 2, 8), 0.125, device="cuda")
+    tokens = torch.tensor([[0, 9]], dtype=torch.int32, device="cuda")
+    parent = torch.tensor([-1, 0], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, n_out, path = capi.tv_tree_accept_sample(p, p, tokens, parent, torch.zeros(1, 2, device="cuda"),
+                                                  torch.full((1,), 0.5, device="cuda"), status=status)
+    assert status.item() == capi.TV_DEV_BAD_TOKEN and n_out.item() == 1
+
+
+def _gpu_verify(p, q, tokens, parent, n_nodes, ua, uf):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out, n_out, _ = capi.tv_tree_accept_sample(t(p), t(q), t(tokens.astype(np.int32)), t(parent.astype(np.int32)),
+                                               t(ua), t(uf), n_nodes=t(n_nodes.astype(np.int32)))
+    return out.cpu().numpy(), n_out.cpu().numpy()
+
+
+def test_gpu_chain_lossless_chi_square(verifier_facts):
+    f = verifier_facts
+    V, n_seq = int(f["chi2_vocab"][0][0]), int(f["chi2_sequences"][0][0])
+    n_tok, K, thr = int(f["chi2_tokens"][0][0]), int(f["chi2_drafts_per_round"][0][0]), float(f["chi2_threshold"][0][0])
+    pt, qt = W.markov_tables(V, 16)
+    seqs = generate(_gpu_verify, pt, qt, np.arange(-1, K), n_seq, n_tok, 130)
+    assert chi_square(seqs, pt) < thr
+
+
+def test_gpu_tree_lossless_chi_square(verifier_facts):
+    f = verifier_facts
+    V, n_tok, thr = int(f["chi2_vocab"][0][0]), int(f["chi2_tokens"][0][0]), float(f["chi2_threshold"][0][0])
+    parent, *_ = OT.build_tree([(0,), (1,), (2,), (0, 0), (2, 0)])
+    pt, qt = W.markov_tables(V, 22)
+    seqs = generate(_gpu_verify, pt, qt, parent, 200_000, n_tok, 131)
+    assert chi_square(seqs, pt) < thr

@@ -1,0 +1,167 @@
+"""GPU parity of the tree-attention path (tree_build -> tree_mask -> rope_apply
+-> tree_attn_verify) against the float64 per-path oracle.
+
+Tolerances are the ones fixed for this path: max-abs 1e-4 for float32 inputs
+and 2e-2 for bf16 inputs (float32 accumulation).  Both kernels are covered:
+the CUDA-core kernel for every shape, the tcgen05 kernel for the shapes it
+accepts.  Small cases compare every output; the full-size workloads compare
+sampled requests (shortest and longest prefix included) in the launch
+configuration the bench times."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import BF16_TOL, F32_TOL, gpu_pipeline, max_err, oracle_rows, to_np
+from oracle import tree as OT
+from speculative_decoding_tree_attn_gb300 import capi
+from speculative_decoding_tree_attn_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [capi.TV_ATTN_SIMT, capi.TV_ATTN_TCGEN05]
+
+
+def tc_available(Hq, Hkv, N, D=128, dtype=torch.bfloat16, bs=16):
+    try:
+        capi.tv_tree_attn_workspace_size(1, N, Hq, Hkv, D, dtype, bs, 0, capi.TV_ATTN_TCGEN05)
+        return True
+    except capi.TVError:
+        return False
+
+
+def _workload(B, Hq, Hkv, D, dtype, bs, N, seed):
+    return W.Workload("case", B, Hq, Hkv, D, dtype, ("fixed", 0), bs, (0.7, 0.15), N, 8, seed)
+
+
+def _check_all(inp, paths, tol, flags, num_ctas=0):
+    B, N = inp["q"].shape[:2]
+    pairs = [(b, i) for b in range(B) for i in range(N)]
+    out, lse = gpu_pipeline(inp, paths, flags=flags, num_ctas=num_ctas, want_lse=True)
+    ref = oracle_rows(inp, paths, pairs)
+    err = max_err(out, ref, pairs)
+    assert err <= tol, err
+    lse_g = to_np(lse)
+    lerr = max(float(np.abs(lse_g[b, i] - ref[(b, i)][1]).max()) for b, i in pairs)
+    assert lerr <= 20 * tol, lerr
+    return out
+
+
+def test_tiny_page_tree_f32():
+    """B=1, one head, D=64, float32, L=32, the mask page's 10-node tree."""
+    w = W.WORKLOADS["tiny_b1_f32"]
+    inp = W.attention_inputs(w, device="cuda")
+    for num_ctas in (0, 1, 2, 5):
+        _check_all(inp, W.PAGE_TREE_PATHS, F32_TOL, capi.TV_ATTN_SIMT, num_ctas)
+
+
+def test_tiny_random_trees_f32():
+    rng = np.random.default_rng(50)
+    for t in range(6):
+        paths = W.random_rank_paths(10, 4, rng)
+        w = _workload(1, 1, 1, 64, "f32", 16, 10, 60 + t)
+        inp = W.attention_inputs(w, device="cuda", seq_lens=[32])
+        _check_all(inp, paths, F32_TOL, capi.TV_ATTN_SIMT)
+
+
+@pytest.mark.parametrize("L", [0, 1, 15, 16, 17, 63, 64, 65, 127, 128, 129])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prefix_edges(L, dtype):
+    """Prefix lengths at tile and block edges with a deep tree (mask offsets)."""
+    rng = np.random.default_rng(51 + L)
+    N = 37
+    paths = W.random_rank_paths(N, 8, rng)
+    w = _workload(2, 8, 2, 128, dtype, 16, N, 70 + L)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[L, max(L - 1, 0)])
+    tol = F32_TOL if dtype == "f32" else BF16_TOL
+    for flags in KERNELS:
+        if flags == capi.TV_ATTN_TCGEN05 and (dtype == "f32" or not tc_available(8, 2, N)):
+            continue
+        for num_ctas in (0, 3):
+            _check_all(inp, paths, tol, flags, num_ctas)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 8, 16, 31, 32, 33, 47, 63, 64])
+def test_node_count_sweep(N):
+    """Every node count from a single root to 64 nodes (hard-coded sizes were
+    the failure mode of the DDTree post-mortem's mask corruption)."""
+    rng = np.random.default_rng(80 + N)
+    paths = W.random_rank_paths(N, 6, rng)
+    for dtype, tol in (("f32", F32_TOL), ("bf16", BF16_TOL)):
+        w = _workload(3, 4, 1, 128, dtype, 16, N, 90 + N)
+        inp = W.attention_inputs(w, device="cuda", seq_lens=[0, 17, 200])
+        for flags in KERNELS:
+            if flags == capi.TV_ATTN_TCGEN05 and (dtype == "f32" or not tc_available(4, 1, N)):
+                continue
+            _check_all(inp, paths, tol, flags)
+
+
+@pytest.mark.parametrize("D", [64, 256])
+def test_other_head_dims_simt(D):
+    rng = np.random.default_rng(95 + D)
+    paths = W.random_rank_paths(12, 4, rng)
+    w = _workload(2, 4, 2, D, "f32", 8, 12, 96)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[45, 3])
+    _check_all(inp, paths, F32_TOL, capi.TV_ATTN_SIMT)
+
+
+def test_mask_sensitive_tree_keys_dominate():
+    """Tree keys scaled up so the tree part carries most of the softmax mass."""
+    rng = np.random.default_rng(97)
+    paths = W.random_rank_paths(26, 5, rng)
+    w = _workload(2, 8, 2, 128, "f32", 16, 26, 98)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[64, 300], tree_scale=3.0)
+    _check_all(inp, paths, F32_TOL, capi.TV_ATTN_SIMT)
+    wb = _workload(2, 8, 2, 128, "bf16", 16, 26, 98)
+    inp = W.attention_inputs(wb, device="cuda", seq_lens=[64, 300], tree_scale=2.0)
+    for flags in KERNELS:
+        if flags == capi.TV_ATTN_TCGEN05 and not tc_available(8, 2, 26):
+            continue
+        _check_all(inp, paths, BF16_TOL, flags)
+
+
+def test_deterministic_and_kernel_agreement():
+    w = W.WORKLOADS["gqa_b8_l512_2048_n26"]
+    inp = W.attention_inputs(w, device="cuda")
+    a, _ = gpu_pipeline(inp, w.paths())
+    b, _ = gpu_pipeline(inp, w.paths())
+    assert torch.equal(a, b)
+    s, _ = gpu_pipeline(inp, w.paths(), flags=capi.TV_ATTN_SIMT)
+    assert (a.float() - s.float()).abs().max().item() <= 2 * BF16_TOL
+
+
+def test_workspace_errors():
+    w = _workload(1, 2, 1, 64, "f32", 16, 4, 99)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[10])
+    parent = torch.tensor([-1, 0, 0, 1], dtype=torch.int32, device="cuda")
+    mask, _, _ = capi.tv_tree_mask(parent, inp["seq_lens"])
+    with pytest.raises(capi.TVError) as e:
+        capi.tv_tree_attn_verify(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"],
+                                 inp["k_tree"], inp["v_tree"], mask, workspace=capi.alloc_workspace(256))
+    assert e.value.code == -5
+    with pytest.raises(capi.TVError) as e:
+        capi.tv_tree_attn_verify(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"],
+                                 inp["k_tree"], inp["v_tree"], mask, flags=capi.TV_ATTN_TCGEN05)
+    assert e.value.code == -4
+
+
+FULL = ["gqa_b8_l512_2048_n26", "b64_l1k_8k_n64_greedy", "long_b16_l32k_n33", "b256_l2k_4k_n10_sample"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """Full workloads in the bench's launch configuration (auto kernel, one
+    wave); sampled requests incl. the shortest and longest prefix."""
+    w = W.WORKLOADS[name]
+    inp = W.attention_inputs(w, device="cuda")
+    paths = w.paths()
+    out, _ = gpu_pipeline(inp, paths)
+    lens = inp["seq_lens"].cpu().numpy()
+    rng = np.random.default_rng(100)
+    bs = sorted({int(lens.argmin()), int(lens.argmax()), *rng.integers(0, w.B, size=2).tolist()})
+    N = w.n_nodes
+    nodes = sorted({0, N - 1, *rng.integers(0, N, size=3).tolist()})
+    pairs = [(b, i) for b in bs for i in nodes]
+    ref = oracle_rows(inp, paths, pairs)
+    assert max_err(out, ref, pairs) <= BF16_TOL
+    assert torch.isfinite(out.float()).all()
