@@ -51,6 +51,7 @@ extern "C" {
 #define TV_DEV_BAD_TOKEN 2      /* draft token outside [0, V): child skipped  */
 #define TV_DEV_OUT_OVERFLOW 4   /* walk longer than out_cols: truncated       */
 #define TV_DEV_BAD_POSITION 8   /* prefix length < 0 or position >= max_pos   */
+#define TV_DEV_TIMEOUT 16       /* a pipeline wait in a kernel exceeded 2 s     */
 
 /* ---- element types ------------------------------------------------------ */
 #define TV_F32 0
@@ -187,10 +188,13 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  * flags      TV_ATTN_* kernel selection.
  * num_ctas   persistent grid size (0 = one wave of the current device);
  *            must equal the value given to tv_tree_attn_workspace_size.
+ * status     device int32 (nullable): TV_DEV_TIMEOUT if a pipeline wait of
+ *            the tensor-core kernel gave up (the output is then incomplete).
  * Supported: N <= 64, D in {64, 128, 256}, dtype TV_F32 or TV_BF16,
- * Hq % Hkv == 0.  The tensor-core kernel needs bf16, D = 128, Hq/Hkv * N <= 256
- * and block_size a multiple of 16; TV_ATTN_AUTO falls back to the CUDA-core
- * kernel otherwise.
+ * Hq % Hkv == 0.  The tensor-core kernel needs an sm_10x device, bf16,
+ * D = 128, G = Hq/Hkv dividing 128, G * N <= 256, block_size a multiple of 16
+ * that divides 64 or is a multiple of 64, and num_blocks * Hkv * block_size
+ * < 2^31; TV_ATTN_AUTO falls back to the CUDA-core kernel otherwise.
  */
 int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                         int64_t num_blocks, int32_t block_size,
@@ -200,7 +204,7 @@ int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                         int32_t B, int32_t N, int32_t Hq, int32_t Hkv, int32_t head_dim,
                         int32_t dtype, float scale, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, int32_t num_ctas,
-                        int32_t flags, void* stream);
+                        int32_t flags, int32_t* status, void* stream);
 
 /*
  * tv_tree_accept_greedy -- device, asynchronous.

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libtreeverify.so")
 
 TV_F32, TV_BF16 = 0, 1
 TV_ATTN_AUTO, TV_ATTN_SIMT, TV_ATTN_TCGEN05 = 0, 1, 2
-TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION = 1, 2, 4, 8
+TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 STATUS_NAMES = {0: "TV_OK", -1: "TV_ERR_INVALID_ARG", -2: "TV_ERR_MISSING_PARENT", -3: "TV_ERR_TOO_MANY_NODES",
                 -4: "TV_ERR_UNSUPPORTED", -5: "TV_ERR_WORKSPACE", -6: "TV_ERR_CUDA"}
 
@@ -36,7 +36,7 @@ SIGNATURES = {
     "tv_rope_apply": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "tv_tree_attn_workspace_size": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "tv_tree_attn_verify": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32,
-                                           _I32, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _I32, _I32, _P]),
+                                           _I32, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _I32, _I32, _P, _P]),
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
                                              _P, _P]),
@@ -173,7 +173,7 @@ def alloc_workspace(nbytes, device="cuda"):
 
 
 def tv_tree_attn_verify(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, mask, *, scale=None,
-                        out=None, lse=None, workspace=None, num_ctas=0, flags=0, stream=None):
+                        out=None, lse=None, workspace=None, num_ctas=0, flags=0, status=None, stream=None):
     """Tree attention; returns out [B, N, Hq, D].  mask is int64 [B, N] (uint64 rows)
     or [N] (shared)."""
     dts = (torch.float32, torch.bfloat16)
@@ -197,7 +197,8 @@ def tv_tree_attn_verify(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tr
            lib().tv_tree_attn_verify(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, block_size, _ptr(block_table),
                                      block_table.shape[1], _ptr(seq_lens), _ptr(k_tree), _ptr(v_tree), _ptr(mask),
                                      mstride, B, N, Hq, Hkv, D, _code(q.dtype), scale, _ptr(out), _ptr(lse),
-                                     _ptr(workspace), workspace.numel(), num_ctas, flags, _stream(stream)))
+                                     _ptr(workspace), workspace.numel(), num_ctas, flags, _ptr(status),
+                                     _stream(stream)))
     return out
 
 

@@ -352,10 +352,11 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
   int st = current_device_info(&dev);
   if (st) return st;
   const int G = Hq / Hkv, R = G * N;
-  const bool tc_ok = tc_supported(dev, dtype, D, R, block_size);
+  const bool tc_ok = tc_supported(dev, dtype, D, R, G, block_size);
   if (sel == TV_ATTN_TCGEN05 && !tc_ok)
-    return fail(TV_ERR_UNSUPPORTED, "tcgen05 tree attention needs sm_10x, bf16, head_dim 128, "
-                "(Hq/Hkv)*N <= %d and block_size %% 16 == 0", kTcMaxRows);
+    return fail(TV_ERR_UNSUPPORTED, "tcgen05 tree attention needs sm_10x, bf16, head_dim 128, Hq/Hkv dividing 128, "
+                "(Hq/Hkv)*N <= %d and a block_size that is a multiple of 16 dividing or divisible by %d",
+                kTcMaxRows, kTcBlk);
   cfg->tc = (sel == TV_ATTN_TCGEN05) || (sel == TV_ATTN_AUTO && tc_ok);
   int per_sm = 1;
   if (cfg->tc) {
@@ -417,7 +418,7 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
                                    const uint64_t* mask, int64_t mask_bstride, int32_t B, int32_t N, int32_t Hq,
                                    int32_t Hkv, int32_t head_dim, int32_t dtype, float scale, void* out, float* lse,
                                    void* workspace, size_t workspace_bytes, int32_t num_ctas, int32_t flags,
-                                   void* stream) {
+                                   int32_t* status, void* stream) {
   using namespace tv;
   clear_error();
   AttnConfig cfg;
@@ -428,6 +429,8 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
     return fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify: null pointer");
   if (num_blocks < 1 || max_blocks < 1 || mask_bstride < 0)
     return fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify: bad num_blocks/max_blocks/mask stride");
+  if (cfg.tc && num_blocks * Hkv * block_size >= (int64_t(1) << 31))
+    return fail(TV_ERR_UNSUPPORTED, "tv_tree_attn_verify: KV cache rows exceed the tensor-map range");
   if (!workspace || workspace_bytes < (size_t)cfg.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(TV_ERR_WORKSPACE, "tv_tree_attn_verify: workspace needs %lld bytes, 256-byte aligned",
                 (long long)cfg.bytes);
@@ -444,7 +447,7 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = (cudaStream_t)stream;
   if ((st = launch_plan(p, s))) return st;
-  st = cfg.tc ? launch_attn_tc(p, s) : simt_dispatch(p, dtype, s, nullptr);
+  st = cfg.tc ? launch_attn_tc(p, status, s) : simt_dispatch(p, dtype, s, nullptr);
   if (st) return st;
   return launch_combine(p, dtype, s);
 }

@@ -1,8 +1,677 @@
-// Placeholder: the tcgen05 kernel is not built yet.
+// Tree attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Same computation as the CUDA-core kernel in attn.cu ("Tree Verification",
+// "Tree Attention"; "Build the tree attention mask that verifies a draft tree
+// in one pass", "The mask."): every (node, query head) row of a GQA group
+// attends to the whole cached prefix with no mask and then to the tree nodes
+// in its ancestor row.  The pages only say that a FlashAttention-style kernel
+// may take the tree part as a parent array expanded per tile; the design here
+// is built for sm_103a:
+//
+//  * rows: the G query heads x N nodes of one KV head are packed into 128-row
+//    MMA tiles (row = node * G + g), so every K/V byte fetched from HBM feeds
+//    up to 256 query rows (two M tiles); one TMA box per M tile loads Q;
+//  * keys: the paged cache ([num_blocks, Hkv, block_size, 128] bf16) is read by
+//    TMA, one box per (block, 64-column half), into 128B-swizzled K-major tiles
+//    of 64 keys; the tree K/V ([B, N, Hkv, 128]) is one more 64-key tile whose
+//    rows beyond N are zero-filled by TMA;
+//  * S = Q K^T and O += P V run as tcgen05.mma kind::f16 (bf16 in, fp32 in
+//    TMEM): S_m uses 64 TMEM columns, O_m 128 columns per M tile;
+//  * softmax: one thread per row reads its S row from TMEM, applies no mask on
+//    prefix tiles except the ragged tail (key position < L) and the ancestor
+//    bit test on the tree tile, keeps a lazily rescaled running max (O is
+//    rescaled in TMEM only when the max grows by more than 2^8), writes P as
+//    bf16 into a swizzled shared-memory tile, and finally normalises O;
+//  * roles: warp 0 issues TMA, warp 1 (one lane) issues MMAs and owns TMEM,
+//    one warpgroup per M tile runs the softmax and the epilogue; stages are
+//    handed over with mbarriers (TMA transaction counts and tcgen05.commit);
+//  * work split: the persistent grid walks the balanced tile plan of
+//    attn_common.cuh; split units write float32 partials for the combine.
+//
+// Every mbarrier wait is bounded (2 s); on timeout the CTA raises
+// TV_DEV_TIMEOUT in the status word, drains its own TMA loads, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
 #include "attn_tc.h"
 
 namespace tv {
-bool tc_supported(const DeviceInfo&, int, int, int, int) { return false; }
+
+namespace {
+
+constexpr int kD = 128;                          // head dim of this kernel
+constexpr int kBlk = kTcBlk;                     // keys per tile (64)
+constexpr int kQTileBytes = 2 * 128 * 128;       // 128 rows x 2 halves x 128 B
+constexpr int kPTileBytes = 128 * 128;           // 128 rows x 64 bf16
+constexpr int kKVHalfBytes = kBlk * 128;         // 64 rows x 128 B
+constexpr int kKVTileBytes = 2 * kKVHalfBytes;   // one K (or V) tile
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+
+template <int M>
+struct Cfg {
+  static constexpr int kStages = (M == 1) ? 5 : 4;
+  static constexpr int kThreads = (M == 1) ? 256 : 384;
+  static constexpr uint32_t kTmemCols = (M == 1) ? 256 : 512;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + M * kQTileBytes;
+  static constexpr int kOffK = kOffP + M * kPTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
+  static constexpr int kBytes = kOffV + kStages * kKVTileBytes;
+  static constexpr int kSmem = kBytes + 1024;    // slack for 1024-byte alignment
+  static constexpr uint32_t kColS = 0;           // S_m at m * 64
+  static constexpr uint32_t kColO = 128;         // O_m at 128 + m * 128
+};
+
+struct Bars {
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t q_full;
+  uint64_t q_empty;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity (one thread); false on timeout,
+// or on another role's abort when honor_abort is set.
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, Bars* bars, int32_t* status, bool honor_abort = true) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (honor_abort && *(volatile int*)&bars->abort) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *(volatile int*)&bars->abort = 1;
+        if (status) atomicOr(status, TV_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// The same wait for a whole warp: every lane polls and all lanes leave
+// together with the same answer (warp-collective tcgen05 ops follow).
+__device__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, Bars* bars, int32_t* status) {
+  bool done = mbar_test(bar, parity);
+  if (__all_sync(0xffffffffu, done)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (!done) done = mbar_test(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if ((it & 255u) == 0) {
+      bool stop = *(volatile int*)&bars->abort != 0 || globaltimer() - t0 > kTimeoutNs;
+      if (__any_sync(0xffffffffu, stop)) {
+        if ((threadIdx.x & 31) == 0 && !*(volatile int*)&bars->abort) {
+          *(volatile int*)&bars->abort = 1;
+          if (status) atomicOr(status, TV_DEV_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: 128B swizzle, 1024-byte aligned atoms.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for sm_10x
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 x bf16 -> f32, A K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+#define TV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define TV_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : TV_R8(0), TV_R8(8), TV_R8(16), TV_R8(24)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      TV_W8(0), TV_W8(8), TV_W8(16), TV_W8(24)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------- work walk
+
+struct Segment {
+  int u, a, e, n;  // unit, local tiles [a, e) of its n tiles
+  int b, kvh, L;
+};
+
+struct Walk {
+  int64_t t0, t1;
+  int u;
+  __device__ Walk(const AttnParams& p) {
+    const int64_t T = p.tile_start[p.U];
+    t0 = cta_start(blockIdx.x, T, p.P);
+    t1 = cta_start(blockIdx.x + 1, T, p.P);
+    u = (t0 < t1) ? find_unit(p.tile_start, p.U, t0) : p.U;
+  }
+  __device__ bool next(const AttnParams& p, Segment& s) {
+    if (u >= p.U || p.tile_start[u] >= t1) return false;
+    const int64_t us = p.tile_start[u], ue = p.tile_start[u + 1];
+    s.u = u;
+    s.a = (int)(max(t0, us) - us);
+    s.e = (int)(min(t1, ue) - us);
+    s.n = (int)(ue - us);
+    int rg;
+    unit_coords(p, u, s.b, s.kvh, rg);
+    s.L = clamp_len(p, s.b);
+    ++u;
+    return true;
+  }
+};
+
+struct TcMaps {
+  CUtensorMap q, kc, vc, kt, vt;
+};
+
+// ---------------------------------------------------------------- the kernel
+
+template <int M>
+__global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
+  using C = Cfg<M>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Bars bars;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sQ = base + C::kOffQ, sP = base + C::kOffP, sK = base + C::kOffK, sV = base + C::kOffV;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  {
+    Walk probe(p);
+    if (probe.t0 >= probe.t1) return;  // empty slice: uniform exit before any setup
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    for (int m = 0; m < M; ++m) {
+      mbar_init(&bars.s_full[m], 1);
+      mbar_init(&bars.p_full[m], 128);
+      mbar_init(&bars.o_done[m], 1);
+    }
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
+    bars.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    const int bs = p.block_size;
+    const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
+    const int nsub = kBlk / br;
+    const int npt = 128 / p.G;            // nodes per M tile
+    const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
+    uint32_t g = 0;
+    int seg_i = 0;
+    bool ok = true;
+    Walk walk(p);
+    Segment s;
+    while (ok && walk.next(p, s)) {
+      if (seg_i > 0) ok = mbar_wait_warp(&bars.q_empty, (seg_i - 1) & 1, &bars, status);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_expect_tx(&bars.q_full, M * kQTileBytes);
+        for (int m = 0; m < M; ++m)
+          for (int h = 0; h < 2; ++h)
+            tma_4d(sQ + m * kQTileBytes + h * (kQTileBytes / 2), &maps.q, h * 64, s.kvh * p.G, m * npt, s.b,
+                   &bars.q_full);
+      }
+      for (int t = s.a; t < s.e && ok; ++t, ++g) {
+        const int stage = g % C::kStages;
+        const uint32_t use = g / C::kStages;
+        if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
+        if (!ok) break;
+        const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
+        if (lane == 0) mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes);
+        __syncwarp();
+        if (t == s.n - 1) {
+          if (lane == 0)
+            for (int h = 0; h < 2; ++h) {
+              tma_4d(dk + h * kKVHalfBytes, &maps.kt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
+              tma_4d(dv + h * kKVHalfBytes, &maps.vt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
+            }
+        } else if (lane < nsub) {
+          int pos = t * kBlk + lane * br;
+          if (pos >= s.L) pos = (s.L - 1) / br * br;  // ragged tail: any finite rows, weighted by zero
+          const int64_t blk = p.block_table[(int64_t)s.b * p.max_blocks + pos / bs];
+          int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
+          if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
+          for (int h = 0; h < 2; ++h) {
+            tma_2d(dk + h * kKVHalfBytes + lane * br * 128, &maps.kc, h * 64, (int)y, &bars.kv_full[stage]);
+            tma_2d(dv + h * kKVHalfBytes + lane * br * 128, &maps.vc, h * 64, (int)y, &bars.kv_full[stage]);
+          }
+        }
+        __syncwarp();
+      }
+      ++seg_i;
+    }
+    // drain: every load this warp issued has landed before the CTA exits
+    if (lane == 0) {
+      const uint32_t first = g > (uint32_t)C::kStages ? g - C::kStages : 0;
+      for (uint32_t i = first; i < g; ++i)
+        mbar_wait(&bars.kv_full[i % C::kStages], (i / C::kStages) & 1, &bars, nullptr, false);
+      if (seg_i > 0) mbar_wait(&bars.q_full, (seg_i - 1) & 1, &bars, nullptr, false);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
+      constexpr uint32_t idO = idesc_bf16(128, kD, true);
+      uint32_t g = 0;
+      int seg_i = 0;
+      bool ok = true;
+      Walk walk(p);
+      Segment s;
+      auto issue_s = [&](int m, int stage) {
+        const uint32_t d = tmem + C::kColS + m * kBlk;
+        const uint32_t qa = sQ + m * kQTileBytes, kb = sK + stage * kKVTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off_a = (kk / 4) * (kQTileBytes / 2) + (kk % 4) * 32;
+          const uint32_t off_b = (kk / 4) * kKVHalfBytes + (kk % 4) * 32;
+          mma_bf16(d, sdesc(qa + off_a, 0, 1024), sdesc(kb + off_b, 0, 1024), idS, kk > 0);
+        }
+        mma_commit(&bars.s_full[m]);
+      };
+      auto issue_pv = [&](int m, int stage, bool accumulate) {
+        const uint32_t d = tmem + C::kColO + m * kD;
+        const uint32_t pa = sP + m * kPTileBytes, vb = sV + stage * kKVTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_bf16(d, sdesc(pa + kk * 32, 0, 1024), sdesc(vb + kk * 2048, kKVHalfBytes, 1024), idO,
+                   (accumulate || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.o_done[m]);
+      };
+      while (ok && walk.next(p, s)) {
+        ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        const int n_seg = s.e - s.a;
+        for (int k = 0; k < n_seg && ok; ++k, ++g) {
+          const int stage = g % C::kStages;
+          ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          for (int m = 0; m < M && ok; ++m) {
+            if (k > 0) {
+              ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
+              if (!ok) break;
+              fence_after();
+              issue_pv(m, (g - 1) % C::kStages, k > 1);
+            }
+            issue_s(m, stage);
+          }
+          if (k > 0) mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
+        }
+        if (!ok) break;
+        for (int m = 0; m < M && ok; ++m) {
+          ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          issue_pv(m, (g - 1) % C::kStages, n_seg > 1);
+        }
+        if (!ok) break;
+        mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
+        mma_commit(&bars.q_empty);
+        ++seg_i;
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 4 + 4 * M) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int m = (warp - 4) / 4;
+    const int quarter = warp % 4;
+    const int rl = quarter * 32 + lane;  // row within the M tile = TMEM lane
+    const int row = m * 128 + rl;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = lane_addr + C::kColS + m * kBlk;
+    const uint32_t tO = lane_addr + C::kColO + m * kD;
+    uint8_t* prow = gbase + C::kOffP + m * kPTileBytes + (rl / 8) * 1024 + (rl % 8) * 128;
+    const bool valid_row = row < p.R;
+    const int node = valid_row ? row / p.G : 0;
+    const int head_in_group = row % p.G;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    uint32_t g = 0;
+    bool ok = true;
+    Walk walk(p);
+    Segment s;
+    while (ok && walk.next(p, s)) {
+      const uint64_t mrow = valid_row ? p.mask[(int64_t)s.b * p.mask_bstride + node] : 1ull;
+      float m_run = -INFINITY, l = 0.f;
+      const int n_seg = s.e - s.a;
+      for (int k = 0; k < n_seg; ++k, ++g) {
+        const int t = s.a + k;
+        ok = mbar_wait_warp(&bars.s_full[m], g & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        float sv[kBlk];
+        {
+          uint32_t r[32];
+          tmem_ld32(tS, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(r[c]);
+          tmem_ld32(tS + 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
+        }
+        float mx = -INFINITY;
+        if (t == s.n - 1) {
+#pragma unroll
+          for (int c = 0; c < kBlk; ++c) {
+            const bool keep = c < p.N && ((mrow >> c) & 1ull);
+            sv[c] = keep ? sv[c] * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, sv[c]);
+          }
+        } else {
+          const int lim = s.L - t * kBlk;  // keys [0, lim) of this tile are in the prefix
+#pragma unroll
+          for (int c = 0; c < kBlk; ++c) {
+            sv[c] = c < lim ? sv[c] * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, sv[c]);
+          }
+        }
+        const float m_new = fmaxf(m_run, mx);
+        const bool grow = m_new > m_run + kRescaleThreshold;
+        if (k > 0) {
+          ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          if (__any_sync(0xffffffffu, grow)) {
+            const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 32) {
+              uint32_t r[32];
+              tmem_ld32(tO + c, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+              tmem_st32(tO + c, r);
+            }
+            tmem_st_wait();
+          }
+        }
+        if (grow) {
+          l *= exp2f(m_run - m_new);
+          m_run = m_new;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float sum = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kBlk / 8; ++ch) {
+          float e[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            e[j] = exp2f(sv[ch * 8 + j] - m_use);
+            sum += e[j];
+          }
+          uint4 v;
+          v.x = pack_bf16(e[0], e[1]);
+          v.y = pack_bf16(e[2], e[3]);
+          v.z = pack_bf16(e[4], e[5]);
+          v.w = pack_bf16(e[6], e[7]);
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (rl % 8)) * 16)) = v;
+        }
+        l += sum;
+        fence_proxy_async();
+        fence_before();
+        mbar_arrive(&bars.p_full[m]);
+      }
+      if (!ok) break;
+      // epilogue: O / l for this unit's rows
+      ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
+      if (!ok) break;
+      fence_after();
+      const bool complete = (s.a == 0 && s.e == s.n);
+      const int64_t us = p.tile_start[s.u];
+      const int slot = (walk.t0 < us) ? 1 : 0;
+      const float inv = 1.f / l;
+      const float lse2 = m_run + log2f(l);
+      const int64_t orow = ((int64_t)s.b * p.N + node) * p.Hq + s.kvh * p.G + head_in_group;
+      const int64_t srow = ((int64_t)blockIdx.x * 2 + slot) * p.RPG + row;
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tO + c, r);
+        tmem_ld_wait();
+        if (!valid_row) continue;
+        if (complete) {
+          uint4* dst = reinterpret_cast<uint4*>(out + orow * kD + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(r[8 * j + 0]) * inv, __uint_as_float(r[8 * j + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv);
+            dst[j] = v;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
+                                 __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+        }
+      }
+      if (valid_row) {
+        if (complete) {
+          if (p.lse) p.lse[orow] = lse2 * 0.69314718055994530942f;
+        } else {
+          p.part_lse[srow] = lse2;
+        }
+      }
+      fence_before();
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiled* fn) {
+  static std::once_flag once;
+  static EncodeTiled cached = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = reinterpret_cast<EncodeTiled>(f);
+  });
+  if (!cached) return fail(TV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorName(err));
+  *fn = cached;
+  return TV_OK;
+}
+
+int encode(EncodeTiled fn, CUtensorMap* map, const void* ptr, int rank, const cuuint64_t* dims,
+           const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+  return TV_OK;
+}
+
+template <int M>
+int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
+  using C = Cfg<M>;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_kernel)");
+  attn_tc_kernel<M><<<p.P, C::kThreads, C::kSmem, stream>>>(p, maps, status);
+  TV_LAUNCH_CHECK("attn_tc_kernel");
+  return TV_OK;
+}
+
+}  // namespace
+
+bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size) {
+  if (dev.cc_major != 10 || dtype != TV_BF16 || head_dim != kD) return false;
+  if (rows > kTcMaxRows || G < 1 || 128 % G) return false;
+  if (block_size % 16) return false;
+  if (!(kBlk % block_size == 0 || block_size % kBlk == 0)) return false;
+  return dev.max_smem_optin >= (size_t)Cfg<2>::kSmem + sizeof(Bars);
+}
+
 int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
-int launch_attn_tc(const AttnParams&, cudaStream_t) { return fail(TV_ERR_UNSUPPORTED, "tcgen05 kernel not built"); }
+
+int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
+  EncodeTiled fn;
+  int st = get_encoder(&fn);
+  if (st) return st;
+  TcMaps maps;
+  const cuuint64_t row_bytes = (cuuint64_t)kD * 2;
+  const int br = p.block_size < kBlk ? p.block_size : kBlk;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.num_blocks * p.Hkv * p.block_size};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, (cuuint32_t)br};
+    if ((st = encode(fn, &maps.kc, p.k_cache, 2, dims, strides, box, "k_cache"))) return st;
+    if ((st = encode(fn, &maps.vc, p.v_cache, 2, dims, strides, box, "v_cache"))) return st;
+  }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.Hkv, (cuuint64_t)p.N, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {row_bytes, row_bytes * p.Hkv, row_bytes * p.Hkv * p.N};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kBlk, 1};
+    if ((st = encode(fn, &maps.kt, p.k_tree, 4, dims, strides, box, "k_tree"))) return st;
+    if ((st = encode(fn, &maps.vt, p.v_tree, 4, dims, strides, box, "v_tree"))) return st;
+  }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.Hq, (cuuint64_t)p.N, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {row_bytes, row_bytes * p.Hq, row_bytes * p.Hq * p.N};
+    cuuint32_t box[4] = {64, (cuuint32_t)p.G, (cuuint32_t)(128 / p.G), 1};
+    if ((st = encode(fn, &maps.q, p.q, 4, dims, strides, box, "q"))) return st;
+  }
+  return p.RPG <= 128 ? launch_m<1>(p, maps, status, stream) : launch_m<2>(p, maps, status, stream);
+}
+
 }  // namespace tv

@@ -6,16 +6,18 @@
 
 namespace tv {
 
-constexpr int kTcBlk = 128;      // KV positions per tile (one MMA N / K extent)
+constexpr int kTcBlk = 64;       // keys per tile (MMA N of S, K of P V)
 constexpr int kTcMaxRows = 256;  // two 128-row M tiles per CTA
 
-// True when the tensor-core kernel can run this shape on this device.
-bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int block_size);
+// True when the tensor-core kernel can run this shape on this device:
+// bf16, head_dim 128, rows = G * N <= 256, G divides 128, block_size a
+// multiple of 16 that divides 64 or is a multiple of 64.
+bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size);
 
 // Rows per unit for `rows` = G * N query rows per KV head (128 or 256).
 int tc_rows_per_unit(int rows);
 
 // Launches the persistent tensor-core kernel (plan already enqueued).
-int launch_attn_tc(const AttnParams& p, cudaStream_t stream);
+int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream);
 
 }  // namespace tv

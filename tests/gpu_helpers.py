@@ -36,7 +36,7 @@ def gpu_pipeline(inp, paths, flags=0, num_ctas=0, rope_base=10000.0, want_lse=Fa
     capi.tv_rope_apply(q, kt, pos, table, status=status)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev) if want_lse else None
     out = capi.tv_tree_attn_verify(q, inp["k_cache"], inp["v_cache"], inp["block_table"], seq_lens, kt,
-                                   inp["v_tree"], mask, lse=lse, flags=flags, num_ctas=num_ctas)
+                                   inp["v_tree"], mask, lse=lse, flags=flags, num_ctas=num_ctas, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return out, lse
