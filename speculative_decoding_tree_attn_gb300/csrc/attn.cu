@@ -354,9 +354,9 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
   const int G = Hq / Hkv, R = G * N;
   const bool tc_ok = tc_supported(dev, dtype, D, R, G, block_size);
   if (sel == TV_ATTN_TCGEN05 && !tc_ok)
-    return fail(TV_ERR_UNSUPPORTED, "tcgen05 tree attention needs sm_10x, bf16, head_dim 128, Hq/Hkv dividing 128, "
-                "(Hq/Hkv)*N <= %d and a block_size that is a multiple of 16 dividing or divisible by %d",
-                kTcMaxRows, kTcBlk);
+    return fail(TV_ERR_UNSUPPORTED, "tcgen05 tree attention: %s (sm_%d%d, opt-in smem %zu B)",
+                tc_unsupported_reason(dev, dtype, D, R, G, block_size), dev.cc_major, dev.cc_minor,
+                dev.max_smem_optin);
   cfg->tc = (sel == TV_ATTN_TCGEN05) || (sel == TV_ATTN_AUTO && tc_ok);
   int per_sm = 1;
   if (cfg->tc) {

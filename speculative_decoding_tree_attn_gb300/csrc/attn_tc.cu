@@ -634,12 +634,20 @@ int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStrea
 
 }  // namespace
 
+const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size) {
+  if (dev.cc_major != 10) return "device is not sm_10x";
+  if (dtype != TV_BF16) return "dtype is not bf16";
+  if (head_dim != kD) return "head_dim is not 128";
+  if (rows > kTcMaxRows) return "(Hq/Hkv)*N exceeds 256";
+  if (G < 1 || 128 % G) return "Hq/Hkv does not divide 128";
+  if (block_size % 16 || !(kBlk % block_size == 0 || block_size % kBlk == 0))
+    return "block_size is not a multiple of 16 that divides or is divisible by 64";
+  if (dev.max_smem_optin < (size_t)Cfg<2>::kSmem + sizeof(Bars)) return "not enough opt-in shared memory";
+  return nullptr;
+}
+
 bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size) {
-  if (dev.cc_major != 10 || dtype != TV_BF16 || head_dim != kD) return false;
-  if (rows > kTcMaxRows || G < 1 || 128 % G) return false;
-  if (block_size % 16) return false;
-  if (!(kBlk % block_size == 0 || block_size % kBlk == 0)) return false;
-  return dev.max_smem_optin >= (size_t)Cfg<2>::kSmem + sizeof(Bars);
+  return tc_unsupported_reason(dev, dtype, head_dim, rows, G, block_size) == nullptr;
 }
 
 int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }

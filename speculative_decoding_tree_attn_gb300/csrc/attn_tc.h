@@ -14,6 +14,9 @@ constexpr int kTcMaxRows = 256;  // two 128-row M tiles per CTA
 // multiple of 16 that divides 64 or is a multiple of 64.
 bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size);
 
+// Why the shape is rejected (nullptr when it is supported).
+const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size);
+
 // Rows per unit for `rows` = G * N query rows per KV head (128 or 256).
 int tc_rows_per_unit(int rows);
 
