@@ -192,7 +192,7 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  *            the tensor-core kernel gave up (the output is then incomplete).
  * Supported: N <= 64, D in {64, 128, 256}, dtype TV_F32 or TV_BF16,
  * Hq % Hkv == 0.  The tensor-core kernel needs an sm_10x device, bf16,
- * D = 128, G = Hq/Hkv dividing 128, G * N <= 256, block_size a multiple of 16
+ * D = 128, G = Hq/Hkv dividing 128, G * N <= 512, block_size a multiple of 16
  * that divides 64 or is a multiple of 64, and num_blocks * Hkv * block_size
  * < 2^31; TV_ATTN_AUTO falls back to the CUDA-core kernel otherwise.
  */

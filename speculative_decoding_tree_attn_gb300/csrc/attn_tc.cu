@@ -72,6 +72,7 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
+  uint64_t s_free[2];
   uint64_t q_full;
   uint64_t q_empty;
   uint32_t tmem_base;
@@ -226,6 +227,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2^x on the special-function unit (approximate, flushes denormals); inputs
+// here are <= 8 and -inf, giving values in [0, 256].
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -236,7 +245,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 struct Segment {
   int u, a, e, n;  // unit, local tiles [a, e) of its n tiles
-  int b, kvh, L;
+  int b, kvh, rg, L;
 };
 
 struct Walk {
@@ -255,8 +264,7 @@ struct Walk {
     s.a = (int)(max(t0, us) - us);
     s.e = (int)(min(t1, ue) - us);
     s.n = (int)(ue - us);
-    int rg;
-    unit_coords(p, u, s.b, s.kvh, rg);
+    unit_coords(p, u, s.b, s.kvh, s.rg);
     s.L = clamp_len(p, s.b);
     ++u;
     return true;
@@ -294,6 +302,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
       mbar_init(&bars.s_full[m], 1);
       mbar_init(&bars.p_full[m], 128);
       mbar_init(&bars.o_done[m], 1);
+      mbar_init(&bars.s_free[m], 128);
     }
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.q_empty, 1);
@@ -330,8 +339,8 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         mbar_expect_tx(&bars.q_full, M * kQTileBytes);
         for (int m = 0; m < M; ++m)
           for (int h = 0; h < 2; ++h)
-            tma_4d(sQ + m * kQTileBytes + h * (kQTileBytes / 2), &maps.q, h * 64, s.kvh * p.G, m * npt, s.b,
-                   &bars.q_full);
+            tma_4d(sQ + m * kQTileBytes + h * (kQTileBytes / 2), &maps.q, h * 64, s.kvh * p.G,
+                   (s.rg * M + m) * npt, s.b, &bars.q_full);
       }
       for (int t = s.a; t < s.e && ok; ++t, ++g) {
         const int stage = g % C::kStages;
@@ -399,39 +408,45 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
                    (accumulate || kk > 0) ? 1u : 0u);
         mma_commit(&bars.o_done[m]);
       };
+      // Per tile g: S_m(g) as soon as K(g) has landed and the softmax has read
+      // S_m(g-1) out of TMEM; then O_m += P_m(g-1) V(g-1) once P_m(g-1) is in
+      // shared memory.  S(g) thus overlaps the softmax of tile g-1.
+      bool have_prev = false, prev_acc = false;
+      int prev_stage = 0;
+      auto finish_prev = [&]() -> bool {
+        for (int m = 0; m < M; ++m) {
+          if (!mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status)) return false;
+          fence_after();
+          issue_pv(m, prev_stage, prev_acc);
+        }
+        mma_commit(&bars.kv_empty[prev_stage]);
+        return true;
+      };
       while (ok && walk.next(p, s)) {
         ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
         if (!ok) break;
         fence_after();
         const int n_seg = s.e - s.a;
-        for (int k = 0; k < n_seg && ok; ++k, ++g) {
+        for (int k = 0; k < n_seg && ok; ++k) {
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
-          if (!ok) break;
-          fence_after();
           for (int m = 0; m < M && ok; ++m) {
-            if (k > 0) {
-              ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
-              if (!ok) break;
-              fence_after();
-              issue_pv(m, (g - 1) % C::kStages, k > 1);
-            }
+            if (g > 0) ok = mbar_wait(&bars.s_free[m], (g - 1) & 1, &bars, status);
+            if (!ok) break;
+            fence_after();
             issue_s(m, stage);
           }
-          if (k > 0) mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
-        }
-        if (!ok) break;
-        for (int m = 0; m < M && ok; ++m) {
-          ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
           if (!ok) break;
-          fence_after();
-          issue_pv(m, (g - 1) % C::kStages, n_seg > 1);
+          if (k == n_seg - 1) mma_commit(&bars.q_empty);  // every S of this segment is issued
+          if (have_prev && !(ok = finish_prev())) break;
+          have_prev = true;
+          prev_stage = stage;
+          prev_acc = k > 0;
+          ++g;
         }
-        if (!ok) break;
-        mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
-        mma_commit(&bars.q_empty);
         ++seg_i;
       }
+      if (ok && have_prev) finish_prev();
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 4 + 4 * M) {
@@ -439,20 +454,21 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
     const int m = (warp - 4) / 4;
     const int quarter = warp % 4;
     const int rl = quarter * 32 + lane;  // row within the M tile = TMEM lane
-    const int row = m * 128 + rl;
+    const int row = m * 128 + rl;         // row within the unit
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = lane_addr + C::kColS + m * kBlk;
     const uint32_t tO = lane_addr + C::kColO + m * kD;
     uint8_t* prow = gbase + C::kOffP + m * kPTileBytes + (rl / 8) * 1024 + (rl % 8) * 128;
-    const bool valid_row = row < p.R;
-    const int node = valid_row ? row / p.G : 0;
-    const int head_in_group = row % p.G;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     uint32_t g = 0;
     bool ok = true;
     Walk walk(p);
     Segment s;
     while (ok && walk.next(p, s)) {
+      const int unit_row = s.rg * p.RPG + row;  // row within the (b, kv head) group
+      const bool valid_row = unit_row < p.R;
+      const int node = valid_row ? unit_row / p.G : 0;
+      const int head_in_group = unit_row % p.G;
       const uint64_t mrow = valid_row ? p.mask[(int64_t)s.b * p.mask_bstride + node] : 1ull;
       float m_run = -INFINITY, l = 0.f;
       const int n_seg = s.e - s.a;
@@ -473,22 +489,24 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
         }
-        float mx = -INFINITY;
+        fence_before();
+        mbar_arrive(&bars.s_free[m]);  // S_m may be overwritten by the next tile's MMA
         if (t == s.n - 1) {
 #pragma unroll
-          for (int c = 0; c < kBlk; ++c) {
-            const bool keep = c < p.N && ((mrow >> c) & 1ull);
-            sv[c] = keep ? sv[c] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, sv[c]);
-          }
+          for (int c = 0; c < kBlk; ++c)
+            if (!(c < p.N && ((mrow >> c) & 1ull))) sv[c] = -INFINITY;
         } else {
           const int lim = s.L - t * kBlk;  // keys [0, lim) of this tile are in the prefix
+          if (lim < kBlk) {
 #pragma unroll
-          for (int c = 0; c < kBlk; ++c) {
-            sv[c] = c < lim ? sv[c] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, sv[c]);
+            for (int c = 0; c < kBlk; ++c)
+              if (c >= lim) sv[c] = -INFINITY;
           }
         }
+        float mx = sv[0];
+#pragma unroll
+        for (int c = 1; c < kBlk; ++c) mx = fmaxf(mx, sv[c]);
+        mx *= p.scale_log2;  // scale > 0: max of scaled = scaled max
         const float m_new = fmaxf(m_run, mx);
         const bool grow = m_new > m_run + kRescaleThreshold;
         if (k > 0) {
@@ -514,15 +532,15 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float sum = 0.f;
+        const float sc = p.scale_log2;
+        float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
         for (int ch = 0; ch < kBlk / 8; ++ch) {
           float e[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            e[j] = exp2f(sv[ch * 8 + j] - m_use);
-            sum += e[j];
-          }
+          for (int j = 0; j < 8; ++j) e[j] = fast_exp2(fmaf(sv[ch * 8 + j], sc, -m_use));
+          sum0 += (e[0] + e[1]) + (e[2] + e[3]);
+          sum1 += (e[4] + e[5]) + (e[6] + e[7]);
           uint4 v;
           v.x = pack_bf16(e[0], e[1]);
           v.y = pack_bf16(e[2], e[3]);
@@ -530,7 +548,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
           v.w = pack_bf16(e[6], e[7]);
           *reinterpret_cast<uint4*>(prow + ((ch ^ (rl % 8)) * 16)) = v;
         }
-        l += sum;
+        l += sum0 + sum1;
         fence_proxy_async();
         fence_before();
         mbar_arrive(&bars.p_full[m]);
@@ -638,7 +656,7 @@ const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim
   if (dev.cc_major != 10) return "device is not sm_10x";
   if (dtype != TV_BF16) return "dtype is not bf16";
   if (head_dim != kD) return "head_dim is not 128";
-  if (rows > kTcMaxRows) return "(Hq/Hkv)*N exceeds 256";
+  if (rows > 2 * kTcMaxRows) return "(Hq/Hkv)*N exceeds 512";
   if (G < 1 || 128 % G) return "Hq/Hkv does not divide 128";
   if (block_size % 16 || !(kBlk % block_size == 0 || block_size % kBlk == 0))
     return "block_size is not a multiple of 16 that divides or is divisible by 64";

@@ -7,10 +7,10 @@
 namespace tv {
 
 constexpr int kTcBlk = 64;       // keys per tile (MMA N of S, K of P V)
-constexpr int kTcMaxRows = 256;  // two 128-row M tiles per CTA
+constexpr int kTcMaxRows = 256;  // two 128-row M tiles per CTA (more rows: row groups)
 
 // True when the tensor-core kernel can run this shape on this device:
-// bf16, head_dim 128, rows = G * N <= 256, G divides 128, block_size a
+// bf16, head_dim 128, rows = G * N <= 512, G divides 128, block_size a
 // multiple of 16 that divides 64 or is a multiple of 64.
 bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size);
 

@@ -96,6 +96,20 @@ def test_node_count_sweep(N):
             _check_all(inp, paths, tol, flags)
 
 
+@pytest.mark.parametrize("G,N", [(8, 33), (16, 20), (4, 64), (2, 64)])
+def test_row_groups_and_gqa_widths(G, N):
+    """G * N above 256 (two row groups) and several GQA widths, both kernels."""
+    rng = np.random.default_rng(120 + G + N)
+    paths = W.random_rank_paths(N, 8, rng)
+    w = _workload(2, 2 * G, 2, 128, "bf16", 64, N, 121 + G)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[130, 64 * 5 + 7])
+    for flags in KERNELS:
+        if flags == capi.TV_ATTN_TCGEN05 and not tc_available(2 * G, 2, N, bs=64):
+            continue
+        for num_ctas in (0, 5):
+            _check_all(inp, paths, BF16_TOL, flags, num_ctas)
+
+
 @pytest.mark.parametrize("D", [64, 256])
 def test_other_head_dims_simt(D):
     rng = np.random.default_rng(95 + D)
