@@ -342,24 +342,41 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
             tma_4d(sQ + m * kQTileBytes + h * (kQTileBytes / 2), &maps.q, h * 64, s.kvh * p.G,
                    (s.rg * M + m) * npt, s.b, &bars.q_full);
       }
+      // Block-table entries of this unit are read in 32-entry windows, one
+      // coalesced load per window, the next window requested a window ahead,
+      // so no TMA issue waits on a dependent global load.
+      const int nb = (s.L + bs - 1) / bs;  // valid table entries of request b
+      const int32_t* trow = p.block_table + (int64_t)s.b * p.max_blocks;
+      int w0 = (s.a * kBlk) / bs;          // first entry held in `cur`
+      int32_t cur = (w0 + lane < nb) ? __ldg(trow + w0 + lane) : 0;
+      int32_t nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
       for (int t = s.a; t < s.e && ok; ++t, ++g) {
         const int stage = g % C::kStages;
         const uint32_t use = g / C::kStages;
+        const bool tree_tile = (t == s.n - 1);
+        if (!tree_tile && (t * kBlk) / bs >= w0 + 32) {
+          w0 += 32;
+          cur = nxt;
+          nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
+        }
+        int pos = t * kBlk + (lane < nsub ? lane : 0) * br;
+        if (pos >= s.L) pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
+        const int rel = pos / bs - w0;
+        const int32_t from_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
+        const int32_t from_nxt = __shfl_sync(0xffffffffu, nxt, rel & 31);
+        const int64_t blk = rel < 32 ? from_cur : from_nxt;
         if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
         if (!ok) break;
         const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
         if (lane == 0) mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes);
         __syncwarp();
-        if (t == s.n - 1) {
+        if (tree_tile) {
           if (lane == 0)
             for (int h = 0; h < 2; ++h) {
               tma_4d(dk + h * kKVHalfBytes, &maps.kt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
               tma_4d(dv + h * kKVHalfBytes, &maps.vt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
             }
         } else if (lane < nsub) {
-          int pos = t * kBlk + lane * br;
-          if (pos >= s.L) pos = (s.L - 1) / br * br;  // ragged tail: any finite rows, weighted by zero
-          const int64_t blk = p.block_table[(int64_t)s.b * p.max_blocks + pos / bs];
           int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
           if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
           for (int h = 0; h < 2; ++h) {
@@ -503,9 +520,15 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
               if (c >= lim) sv[c] = -INFINITY;
           }
         }
-        float mx = sv[0];
+        float mx;
+        {
+          float t8[8];
 #pragma unroll
-        for (int c = 1; c < kBlk; ++c) mx = fmaxf(mx, sv[c]);
+          for (int j = 0; j < 8; ++j)
+            t8[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[8 + j]), fmaxf(sv[16 + j], sv[24 + j])),
+                          fmaxf(fmaxf(sv[32 + j], sv[40 + j]), fmaxf(sv[48 + j], sv[56 + j])));
+          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        }
         mx *= p.scale_log2;  // scale > 0: max of scaled = scaled max
         const float m_new = fmaxf(m_run, mx);
         const bool grow = m_new > m_run + kRescaleThreshold;
