@@ -38,6 +38,19 @@
 
 #include "attn_tc.h"
 
+#ifdef TV_TC_TRACE
+// Development aid: clock64 stamps of pipeline events of CTA 0, one slot per
+// (event, tile).  Not part of the product build.
+namespace tv { namespace trace {
+constexpr int kEvents = 16, kTiles = 512;
+__device__ unsigned long long g_trace[kEvents][kTiles];
+}}  // namespace tv::trace
+#define TV_TRACE(ev, tile) \
+  do { if (blockIdx.x == 0 && (tile) < tv::trace::kTiles) tv::trace::g_trace[ev][tile] = clock64(); } while (0)
+#else
+#define TV_TRACE(ev, tile) do { } while (0)
+#endif
+
 namespace tv {
 
 namespace {
@@ -368,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
         if (!ok) break;
         const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
-        if (lane == 0) mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes);
+        if (lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
         __syncwarp();
         if (tree_tile) {
           if (lane == 0)
@@ -435,6 +448,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
           if (!mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status)) return false;
           fence_after();
           issue_pv(m, prev_stage, prev_acc);
+          TV_TRACE(4 + m, g - 1);
         }
         mma_commit(&bars.kv_empty[prev_stage]);
         return true;
@@ -447,11 +461,13 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         for (int k = 0; k < n_seg && ok; ++k) {
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          TV_TRACE(1, g);
           for (int m = 0; m < M && ok; ++m) {
             if (g > 0) ok = mbar_wait(&bars.s_free[m], (g - 1) & 1, &bars, status);
             if (!ok) break;
             fence_after();
             issue_s(m, stage);
+            TV_TRACE(2 + m, g);
           }
           if (!ok) break;
           if (k == n_seg - 1) mma_commit(&bars.q_empty);  // every S of this segment is issued
@@ -492,6 +508,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
       for (int k = 0; k < n_seg; ++k, ++g) {
         const int t = s.a + k;
         ok = mbar_wait_warp(&bars.s_full[m], g & 1, &bars, status);
+        if (rl == 0) TV_TRACE(6 + 4 * m, g);
         if (!ok) break;
         fence_after();
         float sv[kBlk];
@@ -508,6 +525,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         }
         fence_before();
         mbar_arrive(&bars.s_free[m]);  // S_m may be overwritten by the next tile's MMA
+        if (rl == 0) TV_TRACE(7 + 4 * m, g);
         if (t == s.n - 1) {
 #pragma unroll
           for (int c = 0; c < kBlk; ++c)
@@ -535,6 +553,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         if (k > 0) {
           ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
           if (!ok) break;
+          if (rl == 0) TV_TRACE(8 + 4 * m, g);
           fence_after();
           if (__any_sync(0xffffffffu, grow)) {
             const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
@@ -575,6 +594,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         fence_proxy_async();
         fence_before();
         mbar_arrive(&bars.p_full[m]);
+        if (rl == 0) TV_TRACE(9 + 4 * m, g);
       }
       if (!ok) break;
       // epilogue: O / l for this unit's rows
@@ -692,6 +712,13 @@ bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int 
 }
 
 int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
+
+#ifdef TV_TC_TRACE
+extern "C" int tv_debug_trace(void* dst, size_t bytes) {
+  const size_t n = sizeof(trace::g_trace) < bytes ? sizeof(trace::g_trace) : bytes;
+  return cudaMemcpyFromSymbol(dst, trace::g_trace, n) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
   EncodeTiled fn;
