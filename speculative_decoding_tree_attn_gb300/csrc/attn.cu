@@ -393,6 +393,7 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
   if (cfg->tc) {
     cfg->RPG = tc_rows_per_unit(R);
     cfg->BLK = kTcBlk;
+    per_sm = tc_ctas_per_sm(R);
   } else {
     cfg->RPG = kSimtRows;
     cfg->BLK = kSimtBlk;

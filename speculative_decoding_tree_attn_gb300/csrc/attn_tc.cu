@@ -57,26 +57,29 @@ namespace {
 
 constexpr int kD = 128;                          // head dim of this kernel
 constexpr int kBlk = kTcBlk;                     // keys per tile (64)
-constexpr int kQTileBytes = 2 * 128 * 128;       // 128 rows x 2 halves x 128 B
-constexpr int kPTileBytes = 128 * 128;           // 128 rows x 64 bf16
 constexpr int kKVHalfBytes = kBlk * 128;         // 64 rows x 128 B
 constexpr int kKVTileBytes = 2 * kKVHalfBytes;   // one K (or V) tile
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
+// M query tiles of 128 rows per CTA.  TMEM columns (fp32 cells):
+//   S_m: 64 (one 64-key score tile; P_m, bf16 pairs, overwrites its first 32)
+//   Q_m: 64 (128 bf16 per row, the A operand of S = Q K^T)
+//   O_m: 128 (fp32 accumulator)
+// Shared memory holds only the K/V stage ring.
 template <int M>
 struct Cfg {
-  static constexpr int kStages = (M == 1) ? 5 : 4;
-  static constexpr int kThreads = (M == 1) ? 256 : 384;
+  static constexpr int kStages = (M == 1) ? 3 : 6;
+  static constexpr int kCtasPerSm = (M == 1) ? 2 : 1;
+  static constexpr int kThreads = 64 + M * 128;      // TMA warp, MMA warp, one warpgroup per M tile
   static constexpr uint32_t kTmemCols = (M == 1) ? 256 : 512;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + M * kQTileBytes;
-  static constexpr int kOffK = kOffP + M * kPTileBytes;
+  static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
   static constexpr int kBytes = kOffV + kStages * kKVTileBytes;
-  static constexpr int kSmem = kBytes + 1024;    // slack for 1024-byte alignment
-  static constexpr uint32_t kColS = 0;           // S_m at m * 64
-  static constexpr uint32_t kColO = 128;         // O_m at 128 + m * 128
+  static constexpr int kSmem = kBytes + 1024;        // slack for 1024-byte alignment
+  static constexpr uint32_t col_s(int m) { return m * 64; }
+  static constexpr uint32_t col_q(int m) { return M * 64 + m * 64; }
+  static constexpr uint32_t col_o(int m) { return 128 * M + m * 128; }
 };
 
 struct Bars {
@@ -85,9 +88,7 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
-  uint64_t s_free[2];
   uint64_t q_full;
-  uint64_t q_empty;
   uint32_t tmem_base;
   int abort;
 };
@@ -212,6 +213,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       : "memory");
 }
 
+// A operand in TMEM (row = lane, K packed two bf16 per column), B in smem.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -285,21 +296,20 @@ struct Walk {
 };
 
 struct TcMaps {
-  CUtensorMap q, kc, vc, kt, vt;
+  CUtensorMap kc, vc, kt, vt;
 };
 
 // ---------------------------------------------------------------- the kernel
 
 template <int M>
-__global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
     attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
   using C = Cfg<M>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t sQ = base + C::kOffQ, sP = base + C::kOffP, sK = base + C::kOffK, sV = base + C::kOffV;
-  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sK = base + C::kOffK, sV = base + C::kOffV;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   {
@@ -315,10 +325,8 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
       mbar_init(&bars.s_full[m], 1);
       mbar_init(&bars.p_full[m], 128);
       mbar_init(&bars.o_done[m], 1);
-      mbar_init(&bars.s_free[m], 128);
     }
-    mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, 1);
+    mbar_init(&bars.q_full, 128 * M);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -338,23 +346,12 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
     const int bs = p.block_size;
     const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
     const int nsub = kBlk / br;
-    const int npt = 128 / p.G;            // nodes per M tile
     const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
     uint32_t g = 0;
-    int seg_i = 0;
     bool ok = true;
     Walk walk(p);
     Segment s;
     while (ok && walk.next(p, s)) {
-      if (seg_i > 0) ok = mbar_wait_warp(&bars.q_empty, (seg_i - 1) & 1, &bars, status);
-      if (!ok) break;
-      if (lane == 0) {
-        mbar_expect_tx(&bars.q_full, M * kQTileBytes);
-        for (int m = 0; m < M; ++m)
-          for (int h = 0; h < 2; ++h)
-            tma_4d(sQ + m * kQTileBytes + h * (kQTileBytes / 2), &maps.q, h * 64, s.kvh * p.G,
-                   (s.rg * M + m) * npt, s.b, &bars.q_full);
-      }
       // Block-table entries of this unit are read in 32-entry windows, one
       // coalesced load per window, the next window requested a window ahead,
       // so no TMA issue waits on a dependent global load.
@@ -399,17 +396,19 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         }
         __syncwarp();
       }
-      ++seg_i;
     }
     // drain: every load this warp issued has landed before the CTA exits
     if (lane == 0) {
       const uint32_t first = g > (uint32_t)C::kStages ? g - C::kStages : 0;
       for (uint32_t i = first; i < g; ++i)
         mbar_wait(&bars.kv_full[i % C::kStages], (i / C::kStages) & 1, &bars, nullptr, false);
-      if (seg_i > 0) mbar_wait(&bars.q_full, (seg_i - 1) & 1, &bars, nullptr, false);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per tile g and M tile m: O_m += P_m(g-1) V(g-1), then S_m(g) = Q_m K(g)^T.
+    // The tensor pipe runs them in issue order, so S_m(g) overwrites the TMEM
+    // columns holding P_m(g-1) only after that P has been consumed, and the
+    // commit that signals S_m(g) also covers O_m's update by tile g-1.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
       constexpr uint32_t idO = idesc_bf16(128, kD, true);
@@ -418,80 +417,69 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
       bool ok = true;
       Walk walk(p);
       Segment s;
-      auto issue_s = [&](int m, int stage) {
-        const uint32_t d = tmem + C::kColS + m * kBlk;
-        const uint32_t qa = sQ + m * kQTileBytes, kb = sK + stage * kKVTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off_a = (kk / 4) * (kQTileBytes / 2) + (kk % 4) * 32;
-          const uint32_t off_b = (kk / 4) * kKVHalfBytes + (kk % 4) * 32;
-          mma_bf16(d, sdesc(qa + off_a, 0, 1024), sdesc(kb + off_b, 0, 1024), idS, kk > 0);
-        }
-        mma_commit(&bars.s_full[m]);
-      };
       auto issue_pv = [&](int m, int stage, bool accumulate) {
-        const uint32_t d = tmem + C::kColO + m * kD;
-        const uint32_t pa = sP + m * kPTileBytes, vb = sV + stage * kKVTileBytes;
+        const uint32_t d = tmem + C::col_o(m), a = tmem + C::col_s(m);
+        const uint32_t vb = sV + stage * kKVTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_bf16(d, sdesc(pa + kk * 32, 0, 1024), sdesc(vb + kk * 2048, kKVHalfBytes, 1024), idO,
-                   (accumulate || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(d, a + kk * 8, sdesc(vb + kk * 2048, kKVHalfBytes, 1024), idO, (accumulate || kk > 0) ? 1u : 0u);
         mma_commit(&bars.o_done[m]);
       };
-      // Per tile g: S_m(g) as soon as K(g) has landed and the softmax has read
-      // S_m(g-1) out of TMEM; then O_m += P_m(g-1) V(g-1) once P_m(g-1) is in
-      // shared memory.  S(g) thus overlaps the softmax of tile g-1.
-      bool have_prev = false, prev_acc = false;
-      int prev_stage = 0;
-      auto finish_prev = [&]() -> bool {
-        for (int m = 0; m < M; ++m) {
-          if (!mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status)) return false;
-          fence_after();
-          issue_pv(m, prev_stage, prev_acc);
-          TV_TRACE(4 + m, g - 1);
-        }
-        mma_commit(&bars.kv_empty[prev_stage]);
-        return true;
+      auto issue_s = [&](int m, int stage) {
+        const uint32_t d = tmem + C::col_s(m), a = tmem + C::col_q(m);
+        const uint32_t kb = sK + stage * kKVTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16_ts(d, a + kk * 8, sdesc(kb + (kk / 4) * kKVHalfBytes + (kk % 4) * 32, 0, 1024), idS, kk > 0);
+        mma_commit(&bars.s_full[m]);
       };
       while (ok && walk.next(p, s)) {
+        const int n_seg = s.e - s.a;
         ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
         if (!ok) break;
         fence_after();
-        const int n_seg = s.e - s.a;
-        for (int k = 0; k < n_seg && ok; ++k) {
+        for (int k = 0; k < n_seg && ok; ++k, ++g) {
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
           TV_TRACE(1, g);
           for (int m = 0; m < M && ok; ++m) {
-            if (g > 0) ok = mbar_wait(&bars.s_free[m], (g - 1) & 1, &bars, status);
-            if (!ok) break;
-            fence_after();
+            if (k > 0) {
+              ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
+              if (!ok) break;
+              fence_after();
+              issue_pv(m, (g - 1) % C::kStages, k > 1);
+              TV_TRACE(4 + m, g - 1);
+            }
             issue_s(m, stage);
             TV_TRACE(2 + m, g);
           }
-          if (!ok) break;
-          if (k == n_seg - 1) mma_commit(&bars.q_empty);  // every S of this segment is issued
-          if (have_prev && !(ok = finish_prev())) break;
-          have_prev = true;
-          prev_stage = stage;
-          prev_acc = k > 0;
-          ++g;
+          if (ok && k > 0) mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
         }
+        if (!ok) break;
+        for (int m = 0; m < M && ok; ++m) {
+          ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          issue_pv(m, (g - 1) % C::kStages, n_seg > 1);
+          TV_TRACE(4 + m, g - 1);
+        }
+        if (!ok) break;
+        mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
         ++seg_i;
       }
-      if (ok && have_prev) finish_prev();
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 4 + 4 * M) {
+  } else if (warp >= 2 && warp < 2 + 4 * M) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int m = (warp - 4) / 4;
-    const int quarter = warp % 4;
-    const int rl = quarter * 32 + lane;  // row within the M tile = TMEM lane
+    const int m = (warp - 2) / 4;
+    const int quarter = warp % 4;         // TMEM lanes 32*quarter .. +31
+    const int rl = quarter * 32 + lane;   // row within the M tile = TMEM lane
     const int row = m * 128 + rl;         // row within the unit
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tS = lane_addr + C::kColS + m * kBlk;
-    const uint32_t tO = lane_addr + C::kColO + m * kD;
-    uint8_t* prow = gbase + C::kOffP + m * kPTileBytes + (rl / 8) * 1024 + (rl % 8) * 128;
+    const uint32_t tS = lane_addr + C::col_s(m);
+    const uint32_t tQ = lane_addr + C::col_q(m);
+    const uint32_t tO = lane_addr + C::col_o(m);
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     uint32_t g = 0;
     bool ok = true;
@@ -502,15 +490,34 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
       const bool valid_row = unit_row < p.R;
       const int node = valid_row ? unit_row / p.G : 0;
       const int head_in_group = unit_row % p.G;
+      const int64_t orow = ((int64_t)s.b * p.N + node) * p.Hq + s.kvh * p.G + head_in_group;
       const uint64_t mrow = valid_row ? p.mask[(int64_t)s.b * p.mask_bstride + node] : 1ull;
+      // this row of Q into TMEM (the previous unit's MMAs are complete: its
+      // epilogue waited for the last O update)
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(q + orow * kD);
+#pragma unroll
+        for (int c = 0; c < kD / 64; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = valid_row ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
+            r[4 * j] = v.x; r[4 * j + 1] = v.y; r[4 * j + 2] = v.z; r[4 * j + 3] = v.w;
+          }
+          tmem_st32(tQ + c * 32, r);
+        }
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&bars.q_full);
+      }
       float m_run = -INFINITY, l = 0.f;
       const int n_seg = s.e - s.a;
       for (int k = 0; k < n_seg; ++k, ++g) {
         const int t = s.a + k;
         ok = mbar_wait_warp(&bars.s_full[m], g & 1, &bars, status);
-        if (rl == 0) TV_TRACE(6 + 4 * m, g);
         if (!ok) break;
         fence_after();
+        if (rl == 0) TV_TRACE(6 + 4 * m, g);
         float sv[kBlk];
         {
           uint32_t r[32];
@@ -523,8 +530,6 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
         }
-        fence_before();
-        mbar_arrive(&bars.s_free[m]);  // S_m may be overwritten by the next tile's MMA
         if (rl == 0) TV_TRACE(7 + 4 * m, g);
         if (t == s.n - 1) {
 #pragma unroll
@@ -550,23 +555,17 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         mx *= p.scale_log2;  // scale > 0: max of scaled = scaled max
         const float m_new = fmaxf(m_run, mx);
         const bool grow = m_new > m_run + kRescaleThreshold;
-        if (k > 0) {
-          ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
-          if (!ok) break;
-          if (rl == 0) TV_TRACE(8 + 4 * m, g);
-          fence_after();
-          if (__any_sync(0xffffffffu, grow)) {
-            const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
+        // O_m already holds tiles < g (the S_m(g) commit covered them)
+        if (k > 0 && __any_sync(0xffffffffu, grow)) {
+          const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
 #pragma unroll 1
-            for (int c = 0; c < kD; c += 32) {
-              uint32_t r[32];
-              tmem_ld32(tO + c, r);
-              tmem_ld_wait();
+          for (int c = 0; c < kD; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + c, r);
+            tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-              tmem_st32(tO + c, r);
-            }
-            tmem_st_wait();
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+            tmem_st32(tO + c, r);
           }
         }
         if (grow) {
@@ -576,22 +575,17 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         const float sc = p.scale_log2;
         float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int ch = 0; ch < kBlk / 8; ++ch) {
-          float e[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) e[j] = fast_exp2(fmaf(sv[ch * 8 + j], sc, -m_use));
-          sum0 += (e[0] + e[1]) + (e[2] + e[3]);
-          sum1 += (e[4] + e[5]) + (e[6] + e[7]);
-          uint4 v;
-          v.x = pack_bf16(e[0], e[1]);
-          v.y = pack_bf16(e[2], e[3]);
-          v.z = pack_bf16(e[4], e[5]);
-          v.w = pack_bf16(e[6], e[7]);
-          *reinterpret_cast<uint4*>(prow + ((ch ^ (rl % 8)) * 16)) = v;
+        for (int c = 0; c < kBlk / 2; ++c) {
+          const float e0 = fast_exp2(fmaf(sv[2 * c], sc, -m_use));
+          const float e1 = fast_exp2(fmaf(sv[2 * c + 1], sc, -m_use));
+          if (c & 1) sum1 += e0 + e1; else sum0 += e0 + e1;
+          pk[c] = pack_bf16(e0, e1);
         }
         l += sum0 + sum1;
-        fence_proxy_async();
+        tmem_st32(tS, pk);  // P_m(g) over the first 32 columns of S_m
+        tmem_st_wait();
         fence_before();
         mbar_arrive(&bars.p_full[m]);
         if (rl == 0) TV_TRACE(9 + 4 * m, g);
@@ -606,7 +600,6 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
       const int slot = (walk.t0 < us) ? 1 : 0;
       const float inv = 1.f / l;
       const float lse2 = m_run + log2f(l);
-      const int64_t orow = ((int64_t)s.b * p.N + node) * p.Hq + s.kvh * p.G + head_in_group;
       const int64_t srow = ((int64_t)blockIdx.x * 2 + slot) * p.RPG + row;
 #pragma unroll 1
       for (int c = 0; c < kD; c += 32) {
@@ -713,6 +706,8 @@ bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int 
 
 int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
 
+int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : Cfg<2>::kCtasPerSm; }
+
 #ifdef TV_TC_TRACE
 extern "C" int tv_debug_trace(void* dst, size_t bytes) {
   const size_t n = sizeof(trace::g_trace) < bytes ? sizeof(trace::g_trace) : bytes;
@@ -740,12 +735,6 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
     cuuint32_t box[4] = {64, 1, (cuuint32_t)kBlk, 1};
     if ((st = encode(fn, &maps.kt, p.k_tree, 4, dims, strides, box, "k_tree"))) return st;
     if ((st = encode(fn, &maps.vt, p.v_tree, 4, dims, strides, box, "v_tree"))) return st;
-  }
-  {
-    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.Hq, (cuuint64_t)p.N, (cuuint64_t)p.B};
-    cuuint64_t strides[3] = {row_bytes, row_bytes * p.Hq, row_bytes * p.Hq * p.N};
-    cuuint32_t box[4] = {64, (cuuint32_t)p.G, (cuuint32_t)(128 / p.G), 1};
-    if ((st = encode(fn, &maps.q, p.q, 4, dims, strides, box, "q"))) return st;
   }
   return p.RPG <= 128 ? launch_m<1>(p, maps, status, stream) : launch_m<2>(p, maps, status, stream);
 }

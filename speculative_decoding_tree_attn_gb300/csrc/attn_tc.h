@@ -20,6 +20,9 @@ const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim
 // Rows per unit for `rows` = G * N query rows per KV head (128 or 256).
 int tc_rows_per_unit(int rows);
 
+// Resident CTAs per SM the kernel is built for at this row count.
+int tc_ctas_per_sm(int rows);
+
 // Launches the persistent tensor-core kernel (plan already enqueued).
 int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream);
 
