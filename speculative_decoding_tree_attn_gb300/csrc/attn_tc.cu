@@ -71,7 +71,11 @@ template <int M>
 struct Cfg {
   static constexpr int kStages = (M == 1) ? 3 : 6;
   static constexpr int kCtasPerSm = (M == 1) ? 2 : 1;
-  static constexpr int kThreads = 64 + M * 128;      // TMA warp, MMA warp, one warpgroup per M tile
+  // warp 0: TMA; warps 1..M: one MMA issuer per M tile (a single thread
+  // issues at most about one MMA per 70 cycles, so each tile gets its own);
+  // then one softmax warpgroup per M tile.
+  static constexpr int kSoftmaxWarp0 = 1 + M;
+  static constexpr int kThreads = 32 * (1 + M + 4 * M);
   static constexpr uint32_t kTmemCols = (M == 1) ? 256 : 512;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
@@ -223,6 +227,32 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Matrix descriptors as two 32-bit words: the low word carries the start
+// address (>> 4) and the leading offset, so a K step is one 32-bit add.
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);  // SBO, version 1, SWIZZLE_128B
+}
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo & 0x3FFFFu) >> 4) << 16);
+}
+
+// O/S += A(TMEM) B(smem); the accumulate flag is a literal.
+template <bool kAcc>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
+  if constexpr (kAcc)
+    asm volatile(
+        "{\n\t.reg .b64 bd;\n\tmov.b64 bd, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, 1;\n\t}" ::"r"(d),
+        "r"(a), "r"(b_lo), "r"(b_hi), "r"(idesc)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .b64 bd;\n\tmov.b64 bd, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, 0;\n\t}" ::"r"(d),
+        "r"(a), "r"(b_lo), "r"(b_hi), "r"(idesc)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -319,7 +349,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.kv_empty[s], M);  // one commit per MMA issuer
     }
     for (int m = 0; m < M; ++m) {
       mbar_init(&bars.s_full[m], 1);
@@ -403,34 +433,37 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       for (uint32_t i = first; i < g; ++i)
         mbar_wait(&bars.kv_full[i % C::kStages], (i / C::kStages) & 1, &bars, nullptr, false);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per tile g and M tile m: O_m += P_m(g-1) V(g-1), then S_m(g) = Q_m K(g)^T.
-    // The tensor pipe runs them in issue order, so S_m(g) overwrites the TMEM
+  } else if (warp >= 1 && warp < 1 + M) {
+    // ------------------------------------------------------------ MMA issuer of M tile m
+    // Per tile g: O_m += P_m(g-1) V(g-1), then S_m(g) = Q_m K(g)^T.  The
+    // tensor pipe runs them in issue order, so S_m(g) overwrites the TMEM
     // columns holding P_m(g-1) only after that P has been consumed, and the
     // commit that signals S_m(g) also covers O_m's update by tile g-1.
+    const int m = warp - 1;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
       constexpr uint32_t idO = idesc_bf16(128, kD, true);
+      constexpr uint32_t hi = desc_hi(1024);
+      const uint32_t dS = tmem + C::col_s(m), dO = tmem + C::col_o(m), aQ = tmem + C::col_q(m);
       uint32_t g = 0;
       int seg_i = 0;
       bool ok = true;
       Walk walk(p);
       Segment s;
-      auto issue_pv = [&](int m, int stage, bool accumulate) {
-        const uint32_t d = tmem + C::col_o(m), a = tmem + C::col_s(m);
-        const uint32_t vb = sV + stage * kKVTileBytes;
+      auto issue_pv = [&](int stage, bool accumulate) {
+        const uint32_t lo = desc_lo(sV + stage * kKVTileBytes, kKVHalfBytes);  // MN-major V: LBO = next 64 columns
+        if (accumulate) mma_ts<true>(dO, dS, lo, hi, idO);
+        else mma_ts<false>(dO, dS, lo, hi, idO);
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_bf16_ts(d, a + kk * 8, sdesc(vb + kk * 2048, kKVHalfBytes, 1024), idO, (accumulate || kk > 0) ? 1u : 0u);
+        for (int kk = 1; kk < kBlk / 16; ++kk) mma_ts<true>(dO, dS + kk * 8, lo + kk * (2048 >> 4), hi, idO);
         mma_commit(&bars.o_done[m]);
       };
-      auto issue_s = [&](int m, int stage) {
-        const uint32_t d = tmem + C::col_s(m), a = tmem + C::col_q(m);
-        const uint32_t kb = sK + stage * kKVTileBytes;
+      auto issue_s = [&](int stage) {
+        const uint32_t lo = desc_lo(sK + stage * kKVTileBytes, 0);
+        mma_ts<false>(dS, aQ, lo, hi, idS);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16_ts(d, a + kk * 8, sdesc(kb + (kk / 4) * kKVHalfBytes + (kk % 4) * 32, 0, 1024), idS, kk > 0);
+        for (int kk = 1; kk < kD / 16; ++kk)
+          mma_ts<true>(dS, aQ + kk * 8, lo + (kk / 4) * (kKVHalfBytes >> 4) + (kk % 4) * 2, hi, idS);
         mma_commit(&bars.s_full[m]);
       };
       while (ok && walk.next(p, s)) {
@@ -441,37 +474,33 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
         for (int k = 0; k < n_seg && ok; ++k, ++g) {
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
-          TV_TRACE(1, g);
-          for (int m = 0; m < M && ok; ++m) {
-            if (k > 0) {
-              ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
-              if (!ok) break;
-              fence_after();
-              issue_pv(m, (g - 1) % C::kStages, k > 1);
-              TV_TRACE(4 + m, g - 1);
-            }
-            issue_s(m, stage);
-            TV_TRACE(2 + m, g);
-          }
-          if (ok && k > 0) mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
-        }
-        if (!ok) break;
-        for (int m = 0; m < M && ok; ++m) {
-          ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
           if (!ok) break;
-          fence_after();
-          issue_pv(m, (g - 1) % C::kStages, n_seg > 1);
-          TV_TRACE(4 + m, g - 1);
+          if (m == 0) TV_TRACE(1, g);
+          if (k > 0) {
+            ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
+            if (!ok) break;
+            fence_after();
+            issue_pv((g - 1) % C::kStages, k > 1);
+            mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
+            TV_TRACE(4 + m, g - 1);
+          }
+          issue_s(stage);
+          TV_TRACE(2 + m, g);
         }
         if (!ok) break;
+        ok = mbar_wait(&bars.p_full[m], (g - 1) & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        issue_pv((g - 1) % C::kStages, n_seg > 1);
         mma_commit(&bars.kv_empty[(g - 1) % C::kStages]);
+        TV_TRACE(4 + m, g - 1);
         ++seg_i;
       }
     }
     __syncwarp();
-  } else if (warp >= 2 && warp < 2 + 4 * M) {
+  } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + 4 * M) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int m = (warp - 2) / 4;
+    const int m = (warp - C::kSoftmaxWarp0) / 4;
     const int quarter = warp % 4;         // TMEM lanes 32*quarter .. +31
     const int rl = quarter * 32 + lane;   // row within the M tile = TMEM lane
     const int row = m * 128 + rl;         // row within the unit
