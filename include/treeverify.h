@@ -207,6 +207,42 @@ int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                         int32_t flags, int32_t* status, void* stream);
 
 /*
+ * tv_tree_attn_verify_static -- device, asynchronous; allocation-free variant
+ * of tv_tree_attn_verify.  No page describes it: it exists for callers that
+ * cannot provide device memory when they verify a tree -- a serving loop that
+ * reserves all memory at start-up and forbids allocation afterwards, a host
+ * runtime without a device allocator, or code that must not call cudaMalloc
+ * because it can synchronise the device.  Same arguments and results as
+ * tv_tree_attn_verify without the workspace: the scratch (tile plan and
+ * split partials) is a fixed array of tv_tree_attn_static_workspace_bytes()
+ * (32 MiB) that the library places in device memory of every GPU that loads
+ * it, held until the process exits.
+ *
+ * num_ctas   0 = the widest grid, at most one wave, whose scratch fits the
+ *            array; an explicit grid whose scratch exceeds the array, or a
+ *            shape whose plan alone does not fit, returns TV_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  The call allocates nothing (no cudaMalloc / cudaFree).  Every call
+ * uses the same array, so calls that can overlap on the GPU (different
+ * streams, or graphs replayed concurrently) race and must be serialised by the
+ * caller; the array needs no clearing between calls (everything read is
+ * written earlier in the same call).
+ */
+int tv_tree_attn_verify_static(const void* q, const void* k_cache, const void* v_cache,
+                               int64_t num_blocks, int32_t block_size,
+                               const int32_t* block_table, int32_t max_blocks,
+                               const int32_t* seq_lens, const void* k_tree, const void* v_tree,
+                               const uint64_t* mask, int64_t mask_bstride,
+                               int32_t B, int32_t N, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                               int32_t dtype, float scale, void* out, float* lse,
+                               int32_t num_ctas, int32_t flags, int32_t* status, void* stream);
+
+/* Size in bytes of the fixed scratch array used by tv_tree_attn_verify_static
+ * (no page describes it; see above). */
+size_t tv_tree_attn_static_workspace_bytes(void);
+
+/*
  * tv_tree_accept_greedy -- device, asynchronous.
  * "Build the tree attention mask ...", "The mask." (walk from the root while
  * some child's draft token equals the target's choice after the current

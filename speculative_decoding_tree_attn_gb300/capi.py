@@ -37,6 +37,9 @@ SIGNATURES = {
     "tv_tree_attn_workspace_size": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "tv_tree_attn_verify": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32,
                                            _I32, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _I32, _I32, _P, _P]),
+    "tv_tree_attn_verify_static": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _I64, _I32,
+                                                  _I32, _I32, _I32, _I32, _I32, _F, _P, _P, _I32, _I32, _P, _P]),
+    "tv_tree_attn_static_workspace_bytes": (ctypes.c_size_t, []),
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
                                              _P, _P]),
@@ -199,6 +202,37 @@ def tv_tree_attn_verify(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tr
                                      mstride, B, N, Hq, Hkv, D, _code(q.dtype), scale, _ptr(out), _ptr(lse),
                                      _ptr(workspace), workspace.numel(), num_ctas, flags, _ptr(status),
                                      _stream(stream)))
+    return out
+
+
+def tv_tree_attn_static_workspace_bytes():
+    return lib().tv_tree_attn_static_workspace_bytes()
+
+
+def tv_tree_attn_verify_static(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, mask, *, scale=None,
+                               out=None, lse=None, num_ctas=0, flags=0, status=None, stream=None):
+    """Tree attention without a caller workspace (the library's fixed scratch
+    array is used); same arguments and result as tv_tree_attn_verify."""
+    dts = (torch.float32, torch.bfloat16)
+    _dev(q, "q", dts)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_tree", k_tree), ("v_tree", v_tree)):
+        _dev(t, name, (q.dtype,))
+    _dev(block_table, "block_table", (torch.int32,))
+    _dev(seq_lens, "seq_lens", (torch.int32,))
+    _dev(mask, "mask", (torch.int64,))
+    B, N, Hq, D = q.shape
+    Hkv = k_tree.shape[2]
+    num_blocks, _, block_size, _ = k_cache.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    mstride = 0 if mask.dim() == 1 else mask.stride(0)
+    _check("tv_tree_attn_verify_static",
+           lib().tv_tree_attn_verify_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, block_size,
+                                            _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(k_tree),
+                                            _ptr(v_tree), _ptr(mask), mstride, B, N, Hq, Hkv, D, _code(q.dtype),
+                                            scale, _ptr(out), _ptr(lse), num_ctas, flags, _ptr(status),
+                                            _stream(stream)))
     return out
 
 

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "attn_common.cuh"
 #include "attn_tc.h"
@@ -482,4 +483,84 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
   st = cfg.tc ? launch_attn_tc(p, status, s) : simt_dispatch(p, dtype, s, nullptr);
   if (st) return st;
   return launch_combine(p, dtype, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of tv_tree_attn_verify.
+//
+// Some callers cannot obtain device memory at the point where they verify a
+// tree: a serving loop that reserves all of its memory at start-up and forbids
+// allocation afterwards, a host runtime (another language, an embedded engine)
+// that has no device allocator to hand, or code that must not call cudaMalloc
+// because it can synchronise the device.  For them the split-KV scratch of the
+// attention call (the tile plan and the partial outputs of split units) lives
+// in one fixed array in device memory that this library defines, sized
+// kStaticWorkspaceBytes on every GPU that loads the library, kept until the
+// process exits.
+// ---------------------------------------------------------------------------
+namespace tv {
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;  // 32 MiB per device
+__device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+// Device address of g_static_workspace for the current device, looked up once
+// per device (the host-side name is only a stand-in for the device array).
+int static_workspace_ptr(void** out) {
+  static std::mutex mu;
+  static void* cached[64] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(TV_ERR_UNSUPPORTED, "device id %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_static_workspace)");
+    cached[dev] = ptr;
+  }
+  *out = cached[dev];
+  return TV_OK;
+}
+
+}  // namespace
+}  // namespace tv
+
+extern "C" size_t tv_tree_attn_static_workspace_bytes(void) { return tv::kStaticWorkspaceBytes; }
+
+extern "C" int tv_tree_attn_verify_static(const void* q, const void* k_cache, const void* v_cache,
+                                          int64_t num_blocks, int32_t block_size, const int32_t* block_table,
+                                          int32_t max_blocks, const int32_t* seq_lens, const void* k_tree,
+                                          const void* v_tree, const uint64_t* mask, int64_t mask_bstride, int32_t B,
+                                          int32_t N, int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t dtype,
+                                          float scale, void* out, float* lse, int32_t num_ctas, int32_t flags,
+                                          int32_t* status, void* stream) {
+  using namespace tv;
+  clear_error();
+  AttnConfig cfg;
+  int st = attn_config(B, N, Hq, Hkv, head_dim, dtype, block_size, num_ctas, flags, &cfg);
+  if (st) return st;
+  if (B == 0) return TV_OK;
+  if (num_ctas == 0) {
+    // the widest grid (at most one wave) whose scratch fits the static array
+    const int64_t per_cta = align256((int64_t)2 * cfg.RPG * head_dim * 4) + align256((int64_t)2 * cfg.RPG * 4);
+    const int64_t room = (int64_t)kStaticWorkspaceBytes - align256((int64_t)(cfg.U + 1) * 4) - 512;
+    int fit = room > 0 ? (int)(room / per_cta) : 0;
+    if (fit < 1)
+      return fail(TV_ERR_WORKSPACE, "tv_tree_attn_verify_static: %d units need more than the %zu-byte static scratch",
+                  cfg.U, kStaticWorkspaceBytes);
+    num_ctas = cfg.P < fit ? cfg.P : fit;
+    if ((st = attn_config(B, N, Hq, Hkv, head_dim, dtype, block_size, num_ctas, flags, &cfg))) return st;
+  }
+  if ((size_t)cfg.bytes > kStaticWorkspaceBytes)
+    return fail(TV_ERR_WORKSPACE,
+                "tv_tree_attn_verify_static: this shape and grid need %lld bytes of scratch, above the %zu-byte "
+                "static maximum; pass a smaller num_ctas (or 0) or use tv_tree_attn_verify with a workspace",
+                (long long)cfg.bytes, kStaticWorkspaceBytes);
+  void* ws = nullptr;
+  if ((st = static_workspace_ptr(&ws))) return st;
+  return tv_tree_attn_verify(q, k_cache, v_cache, num_blocks, block_size, block_table, max_blocks, seq_lens, k_tree,
+                             v_tree, mask, mask_bstride, B, N, Hq, Hkv, head_dim, dtype, scale, out, lse, ws,
+                             kStaticWorkspaceBytes, num_ctas, flags, status, stream);
 }
