@@ -92,6 +92,7 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
+  uint64_t s_free[2];
   uint64_t q_full;
   uint32_t tmem_base;
   int abort;
@@ -329,6 +330,74 @@ struct TcMaps {
   CUtensorMap kc, vc, kt, vt;
 };
 
+// TMA producer (warp 0): streams every tile of the CTA's slice into the
+// K/V stage ring, one box per (cache block, 64-column half).
+template <int kStages>
+__device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& maps, Bars& bars, uint32_t sK,
+                                             uint32_t sV, int lane, int32_t* status) {
+    // ------------------------------------------------------------ TMA producer
+    const int bs = p.block_size;
+    const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
+    const int nsub = kBlk / br;
+    const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
+    uint32_t g = 0;
+    bool ok = true;
+    Walk walk(p);
+    Segment s;
+    while (ok && walk.next(p, s)) {
+      // Block-table entries of this unit are read in 32-entry windows, one
+      // coalesced load per window, the next window requested a window ahead,
+      // so no TMA issue waits on a dependent global load.
+      const int nb = (s.L + bs - 1) / bs;  // valid table entries of request b
+      const int32_t* trow = p.block_table + (int64_t)s.b * p.max_blocks;
+      int w0 = (s.a * kBlk) / bs;          // first entry held in `cur`
+      int32_t cur = (w0 + lane < nb) ? __ldg(trow + w0 + lane) : 0;
+      int32_t nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
+      for (int t = s.a; t < s.e && ok; ++t, ++g) {
+        const int stage = g % kStages;
+        const uint32_t use = g / kStages;
+        const bool tree_tile = (t == s.n - 1);
+        if (!tree_tile && (t * kBlk) / bs >= w0 + 32) {
+          w0 += 32;
+          cur = nxt;
+          nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
+        }
+        int pos = t * kBlk + (lane < nsub ? lane : 0) * br;
+        if (pos >= s.L) pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
+        const int rel = pos / bs - w0;
+        const int32_t from_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
+        const int32_t from_nxt = __shfl_sync(0xffffffffu, nxt, rel & 31);
+        const int64_t blk = rel < 32 ? from_cur : from_nxt;
+        if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
+        if (!ok) break;
+        const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
+        if (lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
+        __syncwarp();
+        if (tree_tile) {
+          if (lane == 0)
+            for (int h = 0; h < 2; ++h) {
+              tma_4d(dk + h * kKVHalfBytes, &maps.kt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
+              tma_4d(dv + h * kKVHalfBytes, &maps.vt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
+            }
+        } else if (lane < nsub) {
+          int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
+          if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
+          for (int h = 0; h < 2; ++h) {
+            tma_2d(dk + h * kKVHalfBytes + lane * br * 128, &maps.kc, h * 64, (int)y, &bars.kv_full[stage]);
+            tma_2d(dv + h * kKVHalfBytes + lane * br * 128, &maps.vc, h * 64, (int)y, &bars.kv_full[stage]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // drain: every load this warp issued has landed before the CTA exits
+    if (lane == 0) {
+      const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0;
+      for (uint32_t i = first; i < g; ++i)
+        mbar_wait(&bars.kv_full[i % kStages], (i / kStages) & 1, &bars, nullptr, false);
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <int M>
@@ -372,67 +441,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    const int bs = p.block_size;
-    const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
-    const int nsub = kBlk / br;
-    const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
-    uint32_t g = 0;
-    bool ok = true;
-    Walk walk(p);
-    Segment s;
-    while (ok && walk.next(p, s)) {
-      // Block-table entries of this unit are read in 32-entry windows, one
-      // coalesced load per window, the next window requested a window ahead,
-      // so no TMA issue waits on a dependent global load.
-      const int nb = (s.L + bs - 1) / bs;  // valid table entries of request b
-      const int32_t* trow = p.block_table + (int64_t)s.b * p.max_blocks;
-      int w0 = (s.a * kBlk) / bs;          // first entry held in `cur`
-      int32_t cur = (w0 + lane < nb) ? __ldg(trow + w0 + lane) : 0;
-      int32_t nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
-      for (int t = s.a; t < s.e && ok; ++t, ++g) {
-        const int stage = g % C::kStages;
-        const uint32_t use = g / C::kStages;
-        const bool tree_tile = (t == s.n - 1);
-        if (!tree_tile && (t * kBlk) / bs >= w0 + 32) {
-          w0 += 32;
-          cur = nxt;
-          nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
-        }
-        int pos = t * kBlk + (lane < nsub ? lane : 0) * br;
-        if (pos >= s.L) pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
-        const int rel = pos / bs - w0;
-        const int32_t from_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
-        const int32_t from_nxt = __shfl_sync(0xffffffffu, nxt, rel & 31);
-        const int64_t blk = rel < 32 ? from_cur : from_nxt;
-        if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
-        if (!ok) break;
-        const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
-        if (lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
-        __syncwarp();
-        if (tree_tile) {
-          if (lane == 0)
-            for (int h = 0; h < 2; ++h) {
-              tma_4d(dk + h * kKVHalfBytes, &maps.kt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
-              tma_4d(dv + h * kKVHalfBytes, &maps.vt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
-            }
-        } else if (lane < nsub) {
-          int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
-          if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
-          for (int h = 0; h < 2; ++h) {
-            tma_2d(dk + h * kKVHalfBytes + lane * br * 128, &maps.kc, h * 64, (int)y, &bars.kv_full[stage]);
-            tma_2d(dv + h * kKVHalfBytes + lane * br * 128, &maps.vc, h * 64, (int)y, &bars.kv_full[stage]);
-          }
-        }
-        __syncwarp();
-      }
-    }
-    // drain: every load this warp issued has landed before the CTA exits
-    if (lane == 0) {
-      const uint32_t first = g > (uint32_t)C::kStages ? g - C::kStages : 0;
-      for (uint32_t i = first; i < g; ++i)
-        mbar_wait(&bars.kv_full[i % C::kStages], (i / C::kStages) & 1, &bars, nullptr, false);
-    }
+    run_producer<C::kStages>(p, maps, bars, sK, sV, lane, status);
   } else if (warp >= 1 && warp < 1 + M) {
     // ------------------------------------------------------------ MMA issuer of M tile m
     // Per tile g: O_m += P_m(g-1) V(g-1), then S_m(g) = Q_m K(g)^T.  The
@@ -674,6 +683,339 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
   }
 }
 
+// ---------------------------------------------------------------- two M tiles (up to 256 rows)
+//
+// Every operand placement is chosen so that no single resource is on the
+// critical path of a 64-key tile (about 1400 cycles of HBM time per SM):
+//  * four MMA-issuing warps (S_0, S_1, O_0 += P_0 V, O_1 += P_1 V), because one
+//    thread issues at most one tcgen05.mma about every 70 cycles;
+//  * P_m has its own TMEM columns, so S_m(g+1) is computed while the softmax
+//    of tile g runs;
+//  * TMEM (512 columns) holds S_0 S_1 P_0 P_1 Q_0 O_0 O_1 = 64+64+32+32+64+128+128;
+//    Q_1 therefore stays in shared memory (S_1 = Q_1 K^T reads both operands
+//    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
+struct PairCfg {
+  static constexpr int kStages = 6;
+  static constexpr int kThreads = 32 * 13;  // TMA, 4 issuers, 2 softmax warpgroups
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
+  static constexpr int kOffQ1 = kOffV + kStages * kKVTileBytes;  // 2 halves x 128 rows x 128 B
+  static constexpr int kBytes = kOffQ1 + 2 * 128 * 128;
+  static constexpr int kSmem = kBytes + 1024;
+  static constexpr uint32_t col_s(int m) { return m * 64; }
+  static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
+  static constexpr uint32_t kColQ0 = 192;
+  static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
+  static constexpr int kSoftmaxWarp0 = 5;
+};
+
+__global__ void __launch_bounds__(PairCfg::kThreads, 1)
+    attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
+  using C = PairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Bars bars;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sK = base + C::kOffK, sV = base + C::kOffV, sQ1 = base + C::kOffQ1;
+  uint8_t* gQ1 = smem_raw + (base - raw) + C::kOffQ1;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  {
+    Walk probe(p);
+    if (probe.t0 >= probe.t1) return;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 2);  // one commit from each O issuer
+    }
+    for (int m = 0; m < 2; ++m) {
+      mbar_init(&bars.s_full[m], 1);
+      mbar_init(&bars.s_free[m], 128);
+      mbar_init(&bars.p_full[m], 128);
+      mbar_init(&bars.o_done[m], 1);
+    }
+    mbar_init(&bars.q_full, 256);
+    bars.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  constexpr uint32_t hi = desc_hi(1024);
+
+  if (warp == 0) {
+    run_producer<C::kStages>(p, maps, bars, sK, sV, lane, status);
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ S_m = Q_m K^T issuer
+    const int m = warp - 1;
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
+      const uint32_t dS = tmem + C::col_s(m);
+      uint32_t g = 0;
+      int seg_i = 0;
+      bool ok = true;
+      Walk walk(p);
+      Segment s;
+      while (ok && walk.next(p, s)) {
+        ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        for (int t = s.a; t < s.e && ok; ++t, ++g) {
+          const int stage = g % C::kStages;
+          ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          if (ok && g > 0) ok = mbar_wait(&bars.s_free[m], (g - 1) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          const uint32_t blo = desc_lo(sK + stage * kKVTileBytes, 0);
+          if (m == 0) {
+            const uint32_t aQ = tmem + C::kColQ0;
+            mma_ts<false>(dS, aQ, blo, hi, idS);
+#pragma unroll
+            for (int kk = 1; kk < kD / 16; ++kk)
+              mma_ts<true>(dS, aQ + kk * 8, blo + (kk / 4) * (kKVHalfBytes >> 4) + (kk % 4) * 2, hi, idS);
+          } else {
+            const uint32_t alo = desc_lo(sQ1, 0);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint64_t a = ((uint64_t)hi << 32) | (alo + (kk / 4) * (16384 >> 4) + (kk % 4) * 2);
+              const uint64_t b = ((uint64_t)hi << 32) | (blo + (kk / 4) * (kKVHalfBytes >> 4) + (kk % 4) * 2);
+              mma_bf16(dS, a, b, idS, kk > 0);
+            }
+          }
+          mma_commit(&bars.s_full[m]);
+          if (m == 0) TV_TRACE(2, g);
+        }
+        ++seg_i;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 3 || warp == 4) {
+    // ------------------------------------------------------------ O_m += P_m V issuer
+    const int m = warp - 3;
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_bf16(128, kD, true);
+      const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
+      uint32_t g = 0;
+      bool ok = true;
+      Walk walk(p);
+      Segment s;
+      while (ok && walk.next(p, s)) {
+        for (int t = s.a; t < s.e && ok; ++t, ++g) {
+          const int stage = g % C::kStages;
+          ok = mbar_wait(&bars.p_full[m], g & 1, &bars, status);
+          if (ok) ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          const uint32_t vlo = desc_lo(sV + stage * kKVTileBytes, kKVHalfBytes);
+          if (t > s.a) mma_ts<true>(dO, aP, vlo, hi, idO);
+          else mma_ts<false>(dO, aP, vlo, hi, idO);
+#pragma unroll
+          for (int kk = 1; kk < kBlk / 16; ++kk) mma_ts<true>(dO, aP + kk * 8, vlo + kk * (2048 >> 4), hi, idO);
+          mma_commit(&bars.o_done[m]);
+          mma_commit(&bars.kv_empty[stage]);
+          if (m == 0) TV_TRACE(4, g);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + 8) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int m = (warp - C::kSoftmaxWarp0) / 4;
+    const int quarter = warp % 4;
+    const int rl = quarter * 32 + lane;
+    const int row = m * 128 + rl;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = lane_addr + C::col_s(m), tP = lane_addr + C::col_p(m), tO = lane_addr + C::col_o(m);
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    uint32_t g = 0;
+    bool ok = true;
+    Walk walk(p);
+    Segment s;
+    while (ok && walk.next(p, s)) {
+      const int unit_row = s.rg * p.RPG + row;
+      const bool valid_row = unit_row < p.R;
+      const int node = valid_row ? unit_row / p.G : 0;
+      const int head_in_group = unit_row % p.G;
+      const int64_t orow = ((int64_t)s.b * p.N + node) * p.Hq + s.kvh * p.G + head_in_group;
+      const uint64_t mrow = valid_row ? p.mask[(int64_t)s.b * p.mask_bstride + node] : 1ull;
+      {
+        // Q row: M tile 0 into TMEM, M tile 1 into the swizzled shared tile
+        const uint4* src = reinterpret_cast<const uint4*>(q + orow * kD);
+        if (m == 0) {
+#pragma unroll
+          for (int c = 0; c < kD / 64; ++c) {
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 v = valid_row ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
+              r[4 * j] = v.x; r[4 * j + 1] = v.y; r[4 * j + 2] = v.z; r[4 * j + 3] = v.w;
+            }
+            tmem_st32(lane_addr + C::kColQ0 + c * 32, r);
+          }
+          tmem_st_wait();
+          fence_before();
+        } else {
+          uint8_t* rowp = gQ1 + (rl / 8) * 1024 + (rl % 8) * 128;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint4 v = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(rowp + (c / 8) * 16384 + (((c % 8) ^ (rl % 8)) * 16)) = v;
+          }
+          fence_proxy_async();
+        }
+        mbar_arrive(&bars.q_full);
+      }
+      float m_run = -INFINITY, l = 0.f;
+      const int n_seg = s.e - s.a;
+      for (int k = 0; k < n_seg; ++k, ++g) {
+        const int t = s.a + k;
+        ok = mbar_wait_warp(&bars.s_full[m], g & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        if (rl == 0) TV_TRACE(6 + 4 * m, g);
+        float sv[kBlk];
+        {
+          uint32_t r[32];
+          tmem_ld32(tS, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(r[c]);
+          tmem_ld32(tS + 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
+        }
+        fence_before();
+        mbar_arrive(&bars.s_free[m]);  // the next S_m may be computed now
+        if (rl == 0) TV_TRACE(7 + 4 * m, g);
+        if (t == s.n - 1) {
+#pragma unroll
+          for (int c = 0; c < kBlk; ++c)
+            if (!(c < p.N && ((mrow >> c) & 1ull))) sv[c] = -INFINITY;
+        } else {
+          const int lim = s.L - t * kBlk;
+          if (lim < kBlk) {
+#pragma unroll
+            for (int c = 0; c < kBlk; ++c)
+              if (c >= lim) sv[c] = -INFINITY;
+          }
+        }
+        float mx;
+        {
+          float t8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            t8[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[8 + j]), fmaxf(sv[16 + j], sv[24 + j])),
+                          fmaxf(fmaxf(sv[32 + j], sv[40 + j]), fmaxf(sv[48 + j], sv[56 + j])));
+          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        }
+        mx *= p.scale_log2;
+        const float m_new = fmaxf(m_run, mx);
+        const bool grow = m_new > m_run + kRescaleThreshold;
+        const float m_use = grow ? m_new : ((m_run == -INFINITY) ? 0.f : m_run);
+        const float sc = p.scale_log2;
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < kBlk / 2; ++c) {
+          const float e0 = fast_exp2(fmaf(sv[2 * c], sc, -m_use));
+          const float e1 = fast_exp2(fmaf(sv[2 * c + 1], sc, -m_use));
+          if (c & 1) sum1 += e0 + e1; else sum0 += e0 + e1;
+          pk[c] = pack_bf16(e0, e1);
+        }
+        if (k > 0) {
+          // P_m(g-1) consumed and O_m holds tiles < g
+          ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          if (__any_sync(0xffffffffu, grow)) {
+            const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 32) {
+              uint32_t r[32];
+              tmem_ld32(tO + c, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+              tmem_st32(tO + c, r);
+            }
+          }
+        }
+        if (grow) {
+          l *= exp2f(m_run - m_new);
+          m_run = m_new;
+        }
+        l += sum0 + sum1;
+        tmem_st32(tP, pk);
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&bars.p_full[m]);
+        if (rl == 0) TV_TRACE(9 + 4 * m, g);
+      }
+      if (!ok) break;
+      ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
+      if (!ok) break;
+      fence_after();
+      const bool complete = (s.a == 0 && s.e == s.n);
+      const int64_t us = p.tile_start[s.u];
+      const int slot = (walk.t0 < us) ? 1 : 0;
+      const float inv = 1.f / l;
+      const float lse2 = m_run + log2f(l);
+      const int64_t srow = ((int64_t)blockIdx.x * 2 + slot) * p.RPG + row;
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tO + c, r);
+        tmem_ld_wait();
+        if (!valid_row) continue;
+        if (complete) {
+          uint4* dst = reinterpret_cast<uint4*>(out + orow * kD + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(r[8 * j + 0]) * inv, __uint_as_float(r[8 * j + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv);
+            dst[j] = v;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
+                                 __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+        }
+      }
+      if (valid_row) {
+        if (complete) {
+          if (p.lse) p.lse[orow] = lse2 * 0.69314718055994530942f;
+        } else {
+          p.part_lse[srow] = lse2;
+        }
+      }
+      fence_before();
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -725,7 +1067,7 @@ const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim
   if (G < 1 || 128 % G) return "Hq/Hkv does not divide 128";
   if (block_size % 16 || !(kBlk % block_size == 0 || block_size % kBlk == 0))
     return "block_size is not a multiple of 16 that divides or is divisible by 64";
-  if (dev.max_smem_optin < (size_t)Cfg<2>::kSmem + sizeof(Bars)) return "not enough opt-in shared memory";
+  if (dev.max_smem_optin < (size_t)PairCfg::kSmem + sizeof(Bars)) return "not enough opt-in shared memory";
   return nullptr;
 }
 
@@ -735,7 +1077,7 @@ bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int 
 
 int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
 
-int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : Cfg<2>::kCtasPerSm; }
+int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : 1; }
 
 #ifdef TV_TC_TRACE
 extern "C" int tv_debug_trace(void* dst, size_t bytes) {
@@ -765,7 +1107,12 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
     if ((st = encode(fn, &maps.kt, p.k_tree, 4, dims, strides, box, "k_tree"))) return st;
     if ((st = encode(fn, &maps.vt, p.v_tree, 4, dims, strides, box, "v_tree"))) return st;
   }
-  return p.RPG <= 128 ? launch_m<1>(p, maps, status, stream) : launch_m<2>(p, maps, status, stream);
+  if (p.RPG <= 128) return launch_m<1>(p, maps, status, stream);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
+  attn_tc_pair_kernel<<<p.P, PairCfg::kThreads, PairCfg::kSmem, stream>>>(p, maps, status);
+  TV_LAUNCH_CHECK("attn_tc_pair_kernel");
+  return TV_OK;
 }
 
 }  // namespace tv
