@@ -290,6 +290,56 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of a 64-entry row.
+__device__ __forceinline__ float row_max64(const float (&v)[64]) {
+  float a[22];
+#pragma unroll
+  for (int i = 0; i < 21; ++i) a[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[21] = v[63];
+  float b[8];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) b[i] = max3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[7] = a[21];
+  return max3(max3(b[0], b[1], b[2]), max3(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
+}
+
+// (e0, e1) = 2^(s0 * sc - m), 2^(s1 * sc - m) with one packed FMA; sc2/negm2 hold
+// (sc, sc) and (-m, -m).
+__device__ __forceinline__ void exp2_pair(float s0, float s1, uint64_t sc2, uint64_t negm2, float& e0, float& e1) {
+  asm("{\n\t.reg .b64 s2, t2;\n\t.reg .f32 t0, t1;\n\t"
+      "mov.b64 s2, {%2, %3};\n\t"
+      "fma.rn.f32x2 t2, s2, %4, %5;\n\t"
+      "mov.b64 {t0, t1}, t2;\n\t"
+      "ex2.approx.ftz.f32 %0, t0;\n\t"
+      "ex2.approx.ftz.f32 %1, t1;\n\t}"
+      : "=f"(e0), "=f"(e1)
+      : "f"(s0), "f"(s1), "l"(sc2), "l"(negm2));
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+__device__ __forceinline__ float sum_f32x2(uint64_t a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return lo + hi;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -362,7 +412,9 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& 
           cur = nxt;
           nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
         }
-        int pos = t * kBlk + (lane < nsub ? lane : 0) * br;
+        // lane j < 4 * nsub issues one box: sub-box j / 4, column half (j / 2) % 2, K (even j) or V (odd j)
+        const int sub = (lane >> 2) < nsub ? (lane >> 2) : 0;
+        int pos = t * kBlk + sub * br;
         if (pos >= s.L) pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
         const int rel = pos / bs - w0;
         const int32_t from_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
@@ -373,19 +425,17 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& 
         const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
         if (lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
         __syncwarp();
+        const int h = (lane >> 1) & 1;
+        const bool is_v = lane & 1;
         if (tree_tile) {
-          if (lane == 0)
-            for (int h = 0; h < 2; ++h) {
-              tma_4d(dk + h * kKVHalfBytes, &maps.kt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
-              tma_4d(dv + h * kKVHalfBytes, &maps.vt, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
-            }
-        } else if (lane < nsub) {
+          if (lane < 4)
+            tma_4d((is_v ? dv : dk) + h * kKVHalfBytes, is_v ? &maps.vt : &maps.kt, h * 64, s.kvh, 0, s.b,
+                   &bars.kv_full[stage]);
+        } else if (lane < 4 * nsub) {
           int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
           if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
-          for (int h = 0; h < 2; ++h) {
-            tma_2d(dk + h * kKVHalfBytes + lane * br * 128, &maps.kc, h * 64, (int)y, &bars.kv_full[stage]);
-            tma_2d(dv + h * kKVHalfBytes + lane * br * 128, &maps.vc, h * 64, (int)y, &bars.kv_full[stage]);
-          }
+          tma_2d((is_v ? dv : dk) + h * kKVHalfBytes + sub * br * 128, is_v ? &maps.vc : &maps.kc, h * 64, (int)y,
+                 &bars.kv_full[stage]);
         }
         __syncwarp();
       }
@@ -581,15 +631,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
               if (c >= lim) sv[c] = -INFINITY;
           }
         }
-        float mx;
-        {
-          float t8[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            t8[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[8 + j]), fmaxf(sv[16 + j], sv[24 + j])),
-                          fmaxf(fmaxf(sv[32 + j], sv[40 + j]), fmaxf(sv[48 + j], sv[56 + j])));
-          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
-        }
+        float mx = row_max64(sv);
         mx *= p.scale_log2;  // scale > 0: max of scaled = scaled max
         const float m_new = fmaxf(m_run, mx);
         const bool grow = m_new > m_run + kRescaleThreshold;
@@ -611,17 +653,17 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        const float sc = p.scale_log2;
-        float sum0 = 0.f, sum1 = 0.f;
+        const uint64_t sc2 = pack_f32x2(p.scale_log2, p.scale_log2), negm2 = pack_f32x2(-m_use, -m_use);
+        uint64_t acc0 = 0, acc1 = 0;  // two packed (f32, f32) partial sums
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < kBlk / 2; ++c) {
-          const float e0 = fast_exp2(fmaf(sv[2 * c], sc, -m_use));
-          const float e1 = fast_exp2(fmaf(sv[2 * c + 1], sc, -m_use));
-          if (c & 1) sum1 += e0 + e1; else sum0 += e0 + e1;
+          float e0, e1;
+          exp2_pair(sv[2 * c], sv[2 * c + 1], sc2, negm2, e0, e1);
+          if (c & 1) acc1 = add_f32x2(acc1, pack_f32x2(e0, e1)); else acc0 = add_f32x2(acc0, pack_f32x2(e0, e1));
           pk[c] = pack_bf16(e0, e1);
         }
-        l += sum0 + sum1;
+        l += sum_f32x2(add_f32x2(acc0, acc1));
         tmem_st32(tS, pk);  // P_m(g) over the first 32 columns of S_m
         tmem_st_wait();
         fence_before();
@@ -910,29 +952,22 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
               if (c >= lim) sv[c] = -INFINITY;
           }
         }
-        float mx;
-        {
-          float t8[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            t8[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[8 + j]), fmaxf(sv[16 + j], sv[24 + j])),
-                          fmaxf(fmaxf(sv[32 + j], sv[40 + j]), fmaxf(sv[48 + j], sv[56 + j])));
-          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
-        }
+        float mx = row_max64(sv);
         mx *= p.scale_log2;
         const float m_new = fmaxf(m_run, mx);
         const bool grow = m_new > m_run + kRescaleThreshold;
         const float m_use = grow ? m_new : ((m_run == -INFINITY) ? 0.f : m_run);
-        const float sc = p.scale_log2;
-        float sum0 = 0.f, sum1 = 0.f;
+        const uint64_t sc2 = pack_f32x2(p.scale_log2, p.scale_log2), negm2 = pack_f32x2(-m_use, -m_use);
+        uint64_t acc0 = 0, acc1 = 0;
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < kBlk / 2; ++c) {
-          const float e0 = fast_exp2(fmaf(sv[2 * c], sc, -m_use));
-          const float e1 = fast_exp2(fmaf(sv[2 * c + 1], sc, -m_use));
-          if (c & 1) sum1 += e0 + e1; else sum0 += e0 + e1;
+          float e0, e1;
+          exp2_pair(sv[2 * c], sv[2 * c + 1], sc2, negm2, e0, e1);
+          if (c & 1) acc1 = add_f32x2(acc1, pack_f32x2(e0, e1)); else acc0 = add_f32x2(acc0, pack_f32x2(e0, e1));
           pk[c] = pack_bf16(e0, e1);
         }
+        const float sum0 = sum_f32x2(add_f32x2(acc0, acc1)), sum1 = 0.f;
         if (k > 0) {
           // P_m(g-1) consumed and O_m holds tiles < g
           ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
