@@ -382,9 +382,13 @@ struct TcMaps {
 
 // TMA producer (warp 0): streams every tile of the CTA's slice into the
 // K/V stage ring, one box per (cache block, 64-column half).
-template <int kStages>
+// With kProducers = 2, producer 0 loads the K boxes and producer 1 the V boxes
+// of every tile (one warp issues a TMA box about every 150 cycles, so a
+// single warp cannot keep up with two M tiles); producer 0 posts the stage's
+// byte count.
+template <int kStages, int kProducers = 1>
 __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& maps, Bars& bars, uint32_t sK,
-                                             uint32_t sV, int lane, int32_t* status) {
+                                             uint32_t sV, int lane, int32_t* status, int prod = 0) {
     // ------------------------------------------------------------ TMA producer
     const int bs = p.block_size;
     const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
@@ -412,8 +416,10 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& 
           cur = nxt;
           nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
         }
-        // lane j < 4 * nsub issues one box: sub-box j / 4, column half (j / 2) % 2, K (even j) or V (odd j)
-        const int sub = (lane >> 2) < nsub ? (lane >> 2) : 0;
+        // box j < 4 * nsub: sub-box j / 4, column half (j / 2) % 2, K (even j) or V (odd j);
+        // this warp issues the boxes j = lane * kProducers + prod, one per lane
+        const int j = lane * kProducers + prod;
+        const int sub = (j >> 2) < nsub ? (j >> 2) : 0;
         int pos = t * kBlk + sub * br;
         if (pos >= s.L) pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
         const int rel = pos / bs - w0;
@@ -423,15 +429,15 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& 
         if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
         if (!ok) break;
         const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
-        if (lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
+        if (prod == 0 && lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
         __syncwarp();
-        const int h = (lane >> 1) & 1;
-        const bool is_v = lane & 1;
+        const int h = (j >> 1) & 1;
+        const bool is_v = j & 1;
         if (tree_tile) {
-          if (lane < 4)
+          if (j < 4)
             tma_4d((is_v ? dv : dk) + h * kKVHalfBytes, is_v ? &maps.vt : &maps.kt, h * 64, s.kvh, 0, s.b,
                    &bars.kv_full[stage]);
-        } else if (lane < 4 * nsub) {
+        } else if (j < 4 * nsub) {
           int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
           if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
           tma_2d((is_v ? dv : dk) + h * kKVHalfBytes + sub * br * 128, is_v ? &maps.vc : &maps.kc, h * 64, (int)y,
@@ -738,7 +744,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
 //    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
 struct PairCfg {
   static constexpr int kStages = 6;
-  static constexpr int kThreads = 32 * 13;  // TMA, 4 issuers, 2 softmax warpgroups
+  static constexpr int kThreads = 32 * 14;  // 2 TMA, 4 issuers, 2 softmax warpgroups
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
@@ -749,7 +755,7 @@ struct PairCfg {
   static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
   static constexpr uint32_t kColQ0 = 192;
   static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
-  static constexpr int kSoftmaxWarp0 = 5;
+  static constexpr int kSoftmaxWarp0 = 6;
 };
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -782,7 +788,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
+  if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
                  "r"(C::kTmemCols)
                  : "memory");
@@ -794,11 +800,11 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   constexpr uint32_t hi = desc_hi(1024);
 
-  if (warp == 0) {
-    run_producer<C::kStages>(p, maps, bars, sK, sV, lane, status);
-  } else if (warp == 1 || warp == 2) {
+  if (warp < 2) {
+    run_producer<C::kStages, 2>(p, maps, bars, sK, sV, lane, status, warp);
+  } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ S_m = Q_m K^T issuer
-    const int m = warp - 1;
+    const int m = warp - 2;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
       const uint32_t dS = tmem + C::col_s(m);
@@ -840,9 +846,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 3 || warp == 4) {
+  } else if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ O_m += P_m V issuer
-    const int m = warp - 3;
+    const int m = warp - 4;
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(128, kD, true);
       const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
@@ -1045,7 +1051,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 
   fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
