@@ -382,9 +382,9 @@ struct TcMaps {
 
 // TMA producer (warp 0): streams every tile of the CTA's slice into the
 // K/V stage ring, one box per (cache block, 64-column half).
-// With kProducers = 2, producer 0 loads the K boxes and producer 1 the V boxes
-// of every tile (one warp issues a TMA box about every 150 cycles, so a
-// single warp cannot keep up with two M tiles); producer 0 posts the stage's
+// With kProducers > 1 the boxes of every tile are dealt round-robin to that
+// many warps (one warp issues a TMA box only about every 150 cycles, so a
+// single warp cannot keep a two-M-tile CTA fed); producer 0 posts the stage's
 // byte count.
 template <int kStages, int kProducers = 1>
 __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& maps, Bars& bars, uint32_t sK,
@@ -744,7 +744,8 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
 //    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
 struct PairCfg {
   static constexpr int kStages = 6;
-  static constexpr int kThreads = 32 * 14;  // 2 TMA, 4 issuers, 2 softmax warpgroups
+  static constexpr int kProducers = 4;
+  static constexpr int kThreads = 32 * 16;  // 4 TMA, 4 issuers, 2 softmax warpgroups
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
@@ -755,7 +756,7 @@ struct PairCfg {
   static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
   static constexpr uint32_t kColQ0 = 192;
   static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
-  static constexpr int kSoftmaxWarp0 = 6;
+  static constexpr int kSoftmaxWarp0 = 8;
 };
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -788,7 +789,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 2) {
+  if (warp == 4) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
                  "r"(C::kTmemCols)
                  : "memory");
@@ -800,11 +801,11 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   constexpr uint32_t hi = desc_hi(1024);
 
-  if (warp < 2) {
-    run_producer<C::kStages, 2>(p, maps, bars, sK, sV, lane, status, warp);
-  } else if (warp == 2 || warp == 3) {
+  if (warp < C::kProducers) {
+    run_producer<C::kStages, C::kProducers>(p, maps, bars, sK, sV, lane, status, warp);
+  } else if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ S_m = Q_m K^T issuer
-    const int m = warp - 2;
+    const int m = warp - 4;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
       const uint32_t dS = tmem + C::col_s(m);
@@ -846,9 +847,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 4 || warp == 5) {
+  } else if (warp == 6 || warp == 7) {
     // ------------------------------------------------------------ O_m += P_m V issuer
-    const int m = warp - 4;
+    const int m = warp - 6;
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(128, kD, true);
       const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
@@ -1051,7 +1052,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 
   fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 4) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
