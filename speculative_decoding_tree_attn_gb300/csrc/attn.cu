@@ -251,10 +251,12 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(AttnParams p
 // ---------------------------------------------------------------------------
 // combine: O = sum_k 2^(lse_k - lse*) O_k over the pieces of a split unit
 // ---------------------------------------------------------------------------
-constexpr int kMaxPieces = 1024;  // pieces of one unit held in shared memory at a time
+// One warp per row of a split unit, eight rows per CTA; grid = units x row
+// chunks.  A unit written by a single CTA exits at once.
+constexpr int kCombineRows = 8;
 
 template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
+__global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(AttnParams p) {
   const int u = blockIdx.x;
   const int64_t T_total = p.tile_start[p.U];
   const int64_t us = p.tile_start[u], ue = p.tile_start[u + 1];
@@ -262,70 +264,59 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   if (c0 == c1) return;  // written directly by one CTA
   int b, kvh, rg;
   unit_coords(p, u, b, kvh, rg);
+  const int lane = threadIdx.x % 32;
+  const int r = blockIdx.y * kCombineRows + threadIdx.x / 32;
+  if (r >= p.RPG || rg * p.RPG + r >= p.R) return;
   T* __restrict__ out = static_cast<T*>(p.out);
-  __shared__ int32_t s_slot[kMaxPieces];  // partial-slot index of each piece, -1 if the CTA was empty
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32, nwarps = blockDim.x / 32;
-  const int rows = min(p.RPG, p.R - rg * p.RPG);
+  const int gr = rg * p.RPG + r;
+  const int i = gr / p.G, h = kvh * p.G + gr % p.G;
+  const int64_t orow = ((int64_t)b * p.N + i) * p.Hq + h;
   const int64_t n_all = c1 - c0 + 1;
-  // Partial slot of piece j (the CTA c0 + j), -1 if that CTA had no tiles.
-  // Up to kMaxPieces pieces are tabulated once in shared memory; beyond that
-  // a lane computes its piece's slot itself.
-  const int n_tab = n_all < kMaxPieces ? (int)n_all : kMaxPieces;
-  for (int j = threadIdx.x; j < n_tab; j += blockDim.x) {
-    const int64_t c = c0 + j;
-    const int64_t s0 = cta_start(c, T_total, p.P), s1 = cta_start(c + 1, T_total, p.P);
-    s_slot[j] = (s0 < s1) ? (int32_t)(c * 2 + (s0 < us ? 1 : 0)) : -1;
-  }
-  __syncthreads();
-  auto slot_of = [&](int64_t j) -> int32_t {
-    if (j < n_tab) return s_slot[j];
-    const int64_t c = c0 + j;
-    const int64_t s0 = cta_start(c, T_total, p.P), s1 = cta_start(c + 1, T_total, p.P);
-    return (s0 < s1) ? (int32_t)(c * 2 + (s0 < us ? 1 : 0)) : -1;
-  };
   const int dpl = p.D / 32;  // output elements per lane (<= 8)
-  for (int r = warp; r < rows; r += nwarps) {
-    const int gr = rg * p.RPG + r;
-    const int i = gr / p.G, h = kvh * p.G + gr % p.G;
-    const int64_t orow = ((int64_t)b * p.N + i) * p.Hq + h;
-    float mx = -INFINITY, z = 0.f;
-    float acc[8];
+  float mx = -INFINITY, z = 0.f;
+  float acc[8];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) acc[x] = 0.f;
-    for (int64_t j0 = 0; j0 < n_all; j0 += 32) {
-      const int64_t j = j0 + lane;
-      const int32_t slot = j < n_all ? slot_of(j) : -1;
-      const float l2 = slot >= 0 ? p.part_lse[(int64_t)slot * p.RPG + r] : -INFINITY;
-      float cm = l2;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-      const float m_new = fmaxf(mx, cm);
-      const float alpha = (mx == -INFINITY) ? 0.f : exp2f(mx - m_new);
-      const float w = slot >= 0 ? exp2f(l2 - m_new) : 0.f;
-      float wz = w;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) wz += __shfl_xor_sync(0xffffffffu, wz, o);
-      z = z * alpha + wz;
-      mx = m_new;
-#pragma unroll
-      for (int x = 0; x < 8; ++x) acc[x] *= alpha;
-      const int n_here = (n_all - j0) < 32 ? (int)(n_all - j0) : 32;
-      for (int k = 0; k < n_here; ++k) {
-        const float wk = __shfl_sync(0xffffffffu, w, k);
-        const int32_t sk = __shfl_sync(0xffffffffu, slot, k);
-        if (sk < 0) continue;
-        const float* src = p.part_o + ((int64_t)sk * p.RPG + r) * p.D;
-#pragma unroll
-        for (int x = 0; x < 8; ++x)
-          if (x < dpl) acc[x] = fmaf(wk, src[lane + 32 * x], acc[x]);
-      }
+  for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+  for (int64_t j0 = 0; j0 < n_all; j0 += 32) {
+    // lane k takes piece j0 + k: the slice of CTA c0 + j0 + k (slot 1 only
+    // for the first CTA when the unit began inside its slice; empty slices skipped)
+    const int64_t j = j0 + lane;
+    int32_t slot = -1;
+    if (j < n_all) {
+      const int64_t c = c0 + j;
+      const int64_t s0 = cta_start(c, T_total, p.P), s1 = cta_start(c + 1, T_total, p.P);
+      if (s0 < s1) slot = (int32_t)(c * 2 + (s0 < us ? 1 : 0));
     }
-    const float inv = 1.f / z;
+    const float l2 = slot >= 0 ? p.part_lse[(int64_t)slot * p.RPG + r] : -INFINITY;
+    float cm = l2;
 #pragma unroll
-    for (int x = 0; x < 8; ++x)
-      if (x < dpl) out[orow * p.D + lane + 32 * x] = from_f32<T>(acc[x] * inv);
-    if (p.lse && lane == 0) p.lse[orow] = (mx + log2f(z)) * 0.69314718055994530942f;
+    for (int o = 16; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+    const float m_new = fmaxf(mx, cm);
+    const float alpha = (mx == -INFINITY) ? 0.f : exp2f(mx - m_new);
+    const float w = slot >= 0 ? exp2f(l2 - m_new) : 0.f;
+    float wz = w;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wz += __shfl_xor_sync(0xffffffffu, wz, o);
+    z = z * alpha + wz;
+    mx = m_new;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc[x] *= alpha;
+    const int n_here = (n_all - j0) < 32 ? (int)(n_all - j0) : 32;
+    for (int k = 0; k < n_here; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      const int32_t sk = __shfl_sync(0xffffffffu, slot, k);
+      if (sk < 0) continue;
+      const float* src = p.part_o + ((int64_t)sk * p.RPG + r) * p.D;
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+        if (x < dpl) acc[x] = fmaf(wk, __ldg(src + lane + 32 * x), acc[x]);
+    }
   }
+  const float inv = 1.f / z;
+#pragma unroll
+  for (int x = 0; x < 8; ++x)
+    if (x < dpl) out[orow * p.D + lane + 32 * x] = from_f32<T>(acc[x] * inv);
+  if (p.lse && lane == 0) p.lse[orow] = (mx + log2f(z)) * 0.69314718055994530942f;
 }
 
 template <typename T, int D>
@@ -425,8 +416,9 @@ int launch_plan(const AttnParams& p, cudaStream_t stream) {
 
 int launch_combine(const AttnParams& p, int dtype, cudaStream_t stream) {
   if (p.P <= 1) return TV_OK;
-  if (dtype == TV_F32) combine_kernel<float><<<p.U, 256, 0, stream>>>(p);
-  else combine_kernel<__nv_bfloat16><<<p.U, 256, 0, stream>>>(p);
+  const dim3 grid(p.U, (p.RPG + kCombineRows - 1) / kCombineRows);
+  if (dtype == TV_F32) combine_kernel<float><<<grid, 32 * kCombineRows, 0, stream>>>(p);
+  else combine_kernel<__nv_bfloat16><<<grid, 32 * kCombineRows, 0, stream>>>(p);
   TV_LAUNCH_CHECK("combine_kernel");
   return TV_OK;
 }
