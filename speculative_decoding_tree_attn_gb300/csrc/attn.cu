@@ -251,17 +251,22 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(AttnParams p
 // ---------------------------------------------------------------------------
 // combine: O = sum_k 2^(lse_k - lse*) O_k over the pieces of a split unit
 // ---------------------------------------------------------------------------
-// One warp per row of a split unit, eight rows per CTA; grid = units x row
-// chunks.  A unit written by a single CTA exits at once.
-constexpr int kCombineRows = 8;
+// Only units cut by a slice boundary need merging, and there are fewer such
+// boundaries than CTAs: block x handles the boundary between CTA x and x + 1
+// (the unit holding CTA x + 1's first tile, when that tile is not the unit's
+// first and x is the unit's first CTA); one warp per row, 32 rows per block.
+constexpr int kCombineRows = 32;
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(AttnParams p) {
-  const int u = blockIdx.x;
   const int64_t T_total = p.tile_start[p.U];
+  const int64_t cut = cta_start(blockIdx.x + 1, T_total, p.P);
+  if (cut >= T_total) return;
+  const int u = find_unit(p.tile_start, p.U, cut);
   const int64_t us = p.tile_start[u], ue = p.tile_start[u + 1];
+  if (us == cut) return;                                // the boundary falls between units
   const int64_t c0 = cta_of(us, T_total, p.P), c1 = cta_of(ue - 1, T_total, p.P);
-  if (c0 == c1) return;  // written directly by one CTA
+  if (c0 != (int64_t)blockIdx.x) return;                // merged at the unit's first boundary
   int b, kvh, rg;
   unit_coords(p, u, b, kvh, rg);
   const int lane = threadIdx.x % 32;
@@ -416,7 +421,7 @@ int launch_plan(const AttnParams& p, cudaStream_t stream) {
 
 int launch_combine(const AttnParams& p, int dtype, cudaStream_t stream) {
   if (p.P <= 1) return TV_OK;
-  const dim3 grid(p.U, (p.RPG + kCombineRows - 1) / kCombineRows);
+  const dim3 grid(p.P - 1, (p.RPG + kCombineRows - 1) / kCombineRows);
   if (dtype == TV_F32) combine_kernel<float><<<grid, 32 * kCombineRows, 0, stream>>>(p);
   else combine_kernel<__nv_bfloat16><<<grid, 32 * kCombineRows, 0, stream>>>(p);
   TV_LAUNCH_CHECK("combine_kernel");

@@ -44,11 +44,21 @@
 namespace tv { namespace trace {
 constexpr int kEvents = 16, kTiles = 512;
 __device__ unsigned long long g_trace[kEvents][kTiles];
+__device__ unsigned long long g_cta_time[1024][2];  // globaltimer at entry / exit of every CTA
 }}  // namespace tv::trace
 #define TV_TRACE(ev, tile) \
   do { if (blockIdx.x == 0 && (tile) < tv::trace::kTiles) tv::trace::g_trace[ev][tile] = clock64(); } while (0)
+#define TV_TRACE_CTA(k)                                                                                  \
+  do {                                                                                                    \
+    if (threadIdx.x == 0 && blockIdx.x < 1024) {                                                          \
+      unsigned long long t_;                                                                              \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                              \
+      tv::trace::g_cta_time[blockIdx.x][k] = t_;                                                          \
+    }                                                                                                     \
+  } while (0)
 #else
 #define TV_TRACE(ev, tile) do { } while (0)
+#define TV_TRACE_CTA(k) do { } while (0)
 #endif
 
 namespace tv {
@@ -192,17 +202,6 @@ __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::be
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: 128B swizzle, 1024-byte aligned atoms.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
-  d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version for sm_10x
-  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
-  return d;
-}
-
 // Instruction descriptor, kind::f16: bf16 x bf16 -> f32, A K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
@@ -215,16 +214,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// A operand in TMEM (row = lane, K packed two bf16 per column), B in smem.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -281,14 +270,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// 2^x on the special-function unit (approximate, flushes denormals); inputs
-// here are <= 8 and -inf, giving values in [0, 256].
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
@@ -769,6 +750,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   const uint32_t sK = base + C::kOffK, sV = base + C::kOffV, sQ1 = base + C::kOffQ1;
   uint8_t* gQ1 = smem_raw + (base - raw) + C::kOffQ1;
 
+  TV_TRACE_CTA(0);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   {
     Walk probe(p);
@@ -1050,6 +1032,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     }
   }
 
+  TV_TRACE_CTA(1);
   fence_before();
   __syncthreads();
   if (warp == 4) {
@@ -1125,6 +1108,10 @@ int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : 1; }
 extern "C" int tv_debug_trace(void* dst, size_t bytes) {
   const size_t n = sizeof(trace::g_trace) < bytes ? sizeof(trace::g_trace) : bytes;
   return cudaMemcpyFromSymbol(dst, trace::g_trace, n) == cudaSuccess ? 0 : -1;
+}
+extern "C" int tv_debug_cta_times(void* dst, size_t bytes) {
+  const size_t n = sizeof(trace::g_cta_time) < bytes ? sizeof(trace::g_cta_time) : bytes;
+  return cudaMemcpyFromSymbol(dst, trace::g_cta_time, n) == cudaSuccess ? 0 : -1;
 }
 #endif
 
