@@ -44,7 +44,7 @@
 namespace tv { namespace trace {
 constexpr int kEvents = 16, kTiles = 512;
 __device__ unsigned long long g_trace[kEvents][kTiles];
-__device__ unsigned long long g_cta_time[1024][2];  // globaltimer at entry / exit of every CTA
+__device__ unsigned long long g_cta_time[1024][4];  // globaltimer at entry / exit, segments, first unit
 }}  // namespace tv::trace
 #define TV_TRACE(ev, tile) \
   do { if (blockIdx.x == 0 && (tile) < tv::trace::kTiles) tv::trace::g_trace[ev][tile] = clock64(); } while (0)
@@ -383,6 +383,21 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& 
       // Block-table entries of this unit are read in 32-entry windows, one
       // coalesced load per window, the next window requested a window ahead,
       // so no TMA issue waits on a dependent global load.
+      {
+        // warm L2 with this unit's query rows and ancestor rows: the softmax
+        // warps read them when the consumer side reaches the unit, a few
+        // tiles from now
+        const int rows = p.R - s.rg * p.RPG < p.RPG ? p.R - s.rg * p.RPG : p.RPG;
+        const char* qb = static_cast<const char*>(p.q);
+        for (int r = lane * kProducers + prod; r < rows; r += 32 * kProducers) {
+          const int ur = s.rg * p.RPG + r;
+          const int64_t orow = ((int64_t)s.b * p.N + ur / p.G) * p.Hq + s.kvh * p.G + ur % p.G;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + orow * (kD * 2)));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + orow * (kD * 2) + 128));
+        }
+        if (lane == 0 && prod == 0)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.mask + (int64_t)s.b * p.mask_bstride));
+      }
       const int nb = (s.L + bs - 1) / bs;  // valid table entries of request b
       const int32_t* trow = p.block_table + (int64_t)s.b * p.max_blocks;
       int w0 = (s.a * kBlk) / bs;          // first entry held in `cur`
@@ -725,8 +740,8 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
 //    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
 struct PairCfg {
   static constexpr int kStages = 6;
-  static constexpr int kProducers = 4;
-  static constexpr int kThreads = 32 * 16;  // 4 TMA, 4 issuers, 2 softmax warpgroups
+  static constexpr int kProducers = 2;
+  static constexpr int kThreads = 32 * 14;  // 2 TMA, 4 issuers, 2 softmax warpgroups
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
@@ -737,7 +752,7 @@ struct PairCfg {
   static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
   static constexpr uint32_t kColQ0 = 192;
   static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
-  static constexpr int kSoftmaxWarp0 = 8;
+  static constexpr int kSoftmaxWarp0 = 6;
 };
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -771,7 +786,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) {
+  if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
                  "r"(C::kTmemCols)
                  : "memory");
@@ -785,9 +800,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 
   if (warp < C::kProducers) {
     run_producer<C::kStages, C::kProducers>(p, maps, bars, sK, sV, lane, status, warp);
-  } else if (warp == 4 || warp == 5) {
+  } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ S_m = Q_m K^T issuer
-    const int m = warp - 4;
+    const int m = warp - 2;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
       const uint32_t dS = tmem + C::col_s(m);
@@ -829,9 +844,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 6 || warp == 7) {
+  } else if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ O_m += P_m V issuer
-    const int m = warp - 6;
+    const int m = warp - 4;
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(128, kD, true);
       const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
@@ -872,40 +887,76 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     bool ok = true;
     Walk walk(p);
     Segment s;
-    while (ok && walk.next(p, s)) {
-      const int unit_row = s.rg * p.RPG + row;
-      const bool valid_row = unit_row < p.R;
-      const int node = valid_row ? unit_row / p.G : 0;
-      const int head_in_group = unit_row % p.G;
-      const int64_t orow = ((int64_t)s.b * p.N + node) * p.Hq + s.kvh * p.G + head_in_group;
-      const uint64_t mrow = valid_row ? p.mask[(int64_t)s.b * p.mask_bstride + node] : 1ull;
-      {
-        // Q row: M tile 0 into TMEM, M tile 1 into the swizzled shared tile
-        const uint4* src = reinterpret_cast<const uint4*>(q + orow * kD);
-        if (m == 0) {
+#ifdef TV_TC_TRACE
+    int n_segs_traced = 0;
+#endif
+    // Row identity of this thread inside a unit, and the unit's Q row and
+    // ancestor row (the producer warps have already pulled both into L2).
+    struct RowOf {
+      bool valid;
+      int node;
+      int64_t orow;
+    };
+    auto row_of = [&](const Segment& sg) {
+      RowOf r;
+      const int unit_row = sg.rg * p.RPG + row;
+      r.valid = unit_row < p.R;
+      r.node = r.valid ? unit_row / p.G : 0;
+      r.orow = ((int64_t)sg.b * p.N + r.node) * p.Hq + sg.kvh * p.G + unit_row % p.G;
+      return r;
+    };
+    uint4 qreg[16];
+    uint64_t mrow_next = 1ull;
+    auto fetch_q = [&](const Segment& sg) {
+      const RowOf r = row_of(sg);
+      const uint4* src = reinterpret_cast<const uint4*>(q + r.orow * kD);
 #pragma unroll
-          for (int c = 0; c < kD / 64; ++c) {
-            uint32_t r[32];
+      for (int c = 0; c < 16; ++c) qreg[c] = r.valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      mrow_next = r.valid ? __ldg(reinterpret_cast<const unsigned long long*>(p.mask) +
+                                  (int64_t)sg.b * p.mask_bstride + r.node)
+                          : 1ull;
+    };
+    // Q row into its operand slot: M tile 0 into TMEM, M tile 1 into the
+    // swizzled shared tile; then tell the S issuers.
+    auto place_q = [&]() {
+      if (m == 0) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint4 v = valid_row ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
-              r[4 * j] = v.x; r[4 * j + 1] = v.y; r[4 * j + 2] = v.z; r[4 * j + 3] = v.w;
-            }
-            tmem_st32(lane_addr + C::kColQ0 + c * 32, r);
+        for (int c = 0; c < kD / 64; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            r[4 * j] = qreg[c * 8 + j].x; r[4 * j + 1] = qreg[c * 8 + j].y;
+            r[4 * j + 2] = qreg[c * 8 + j].z; r[4 * j + 3] = qreg[c * 8 + j].w;
           }
-          tmem_st_wait();
-          fence_before();
-        } else {
-          uint8_t* rowp = gQ1 + (rl / 8) * 1024 + (rl % 8) * 128;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint4 v = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(rowp + (c / 8) * 16384 + (((c % 8) ^ (rl % 8)) * 16)) = v;
-          }
-          fence_proxy_async();
+          tmem_st32(lane_addr + C::kColQ0 + c * 32, r);
         }
-        mbar_arrive(&bars.q_full);
+        tmem_st_wait();
+        fence_before();
+      } else {
+        uint8_t* rowp = gQ1 + (rl / 8) * 1024 + (rl % 8) * 128;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4*>(rowp + (c / 8) * 16384 + (((c % 8) ^ (rl % 8)) * 16)) = qreg[c];
+        fence_proxy_async();
       }
+      mbar_arrive(&bars.q_full);
+    };
+    bool have = walk.next(p, s);
+    if (have) {
+      fetch_q(s);
+      place_q();
+    }
+    while (ok && have) {
+#ifdef TV_TC_TRACE
+      if (threadIdx.x == C::kSoftmaxWarp0 * 32 && blockIdx.x < 1024) {
+        if (n_segs_traced == 0) tv::trace::g_cta_time[blockIdx.x][3] = s.u;
+        tv::trace::g_cta_time[blockIdx.x][2] = ++n_segs_traced;
+      }
+#endif
+      const RowOf rid = row_of(s);
+      const bool valid_row = rid.valid;
+      const int64_t orow = rid.orow;
+      const uint64_t mrow = mrow_next;
       float m_run = -INFINITY, l = 0.f;
       const int n_seg = s.e - s.a;
       for (int k = 0; k < n_seg; ++k, ++g) {
@@ -990,6 +1041,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
       if (!ok) break;
       fence_after();
+      Segment s_next;
+      const bool have_next = walk.next(p, s_next);
       const bool complete = (s.a == 0 && s.e == s.n);
       const int64_t us = p.tile_start[s.u];
       const int slot = (walk.t0 < us) ? 1 : 0;
@@ -1029,13 +1082,19 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         }
       }
       fence_before();
+      if (have_next) {  // every MMA of the finished unit has completed; its Q rows are warm in L2
+        fetch_q(s_next);
+        place_q();
+      }
+      s = s_next;
+      have = have_next;
     }
   }
 
   TV_TRACE_CTA(1);
   fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 2) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
