@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
     if (u < p.U) {
       int b, kvh, rg;
       unit_coords(p, u, b, kvh, rg);
-      n = (clamp_len(p, b) + p.BLK - 1) / p.BLK + 1;
+      n = (clamp_len(p, b) + p.BLK - 1) / p.BLK + 1 + p.unit_cost;
     }
     int incl = n;
 #pragma unroll
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(AttnParams p
   const int64_t cut = cta_start(blockIdx.x + 1, T_total, p.P);
   if (cut >= T_total) return;
   const int u = find_unit(p.tile_start, p.U, cut);
-  const int64_t us = p.tile_start[u], ue = p.tile_start[u + 1];
-  if (us == cut) return;                                // the boundary falls between units
+  const int64_t us = p.tile_start[u] + p.unit_cost, ue = p.tile_start[u + 1];  // real tiles [us, ue)
+  if (cut <= us) return;                                // the boundary does not cut real tiles
   const int64_t c0 = cta_of(us, T_total, p.P), c1 = cta_of(ue - 1, T_total, p.P);
   if (c0 != (int64_t)blockIdx.x) return;                // merged at the unit's first boundary
   int b, kvh, rg;
@@ -474,6 +474,7 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
   p.num_blocks = num_blocks; p.block_size = block_size; p.max_blocks = max_blocks;
   p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.D = head_dim; p.G = Hq / Hkv;
   p.R = p.G * N; p.RPG = cfg.RPG; p.RG = cfg.RG; p.U = cfg.U; p.BLK = cfg.BLK; p.P = cfg.P;
+  p.unit_cost = cfg.tc ? tc_unit_cost(cfg.RPG) : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = (cudaStream_t)stream;
   if ((st = launch_plan(p, s))) return st;

@@ -1,5 +1,11 @@
 // Work decomposition shared by the tree-attention kernels and the combine.
 //
+// Units also carry `unit_cost` virtual tiles placed before their real ones: a
+// kernel pays a fixed cost at every unit it starts or finishes (epilogue,
+// loading the next queries), so a CTA whose slice crosses many short units is
+// given fewer real tiles.  A unit's real tiles are [tile_start[u] + unit_cost,
+// tile_start[u + 1]).
+//
 // A "unit" is one (request b, KV head, row group): the rows of a unit are the
 // (node, query head) pairs of one GQA group, row r = node * G + g.  A unit's
 // work is a sequence of KV tiles: ceil(L_b / BLK) prefix tiles followed by one
@@ -44,6 +50,7 @@ struct AttnParams {
   int U;    // number of units
   int BLK;  // KV positions per tile
   int P;    // persistent CTAs
+  int unit_cost;  // extra virtual tiles charged per unit (its fixed start/finish cost)
   float scale_log2;  // softmax scale * log2(e)
 };
 

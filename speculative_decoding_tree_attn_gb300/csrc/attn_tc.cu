@@ -330,8 +330,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // ---------------------------------------------------------------- work walk
 
 struct Segment {
-  int u, a, e, n;  // unit, local tiles [a, e) of its n tiles
+  int u, a, e, n;  // unit, local real tiles [a, e) of its n real tiles
   int b, kvh, rg, L;
+  int64_t real_start;  // index of the unit's first real tile in the plan
 };
 
 struct Walk {
@@ -343,17 +344,24 @@ struct Walk {
     t1 = cta_start(blockIdx.x + 1, T, p.P);
     u = (t0 < t1) ? find_unit(p.tile_start, p.U, t0) : p.U;
   }
+  // Next unit with real tiles in this CTA's slice (units whose slice part is
+  // only their virtual cost tiles are skipped).
   __device__ bool next(const AttnParams& p, Segment& s) {
-    if (u >= p.U || p.tile_start[u] >= t1) return false;
-    const int64_t us = p.tile_start[u], ue = p.tile_start[u + 1];
-    s.u = u;
-    s.a = (int)(max(t0, us) - us);
-    s.e = (int)(min(t1, ue) - us);
-    s.n = (int)(ue - us);
-    unit_coords(p, u, s.b, s.kvh, s.rg);
-    s.L = clamp_len(p, s.b);
-    ++u;
-    return true;
+    while (u < p.U && p.tile_start[u] < t1) {
+      const int64_t us = p.tile_start[u] + p.unit_cost, ue = p.tile_start[u + 1];  // real tiles
+      const int64_t a = max(t0, us), e = min(t1, ue);
+      const int uu = u++;
+      if (a >= e) continue;
+      s.u = uu;
+      s.a = (int)(a - us);
+      s.e = (int)(e - us);
+      s.n = (int)(ue - us);
+      s.real_start = us;
+      unit_coords(p, uu, s.b, s.kvh, s.rg);
+      s.L = clamp_len(p, s.b);
+      return true;
+    }
+    return false;
   }
 };
 
@@ -678,8 +686,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       if (!ok) break;
       fence_after();
       const bool complete = (s.a == 0 && s.e == s.n);
-      const int64_t us = p.tile_start[s.u];
-      const int slot = (walk.t0 < us) ? 1 : 0;
+      const int slot = (walk.t0 < s.real_start) ? 1 : 0;
       const float inv = 1.f / l;
       const float lse2 = m_run + log2f(l);
       const int64_t srow = ((int64_t)blockIdx.x * 2 + slot) * p.RPG + row;
@@ -815,6 +822,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
         if (!ok) break;
         fence_after();
+        if (m == 0) TV_TRACE(3, g);
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
@@ -1041,11 +1049,11 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
       if (!ok) break;
       fence_after();
+      if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
       Segment s_next;
       const bool have_next = walk.next(p, s_next);
       const bool complete = (s.a == 0 && s.e == s.n);
-      const int64_t us = p.tile_start[s.u];
-      const int slot = (walk.t0 < us) ? 1 : 0;
+      const int slot = (walk.t0 < s.real_start) ? 1 : 0;
       const float inv = 1.f / l;
       const float lse2 = m_run + log2f(l);
       const int64_t srow = ((int64_t)blockIdx.x * 2 + slot) * p.RPG + row;
@@ -1082,10 +1090,12 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         }
       }
       fence_before();
+      if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       if (have_next) {  // every MMA of the finished unit has completed; its Q rows are warm in L2
         fetch_q(s_next);
         place_q();
       }
+      if (m == 0 && rl == 0) TV_TRACE(15, g - 1);
       s = s_next;
       have = have_next;
     }
@@ -1162,6 +1172,10 @@ bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int 
 int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
 
 int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : 1; }
+
+// Virtual tiles charged per unit: measured cost of finishing one unit and
+// starting the next, in units of one 64-key tile of the steady state.
+int tc_unit_cost(int rows_per_unit) { return rows_per_unit <= 128 ? 3 : 6; }
 
 #ifdef TV_TC_TRACE
 extern "C" int tv_debug_trace(void* dst, size_t bytes) {

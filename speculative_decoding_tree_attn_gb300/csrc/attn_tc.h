@@ -23,6 +23,9 @@ int tc_rows_per_unit(int rows);
 // Resident CTAs per SM the kernel is built for at this row count.
 int tc_ctas_per_sm(int rows);
 
+// Virtual tiles the plan charges per unit for this kernel (see AttnParams).
+int tc_unit_cost(int rows_per_unit);
+
 // Launches the persistent tensor-core kernel (plan already enqueued).
 int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream);
 
