@@ -270,7 +270,18 @@ class Step:
         self.acc_path = torch.empty(B, cols, dtype=torch.int32, device=dev)
         self.esize = 2 if dt == torch.bfloat16 else 4
         self.attn_bytes = attention_bytes(w, self.lens, n, self.esize)
-        self.launches = 5 + (1 if w.accept != "none" else 0)
+        # tree_mask, rope_apply, the attention kernel(s), the acceptance kernel;
+        # the tcgen05 path is one kernel (plus a counter memset), the CUDA-core
+        # path plan + attention + combine
+        uses_tc = flags == capi.TV_ATTN_TCGEN05
+        if flags == capi.TV_ATTN_AUTO:
+            try:
+                capi.tv_tree_attn_workspace_size(B, n, w.Hq, w.Hkv, w.D, dt, w.block_size, num_ctas,
+                                                 capi.TV_ATTN_TCGEN05)
+                uses_tc = True
+            except capi.TVError:
+                uses_tc = False
+        self.launches = 2 + (1 if uses_tc else 3) + (1 if w.accept != "none" else 0)
 
     def run(self, ev_attn=None):
         c, i = self.capi, self.inp

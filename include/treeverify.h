@@ -64,6 +64,11 @@ extern "C" {
 #define TV_ATTN_SIMT 1      /* CUDA-core FP32 kernel (any supported shape)  */
 #define TV_ATTN_TCGEN05 2   /* tcgen05/TMEM/TMA kernel; TV_ERR_UNSUPPORTED
                                if the shape or device does not allow it   */
+/* Optional flag bit, tcgen05 kernel only: a unit split across CTAs is always
+ * merged from the pieces' published partials by the piece that finishes last,
+ * never directly from the finishing CTA's accumulator.  Same results up to
+ * rounding; for testing the second merge route. */
+#define TV_ATTN_PUBLISH_ALL 4
 
 /* Description of the last failure on this thread ("" if none). */
 const char* tv_last_error(void);
@@ -184,8 +189,10 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  * lse        device float32 [B, N, Hq] out (nullable): natural-log softmax
  *            normaliser of each row.
  * workspace  device buffer of at least tv_tree_attn_workspace_size bytes,
- *            256-byte aligned; its contents on entry are irrelevant.
- * flags      TV_ATTN_* kernel selection.
+ *            256-byte aligned; its contents on entry are irrelevant (the
+ *            tensor-core path clears its arrival counters in it with a
+ *            cudaMemsetAsync on `stream`).
+ * flags      TV_ATTN_* kernel selection, optionally | TV_ATTN_PUBLISH_ALL.
  * num_ctas   persistent grid size (0 = one wave of the current device);
  *            must equal the value given to tv_tree_attn_workspace_size.
  * status     device int32 (nullable): TV_DEV_TIMEOUT if a pipeline wait of
@@ -195,6 +202,10 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  * D = 128, G = Hq/Hkv dividing 128, G * N <= 512, block_size a multiple of 16
  * that divides 64 or is a multiple of 64, and num_blocks * Hkv * block_size
  * < 2^31; TV_ATTN_AUTO falls back to the CUDA-core kernel otherwise.
+ * TV_ERR_UNSUPPORTED as well when the work plan could reach 2^31 tiles:
+ * units x (ceil(max_blocks * block_size / 64) + 1 + c), where units =
+ * B * Hkv * ceil(G * N / rows per unit) and c is the per-unit cost in tiles
+ * (at most 6 for the tensor-core kernel, 0 for the CUDA-core one).
  */
 int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                         int64_t num_blocks, int32_t block_size,

@@ -362,8 +362,22 @@ int simt_dispatch(const AttnParams& p, int dtype, cudaStream_t stream, int* bloc
 struct AttnConfig {
   bool tc;
   int RPG, RG, U, BLK, P;
-  int64_t off_part_o, off_part_lse, bytes;
+  int64_t off_arrive, off_part_o, off_part_lse, bytes;
 };
+
+// Scratch of one call: the tile plan [U + 1] (CUDA-core path), the arrival
+// counters [P][RPG] (tcgen05 path), the partial outputs [P][2][RPG][D] and
+// their log2-sum-exps [P][2][RPG].
+void layout_workspace(AttnConfig* cfg, int D) {
+  const int64_t plan = align256((int64_t)(cfg->U + 1) * 4);
+  const int64_t arrive = align256((int64_t)cfg->P * cfg->RPG * 4);
+  const int64_t po = align256((int64_t)cfg->P * 2 * cfg->RPG * D * 4);
+  const int64_t pl = align256((int64_t)cfg->P * 2 * cfg->RPG * 4);
+  cfg->off_arrive = plan;
+  cfg->off_part_o = plan + arrive;
+  cfg->off_part_lse = plan + arrive + po;
+  cfg->bytes = plan + arrive + po + pl;
+}
 
 int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size, int num_ctas, int flags,
                 AttnConfig* cfg) {
@@ -375,7 +389,7 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
   if (block_size < 1) return fail(TV_ERR_INVALID_ARG, "tree attention: block_size %d", block_size);
   if (num_ctas < 0) return fail(TV_ERR_INVALID_ARG, "tree attention: num_ctas %d", num_ctas);
   const int sel = flags & 3;
-  if (sel == 3) return fail(TV_ERR_INVALID_ARG, "tree attention: bad kernel selection flags %d", flags);
+  if (sel == 3 || (flags & ~7)) return fail(TV_ERR_INVALID_ARG, "tree attention: bad flags %d", flags);
   DeviceInfo dev;
   int st = current_device_info(&dev);
   if (st) return st;
@@ -402,12 +416,7 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
   cfg->RG = (int)ceil_div(R, cfg->RPG);
   cfg->U = B * Hkv * cfg->RG;
   cfg->P = num_ctas > 0 ? num_ctas : dev.sm_count * per_sm;
-  const int64_t plan = align256((int64_t)(cfg->U + 1) * 4);
-  const int64_t po = align256((int64_t)cfg->P * 2 * cfg->RPG * D * 4);
-  const int64_t pl = align256((int64_t)cfg->P * 2 * cfg->RPG * 4);
-  cfg->off_part_o = plan;
-  cfg->off_part_lse = plan + po;
-  cfg->bytes = plan + po + pl;
+  layout_workspace(cfg, D);
   return TV_OK;
 }
 
@@ -469,17 +478,30 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
   p.k_tree = k_tree; p.v_tree = v_tree; p.mask = mask; p.mask_bstride = mask_bstride; p.out = out; p.lse = lse;
   char* ws = static_cast<char*>(workspace);
   p.tile_start = reinterpret_cast<int32_t*>(ws);
+  p.arrive = reinterpret_cast<uint32_t*>(ws + cfg.off_arrive);
   p.part_o = reinterpret_cast<float*>(ws + cfg.off_part_o);
   p.part_lse = reinterpret_cast<float*>(ws + cfg.off_part_lse);
   p.num_blocks = num_blocks; p.block_size = block_size; p.max_blocks = max_blocks;
   p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.D = head_dim; p.G = Hq / Hkv;
   p.R = p.G * N; p.RPG = cfg.RPG; p.RG = cfg.RG; p.U = cfg.U; p.BLK = cfg.BLK; p.P = cfg.P;
   p.unit_cost = cfg.tc ? tc_unit_cost(cfg.RPG) : 0;
+  p.direct_merge = (flags & TV_ATTN_PUBLISH_ALL) ? 0 : 1;
+  // tile indices of the plan are 32-bit
+  const int64_t unit_tiles_max = ((int64_t)max_blocks * block_size + cfg.BLK - 1) / cfg.BLK + 1 + p.unit_cost;
+  if ((int64_t)cfg.U * unit_tiles_max >= (int64_t(1) << 31))
+    return fail(TV_ERR_UNSUPPORTED, "tv_tree_attn_verify: %d units of up to %lld tiles exceed 2^31 plan tiles", cfg.U,
+                (long long)unit_tiles_max);
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = (cudaStream_t)stream;
+  if (cfg.tc) {
+    // the tcgen05 kernel plans its own slice and merges split units itself;
+    // it only needs the arrival counters at zero
+    cudaError_t e = cudaMemsetAsync(p.arrive, 0, (size_t)p.P * p.RPG * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(arrival counters)");
+    return launch_attn_tc(p, status, s);
+  }
   if ((st = launch_plan(p, s))) return st;
-  st = cfg.tc ? launch_attn_tc(p, status, s) : simt_dispatch(p, dtype, s, nullptr);
-  if (st) return st;
+  if ((st = simt_dispatch(p, dtype, s, nullptr))) return st;
   return launch_combine(p, dtype, s);
 }
 
@@ -542,8 +564,9 @@ extern "C" int tv_tree_attn_verify_static(const void* q, const void* k_cache, co
   if (B == 0) return TV_OK;
   if (num_ctas == 0) {
     // the widest grid (at most one wave) whose scratch fits the static array
-    const int64_t per_cta = align256((int64_t)2 * cfg.RPG * head_dim * 4) + align256((int64_t)2 * cfg.RPG * 4);
-    const int64_t room = (int64_t)kStaticWorkspaceBytes - align256((int64_t)(cfg.U + 1) * 4) - 512;
+    const int64_t per_cta = align256((int64_t)2 * cfg.RPG * head_dim * 4) + align256((int64_t)2 * cfg.RPG * 4) +
+                            align256((int64_t)cfg.RPG * 4);
+    const int64_t room = (int64_t)kStaticWorkspaceBytes - align256((int64_t)(cfg.U + 1) * 4) - 768;
     int fit = room > 0 ? (int)(room / per_cta) : 0;
     if (fit < 1)
       return fail(TV_ERR_WORKSPACE, "tv_tree_attn_verify_static: %d units need more than the %zu-byte static scratch",

@@ -17,6 +17,14 @@
 // output and its log2-sum-exp to one of its two slots (0 = the CTA's first
 // unit, 1 = its last) and the combine kernel merges the pieces.  Units inside
 // one slice are written to the output directly.
+//
+// The CUDA-core kernel reads the plan from tile_start[] (filled by the plan
+// kernel) and leaves split units to the combine kernel.  The tcgen05 kernels
+// derive their slice from seq_lens themselves (all units of one request have
+// the same tile count, so the prefix sums run over requests) and merge split
+// units in their own epilogue: each piece counts its real tiles into a per-row
+// arrival counter, and the piece that brings the count to the unit's total
+// merges that row.
 #pragma once
 
 #include <cstdint>
@@ -40,6 +48,7 @@ struct AttnParams {
   int32_t* tile_start;  // [U + 1]
   float* part_o;        // [P][2][RPG][D]
   float* part_lse;      // [P][2][RPG]
+  uint32_t* arrive;     // [P][RPG] arrival counters of split units, by first CTA (tcgen05 kernels)
   int64_t num_blocks;
   int block_size;
   int max_blocks;
@@ -51,6 +60,7 @@ struct AttnParams {
   int BLK;  // KV positions per tile
   int P;    // persistent CTAs
   int unit_cost;  // extra virtual tiles charged per unit (its fixed start/finish cost)
+  int direct_merge;  // tcgen05: the last piece may merge straight from its accumulator
   float scale_log2;  // softmax scale * log2(e)
 };
 

@@ -44,7 +44,9 @@
 namespace tv { namespace trace {
 constexpr int kEvents = 16, kTiles = 512;
 __device__ unsigned long long g_trace[kEvents][kTiles];
-__device__ unsigned long long g_cta_time[1024][4];  // globaltimer at entry / exit, segments, first unit
+// per CTA: globaltimer at entry, exit; segments; first unit; last epilogue
+// start, end; total epilogue ns
+__device__ unsigned long long g_cta_time[1024][8];
 }}  // namespace tv::trace
 #define TV_TRACE(ev, tile) \
   do { if (blockIdx.x == 0 && (tile) < tv::trace::kTiles) tv::trace::g_trace[ev][tile] = clock64(); } while (0)
@@ -56,9 +58,14 @@ __device__ unsigned long long g_cta_time[1024][4];  // globaltimer at entry / ex
       tv::trace::g_cta_time[blockIdx.x][k] = t_;                                                          \
     }                                                                                                     \
   } while (0)
+#define TV_TRACE_ROW0(k, v)                                                  \
+  do {                                                                      \
+    if (row == 0 && blockIdx.x < 1024) tv::trace::g_cta_time[blockIdx.x][k] = (v); \
+  } while (0)
 #else
 #define TV_TRACE(ev, tile) do { } while (0)
 #define TV_TRACE_CTA(k) do { } while (0)
+#define TV_TRACE_ROW0(k, v) do { } while (0)
 #endif
 
 namespace tv {
@@ -260,6 +267,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// 16 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : TV_R8(0), TV_R8(8)
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -329,41 +345,280 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // ---------------------------------------------------------------- work walk
 
+// This CTA's slice of the tile sequence and the unit holding its first tile.
+struct SlicePlan {
+  int T, t0, t1;
+  int us0;  // first (virtual) tile of unit u0
+  int u0;
+};
+
+// Tiles of every unit of request b, virtual ones included.
+__device__ __forceinline__ int unit_tiles(const AttnParams& p, int b) {
+  return (clamp_len(p, b) + kBlk - 1) / kBlk + 1 + p.unit_cost;
+}
+
+// Warp-collective.  The units of request b are consecutive and all have
+// unit_tiles(b) tiles, so the tile prefix sums are taken over requests.
+__device__ void plan_slice(const AttnParams& p, int lane, SlicePlan& sp) {
+  const int64_t upb = (int64_t)p.Hkv * p.RG;
+  long long tot = 0;
+  for (int b = lane; b < p.B; b += 32) tot += unit_tiles(p, b);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const int T = (int)(tot * upb);  // the host bounds the plan below 2^31 tiles
+  const int t0 = (int)cta_start(blockIdx.x, T, p.P), t1 = (int)cta_start(blockIdx.x + 1, T, p.P);
+  int u0 = p.U, us0 = T;
+  if (t0 < t1) {
+    long long carry = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      const int nt = b < p.B ? unit_tiles(p, b) : 0;
+      const long long n = (long long)nt * upb;
+      long long incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && carry + incl > t0);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        const long long start = __shfl_sync(0xffffffffu, carry + incl - n, src);
+        const int ntb = __shfl_sync(0xffffffffu, nt, src);
+        const int k = (int)((t0 - start) / ntb);
+        u0 = (int)((base + src) * upb + k);
+        us0 = (int)(start + (long long)k * ntb);
+        break;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (lane == 0) {
+    sp.T = T;
+    sp.t0 = t0;
+    sp.t1 = t1;
+    sp.u0 = u0;
+    sp.us0 = us0;
+  }
+}
+
 struct Segment {
   int u, a, e, n;  // unit, local real tiles [a, e) of its n real tiles
   int b, kvh, rg, L;
-  int64_t real_start;  // index of the unit's first real tile in the plan
+  int real_start;  // index of the unit's first real tile in the plan
 };
 
 struct Walk {
-  int64_t t0, t1;
+  int t0, t1, us;
   int u;
-  __device__ Walk(const AttnParams& p) {
-    const int64_t T = p.tile_start[p.U];
-    t0 = cta_start(blockIdx.x, T, p.P);
-    t1 = cta_start(blockIdx.x + 1, T, p.P);
-    u = (t0 < t1) ? find_unit(p.tile_start, p.U, t0) : p.U;
-  }
+  __device__ explicit Walk(const SlicePlan& sp) : t0(sp.t0), t1(sp.t1), us(sp.us0), u(sp.u0) {}
   // Next unit with real tiles in this CTA's slice (units whose slice part is
   // only their virtual cost tiles are skipped).
   __device__ bool next(const AttnParams& p, Segment& s) {
-    while (u < p.U && p.tile_start[u] < t1) {
-      const int64_t us = p.tile_start[u] + p.unit_cost, ue = p.tile_start[u + 1];  // real tiles
-      const int64_t a = max(t0, us), e = min(t1, ue);
+    while (u < p.U && us < t1) {
+      int b, kvh, rg;
+      unit_coords(p, u, b, kvh, rg);
+      const int L = clamp_len(p, b);
+      const int rs = us + p.unit_cost, ue = rs + (L + kBlk - 1) / kBlk + 1;  // real tiles [rs, ue)
+      const int a = max(t0, rs), e = min(t1, ue);
       const int uu = u++;
+      us = ue;
       if (a >= e) continue;
       s.u = uu;
-      s.a = (int)(a - us);
-      s.e = (int)(e - us);
-      s.n = (int)(ue - us);
-      s.real_start = us;
-      unit_coords(p, uu, s.b, s.kvh, s.rg);
-      s.L = clamp_len(p, s.b);
+      s.a = a - rs;
+      s.e = e - rs;
+      s.n = ue - rs;
+      s.real_start = rs;
+      s.b = b;
+      s.kvh = kvh;
+      s.rg = rg;
+      s.L = L;
       return true;
     }
     return false;
   }
 };
+
+// ---------------------------------------------------------------- output of a finished segment
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* ptr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
+}
+
+// The pieces of a split unit: CTAs c0..c1 whose slice is not empty.  Each
+// wrote its normalised partial rows and log2-sum-exp to slot 0 of its two
+// slots, except c0 when the unit began after the start of its slice (slot 1).
+struct Pieces {
+  int T, P, c0, c1;
+  bool c0_slot1;
+  __device__ Pieces(const SlicePlan& sp, int P_, int real_start, int n_real)
+      : T(sp.T), P(P_) {
+    c0 = (int)cta_of(real_start, T, P);
+    c1 = (int)cta_of(real_start + n_real - 1, T, P);
+    c0_slot1 = cta_start(c0, T, P) < real_start;
+  }
+  __device__ bool present(int c) const { return T >= P || cta_start(c, T, P) < cta_start(c + 1, T, P); }
+  __device__ int64_t slot(int c) const { return (int64_t)c * 2 + ((c == c0 && c0_slot1) ? 1 : 0); }
+};
+
+// Both merge routes below take the same arithmetic in the same order (pieces
+// c0..c1, the finishing CTA's piece as the float32 values it would publish),
+// so the merged row does not depend on which piece finished last.
+
+// (mx, z): maximum and normaliser of the pieces' log2-sum-exps; with kSelf the
+// piece of CTA `self` is self_lse instead of its published value.
+template <bool kSelf>
+__device__ __forceinline__ void piece_stats(const AttnParams& p, const Pieces& pc, int self, float self_lse, int row,
+                                            float& mx, float& z) {
+  mx = -INFINITY;
+  for (int c = pc.c0; c <= pc.c1; ++c)
+    if (pc.present(c)) mx = fmaxf(mx, (kSelf && c == self) ? self_lse : __ldcg(p.part_lse + pc.slot(c) * p.RPG + row));
+  z = 0.f;
+  for (int c = pc.c0; c <= pc.c1; ++c)
+    if (pc.present(c))
+      z += exp2f(((kSelf && c == self) ? self_lse : __ldcg(p.part_lse + pc.slot(c) * p.RPG + row)) - mx);
+}
+
+// acc += sum over pieces of 2^(lse_c - mx) / z * O_c[row][col0 .. col0 + 15]
+// (with kSelf, CTA self's columns are selfv).
+template <bool kSelf>
+__device__ __forceinline__ void accum_pieces(float (&acc)[16], const AttnParams& p, const Pieces& pc, int self,
+                                             const float (&selfv)[16], float self_lse, int row, int col0, float mx,
+                                             float zinv) {
+  for (int c = pc.c0; c <= pc.c1; ++c) {
+    if (!pc.present(c)) continue;
+    const int64_t sr = pc.slot(c) * p.RPG + row;
+    if (kSelf && c == self) {
+      const float w = exp2f(self_lse - mx) * zinv;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = fmaf(w, selfv[j], acc[j]);
+      continue;
+    }
+    const float w = exp2f(__ldcg(p.part_lse + sr) - mx) * zinv;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + sr * kD + col0);
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + j);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[4 * j] = fmaf(w, v[j].x, acc[4 * j]);
+      acc[4 * j + 1] = fmaf(w, v[j].y, acc[4 * j + 1]);
+      acc[4 * j + 2] = fmaf(w, v[j].z, acc[4 * j + 2]);
+      acc[4 * j + 3] = fmaf(w, v[j].w, acc[4 * j + 3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_bf16_16(__nv_bfloat16* dst, const float (&acc)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint4 v;
+    v.x = pack_bf16(acc[8 * j + 0], acc[8 * j + 1]);
+    v.y = pack_bf16(acc[8 * j + 2], acc[8 * j + 3]);
+    v.z = pack_bf16(acc[8 * j + 4], acc[8 * j + 5]);
+    v.w = pack_bf16(acc[8 * j + 6], acc[8 * j + 7]);
+    d[j] = v;
+  }
+}
+
+// Writes this thread's row of a finished segment; warp-collective (reads the
+// row's O accumulator, 128 TMEM columns at tO, 16 at a time).  O / l and its log2-sum-exp
+// m + log2 l are exact for this CTA's share of the unit's keys.
+//  * whole unit in this slice: O / l straight to the output;
+//  * split unit, every other piece already published (the arrival counter
+//    already holds all other real tiles): merge here, from TMEM and the
+//    others' partials;
+//  * otherwise publish the partial, count this piece's tiles in, and merge
+//    from memory if that completed the count (a piece that finished in the
+//    meantime saw the count short and left the merge to this one).
+__device__ __forceinline__ void finish_row_impl(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
+                                                bool valid_row, int64_t orow, uint32_t tO, float m_run, float l) {
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  constexpr float kLn2 = 0.69314718055994530942f;
+  const float inv = 1.f / l;
+  const float lse2 = m_run + log2f(l);
+  const bool complete = (s.a == 0 && s.e == s.n);
+  const Pieces pc(sp, p.P, s.real_start, s.n);
+  const int self = blockIdx.x;
+  uint32_t* ctr = p.arrive + (int64_t)pc.c0 * p.RPG + row;
+  const uint32_t mine = (uint32_t)(s.e - s.a);
+  bool direct = false;
+  float mx = lse2, z = 1.f;
+  if (!complete && valid_row && p.direct_merge) {
+    direct = ld_acquire_u32(ctr) + mine == (uint32_t)s.n;
+    if (direct) piece_stats<true>(p, pc, self, lse2, row, mx, z);
+  }
+  const float zinv = 1.f / z;
+  const int64_t srow = pc.slot(self) * p.RPG + row;
+#pragma unroll 1
+  for (int c = 0; c < kD; c += 16) {
+    uint32_t r[16];
+    __syncwarp();
+    tmem_ld16(tO + c, r);
+    tmem_ld_wait();
+    if (!valid_row) continue;
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) * inv;
+    if (complete) {
+      store_bf16_16(out + orow * kD + c, v);
+    } else if (direct) {
+      float acc[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+      accum_pieces<true>(acc, p, pc, self, v, lse2, row, c, mx, zinv);
+      store_bf16_16(out + orow * kD + c, acc);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + c);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+  }
+  __syncwarp();
+  if (!valid_row) return;
+  if (complete || direct) {
+    if (p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+    return;
+  }
+  p.part_lse[srow] = lse2;
+  if (atom_add_acq_rel(ctr, mine) + mine != (uint32_t)s.n) return;
+  // every piece is published: merge from memory
+  piece_stats<false>(p, pc, -1, 0.f, row, mx, z);
+  const float zinv2 = 1.f / z;
+#pragma unroll 1
+  for (int c = 0; c < kD; c += 16) {
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    accum_pieces<false>(acc, p, pc, -1, acc, 0.f, row, c, mx, zinv2);
+    store_bf16_16(out + orow * kD + c, acc);
+  }
+  if (p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+}
+
+__device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
+                                           bool valid_row, int64_t orow, uint32_t tO, float m_run, float l) {
+#ifdef TV_TC_TRACE
+  const unsigned long long t_in = globaltimer();
+  TV_TRACE_ROW0(4, t_in);
+#endif
+  finish_row_impl(p, sp, s, row, valid_row, orow, tO, m_run, l);
+#ifdef TV_TC_TRACE
+  const unsigned long long t_out = globaltimer();
+  TV_TRACE_ROW0(5, t_out);
+  if (row == 0 && blockIdx.x < 1024) tv::trace::g_cta_time[blockIdx.x][6] += t_out - t_in;
+#endif
+}
+
 
 struct TcMaps {
   CUtensorMap kc, vc, kt, vt;
@@ -376,8 +631,8 @@ struct TcMaps {
 // single warp cannot keep a two-M-tile CTA fed); producer 0 posts the stage's
 // byte count.
 template <int kStages, int kProducers = 1>
-__device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& maps, Bars& bars, uint32_t sK,
-                                             uint32_t sV, int lane, int32_t* status, int prod = 0) {
+__device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePlan& sp, const TcMaps& maps, Bars& bars,
+                                             uint32_t sK, uint32_t sV, int lane, int32_t* status, int prod = 0) {
     // ------------------------------------------------------------ TMA producer
     const int bs = p.block_size;
     const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
@@ -385,7 +640,7 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const TcMaps& 
     const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
     uint32_t g = 0;
     bool ok = true;
-    Walk walk(p);
+    Walk walk(sp);
     Segment s;
     while (ok && walk.next(p, s)) {
       // Block-table entries of this unit are read in 32-entry windows, one
@@ -470,11 +725,12 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t sK = base + C::kOffK, sV = base + C::kOffV;
 
+  TV_TRACE_CTA(0);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  {
-    Walk probe(p);
-    if (probe.t0 >= probe.t1) return;  // empty slice: uniform exit before any setup
-  }
+  __shared__ SlicePlan sp;
+  if (warp == 0) plan_slice(p, lane, sp);
+  __syncthreads();
+  if (sp.t0 >= sp.t1) return;  // empty slice: uniform exit before any setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
@@ -501,7 +757,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp == 0) {
-    run_producer<C::kStages>(p, maps, bars, sK, sV, lane, status);
+    run_producer<C::kStages>(p, sp, maps, bars, sK, sV, lane, status);
   } else if (warp >= 1 && warp < 1 + M) {
     // ------------------------------------------------------------ MMA issuer of M tile m
     // Per tile g: O_m += P_m(g-1) V(g-1), then S_m(g) = Q_m K(g)^T.  The
@@ -517,7 +773,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       uint32_t g = 0;
       int seg_i = 0;
       bool ok = true;
-      Walk walk(p);
+      Walk walk(sp);
       Segment s;
       auto issue_pv = [&](int stage, bool accumulate) {
         const uint32_t lo = desc_lo(sV + stage * kKVTileBytes, kKVHalfBytes);  // MN-major V: LBO = next 64 columns
@@ -578,10 +834,9 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
     const uint32_t tQ = lane_addr + C::col_q(m);
     const uint32_t tO = lane_addr + C::col_o(m);
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     uint32_t g = 0;
     bool ok = true;
-    Walk walk(p);
+    Walk walk(sp);
     Segment s;
     while (ok && walk.next(p, s)) {
       const int unit_row = s.rg * p.RPG + row;  // row within the (b, kv head) group
@@ -685,47 +940,12 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
       if (!ok) break;
       fence_after();
-      const bool complete = (s.a == 0 && s.e == s.n);
-      const int slot = (walk.t0 < s.real_start) ? 1 : 0;
-      const float inv = 1.f / l;
-      const float lse2 = m_run + log2f(l);
-      const int64_t srow = ((int64_t)blockIdx.x * 2 + slot) * p.RPG + row;
-#pragma unroll 1
-      for (int c = 0; c < kD; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tO + c, r);
-        tmem_ld_wait();
-        if (!valid_row) continue;
-        if (complete) {
-          uint4* dst = reinterpret_cast<uint4*>(out + orow * kD + c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(r[8 * j + 0]) * inv, __uint_as_float(r[8 * j + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv);
-            dst[j] = v;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + c);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
-                                 __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
-        }
-      }
-      if (valid_row) {
-        if (complete) {
-          if (p.lse) p.lse[orow] = lse2 * 0.69314718055994530942f;
-        } else {
-          p.part_lse[srow] = lse2;
-        }
-      }
+      finish_row(p, sp, s, row, valid_row, orow, tO, m_run, l);
       fence_before();
     }
   }
 
+  TV_TRACE_CTA(1);
   fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -774,10 +994,10 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 
   TV_TRACE_CTA(0);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  {
-    Walk probe(p);
-    if (probe.t0 >= probe.t1) return;
-  }
+  __shared__ SlicePlan sp;
+  if (warp == 0) plan_slice(p, lane, sp);
+  __syncthreads();
+  if (sp.t0 >= sp.t1) return;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
@@ -806,7 +1026,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   constexpr uint32_t hi = desc_hi(1024);
 
   if (warp < C::kProducers) {
-    run_producer<C::kStages, C::kProducers>(p, maps, bars, sK, sV, lane, status, warp);
+    run_producer<C::kStages, C::kProducers>(p, sp, maps, bars, sK, sV, lane, status, warp);
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ S_m = Q_m K^T issuer
     const int m = warp - 2;
@@ -816,7 +1036,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       uint32_t g = 0;
       int seg_i = 0;
       bool ok = true;
-      Walk walk(p);
+      Walk walk(sp);
       Segment s;
       while (ok && walk.next(p, s)) {
         ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
@@ -860,7 +1080,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
       uint32_t g = 0;
       bool ok = true;
-      Walk walk(p);
+      Walk walk(sp);
       Segment s;
       while (ok && walk.next(p, s)) {
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
@@ -890,10 +1110,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = lane_addr + C::col_s(m), tP = lane_addr + C::col_p(m), tO = lane_addr + C::col_o(m);
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     uint32_t g = 0;
     bool ok = true;
-    Walk walk(p);
+    Walk walk(sp);
     Segment s;
 #ifdef TV_TC_TRACE
     int n_segs_traced = 0;
@@ -1052,43 +1271,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
       Segment s_next;
       const bool have_next = walk.next(p, s_next);
-      const bool complete = (s.a == 0 && s.e == s.n);
-      const int slot = (walk.t0 < s.real_start) ? 1 : 0;
-      const float inv = 1.f / l;
-      const float lse2 = m_run + log2f(l);
-      const int64_t srow = ((int64_t)blockIdx.x * 2 + slot) * p.RPG + row;
-#pragma unroll 1
-      for (int c = 0; c < kD; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tO + c, r);
-        tmem_ld_wait();
-        if (!valid_row) continue;
-        if (complete) {
-          uint4* dst = reinterpret_cast<uint4*>(out + orow * kD + c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(r[8 * j + 0]) * inv, __uint_as_float(r[8 * j + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv);
-            dst[j] = v;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + c);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
-                                 __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
-        }
-      }
-      if (valid_row) {
-        if (complete) {
-          if (p.lse) p.lse[orow] = lse2 * 0.69314718055994530942f;
-        } else {
-          p.part_lse[srow] = lse2;
-        }
-      }
+      finish_row(p, sp, s, row, valid_row, orow, tO, m_run, l);
       fence_before();
       if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       if (have_next) {  // every MMA of the finished unit has completed; its Q rows are warm in L2

@@ -134,6 +134,34 @@ def test_mask_sensitive_tree_keys_dominate():
         _check_all(inp, paths, BF16_TOL, flags)
 
 
+@pytest.mark.parametrize("G,N", [(4, 26), (4, 64)])
+def test_split_unit_merge_routes(G, N):
+    """Units cut into many pieces (long prefixes, wide grids, grids wider than
+    the plan so that some slices are empty).  The tensor-core kernel merges a
+    split row either in the last piece straight from its accumulator, or from
+    every piece's published partial (forced by TV_ATTN_PUBLISH_ALL); both
+    routes must match the oracle and each other bit for bit."""
+    if not tc_available(2 * G, 2, N):
+        pytest.skip("tensor-core kernel unavailable for this shape")
+    rng = np.random.default_rng(140 + G + N)
+    paths = W.random_rank_paths(N, 6, rng)
+    for lens, grids in (([3000, 70, 1500], (2, 7, 40, 152)), ([70, 0, 10], (300,))):
+        w = _workload(3, 2 * G, 2, 128, "bf16", 16, N, 141 + N)
+        inp = W.attention_inputs(w, device="cuda", seq_lens=lens)
+        pairs = [(b, i) for b in range(3) for i in range(N)]
+        ref = oracle_rows(inp, paths, pairs)
+        for num_ctas in grids:
+            res = []
+            for extra in (0, capi.TV_ATTN_PUBLISH_ALL):
+                out, lse = gpu_pipeline(inp, paths, flags=capi.TV_ATTN_TCGEN05 | extra, num_ctas=num_ctas,
+                                        want_lse=True)
+                assert max_err(out, ref, pairs) <= BF16_TOL, (lens, num_ctas, extra)
+                lse_g = to_np(lse)
+                assert max(float(np.abs(lse_g[b, i] - ref[(b, i)][1]).max()) for b, i in pairs) <= 20 * BF16_TOL
+                res.append((out, lse))
+            assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1]), (lens, num_ctas)
+
+
 def test_deterministic_and_kernel_agreement():
     w = W.WORKLOADS["gqa_b8_l512_2048_n26"]
     inp = W.attention_inputs(w, device="cuda")
