@@ -4,17 +4,22 @@
 A step is one pass of the whole path over one batch: tree mask and positions
 (tv_tree_mask), depth-indexed RoPE of the tree queries and keys
 (tv_rope_apply), tree attention over the paged KV cache (tv_tree_attn_verify:
-plan, split kernel, combine) and tree acceptance (tv_tree_accept_greedy from
-the target logits, or tv_tree_accept_sample).  The static tree's rank paths
-are built once with tv_tree_build, as a static tree is in serving.
+one persistent tcgen05 kernel, or plan + CUDA-core kernel + combine) and tree
+acceptance (tv_tree_accept_greedy from the target logits, or
+tv_tree_accept_sample).  The static tree's rank paths are built once with
+tv_tree_build, as a static tree is in serving.
 
 Reported (one JSON line on rank 0):
   value       tree-verify nodes/s (B * N per step) over the timed steps with
-              every input resident in HBM, max over ranks;
+              every input resident in HBM, max over ranks; the step is
+              captured once as a CUDA graph and replayed (--eager: direct
+              calls, host work between the launches included);
   roofline    the tree-attention call: algorithmic bytes (prefix K+V + tree
-              K+V + Q + O) / its CUDA-event time, against the measured HBM peak;
-  e2e         the same metric through the public API with the step's inputs
-              copied from pinned host memory and the accepted tokens read back;
+              K+V + Q + O) / its CUDA-event time (graph replays of that call
+              alone), against the measured HBM peak;
+  e2e         the same metric through the public API, called directly (no
+              graph), with the step's inputs copied from pinned host memory
+              and the accepted tokens read back;
   cpu_baseline the CPU oracle timed on a bounded sample of the same workload.
 With --impl reference the CPU oracle itself is timed (the reference arm).
 """
@@ -59,6 +64,7 @@ def parse_args():
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
 
@@ -283,15 +289,19 @@ class Step:
                 uses_tc = False
         self.launches = 2 + (1 if uses_tc else 3) + (1 if w.accept != "none" else 0)
 
+    def run_attn(self):
+        i = self.inp
+        self.capi.tv_tree_attn_verify(i["q"], i["k_cache"], i["v_cache"], i["block_table"], self.seq_lens,
+                                      i["k_tree"], i["v_tree"], self.mask, out=self.out, workspace=self.ws,
+                                      num_ctas=self.num_ctas, flags=self.flags)
+
     def run(self, ev_attn=None):
         c, i = self.capi, self.inp
         c.tv_tree_mask(self.parent, self.seq_lens, mask=self.mask, depth=self.depth, pos=self.pos)
         c.tv_rope_apply(i["q"], i["k_tree"], self.pos, self.table)
         if ev_attn:
             ev_attn[0].record()
-        c.tv_tree_attn_verify(i["q"], i["k_cache"], i["v_cache"], i["block_table"], self.seq_lens, i["k_tree"],
-                              i["v_tree"], self.mask, out=self.out, workspace=self.ws, num_ctas=self.num_ctas,
-                              flags=self.flags)
+        self.run_attn()
         if ev_attn:
             ev_attn[1].record()
         if self.greedy is not None:
@@ -329,6 +339,24 @@ def run_ours(args, world, rank, local):
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    graphs = None
+    if not args.eager:
+        # The step (and, for the roofline, the attention call alone) captured
+        # once as CUDA graphs and replayed: the same kernels as an eager call,
+        # without the per-call host work between them.
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            st.run()
+        torch.cuda.current_stream().wait_stream(side)
+        g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            st.run()
+        with torch.cuda.graph(g_attn):
+            st.run_attn()
+        for _ in range(args.warmup):
+            g_step.replay()
+        graphs = (g_step, g_attn)
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device())
     with sampler:
@@ -336,8 +364,18 @@ def run_ours(args, world, rank, local):
             if flush is not None:
                 flush.zero_()
             evs[k][0].record()
-            st.run(eva[k])
+            if graphs:
+                graphs[0].replay()
+            else:
+                st.run(eva[k])
             evs[k][1].record()
+        if graphs:
+            for k in range(args.steps):
+                if flush is not None:
+                    flush.zero_()
+                eva[k][0].record()
+                graphs[1].replay()
+                eva[k][1].record()
         torch.cuda.synchronize()
     clocks = sampler.summary()
     step_ms = [a.elapsed_time(b) for a, b in evs]
@@ -384,7 +422,7 @@ def run_ours(args, world, rank, local):
     achieved = st.attn_bytes / (attn_mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": "tv_tree_attn_verify (plan + split kernel + combine)",
+                "kernel": "tv_tree_attn_verify (tcgen05: counter memset + one persistent kernel)",
                 "algorithmic_bytes_per_call": int(st.attn_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
                 "attn_ms_mean": round(attn_mean_ms, 4)}
 
@@ -407,7 +445,8 @@ def run_ours(args, world, rank, local):
                        "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab,
                        "l2": ("L2 flushed between steps" if flush is not None
                               else f"inputs larger than L2 ({ws_bytes / 2**30:.2f} GiB per step)"),
-                       "kernel_flags": args.flags, "parallelism": f"replicas x{world} (requests sharded)"},
+                       "kernel_flags": args.flags, "parallelism": f"replicas x{world} (requests sharded)",
+                       "timing": "eager calls" if args.eager else "CUDA graph replays of the step"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": st.launches * args.steps,
             "kv_read_gbs": round(achieved, 1), "kv_read_frac_of_peak": round(achieved / peak, 4),

@@ -350,7 +350,14 @@ struct SlicePlan {
   int T, t0, t1;
   int us0;  // first (virtual) tile of unit u0
   int u0;
+  int P;    // slices the plan is cut into (CTAs from P on have no work)
 };
+
+// Fewest tiles a slice gets: a small plan goes to fewer CTAs rather than
+// cutting every unit into many pieces whose merge costs more than it saves.
+#ifndef TV_MIN_SLICE_TILES
+#define TV_MIN_SLICE_TILES 12
+#endif
 
 // Tiles of every unit of request b, virtual ones included.
 __device__ __forceinline__ int unit_tiles(const AttnParams& p, int b) {
@@ -366,7 +373,10 @@ __device__ void plan_slice(const AttnParams& p, int lane, SlicePlan& sp) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const int T = (int)(tot * upb);  // the host bounds the plan below 2^31 tiles
-  const int t0 = (int)cta_start(blockIdx.x, T, p.P), t1 = (int)cta_start(blockIdx.x + 1, T, p.P);
+  int P = (T + TV_MIN_SLICE_TILES - 1) / TV_MIN_SLICE_TILES;
+  P = P < 1 ? 1 : (P > p.P ? p.P : P);
+  const int c = blockIdx.x;
+  const int t0 = c < P ? (int)cta_start(c, T, P) : T, t1 = c < P ? (int)cta_start(c + 1, T, P) : T;
   int u0 = p.U, us0 = T;
   if (t0 < t1) {
     long long carry = 0;
@@ -395,6 +405,7 @@ __device__ void plan_slice(const AttnParams& p, int lane, SlicePlan& sp) {
   }
   if (lane == 0) {
     sp.T = T;
+    sp.P = P;
     sp.t0 = t0;
     sp.t1 = t1;
     sp.u0 = u0;
@@ -459,8 +470,7 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* ptr, uint32_t v) 
 struct Pieces {
   int T, P, c0, c1;
   bool c0_slot1;
-  __device__ Pieces(const SlicePlan& sp, int P_, int real_start, int n_real)
-      : T(sp.T), P(P_) {
+  __device__ Pieces(const SlicePlan& sp, int real_start, int n_real) : T(sp.T), P(sp.P) {
     c0 = (int)cta_of(real_start, T, P);
     c1 = (int)cta_of(real_start + n_real - 1, T, P);
     c0_slot1 = cta_start(c0, T, P) < real_start;
@@ -547,7 +557,7 @@ __device__ __forceinline__ void finish_row_impl(const AttnParams& p, const Slice
   const float inv = 1.f / l;
   const float lse2 = m_run + log2f(l);
   const bool complete = (s.a == 0 && s.e == s.n);
-  const Pieces pc(sp, p.P, s.real_start, s.n);
+  const Pieces pc(sp, s.real_start, s.n);
   const int self = blockIdx.x;
   uint32_t* ctr = p.arrive + (int64_t)pc.c0 * p.RPG + row;
   const uint32_t mine = (uint32_t)(s.e - s.a);
