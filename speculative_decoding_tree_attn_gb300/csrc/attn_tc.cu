@@ -42,7 +42,7 @@
 // Development aid: clock64 stamps of pipeline events of CTA 0, one slot per
 // (event, tile).  Not part of the product build.
 namespace tv { namespace trace {
-constexpr int kEvents = 16, kTiles = 512;
+constexpr int kEvents = 32, kTiles = 512;
 __device__ unsigned long long g_trace[kEvents][kTiles];
 // per CTA: globaltimer at entry, exit; segments; first unit; last epilogue
 // start, end; total epilogue ns
@@ -713,6 +713,23 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePla
                  &bars.kv_full[stage]);
         }
         __syncwarp();
+        if (prod == 0 && lane == 0) TV_TRACE(31, g);
+      }
+      if (ok && s.a == 0 && s.e < s.n) {
+        // This slice holds the head of a split unit and finishes it last (the
+        // other pieces start their slices with it), merging their published
+        // partials in its epilogue: pull them into L2 while the last tiles run.
+        const Pieces pc(sp, s.real_start, s.n);
+        const int64_t bytes = (int64_t)p.RPG * kD * 4;
+        for (int c = pc.c0 + 1; c <= pc.c1; ++c) {
+          if (!pc.present(c)) continue;
+          const char* po = reinterpret_cast<const char*>(p.part_o + pc.slot(c) * p.RPG * kD);
+          for (int64_t off = (int64_t)(prod * 32 + lane) * 128; off < bytes; off += kProducers * 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(po + off));
+          const char* pl = reinterpret_cast<const char*>(p.part_lse + pc.slot(c) * p.RPG);
+          for (int off = (prod * 32 + lane) * 128; off < p.RPG * 4; off += kProducers * 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(pl + off));
+        }
       }
     }
     // drain: every load this warp issued has landed before the CTA exits
@@ -977,8 +994,12 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
 //    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
 struct PairCfg {
   static constexpr int kStages = 6;
-  static constexpr int kProducers = 2;
-  static constexpr int kThreads = 32 * 14;  // 2 TMA, 4 issuers, 2 softmax warpgroups
+  // Warps 0-3 issue TMA, 4-7 issue MMAs (S_0, S_1, PV_0, PV_1), 8-15 are the
+  // two softmax warpgroups: warp w runs on sub-partition w % 4, so each
+  // sub-partition carries one producer, one issuer and two softmax warps.
+  static constexpr int kProducers = 4;
+  static constexpr int kThreads = 32 * 16;
+  static constexpr int kAllocWarp = 4;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
@@ -989,7 +1010,7 @@ struct PairCfg {
   static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
   static constexpr uint32_t kColQ0 = 192;
   static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
-  static constexpr int kSoftmaxWarp0 = 6;
+  static constexpr int kSoftmaxWarp0 = 8;
 };
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -1023,7 +1044,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 2) {
+  if (warp == C::kAllocWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
                  "r"(C::kTmemCols)
                  : "memory");
@@ -1037,9 +1058,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 
   if (warp < C::kProducers) {
     run_producer<C::kStages, C::kProducers>(p, sp, maps, bars, sK, sV, lane, status, warp);
-  } else if (warp == 2 || warp == 3) {
+  } else if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ S_m = Q_m K^T issuer
-    const int m = warp - 2;
+    const int m = warp - 4;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
       const uint32_t dS = tmem + C::col_s(m);
@@ -1056,9 +1077,11 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          if (m == 0) TV_TRACE(29, g);
           if (ok && g > 0) ok = mbar_wait(&bars.s_free[m], (g - 1) & 1, &bars, status);
           if (!ok) break;
           fence_after();
+          if (m == 0) TV_TRACE(30, g);
           const uint32_t blo = desc_lo(sK + stage * kKVTileBytes, 0);
           if (m == 0) {
             const uint32_t aQ = tmem + C::kColQ0;
@@ -1082,9 +1105,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 4 || warp == 5) {
+  } else if (warp == 6 || warp == 7) {
     // ------------------------------------------------------------ O_m += P_m V issuer
-    const int m = warp - 4;
+    const int m = warp - 6;
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(128, kD, true);
       const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
@@ -1275,20 +1298,23 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         if (rl == 0) TV_TRACE(9 + 4 * m, g);
       }
       if (!ok) break;
-      ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
-      if (!ok) break;
-      fence_after();
-      if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
+      // The next unit's Q goes in first (its S_m MMAs then run during this
+      // epilogue): this unit's S_m MMAs have all completed -- the softmax has
+      // read every S_m tile -- and its rows are warm in L2.
       Segment s_next;
       const bool have_next = walk.next(p, s_next);
-      finish_row(p, sp, s, row, valid_row, orow, tO, m_run, l);
-      fence_before();
-      if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
-      if (have_next) {  // every MMA of the finished unit has completed; its Q rows are warm in L2
+      if (have_next) {
         fetch_q(s_next);
         place_q();
       }
       if (m == 0 && rl == 0) TV_TRACE(15, g - 1);
+      ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
+      if (!ok) break;
+      fence_after();
+      if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
+      finish_row(p, sp, s, row, valid_row, orow, tO, m_run, l);
+      fence_before();
+      if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       s = s_next;
       have = have_next;
     }
@@ -1297,7 +1323,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   TV_TRACE_CTA(1);
   fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == C::kAllocWarp) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
