@@ -191,10 +191,21 @@ __device__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, Bars* bars, int32
   }
 }
 
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+// Cache-hinted 2-D load: the prefix K/V stream is read once, so its lines
+// are marked first to leave L2 (keeping Q rows, ancestor rows and the
+// partials of split units resident while the stream passes through).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_2d_stream(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                              uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], "
+      "[%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 
@@ -648,6 +659,7 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePla
     const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
     const int nsub = kBlk / br;
     const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
+    const uint64_t pol = policy_evict_first();
     uint32_t g = 0;
     bool ok = true;
     Walk walk(sp);
@@ -709,8 +721,8 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePla
         } else if (j < 4 * nsub) {
           int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
           if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
-          tma_2d((is_v ? dv : dk) + h * kKVHalfBytes + sub * br * 128, is_v ? &maps.vc : &maps.kc, h * 64, (int)y,
-                 &bars.kv_full[stage]);
+          tma_2d_stream((is_v ? dv : dk) + h * kKVHalfBytes + sub * br * 128, is_v ? &maps.vc : &maps.kc, h * 64,
+                        (int)y, &bars.kv_full[stage], pol);
         }
         __syncwarp();
         if (prod == 0 && lane == 0) TV_TRACE(31, g);
