@@ -143,7 +143,8 @@ int tv_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base
  * pos     device int32 [B, N] (from tv_tree_mask).
  * cos_sin device float32 [max_pos, 2, D/2] from tv_rope_table.
  * A position outside [0, max_pos) leaves the row untouched and sets
- * TV_DEV_BAD_POSITION.  D must be even and a multiple of 16.
+ * TV_DEV_BAD_POSITION.  D in {16, 32, 64, 128, 256}; B*N*(Hq+Hkv)*D/16 < 2^31
+ * (else TV_ERR_UNSUPPORTED).
  */
 int tv_rope_apply(void* q, void* k_tree, const int32_t* pos, const float* cos_sin,
                   int32_t max_pos, int32_t B, int32_t N, int32_t Hq, int32_t Hkv,

@@ -26,6 +26,8 @@
 // The row of a level is split into 32 contiguous segments, one per warp; a
 // pass over the row leaves each warp's segment total in shared memory, so the
 // draw only re-reads the one segment that holds the crossing.
+#include <cooperative_groups.h>
+
 #include <climits>
 
 #include "common.h"
@@ -170,6 +172,123 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(const float* __restric
     node = nxt;
   }
   finish_walk(o, b, k);
+}
+
+// Greedy walk from logits by a cluster of kGreedyCtas CTAs per request: each
+// CTA takes the argmax of its contiguous slice of the visited row, the slices'
+// results are exchanged through distributed shared memory, and every CTA of
+// the cluster continues the walk with the same choice (CTA rank 0 writes the
+// outputs).  A row is 128 KB at a 32000-token vocabulary: split eight ways,
+// one load per thread fetches a slice, so a step of the walk costs about one
+// memory round trip instead of several.
+constexpr int kGreedyCtas = 8;
+constexpr int kGreedyThreads = 256;
+
+__global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThreads)
+    greedy_cluster_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tokens,
+                          const int32_t* __restrict__ parent, int64_t pstride, const int32_t* __restrict__ n_nodes,
+                          int N, int V, AcceptOut o) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
+  __shared__ float s_v[kGreedyThreads / 32];
+  __shared__ int s_i[kGreedyThreads / 32];
+  __shared__ float s_res_v[2];  // this CTA's slice result, by step parity (read by the peers)
+  __shared__ int s_res_i[2];
+  __shared__ int s_choice, s_best;
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / kGreedyCtas;
+  load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
+  __syncthreads();
+  const int n = clamp_nodes(n_nodes, b, N);
+  const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+  int seg = (V + kGreedyCtas - 1) / kGreedyCtas;
+  seg = (seg + 3) / 4 * 4;
+  const int lo = rank * seg, hi = min(lo + seg, V);
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int node = 0, k = 0;
+  for (int step = 0;; ++step) {
+    const float* row = logits + ((int64_t)b * N + node) * V;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    if (vec) {
+      // kBatch float4 per thread requested together, then compared
+      constexpr int kBatch = 4;
+      const float4* r4 = reinterpret_cast<const float4*>(row) + lo / 4;
+      const int n4 = (hi - lo) / 4;
+      for (int base = threadIdx.x; base < n4; base += kBatch * kGreedyThreads) {
+        float4 x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int t = base + u * kGreedyThreads;
+          if (t < n4) x[u] = __ldg(r4 + t);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (base + u * kGreedyThreads >= n4) break;
+          const int i = lo + 4 * (base + u * kGreedyThreads);
+          if (better(x[u].x, i, bv, bi)) { bv = x[u].x; bi = i; }
+          if (better(x[u].y, i + 1, bv, bi)) { bv = x[u].y; bi = i + 1; }
+          if (better(x[u].z, i + 2, bv, bi)) { bv = x[u].z; bi = i + 2; }
+          if (better(x[u].w, i + 3, bv, bi)) { bv = x[u].w; bi = i + 3; }
+        }
+      }
+    } else {
+      for (int i = lo + threadIdx.x; i < hi; i += kGreedyThreads) {
+        const float x = __ldg(row + i);
+        if (better(x, i, bv, bi)) { bv = x; bi = i; }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) { s_v[warp] = bv; s_i[warp] = bi; }
+    __syncthreads();
+    const int par = step & 1;
+    if (warp == 0) {
+      bv = lane < kGreedyThreads / 32 ? s_v[lane] : -INFINITY;
+      bi = lane < kGreedyThreads / 32 ? s_i[lane] : INT_MAX;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) { s_res_v[par] = bv; s_res_i[par] = bi; }
+    }
+    cluster.sync();  // every slice result of this step is visible cluster-wide
+    if (warp == 0) {
+      bv = -INFINITY;
+      bi = INT_MAX;
+      if (lane < kGreedyCtas) {
+        bv = *cluster.map_shared_rank(&s_res_v[par], lane);
+        bi = *cluster.map_shared_rank(&s_res_i[par], lane);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) s_choice = bi;
+    }
+    __syncthreads();
+    const int choice = s_choice;
+    if (rank == 0) emit(o, b, k, choice, node);
+    ++k;
+    const int nxt = find_child(s_par, s_tok, node, n, choice, &s_best);
+    if (nxt == INT_MAX) break;
+    if (k == o.out_cols) {
+      if (rank == 0 && threadIdx.x == 0 && o.status) atomicOr(o.status, TV_DEV_OUT_OVERFLOW);
+      break;
+    }
+    node = nxt;
+  }
+  cluster.sync();  // no CTA leaves while a peer may still read its slice result
+  if (rank == 0) finish_walk(o, b, k);
 }
 
 // ------------------------------------------------------------------ stochastic
@@ -417,6 +536,12 @@ extern "C" int tv_tree_accept_greedy(const float* logits, const int32_t* target_
   if (!logits && !target_argmax)
     return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_greedy: need logits or target_argmax");
   AcceptOut o{out, n_out, path, out_cols, status};
+  if (logits) {
+    greedy_cluster_kernel<<<B * kGreedyCtas, kGreedyThreads, 0, (cudaStream_t)stream>>>(
+        logits, tokens, parent, parent_bstride, n_nodes, N, V, o);
+    TV_LAUNCH_CHECK("greedy_cluster_kernel");
+    return TV_OK;
+  }
   greedy_kernel<<<B, kThreads, 0, (cudaStream_t)stream>>>(logits, target_argmax, tokens, parent, parent_bstride,
                                                            n_nodes, N, V, o);
   TV_LAUNCH_CHECK("greedy_kernel");

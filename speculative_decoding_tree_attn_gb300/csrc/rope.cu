@@ -12,6 +12,7 @@
 // cos_sin[p][1][k] = sin(...), k < D/2, computed in float64 and rounded once.
 // Rotate-half pairing: element k is paired with element k + D/2.
 #include <algorithm>
+#include <climits>
 
 #include <cuda_bf16.h>
 
@@ -71,26 +72,27 @@ struct Vec8<float> {
 
 // One thread rotates 8 pairs (elements k..k+7 and k+D/2..k+D/2+7) of one row.
 // Rows are enumerated as (b, i, head) with the Hq query heads first, then the
-// Hkv tree-key heads of the same node.
-template <typename T>
-__global__ void rope_apply_kernel(T* __restrict__ q, T* __restrict__ kt, const int32_t* __restrict__ pos,
-                                  const float* __restrict__ cs, int max_pos, int64_t BN, int Hq, int Hkv,
-                                  int D, int32_t* __restrict__ status) {
-  const int half = D / 2;
-  const int chunks = half / 8;
+// Hkv tree-key heads of the same node.  Index arithmetic in 32 bits (the
+// launcher checks the item count) with the per-row chunk count a constant.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) rope_apply_kernel(T* __restrict__ q, T* __restrict__ kt,
+                                                         const int32_t* __restrict__ pos, const float* __restrict__ cs,
+                                                         int max_pos, int total, int Hq, int Hkv,
+                                                         int32_t* __restrict__ status) {
+  constexpr int half = D / 2;
+  constexpr int chunks = half / 8;
   const int heads = Hq + (kt ? Hkv : 0);
-  const int64_t total = BN * heads * chunks;
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(t % chunks);
-    const int64_t r = t / chunks;
-    const int h = (int)(r % heads);
-    const int64_t bi = r / heads;
-    const int32_t p = pos[bi];
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
+    const int c = t % chunks;
+    const int r = t / chunks;
+    const int bi = r / heads;
+    const int h = r - bi * heads;
+    const int32_t p = __ldg(pos + bi);
     if (p < 0 || p >= max_pos) {
       if (status && c == 0) atomicOr(status, TV_DEV_BAD_POSITION);
       continue;
     }
-    T* row = (h < Hq) ? q + (bi * Hq + h) * D : kt + (bi * Hkv + (h - Hq)) * D;
+    T* row = (h < Hq) ? q + ((int64_t)bi * Hq + h) * D : kt + ((int64_t)bi * Hkv + (h - Hq)) * D;
     const float* cosr = cs + (int64_t)p * D + c * 8;
     const float* sinr = cosr + half;
     float x1[8], x2[8], co[8], si[8];
@@ -107,6 +109,22 @@ __global__ void rope_apply_kernel(T* __restrict__ q, T* __restrict__ kt, const i
     Vec8<T>::store(row + c * 8, y1);
     Vec8<T>::store(row + half + c * 8, y2);
   }
+}
+
+template <typename T>
+int launch_rope(T* q, T* kt, const int32_t* pos, const float* cs, int max_pos, int total, int Hq, int Hkv, int D,
+                int32_t* status, cudaStream_t stream) {
+  const int blocks = (int)std::min<int64_t>(tv::ceil_div(total, 256), 152 * 16);
+  switch (D) {
+    case 16: rope_apply_kernel<T, 16><<<blocks, 256, 0, stream>>>(q, kt, pos, cs, max_pos, total, Hq, Hkv, status); break;
+    case 32: rope_apply_kernel<T, 32><<<blocks, 256, 0, stream>>>(q, kt, pos, cs, max_pos, total, Hq, Hkv, status); break;
+    case 64: rope_apply_kernel<T, 64><<<blocks, 256, 0, stream>>>(q, kt, pos, cs, max_pos, total, Hq, Hkv, status); break;
+    case 128: rope_apply_kernel<T, 128><<<blocks, 256, 0, stream>>>(q, kt, pos, cs, max_pos, total, Hq, Hkv, status); break;
+    case 256: rope_apply_kernel<T, 256><<<blocks, 256, 0, stream>>>(q, kt, pos, cs, max_pos, total, Hq, Hkv, status); break;
+    default: return tv::fail(TV_ERR_UNSUPPORTED, "tv_rope_apply: head_dim %d not in {16, 32, 64, 128, 256}", D);
+  }
+  TV_LAUNCH_CHECK("rope_apply_kernel");
+  return TV_OK;
 }
 
 }  // namespace
@@ -136,13 +154,10 @@ extern "C" int tv_rope_apply(void* q, void* k_tree, const int32_t* pos, const fl
     return tv::fail(TV_ERR_INVALID_ARG, "tv_rope_apply: buffers must be 16-byte aligned");
   const int64_t BN = (int64_t)B * N;
   const int64_t total = BN * (Hq + (k_tree ? Hkv : 0)) * (head_dim / 16);
-  const int blocks = (int)std::min<int64_t>(tv::ceil_div(total, 256), 152 * 16);
+  if (total >= INT32_MAX) return tv::fail(TV_ERR_UNSUPPORTED, "tv_rope_apply: %lld rotations exceed 2^31", (long long)total);
+  cudaStream_t s = (cudaStream_t)stream;
   if (dtype == TV_BF16)
-    rope_apply_kernel<__nv_bfloat16><<<blocks, 256, 0, (cudaStream_t)stream>>>(
-        (__nv_bfloat16*)q, (__nv_bfloat16*)k_tree, pos, cos_sin, max_pos, BN, Hq, Hkv, head_dim, status);
-  else
-    rope_apply_kernel<float><<<blocks, 256, 0, (cudaStream_t)stream>>>(
-        (float*)q, (float*)k_tree, pos, cos_sin, max_pos, BN, Hq, Hkv, head_dim, status);
-  TV_LAUNCH_CHECK("rope_apply_kernel");
-  return TV_OK;
+    return launch_rope((__nv_bfloat16*)q, (__nv_bfloat16*)k_tree, pos, cos_sin, max_pos, (int)total, Hq, Hkv,
+                       head_dim, status, s);
+  return launch_rope((float*)q, (float*)k_tree, pos, cos_sin, max_pos, (int)total, Hq, Hkv, head_dim, status, s);
 }
