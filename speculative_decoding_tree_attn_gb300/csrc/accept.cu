@@ -23,9 +23,9 @@
 //   level m >= 1       : accept iff fl64(fl64(u * q(x)) * W_m) < w_m(x)
 //   final draw         : min(#{x : prefix_sum(w)(x) < ceil(fl64(u_final * W))}, V - 1)
 //
-// The row of a level is split into 32 contiguous segments, one per warp; a
-// pass over the row leaves each warp's segment total in shared memory, so the
-// draw only re-reads the one segment that holds the crossing.
+// A pass over a level's row leaves the weight total of every 128-element
+// chunk in shared memory, so the draw re-reads only the chunk that holds the
+// crossing.
 #include <cooperative_groups.h>
 
 #include <climits>
@@ -33,6 +33,19 @@
 #include "common.h"
 
 namespace {
+
+#ifdef TV_TC_TRACE
+// Development aid: globaltimer stamps of the sampler's phases per request.
+__device__ unsigned long long g_sample_t[4096][8];
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define TV_SAMPLE_T(k) do { if (threadIdx.x == 0 && blockIdx.x < 4096) g_sample_t[blockIdx.x][k] = gtimer(); } while (0)
+#else
+#define TV_SAMPLE_T(k) do { } while (0)
+#endif
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
@@ -293,7 +306,44 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
 
 // ------------------------------------------------------------------ stochastic
 
-__device__ __forceinline__ int64_t fix40(float x) { return __float2ll_rn(x * 1099511627776.0f); }
+// rint(x * 2^40) as an integer using only float32 additions and integer
+// arithmetic on the bit patterns: float-to-integer conversions run on the
+// double-precision pipe, which is slow on this GPU and would bound the
+// sampler.  With a = |x| < 8:
+//   H   = floor(a * 2^20)            (a * 2^20 + 2^23 added toward zero: the
+//                                     sum's low mantissa bits hold H)
+//   rem = a * 2^40 - H * 2^20        in [0, 2^20), exact (fused multiply-add
+//                                     of values that are multiples of ulp(a*2^40))
+//   L   = rint(rem)                  (rem + 1.5 * 2^23 rounded to nearest even)
+//   rint(a * 2^40) = H * 2^20 + L    since H * 2^20 is an integer.
+// Rows are probability rows (no negative entries): an entry below zero is
+// taken as 0, which gives it weight 0 at every level as its rint image would.
+// The two parts of fix40(x): rint(max(x, 0) * 2^40) = H * 2^20 + L with
+// 0 <= H, L <= 2^20 (the same arithmetic as fix40, kept in 32 bits).
+__device__ __forceinline__ void fix40_parts(float x, int32_t& H, int32_t& L) {
+  const float a = fmaxf(x, 0.f);
+  const float y = a * 1099511627776.0f;
+  float hf;
+  asm("add.rz.f32 %0, %1, %2;" : "=f"(hf) : "f"(a * 1048576.0f), "f"(8388608.0f));
+  const float h = hf - 8388608.0f;
+  const float rem = fmaf(h, -1048576.0f, y);
+  const float lt = rem + 12582912.0f;
+  H = (int32_t)(__float_as_uint(hf) - 0x4B000000u);
+  L = (int32_t)(__float_as_uint(lt) - 0x4B400000u);
+}
+
+__device__ __forceinline__ int64_t fix40(float x) {
+  const float a = fmaxf(x, 0.f);  // probabilities; a negative entry weighs 0 like its clamped image
+  const float y = a * 1099511627776.0f;
+  float hf;
+  asm("add.rz.f32 %0, %1, %2;" : "=f"(hf) : "f"(a * 1048576.0f), "f"(8388608.0f));
+  const float h = hf - 8388608.0f;
+  const float rem = fmaf(h, -1048576.0f, y);
+  const float lt = rem + 12582912.0f;
+  const uint32_t H = __float_as_uint(hf) - 0x4B000000u;
+  const uint32_t L = __float_as_uint(lt) - 0x4B400000u;
+  return (int64_t)(((uint64_t)H << 20) + L);
+}
 
 // floor((S * Q + 2^39) / 2^40) for S < 2^53, 0 <= Q <= 2^42, exactly.
 __device__ __forceinline__ int64_t scaled_round(uint64_t S, uint64_t Q) {
@@ -306,127 +356,299 @@ __device__ __forceinline__ int64_t scaled_round(uint64_t S, uint64_t Q) {
 
 // Weight of one element at level m given the scale history S[0..m).
 __device__ __forceinline__ int64_t level_weight(float p, float q, const uint64_t* S, int m) {
-  int64_t w = fix40(p);
-  if (m == 0) return w < 0 ? 0 : w;
+  const int64_t P = fix40(p);
+  if (m == 0) return P;
   const int64_t Q = fix40(q);
-  for (int j = 0; j < m; ++j) {
-    const int64_t sub = (j == 0) ? Q : scaled_round(S[j], (uint64_t)(Q < 0 ? 0 : Q));
-    w -= sub;
-    if (w < 0) w = 0;
+  int64_t w = P > Q ? P - Q : 0;
+  for (int j = 1; j < m; ++j) {
+    const int64_t sub = scaled_round(S[j], (uint64_t)Q);
+    w = w > sub ? w - sub : 0;
   }
   return w;
 }
+
+// A row is cut into chunks of ch = 128 * k consecutive elements (k chosen so
+// that there are at most kMaxChunks chunks); chunk c belongs to warp
+// c % kSampleWarps.
+// A pass over the row leaves every chunk's weight total in shared memory, so
+// the final draw finds the chunk holding the crossing with one block-wide
+// prefix scan and re-reads only that chunk.
+constexpr int kMaxChunks = 1024;
+constexpr int kChunkBatch = 2;  // chunks a warp loads together (their loads in flight at once)
+constexpr int kSampleThreads = 512;
+constexpr int kSampleWarps = kSampleThreads / 32;
+constexpr int kScanPer = kMaxChunks / kSampleThreads;  // chunk totals per thread in the prefix scan
 
 struct RowView {
   const float* p;
   const float* q;
   int V;
-  int seg;    // elements per warp segment (multiple of 128 when vec)
-  bool vec;
+  int k;      // float4 groups of 32 lanes per chunk: chunk = 128 * k elements
+  int nc;     // number of chunks
+  bool vec;   // rows 16-byte aligned and V % 4 == 0
 };
 
-// Sum of the level-m weights over the calling warp's segment (all lanes get it).
-__device__ uint64_t segment_total(const RowView& r, const uint64_t* S, int m, int warp, int lane) {
-  const int lo = warp * r.seg;
-  const int hi = min(lo + r.seg, r.V);
-  uint64_t acc = 0;
+// Elements e .. e + 3 of the row (4 * lane + 128 * i within a chunk), zero
+// past the end.
+__device__ __forceinline__ void load4(const RowView& r, int e, int m, float4& pv, float4& qv) {
+  pv = make_float4(0.f, 0.f, 0.f, 0.f);
+  qv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (e >= r.V) return;
   if (r.vec) {
-    for (int base = lo + 4 * lane; base < hi; base += 128) {
-      const float4 pv = __ldg(reinterpret_cast<const float4*>(r.p + base));
-      float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (m) qv = __ldg(reinterpret_cast<const float4*>(r.q + base));
-      acc += (uint64_t)level_weight(pv.x, qv.x, S, m) + (uint64_t)level_weight(pv.y, qv.y, S, m) +
-             (uint64_t)level_weight(pv.z, qv.z, S, m) + (uint64_t)level_weight(pv.w, qv.w, S, m);
-    }
+    pv = __ldg(reinterpret_cast<const float4*>(r.p + e));
+    if (m) qv = __ldg(reinterpret_cast<const float4*>(r.q + e));
   } else {
-    for (int x = lo + lane; x < hi; x += 32)
-      acc += (uint64_t)level_weight(__ldg(r.p + x), m ? __ldg(r.q + x) : 0.f, S, m);
+    pv.x = __ldg(r.p + e);
+    if (e + 1 < r.V) pv.y = __ldg(r.p + e + 1);
+    if (e + 2 < r.V) pv.z = __ldg(r.p + e + 2);
+    if (e + 3 < r.V) pv.w = __ldg(r.p + e + 3);
+    if (m) {
+      qv.x = __ldg(r.q + e);
+      if (e + 1 < r.V) qv.y = __ldg(r.q + e + 1);
+      if (e + 2 < r.V) qv.z = __ldg(r.q + e + 2);
+      if (e + 3 < r.V) qv.w = __ldg(r.q + e + 3);
+    }
   }
-#pragma unroll
-  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  return acc;
 }
 
-// One pass: every warp's segment total into seg[], returns the row total.
-__device__ uint64_t row_pass(const RowView& r, const uint64_t* S, int m, uint64_t* seg, uint64_t* s_total) {
+// Level-m weights of elements e .. e + 3 (zero past the end of the row).
+__device__ __forceinline__ void weights4(const RowView& r, int e, const float4& pv, const float4& qv,
+                                         const uint64_t* S, int m, int64_t (&w)[4]) {
+  w[0] = e < r.V ? level_weight(pv.x, qv.x, S, m) : 0;
+  w[1] = e + 1 < r.V ? level_weight(pv.y, qv.y, S, m) : 0;
+  w[2] = e + 2 < r.V ? level_weight(pv.z, qv.z, S, m) : 0;
+  w[3] = e + 3 < r.V ? level_weight(pv.w, qv.w, S, m) : 0;
+}
+
+// One pass at level m: every chunk's weight total into cs[], returns the row
+// total (all threads).
+__device__ uint64_t row_pass(const RowView& r, const uint64_t* S, int m, uint64_t* cs, uint64_t* s_red) {
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  const uint64_t t = segment_total(r, S, m, warp, lane);
-  if (lane == 0) seg[warp] = t;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint64_t w = 0;
-    for (int i = 0; i < kWarps; ++i) w += seg[i];
-    *s_total = w;
+  for (int c0 = warp; c0 < r.nc; c0 += kSampleWarps * kChunkBatch) {
+    uint64_t sum[kChunkBatch];
+#pragma unroll
+    for (int j = 0; j < kChunkBatch; ++j) sum[j] = 0;
+    for (int i = 0; i < r.k; ++i) {
+      float4 pv[kChunkBatch], qv[kChunkBatch];
+#pragma unroll
+      for (int j = 0; j < kChunkBatch; ++j) {
+        const int c = c0 + kSampleWarps * j;
+        load4(r, c < r.nc ? c * 128 * r.k + 128 * i + 4 * lane : r.V, m, pv[j], qv[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < kChunkBatch; ++j) {
+        const int c = c0 + kSampleWarps * j;
+        int64_t w[4];
+        weights4(r, c < r.nc ? c * 128 * r.k + 128 * i + 4 * lane : r.V, pv[j], qv[j], S, m, w);
+        sum[j] += (uint64_t)(w[0] + w[1] + w[2] + w[3]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kChunkBatch; ++j) {
+      uint64_t v = sum[j];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      const int c = c0 + kSampleWarps * j;
+      if (lane == 0 && c < r.nc) cs[c] = v;
+    }
   }
   __syncthreads();
-  const uint64_t w = *s_total;
+  uint64_t t = 0;
+  for (int c = threadIdx.x; c < r.nc; c += kSampleThreads) t += cs[c];
+#pragma unroll
+  for (int off = 16; off; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  if (lane == 0) s_red[warp] = t;
+  __syncthreads();
+  uint64_t w = 0;
+#pragma unroll
+  for (int i = 0; i < kSampleWarps; ++i) w += s_red[i];
   __syncthreads();
   return w;
 }
 
-// Index of the first element whose inclusive prefix sum reaches thr (V if none).
-__device__ int find_crossing(const RowView& r, const uint64_t* S, int m, const uint64_t* seg, uint64_t thr,
-                             int* s_idx) {
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  __shared__ int s_seg;
-  __shared__ uint64_t s_base;
-  if (threadIdx.x == 0) {
-    uint64_t base = 0;
-    int s = kWarps;
-    for (int i = 0; i < kWarps; ++i) {
-      if (base + seg[i] >= thr && seg[i] > 0) { s = i; break; }
-      base += seg[i];
+// The same pass with the row streamed through a ring of shared-memory stages
+// by cp.async copies, so a CTA keeps far more of the row in flight than its
+// registers could hold.  Stage = kStageElems elements of p (and q), one
+// 256-element chunk per warp.  Needs 16-byte aligned rows, V % 4 == 0 and
+// 256-element chunks (k == 2).
+constexpr int kStreamStages = 2;
+constexpr int kChunkElems = 256;                  // a chunk: two float4 per lane of one warp
+constexpr int kStageElems = kChunkElems * kSampleWarps;  // 4096: one chunk per warp and stage
+static_assert(kStageElems % (4 * kSampleThreads) == 0, "whole float4 copies per thread");
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Level 0/1 weights of four in-row elements added into (h, l), the sum being
+// h * 2^20 + l: w0 = P, w1 = max(0, P - Q) with P - Q = dH * 2^20 + dL and
+// |dL| <= 2^20, so P - Q > 0 iff dH > 0, or dH == 0 and dL > 0.
+__device__ __forceinline__ void add_weights4(const float4& pv, const float4& qv, int m, int32_t& h, int32_t& l) {
+  const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
+  const float qs[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int32_t Hp, Lp;
+    fix40_parts(ps[i], Hp, Lp);
+    if (m == 0) {
+      h += Hp;
+      l += Lp;
+    } else {
+      int32_t Hq, Lq;
+      fix40_parts(qs[i], Hq, Lq);
+      const int32_t dH = Hp - Hq, dL = Lp - Lq;
+      const bool pos = dH > 0 || (dH == 0 && dL > 0);
+      h += pos ? dH : 0;
+      l += pos ? dL : 0;
     }
-    if (thr == 0) { s = 0; base = 0; }
-    s_seg = s;
-    s_base = base;
+  }
+}
+
+__device__ uint64_t row_pass_stream(const RowView& r, const uint64_t* S, int m, uint64_t* cs, uint64_t* s_red,
+                                    float4* ring) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  constexpr int kRow4 = kStageElems / 4;  // float4 per row and stage
+  const int nst = (r.V + kStageElems - 1) / kStageElems;
+  auto issue = [&](int st) {
+    if (st < nst) {
+      const int slot = st % kStreamStages;
+#pragma unroll
+      for (int j = 0; j < kRow4 / kSampleThreads; ++j) {
+        const int i4 = j * kSampleThreads + threadIdx.x;
+        const int e = st * kStageElems + 4 * i4;
+        if (e < r.V) {
+          cp_async16(&ring[(2 * slot) * kRow4 + i4], r.p + e);
+          if (m) cp_async16(&ring[(2 * slot + 1) * kRow4 + i4], r.q + e);
+        }
+      }
+    }
+    cp_async_commit();  // an empty group past the end keeps the group count uniform
+  };
+#pragma unroll
+  for (int st = 0; st < kStreamStages - 1; ++st) issue(st);
+  for (int g = 0; g < nst; ++g) {
+    issue(g + kStreamStages - 1);
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStreamStages - 1) : "memory");  // stage g has landed
+    __syncthreads();
+    const int slot = g % kStreamStages;
+    const int c = g * kSampleWarps + warp;  // this warp's chunk
+    uint64_t v;
+    if ((g + 1) * kStageElems <= r.V && m <= 1) {  // the whole stage lies inside the row
+      int32_t h = 0, l = 0;
+#pragma unroll
+      for (int j = 0; j < kChunkElems / 128; ++j) {
+        const int i4 = warp * (kChunkElems / 4) + j * 32 + lane;
+        const float4 pv = ring[(2 * slot) * kRow4 + i4];
+        const float4 qv = m ? ring[(2 * slot + 1) * kRow4 + i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        add_weights4(pv, qv, m, h, l);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        h += __shfl_xor_sync(0xffffffffu, h, off);
+        l += __shfl_xor_sync(0xffffffffu, l, off);
+      }
+      v = (uint64_t)(((int64_t)h << 20) + l);
+    } else {
+      uint64_t acc = 0;
+#pragma unroll
+      for (int j = 0; j < kChunkElems / 128; ++j) {
+        const int i4 = warp * (kChunkElems / 4) + j * 32 + lane;
+        const int e = g * kStageElems + 4 * i4;
+        const float4 pv = ring[(2 * slot) * kRow4 + i4];
+        const float4 qv = m ? ring[(2 * slot + 1) * kRow4 + i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        int64_t w[4];
+        weights4(r, e, pv, qv, S, m, w);  // zero past the end of the row
+        acc += (uint64_t)(w[0] + w[1] + w[2] + w[3]);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      v = acc;
+    }
+    if (lane == 0 && c < r.nc) cs[c] = v;
+    __syncthreads();  // every warp is done with this slot before it is refilled
+  }
+  uint64_t t = 0;
+  for (int c = threadIdx.x; c < r.nc; c += kSampleThreads) t += cs[c];
+#pragma unroll
+  for (int off = 16; off; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  if (lane == 0) s_red[warp] = t;
+  __syncthreads();
+  uint64_t w = 0;
+#pragma unroll
+  for (int i = 0; i < kSampleWarps; ++i) w += s_red[i];
+  __syncthreads();
+  return w;
+}
+
+// Index of the first element whose inclusive prefix sum of level-m weights
+// reaches thr (V if none), from the chunk totals cs[] of the same level.
+__device__ int find_crossing(const RowView& r, const uint64_t* S, int m, const uint64_t* cs, uint64_t thr,
+                             uint64_t* s_red, int* s_chunk, uint64_t* s_base, int* s_idx) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  if (thr == 0) return 0;
+  // block exclusive prefix over the chunk totals, kScanPer consecutive chunks per thread
+  const int c_first = kScanPer * threadIdx.x;
+  uint64_t v[kScanPer];
+  uint64_t mine_sum = 0;
+#pragma unroll
+  for (int j = 0; j < kScanPer; ++j) {
+    v[j] = c_first + j < r.nc ? cs[c_first + j] : 0;
+    mine_sum += v[j];
+  }
+  uint64_t incl = mine_sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint64_t x = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += x;
+  }
+  if (lane == 31) s_red[warp] = incl;
+  if (threadIdx.x == 0) {
+    *s_chunk = -1;
     *s_idx = r.V;
   }
   __syncthreads();
-  const int s = s_seg;
-  if (s < kWarps && warp == s) {
-    uint64_t base = s_base;
-    const int lo = s * r.seg, hi = min(lo + r.seg, r.V);
-    const int per = r.vec ? 4 : 1;
-    for (int cbase = lo; cbase < hi; cbase += 32 * per) {
-      int64_t w[4] = {0, 0, 0, 0};
-      const int x0 = cbase + lane * per;
-      if (r.vec) {
-        if (x0 < hi) {
-          const float4 pv = __ldg(reinterpret_cast<const float4*>(r.p + x0));
-          float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (m) qv = __ldg(reinterpret_cast<const float4*>(r.q + x0));
-          w[0] = level_weight(pv.x, qv.x, S, m);
-          w[1] = level_weight(pv.y, qv.y, S, m);
-          w[2] = level_weight(pv.z, qv.z, S, m);
-          w[3] = level_weight(pv.w, qv.w, S, m);
-        }
-      } else if (x0 < hi) {
-        w[0] = level_weight(__ldg(r.p + x0), m ? __ldg(r.q + x0) : 0.f, S, m);
-      }
+  uint64_t ex = incl - mine_sum;
+  for (int i = 0; i < warp; ++i) ex += s_red[i];
+#pragma unroll
+  for (int j = 0; j < kScanPer; ++j) {
+    if (v[j] > 0 && ex < thr && thr <= ex + v[j]) { *s_chunk = c_first + j; *s_base = ex; }
+    ex += v[j];
+  }
+  __syncthreads();
+  const int c = *s_chunk;
+  if (c >= 0 && warp == 0) {
+    uint64_t base = *s_base;
+    for (int i = 0; i < r.k; ++i) {
+      const int e = c * 128 * r.k + 128 * i + 4 * lane;
+      float4 pv, qv;
+      load4(r, e, m, pv, qv);
+      int64_t w[4];
+      weights4(r, e, pv, qv, S, m, w);
       const uint64_t mine = (uint64_t)(w[0] + w[1] + w[2] + w[3]);
-      uint64_t incl = mine;
+      uint64_t inc = mine;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const uint64_t v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
+        const uint64_t v = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += v;
       }
-      const uint64_t chunk = __shfl_sync(0xffffffffu, incl, 31);
-      const unsigned hit = __ballot_sync(0xffffffffu, base + incl >= thr);
+      const unsigned hit = __ballot_sync(0xffffffffu, base + inc >= thr);
       if (hit) {
         const int l = __ffs(hit) - 1;
         if (lane == l) {
-          uint64_t run = base + incl - mine;
-          int x = x0;
-          for (int e = 0; e < per; ++e) {
-            run += (uint64_t)w[e];
-            if (run >= thr) { x = x0 + e; break; }
+          uint64_t run = base + inc - mine;
+          int x = e;
+          for (int q4 = 0; q4 < 4; ++q4) {
+            run += (uint64_t)w[q4];
+            if (run >= thr) { x = e + q4; break; }
           }
           *s_idx = x;
         }
         break;
       }
-      base += chunk;
+      base += __shfl_sync(0xffffffffu, inc, 31);
     }
   }
   __syncthreads();
@@ -435,7 +657,7 @@ __device__ int find_crossing(const RowView& r, const uint64_t* S, int m, const u
   return x;
 }
 
-__global__ void __launch_bounds__(kThreads) sample_kernel(const float* __restrict__ p, const float* __restrict__ q,
+__global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* __restrict__ p, const float* __restrict__ q,
                                                           const int32_t* __restrict__ tokens,
                                                           const int32_t* __restrict__ parent, int64_t pstride,
                                                           const int32_t* __restrict__ n_nodes,
@@ -444,19 +666,30 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* __restric
                                                           AcceptOut o) {
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
   __shared__ uint64_t S[TV_MAX_NODES + 1];
-  __shared__ uint64_t seg_cur[kWarps], seg_tmp[kWarps];
-  __shared__ uint64_t s_total;
-  __shared__ int s_flag, s_idx;
+  __shared__ uint64_t s_red[kSampleWarps], s_base;
+  extern __shared__ float4 dsm[];  // stream ring, then the chunk totals of the current / next level
+  float4* ring = dsm;
+  uint64_t* cs_cur = reinterpret_cast<uint64_t*>(dsm + 2 * kStreamStages * (kStageElems / 4));
+  uint64_t* cs_tmp = cs_cur + kMaxChunks;
+  __shared__ int s_flag, s_idx, s_chunk;
   const int b = blockIdx.x;
+  TV_SAMPLE_T(0);
   load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
   __syncthreads();
+  TV_SAMPLE_T(1);
   const int n = clamp_nodes(n_nodes, b, N);
   const bool vec = (V % 4 == 0) && (((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q)) & 15) == 0);
-  int seg = (V + kWarps - 1) / kWarps;
-  if (vec) seg = (seg + 127) / 128 * 128;
+  const int groups = (V + 127) / 128;
+  int kk = (groups + kMaxChunks - 1) / kMaxChunks;
+  kk = kk < 2 ? 2 : kk;  // chunks of at least 256 elements
+  const int nc = (groups + kk - 1) / kk;
+  const bool stream = vec && kk == 2;
+  auto pass = [&](const RowView& rv, int level, uint64_t* cs) {
+    return stream ? row_pass_stream(rv, S, level, cs, s_red, ring) : row_pass(rv, S, level, cs, s_red);
+  };
   int node = 0, k = 0;
   while (true) {
-    RowView row{p + ((int64_t)b * N + node) * V, q + ((int64_t)b * N + node) * V, V, seg, vec};
+    RowView row{p + ((int64_t)b * N + node) * V, q + ((int64_t)b * N + node) * V, V, kk, nc, vec};
     int m = 0;
     uint64_t Wm = 0;     // total of the current level (valid for m >= 1)
     if (threadIdx.x == 0) S[0] = 1ull << 40;
@@ -482,12 +715,14 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* __restric
       __syncthreads();
       if (ok) { taken = c; break; }
       // rejected: the target moves to the residual of the current level
-      const uint64_t Wn = row_pass(row, S, m + 1, seg_tmp, &s_total);
+      TV_SAMPLE_T(6);
+      const uint64_t Wn = pass(row, m + 1, cs_tmp);
+      TV_SAMPLE_T(7);
       if (Wn > 0) {
         ++m;
         Wm = Wn;
         if (threadIdx.x == 0) S[m] = Wn;
-        if (threadIdx.x < kWarps) seg_cur[threadIdx.x] = seg_tmp[threadIdx.x];
+        for (int c = threadIdx.x; c < nc; c += blockDim.x) cs_cur[c] = cs_tmp[c];
         __syncthreads();
       }
     }
@@ -502,15 +737,19 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* __restric
       continue;
     }
     // replacement (after rejections) or bonus (leaf / all children absent)
-    if (m == 0) Wm = row_pass(row, S, 0, seg_cur, &s_total);
+    TV_SAMPLE_T(2);
+    if (m == 0) Wm = pass(row, 0, cs_cur);
+    TV_SAMPLE_T(3);
     const double t = __dmul_rn((double)u_final[b], (double)Wm);
     const uint64_t thr = (uint64_t)ceil(t);
-    int x = find_crossing(row, S, m, seg_cur, thr, &s_idx);
+    int x = find_crossing(row, S, m, cs_cur, thr, s_red, &s_chunk, &s_base, &s_idx);
+    TV_SAMPLE_T(4);
     if (x > V - 1) x = V - 1;
     emit(o, b, k, x, node);
     ++k;
     break;
   }
+  TV_SAMPLE_T(5);
   finish_walk(o, b, k);
 }
 
@@ -524,6 +763,13 @@ int check_accept_args(int B, int N, int V, const void* tokens, const void* paren
 }
 
 }  // namespace
+
+#ifdef TV_TC_TRACE
+extern "C" int tv_debug_sample_times(void* dst, size_t bytes) {
+  const size_t n = sizeof(g_sample_t) < bytes ? sizeof(g_sample_t) : bytes;
+  return cudaMemcpyFromSymbol(dst, g_sample_t, n) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 extern "C" int tv_tree_accept_greedy(const float* logits, const int32_t* target_argmax, const int32_t* tokens,
                                      const int32_t* parent, int64_t parent_bstride, const int32_t* n_nodes,
@@ -559,7 +805,10 @@ extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32
   if (B == 0) return TV_OK;
   if (!p || !q || !u_accept || !u_final) return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: null pointer");
   AcceptOut o{out, n_out, path, out_cols, status};
-  sample_kernel<<<B, kThreads, 0, (cudaStream_t)stream>>>(p, q, tokens, parent, parent_bstride, n_nodes, u_accept,
+  constexpr size_t kDyn = sizeof(float4) * 2 * kStreamStages * (kStageElems / 4) + sizeof(uint64_t) * 2 * kMaxChunks;
+  cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDyn);
+  if (e != cudaSuccess) return tv::cuda_fail(e, "cudaFuncSetAttribute(sample_kernel)");
+  sample_kernel<<<B, kSampleThreads, kDyn, (cudaStream_t)stream>>>(p, q, tokens, parent, parent_bstride, n_nodes, u_accept,
                                                            u_final, N, V, o);
   TV_LAUNCH_CHECK("sample_kernel");
   return TV_OK;
