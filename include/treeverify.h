@@ -302,7 +302,8 @@ int tv_tree_accept_greedy(const float* logits, const int32_t* target_argmax,
  *  - level m >= 1: accept iff fl64(fl64(u * q(x)) * W_m) < w_m(x);
  *  - the final draw (replacement, or bonus from p at level 0 with W = sum P)
  *    returns min(#{x : prefix_sum_w(x) < ceil(fl64(u_final * W))}, V - 1).
- * Contract: every p and q row sums to at most 2 (probability rows).
+ * Contract: every p and q row sums to at most 2 and holds no negative entry
+ * (probability rows; an entry below zero is taken as 0).
  *
  * p, q      device float32 [B, N, V]: target distribution after node i and the
  *           draft distribution node i's children were drawn from.
