@@ -47,6 +47,7 @@ __device__ unsigned long long g_trace[kEvents][kTiles];
 // per CTA: globaltimer at entry, exit; segments; first unit; last epilogue
 // start, end; total epilogue ns
 __device__ unsigned long long g_cta_time[1024][8];
+__device__ unsigned long long g_epi[1024][8];  // row 0: ns per route (complete, direct, publish, publish + merge), counts
 }}  // namespace tv::trace
 #define TV_TRACE(ev, tile) \
   do { if (blockIdx.x == 0 && (tile) < tv::trace::kTiles) tv::trace::g_trace[ev][tile] = clock64(); } while (0)
@@ -561,8 +562,123 @@ __device__ __forceinline__ void store_bf16_16(__nv_bfloat16* dst, const float (&
 //  * otherwise publish the partial, count this piece's tiles in, and merge
 //    from memory if that completed the count (a piece that finished in the
 //    meantime saw the count short and left the merge to this one).
-__device__ __forceinline__ void finish_row_impl(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
-                                                bool valid_row, int64_t orow, uint32_t tO, float m_run, float l) {
+// Merge of a split unit's row when the K/V stage ring is idle (the slice's
+// last segment): every other piece's row is copied into shared memory by
+// cp.async -- with two pieces the other's whole row at once, else a 32-column
+// quarter of all pieces at a time: one memory round trip per batch and no
+// registers held for the loads -- and combined with this CTA's O from TMEM in
+// piece order, with the same float32 arithmetic as the other merge routes.
+// A 16 KB slot holds one quarter of one piece (slot = quarter with two
+// pieces, else piece index k = c - c0 < np <= kStagePieces): row rl, 16-byte
+// chunk j at slot * 16384 + rl * 128 + ((j ^ (rl & 7)) * 16), so eight
+// consecutive rows hit eight different bank groups.  Warp-collective (TMEM
+// reads); `active` lanes merge their row.
+constexpr int kStagePieces = 4;
+constexpr int kStageBytes = kStagePieces * 16384;
+static_assert(3 * kKVTileBytes * 2 >= kStageBytes, "the single-M-tile ring holds the staging slots");
+
+__device__ __forceinline__ void staged_merge(const AttnParams& p, const Pieces& pc, float lse2, float inv, int row,
+                                             int rl, int64_t orow, uint32_t tO, uint8_t* stage, bool active) {
+  constexpr float kLn2 = 0.69314718055994530942f;
+  const int self = blockIdx.x;
+  const int np = pc.c1 - pc.c0 + 1;
+  float lse[kStagePieces], w[kStagePieces];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kStagePieces; ++k) {
+    const int c = pc.c0 + k;
+    lse[k] = 0.f;
+    if (k < np) {
+      lse[k] = (c == self) ? lse2 : (active ? __ldcg(p.part_lse + pc.slot(c) * p.RPG + row) : 0.f);
+      mx = fmaxf(mx, lse[k]);
+    }
+  }
+  float z = 0.f;
+#pragma unroll
+  for (int k = 0; k < kStagePieces; ++k)
+    if (k < np) z += exp2f(lse[k] - mx);
+  const float zinv = 1.f / z;
+#pragma unroll
+  for (int k = 0; k < kStagePieces; ++k) w[k] = exp2f(lse[k] - mx) * zinv;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  const uint32_t sbase = smem_u32(stage);
+  // quarter qq of piece c into slot `sl`
+  auto issue = [&](int c, int qq, int sl) {
+    const float* src = p.part_o + (pc.slot(c) * p.RPG + row) * kD + qq * 32;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sbase + sl * 16384 + rl * 128 + ((j ^ (rl & 7)) << 4)),
+                   "l"(src + 4 * j)
+                   : "memory");
+  };
+  // two pieces: the other piece's whole row goes in at once (quarter qq in slot qq)
+  const bool whole = np == 2;
+  if (whole) {
+    if (active)
+      for (int qq = 0; qq < kD / 32; ++qq) issue(self == pc.c0 ? pc.c1 : pc.c0, qq, qq);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  }
+#pragma unroll 1
+  for (int qq = 0; qq < kD / 32; ++qq) {
+    if (!whole) {
+      if (active) {
+#pragma unroll
+        for (int k = 0; k < kStagePieces; ++k) {
+          const int c = pc.c0 + k;
+          if (k < np && c != self) issue(c, qq, k);
+        }
+      }
+      asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    }
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(tO + qq * 32, r);
+    tmem_ld_wait();
+    if (!active) continue;
+    float acc[32];
+#pragma unroll
+    for (int g4 = 0; g4 < 8; ++g4) {
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int k = 0; k < kStagePieces; ++k) {
+        const int c = pc.c0 + k;
+        if (k >= np) continue;
+        float4 v;
+        if (c == self) {
+          v = make_float4(__uint_as_float(r[4 * g4]) * inv, __uint_as_float(r[4 * g4 + 1]) * inv,
+                          __uint_as_float(r[4 * g4 + 2]) * inv, __uint_as_float(r[4 * g4 + 3]) * inv);
+        } else {
+          v = *reinterpret_cast<const float4*>(stage + (whole ? qq : k) * 16384 + rl * 128 + ((g4 ^ (rl & 7)) << 4));
+        }
+        a0 = fmaf(w[k], v.x, a0);
+        a1 = fmaf(w[k], v.y, a1);
+        a2 = fmaf(w[k], v.z, a2);
+        a3 = fmaf(w[k], v.w, a3);
+      }
+      acc[4 * g4] = a0;
+      acc[4 * g4 + 1] = a1;
+      acc[4 * g4 + 2] = a2;
+      acc[4 * g4 + 3] = a3;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + orow * kD + qq * 32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 v;
+      v.x = pack_bf16(acc[8 * j + 0], acc[8 * j + 1]);
+      v.y = pack_bf16(acc[8 * j + 2], acc[8 * j + 3]);
+      v.z = pack_bf16(acc[8 * j + 4], acc[8 * j + 5]);
+      v.w = pack_bf16(acc[8 * j + 6], acc[8 * j + 7]);
+      dst[j] = v;
+    }
+  }
+  __syncwarp();
+  if (active && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+}
+
+template <bool kStage>
+__device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
+                                               bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
+                                               uint8_t* stage) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   constexpr float kLn2 = 0.69314718055994530942f;
   const float inv = 1.f / l;
@@ -574,10 +690,17 @@ __device__ __forceinline__ void finish_row_impl(const AttnParams& p, const Slice
   const uint32_t mine = (uint32_t)(s.e - s.a);
   bool direct = false;
   float mx = lse2, z = 1.f;
-  if (!complete && valid_row && p.direct_merge) {
-    direct = ld_acquire_u32(ctr) + mine == (uint32_t)s.n;
-    if (direct) piece_stats<true>(p, pc, self, lse2, row, mx, z);
+  const int rl = row & 127;
+  const bool staged = kStage && stage != nullptr && !complete && pc.c1 - pc.c0 < kStagePieces && pc.T >= pc.P;
+  if (!complete && valid_row && p.direct_merge) direct = ld_acquire_u32(ctr) + mine == (uint32_t)s.n;
+  if constexpr (kStage) {
+    if (staged && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
+      staged_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
+      return 1;
+    }
   }
+  if (staged) direct = false;  // a mixed warp publishes; its last arriver merges below
+  if (direct) piece_stats<true>(p, pc, self, lse2, row, mx, z);
   const float zinv = 1.f / z;
   const int64_t srow = pc.slot(self) * p.RPG + row;
 #pragma unroll 1
@@ -605,13 +728,27 @@ __device__ __forceinline__ void finish_row_impl(const AttnParams& p, const Slice
     }
   }
   __syncwarp();
-  if (!valid_row) return;
   if (complete || direct) {
-    if (p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
-    return;
+    if (valid_row && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+    return complete ? 0 : 1;
   }
+  if constexpr (kStage) {
+    if (staged) {
+      bool last = false;
+      if (valid_row) {
+        p.part_lse[srow] = lse2;
+        last = atom_add_acq_rel(ctr, mine) + mine == (uint32_t)s.n;
+      }
+      if (__any_sync(0xffffffffu, last)) {
+        staged_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, last);
+        return last ? 3 : 2;
+      }
+      return 2;
+    }
+  }
+  if (!valid_row) return 0;
   p.part_lse[srow] = lse2;
-  if (atom_add_acq_rel(ctr, mine) + mine != (uint32_t)s.n) return;
+  if (atom_add_acq_rel(ctr, mine) + mine != (uint32_t)s.n) return 2;
   // every piece is published: merge from memory
   piece_stats<false>(p, pc, -1, 0.f, row, mx, z);
   const float zinv2 = 1.f / z;
@@ -624,19 +761,30 @@ __device__ __forceinline__ void finish_row_impl(const AttnParams& p, const Slice
     store_bf16_16(out + orow * kD + c, acc);
   }
   if (p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+  return 3;
 }
 
+// kStage: merges at the slice's last segment may stage through `stage`.
+template <bool kStage>
 __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
-                                           bool valid_row, int64_t orow, uint32_t tO, float m_run, float l) {
+                                           bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
+                                           uint8_t* stage) {
 #ifdef TV_TC_TRACE
   const unsigned long long t_in = globaltimer();
   TV_TRACE_ROW0(4, t_in);
 #endif
-  finish_row_impl(p, sp, s, row, valid_row, orow, tO, m_run, l);
+#ifdef TV_TC_TRACE
+  const int route =
+#endif
+  finish_row_impl<kStage>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
 #ifdef TV_TC_TRACE
   const unsigned long long t_out = globaltimer();
   TV_TRACE_ROW0(5, t_out);
-  if (row == 0 && blockIdx.x < 1024) tv::trace::g_cta_time[blockIdx.x][6] += t_out - t_in;
+  if (row == 0 && blockIdx.x < 1024) {
+    tv::trace::g_cta_time[blockIdx.x][6] += t_out - t_in;
+    tv::trace::g_epi[blockIdx.x][route] += t_out - t_in;
+    tv::trace::g_epi[blockIdx.x][4 + route] += 1;
+  }
 #endif
 }
 
@@ -979,7 +1127,11 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
       if (!ok) break;
       fence_after();
-      finish_row(p, sp, s, row, valid_row, orow, tO, m_run, l);
+      Walk ahead = walk;
+      Segment s_ahead;
+      // after the slice's last tile the K/V ring is idle: merges stage through it
+      uint8_t* stage = ahead.next(p, s_ahead) ? nullptr : smem_raw + (base - raw) + C::kOffK;
+      finish_row<true>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
       fence_before();
     }
   }
@@ -1324,7 +1476,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       if (!ok) break;
       fence_after();
       if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
-      finish_row(p, sp, s, row, valid_row, orow, tO, m_run, l);
+      finish_row<false>(p, sp, s, row, valid_row, orow, tO, m_run, l, nullptr);
       fence_before();
       if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       s = s_next;
@@ -1412,6 +1564,10 @@ int tc_unit_cost(int rows_per_unit) { return rows_per_unit <= 128 ? 3 : 6; }
 extern "C" int tv_debug_trace(void* dst, size_t bytes) {
   const size_t n = sizeof(trace::g_trace) < bytes ? sizeof(trace::g_trace) : bytes;
   return cudaMemcpyFromSymbol(dst, trace::g_trace, n) == cudaSuccess ? 0 : -1;
+}
+extern "C" int tv_debug_epi_times(void* dst, size_t bytes) {
+  const size_t n = sizeof(trace::g_epi) < bytes ? sizeof(trace::g_epi) : bytes;
+  return cudaMemcpyFromSymbol(dst, trace::g_epi, n) == cudaSuccess ? 0 : -1;
 }
 extern "C" int tv_debug_cta_times(void* dst, size_t bytes) {
   const size_t n = sizeof(trace::g_cta_time) < bytes ? sizeof(trace::g_cta_time) : bytes;
