@@ -1557,8 +1557,15 @@ int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
 int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : 1; }
 
 // Virtual tiles charged per unit: measured cost of finishing one unit and
-// starting the next, in units of one 64-key tile of the steady state.
-int tc_unit_cost(int rows_per_unit) { return rows_per_unit <= 128 ? 3 : 6; }
+// starting the next, in units of one 64-key tile of the steady state (chosen
+// by sweeping: 3 for one M tile, 8 for two on the 64-request workload).
+#ifndef TV_UNIT_COST_M1
+#define TV_UNIT_COST_M1 3
+#endif
+#ifndef TV_UNIT_COST_M2
+#define TV_UNIT_COST_M2 8
+#endif
+int tc_unit_cost(int rows_per_unit) { return rows_per_unit <= 128 ? TV_UNIT_COST_M1 : TV_UNIT_COST_M2; }
 
 #ifdef TV_TC_TRACE
 extern "C" int tv_debug_trace(void* dst, size_t bytes) {
