@@ -17,10 +17,12 @@ Everything is written as the plain definition the pages give, in float64
 * ``accept``      -- greedy tree walk, the chain verifier of the sampling
                      page, the tree walk with sibling residual updates, and
                      the fixed-point inverse-CDF sampler they share.
+* ``kvcache``     -- commit of the accepted path's tree K/V into the paged
+                     cache.
 
 Every function is pinned by ``tests/test_oracle_*.py`` (``-m "not gpu"``)
 against facts the pages print or mathematics fixes; no function here is
 "parity unpinned".
 """
 
-from . import accept, attention, tree  # noqa: F401
+from . import accept, attention, kvcache, tree  # noqa: F401
