@@ -249,7 +249,9 @@ class Step:
         from speculative_decoding_tree_attn_gb300 import capi
         self.capi, self.w, self.dev = capi, w, dev
         self.paths = w.paths()
-        self.inp = W.attention_inputs(w, device=dev)
+        # blocks placed for max_depth + 1 positions past each prefix: room to
+        # commit the accepted path (timed separately, see kv_commit)
+        self.inp = W.attention_inputs(w, device=dev, reserve=w.max_depth + 1)
         parent, depth, rows, _, n = capi.tv_tree_build(self.paths)
         self.N = n
         self.parent = torch.from_numpy(parent).to(dev)
@@ -311,6 +313,28 @@ class Step:
             s = self.sample
             c.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
                                     n_nodes=s["n_nodes"], out=self.acc_out, n_out=self.acc_n, path=self.acc_path)
+
+    def commit_path(self):
+        """The accepted path of the last step (the deepest chain when the
+        workload has no acceptance) as (path int32 [B, cols], n_out int32 [B])."""
+        if self.greedy is not None or self.sample is not None:
+            return self.acc_path, self.acc_n
+        par = self.parent.cpu().numpy()
+        depth = np.zeros(par.size, dtype=np.int64)
+        for i in range(1, par.size):
+            depth[i] = depth[par[i]] + 1
+        chain = [int(np.argmax(depth))]
+        while chain[-1] != 0:
+            chain.append(int(par[chain[-1]]))
+        chain = chain[::-1]
+        path = torch.tensor([chain] * self.w.B, dtype=torch.int32, device=self.dev)
+        n = torch.full((self.w.B,), len(chain), dtype=torch.int32, device=self.dev)
+        return path, n
+
+    def run_commit(self, path, n_out, new_lens):
+        i = self.inp
+        self.capi.tv_kv_commit(i["k_cache"], i["v_cache"], i["block_table"], self.seq_lens, i["k_tree"], i["v_tree"],
+                               path, n_out, new_seq_lens=new_lens)
 
     def per_step_inputs(self):
         """Tensors a caller supplies fresh every step (the KV cache is resident state)."""
@@ -417,6 +441,29 @@ def run_ours(args, world, rank, local):
         e2e = {"value": world * nodes * args.steps / (e_ms / 1e3), "unit": "nodes/s",
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
 
+    # the accepted path's K/V committed to the cache (a separate call, not in the step)
+    commit = None
+    if graphs:
+        path, n_commit = st.commit_path()
+        new_lens = torch.empty_like(st.seq_lens)
+        g_commit = torch.cuda.CUDAGraph()
+        st.run_commit(path, n_commit, new_lens)
+        with torch.cuda.graph(g_commit):
+            st.run_commit(path, n_commit, new_lens)
+        for _ in range(args.warmup):
+            g_commit.replay()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        c0.record()
+        for _ in range(args.steps):
+            g_commit.replay()
+        c1.record()
+        torch.cuda.synchronize()
+        us = c0.elapsed_time(c1) * 1e3 / args.steps
+        rows = int(n_commit.sum().item())
+        moved = rows * w.Hkv * w.D * st.esize * 2 * 2  # K and V rows, read and written
+        commit = {"us_per_call": round(us, 2), "rows": rows, "bytes": moved, "gbs": round(moved / (us * 1e-6) / 1e9, 1)}
+
     peak, peak_kind = measured_hbm_peak()
     attn_mean_ms = statistics.mean(attn_ms)
     achieved = st.attn_bytes / (attn_mean_ms / 1e3) / 1e9
@@ -449,6 +496,7 @@ def run_ours(args, world, rank, local):
                        "timing": "eager calls" if args.eager else "CUDA graph replays of the step"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": st.launches * args.steps,
+            "kv_commit": commit,
             "kv_read_gbs": round(achieved, 1), "kv_read_frac_of_peak": round(achieved / peak, 4),
         }
         print(json.dumps(line))

@@ -320,6 +320,41 @@ int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,
                           int32_t* out, int32_t* n_out, int32_t* path, int32_t out_cols,
                           int32_t* status, void* stream);
 
+/*
+ * tv_kv_commit -- device, asynchronous.  Copies the accepted path's tree K/V
+ * into the paged cache.  "Build the tree attention mask ...", "What it
+ * costs." (tree K/V in scratch, the accepted path copied into the cache);
+ * "Tree Verification", "The Cost Side".  Node path[b, j] (j < n_out[b]) sits
+ * at depth j: its K and V rows, every KV head, go to cache position
+ * L_b + j, i.e. block block_table[b, (L_b + j) / block_size], slot
+ * (L_b + j) % block_size.  The tree keys are copied as given (after
+ * tv_rope_apply they are rotated at L_b + depth, their cache position).
+ *
+ * k_cache, v_cache  device [num_blocks, Hkv, block_size, D] (dtype), written.
+ * block_table       device int32 [B, max_blocks]; the caller has placed
+ *                   blocks for positions up to L_b + n_out[b] - 1.
+ * seq_lens          device int32 [B]: L_b (read).
+ * new_seq_lens      device int32 [B] out (nullable, must not alias
+ *                   seq_lens): L_b + n_out[b].
+ * k_tree, v_tree    device [B, N, Hkv, D] (dtype).
+ * path              device int32 [B, path_cols]: the accepted path as
+ *                   tv_tree_accept_* return it (node indices, root first).
+ * n_out             device int32 [B]: path length per request (values are
+ *                   clamped to [0, path_cols]).
+ * A node index outside [0, N) is skipped and flags TV_DEV_BAD_TOPOLOGY; a
+ * position beyond the block table, or a table entry outside
+ * [0, num_blocks), is skipped and flags TV_DEV_OUT_OVERFLOW.  D * element
+ * size must be a multiple of 16 bytes and the K/V buffers 16-byte aligned.
+ * No page defines a separate entry point: it is the copy the mask page's
+ * serving loop performs after acceptance.
+ */
+int tv_kv_commit(void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size,
+                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                 int32_t* new_seq_lens, const void* k_tree, const void* v_tree,
+                 const int32_t* path, int32_t path_cols, const int32_t* n_out, int32_t B,
+                 int32_t N, int32_t Hkv, int32_t head_dim, int32_t dtype, int32_t* status,
+                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -44,6 +44,8 @@ SIGNATURES = {
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
                                              _P, _P]),
+    "tv_kv_commit": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                    _I32, _I32, _P, _P]),
 }
 
 
@@ -287,3 +289,23 @@ def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=No
                                        _ptr(u_accept), _ptr(u_final), B, N, V, _ptr(out), _ptr(n_out), _ptr(path),
                                        out_cols, _ptr(status), _stream(stream)))
     return out, n_out, path
+
+
+def tv_kv_commit(k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, path, n_out, *, new_seq_lens=None,
+                 status=None, stream=None):
+    """Copy the accepted path's tree K/V rows into the paged cache (in place);
+    returns new_seq_lens int32 [B] = seq_lens + n_out."""
+    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_tree, "k_tree"), (v_tree, "v_tree")):
+        _dev(t, nm, (torch.float32, torch.bfloat16))
+    for t, nm in ((block_table, "block_table"), (seq_lens, "seq_lens"), (path, "path"), (n_out, "n_out")):
+        _dev(t, nm, (torch.int32,))
+    num_blocks, Hkv, bs, D = k_cache.shape
+    B, N = k_tree.shape[0], k_tree.shape[1]
+    if new_seq_lens is None:
+        new_seq_lens = torch.empty_like(seq_lens)
+    _check("tv_kv_commit",
+           lib().tv_kv_commit(_ptr(k_cache), _ptr(v_cache), num_blocks, bs, _ptr(block_table), block_table.shape[1],
+                              _ptr(seq_lens), _ptr(new_seq_lens), _ptr(k_tree), _ptr(v_tree), _ptr(path),
+                              path.shape[1], _ptr(n_out), B, N, Hkv, D, _code(k_cache.dtype), _ptr(status),
+                              _stream(stream)))
+    return new_seq_lens

@@ -154,18 +154,20 @@ def block_table_for(seq_lens, block_size, seed, spare_blocks=0):
     return table, max(total, 1)
 
 
-def attention_inputs(w: Workload, device="cpu", seq_lens=None, n_nodes=None, tree_scale=1.0):
+def attention_inputs(w: Workload, device="cpu", seq_lens=None, n_nodes=None, tree_scale=1.0, reserve=0):
     """Q, paged K/V cache, block table, prefix lengths and tree K/V ~ N(0, 1).
 
     Returns a dict of tensors on ``device``: q [B, N, Hq, D], k_cache/v_cache
     [num_blocks, Hkv, block_size, D], block_table [B, max_blocks] int32,
     seq_lens [B] int32, k_tree/v_tree [B, N, Hkv, D]; values in ``w.dtype``.
-    ``tree_scale`` multiplies the tree keys (mask-sensitivity cases).
+    ``tree_scale`` multiplies the tree keys (mask-sensitivity cases);
+    ``reserve`` places blocks for that many positions past each prefix (room
+    to commit an accepted path).
     """
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     N = w.n_nodes if n_nodes is None else int(n_nodes)
     lens = prefix_lengths(w) if seq_lens is None else np.asarray(seq_lens, dtype=np.int32)
-    table, num_blocks = block_table_for(lens, w.block_size, w.seed * 1000 + 13)
+    table, num_blocks = block_table_for(lens + int(reserve), w.block_size, w.seed * 1000 + 13)
     g = _gen(w.seed * 1000 + 17, device)
 
     def randn(*shape):
