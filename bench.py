@@ -179,15 +179,21 @@ def attention_bytes(w, lens, N, esize):
 
 # --------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample_run(w, inp_cpu, paths, greedy, sample, requests):
+def request_paths(w):
+    """Rank paths of every request's tree: one best-first tree per request for
+    a dynamic workload, else the workload's static tree for all."""
+    return W.dynamic_rank_paths(w) if w.dynamic else [w.paths()] * w.B
+
+
+def oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, requests):
     """The oracle on a list of requests (all nodes, all heads) plus acceptance."""
     from oracle import accept as OA
     from oracle import attention as OAt
     from oracle import tree as OT
 
-    parent, depth, rows, _ = OT.build_tree(paths)
-    OT.tree_mask_batch(np.broadcast_to(parent, (len(requests), parent.size)), inp_cpu["seq_lens"][requests])
     for b in requests:
+        parent, depth, rows, _ = OT.build_tree(req_paths[b])
+        OT.tree_mask_batch(parent[None], inp_cpu["seq_lens"][b:b + 1])
         sl = slice(b, b + 1)
         OAt.tree_attention(inp_cpu["q"][sl], inp_cpu["k_cache"], inp_cpu["v_cache"], inp_cpu["block_table"][sl],
                            inp_cpu["seq_lens"][sl], inp_cpu["k_tree"][sl], inp_cpu["v_tree"][sl], parent)
@@ -222,12 +228,12 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def time_oracle(w, inp_cpu, paths, greedy, sample, seconds, order):
+def time_oracle(w, inp_cpu, req_paths, greedy, sample, seconds, order):
     """Times the oracle request by request until `seconds` elapse; returns
     (nodes/s, requests used, elapsed)."""
     done, t0 = [], time.perf_counter()
     for b in order:
-        oracle_sample_run(w, inp_cpu, paths, greedy, sample, [b])
+        oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, [b])
         done.append(int(b))
         if time.perf_counter() - t0 >= seconds:
             break
@@ -249,10 +255,15 @@ class Step:
         from speculative_decoding_tree_attn_gb300 import capi
         self.capi, self.w, self.dev = capi, w, dev
         self.paths = w.paths()
+        self.req_paths = request_paths(w)
         # blocks placed for max_depth + 1 positions past each prefix: room to
         # commit the accepted path (timed separately, see kv_commit)
         self.inp = W.attention_inputs(w, device=dev, reserve=w.max_depth + 1)
-        parent, depth, rows, _, n = capi.tv_tree_build(self.paths)
+        if w.dynamic:  # one tree per request: parent [B, N]
+            parent = np.stack([capi.tv_tree_build(p)[0] for p in self.req_paths]).astype(np.int32)
+            n = parent.shape[1]
+        else:
+            parent, depth, rows, _, n = capi.tv_tree_build(self.paths)
         self.N = n
         self.parent = torch.from_numpy(parent).to(dev)
         B = w.B
@@ -319,16 +330,20 @@ class Step:
         workload has no acceptance) as (path int32 [B, cols], n_out int32 [B])."""
         if self.greedy is not None or self.sample is not None:
             return self.acc_path, self.acc_n
-        par = self.parent.cpu().numpy()
-        depth = np.zeros(par.size, dtype=np.int64)
-        for i in range(1, par.size):
-            depth[i] = depth[par[i]] + 1
-        chain = [int(np.argmax(depth))]
-        while chain[-1] != 0:
-            chain.append(int(par[chain[-1]]))
-        chain = chain[::-1]
-        path = torch.tensor([chain] * self.w.B, dtype=torch.int32, device=self.dev)
-        n = torch.full((self.w.B,), len(chain), dtype=torch.int32, device=self.dev)
+        par_all = self.parent.cpu().numpy().reshape(-1, self.N)
+        chains = []
+        for b in range(self.w.B):
+            par = par_all[b % par_all.shape[0]]
+            depth = np.zeros(par.size, dtype=np.int64)
+            for i in range(1, par.size):
+                depth[i] = depth[par[i]] + 1
+            chain = [int(np.argmax(depth))]
+            while chain[-1] != 0:
+                chain.append(int(par[chain[-1]]))
+            chains.append(chain[::-1])
+        cols = max(len(c) for c in chains)
+        path = torch.tensor([c + [0] * (cols - len(c)) for c in chains], dtype=torch.int32, device=self.dev)
+        n = torch.tensor([len(c) for c in chains], dtype=torch.int32, device=self.dev)
         return path, n
 
     def run_commit(self, path, n_out, new_lens):
@@ -476,7 +491,7 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp_cpu, g, s = cpu_inputs(w, st.inp, st.greedy, st.sample)
-        nps, used, el = time_oracle(w, inp_cpu, st.paths, g, s, args.cpu_seconds, sample_order(st.lens))
+        nps, used, el = time_oracle(w, inp_cpu, st.req_paths, g, s, args.cpu_seconds, sample_order(st.lens))
         cpu = {"value": nps, "unit": "nodes/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{len(used)} of {w.B} requests (all {st.N} nodes, all {w.Hq} heads, acceptance incl.), "
                          f"prefix lengths {[int(st.lens[b]) for b in used][:6]}..., {el:.1f} s"}
@@ -490,6 +505,7 @@ def run_ours(args, world, rank, local):
             "data": "synthetic (seeded; no model weights)",
             "config": {"workload": w.name, "B": w.B, "N": st.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab,
+                       "tree": "one per request" if w.dynamic else "shared",
                        "l2": ("L2 flushed between steps" if flush is not None
                               else f"inputs larger than L2 ({ws_bytes / 2**30:.2f} GiB per step)"),
                        "kernel_flags": args.flags, "parallelism": f"replicas x{world} (requests sharded)",
@@ -507,21 +523,21 @@ def run_reference(args, world, rank):
         return
     w = W.WORKLOADS[args.workload]
     inp = W.attention_inputs(w, device="cpu")
-    parent = None
     from oracle import tree as OT
-    parent = OT.build_tree(w.paths())[0]
+    req_paths = request_paths(w)
+    parent = (np.stack([OT.build_tree(p)[0] for p in req_paths]) if w.dynamic else OT.build_tree(w.paths())[0])
     greedy = W.greedy_inputs(w, parent, device="cpu") if w.accept == "greedy" else None
     sample = W.sample_chain_inputs(w, device="cpu") if w.accept == "sample" else None
     inp_cpu, g, s = cpu_inputs(w, inp, greedy, sample)
     lens = inp_cpu["seq_lens"]
     order = sample_order(lens)
     for k in range(args.warmup):
-        oracle_sample_run(w, inp_cpu, w.paths(), g, s, [order[k % len(order)]])
+        oracle_sample_run(w, inp_cpu, req_paths, g, s, [order[k % len(order)]])
     t0 = time.perf_counter()
     used = []
     for k in range(args.steps):
         b = order[k % len(order)]
-        oracle_sample_run(w, inp_cpu, w.paths(), g, s, [b])
+        oracle_sample_run(w, inp_cpu, req_paths, g, s, [b])
         used.append(b)
     el = time.perf_counter() - t0
     value = args.steps * w.n_nodes / el
@@ -533,7 +549,8 @@ def run_reference(args, world, rank):
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded; no model weights)",
         "config": {"workload": w.name, "B": w.B, "N": w.n_nodes, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab},
+                   "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab,
+                   "tree": "one per request" if w.dynamic else "shared"},
         "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle",
                          "sample": f"one request per step (all {w.n_nodes} nodes, all heads, acceptance incl.), "
                                    f"requests {used[:6]}..."},

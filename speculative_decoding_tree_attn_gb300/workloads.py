@@ -96,10 +96,28 @@ class Workload:
     accept: str = "none"       # "none" | "greedy" | "sample"
     vocab: int = 0
     sample_max_draft: int = 4
+    dynamic: bool = False      # one tree per request (dynamic_rank_paths)
     notes: str = field(default="", compare=False)
 
     def paths(self):
         return best_first_paths(self.rank_probs, self.n_nodes, self.max_depth)
+
+
+def dynamic_rank_paths(w: Workload, B=None):
+    """One tree per request with the workload's node budget, as dynamic trees
+    (EAGLE-2 / DDTree-style budgeted best-first selection) build them: each
+    request's per-rank confidences are drawn around the workload's rank
+    probabilities (Dirichlet, concentration 20, sorted so rank 0 stays the
+    most likely) and its tree is the best-first selection under them."""
+    B = w.B if B is None else B
+    rng = np.random.default_rng(w.seed * 1000 + 29)
+    base = np.asarray(w.rank_probs, dtype=np.float64)
+    total = float(base.sum())
+    out = []
+    for _ in range(B):
+        conf = np.sort(rng.dirichlet(base / total * 20.0) * total)[::-1]
+        out.append(best_first_paths(tuple(float(x) for x in conf), w.n_nodes, w.max_depth))
+    return out
 
 
 WORKLOADS = {
@@ -119,6 +137,10 @@ WORKLOADS = {
         Workload("b256_l2k_4k_n10_sample", 256, 32, 8, 128, "bf16", ("uniform", 2048, 4096), 16,
                  PAGE_TREE_RANK_PROBS, 10, 4, 5, accept="sample", vocab=128000,
                  sample_max_draft=4),
+        Workload("b64_l1k_8k_n64_dynamic", 64, 32, 8, 128, "bf16", ("uniform", 1024, 8192), 16,
+                 (0.45, 0.2, 0.12, 0.08, 0.06, 0.04, 0.03, 0.02), 64, 6, 6,
+                 accept="greedy", vocab=32000, dynamic=True,
+                 notes="the 64-request workload with one best-first tree per request"),
     ]
 }
 
@@ -206,20 +228,26 @@ def greedy_inputs(w: Workload, parent, device="cpu", rank_probs=None, B=None):
     At each node the target's choice is the draft token of its rank-k child
     with probability rank_probs[k] (when that child exists), otherwise a token
     that no child carries.  Sibling draft tokens are distinct.  ``parent`` is
-    the [N] parent array of the static tree.
+    the [N] parent array of the static tree, or [B, N] for one tree per
+    request.
     """
     rank_probs = w.rank_probs if rank_probs is None else rank_probs
     B = w.B if B is None else B
     V = w.vocab
     parent = np.asarray(parent)
-    N = parent.size
+    N = parent.shape[-1]
     rng = np.random.default_rng(w.seed * 1000 + 19)
-    rank = sibling_rank(parent)
-    kids = [[c for c in range(N) if parent[c] == n] for n in range(N)]
+    shared = parent.ndim == 1
+    if shared:
+        rank = sibling_rank(parent)
+        kids = [[c for c in range(N) if parent[c] == n] for n in range(N)]
     tokens = np.zeros((B, N), dtype=np.int32)
     choice = np.zeros((B, N), dtype=np.int64)
     cum = np.cumsum(np.asarray(rank_probs, dtype=np.float64))
     for b in range(B):
+        if not shared:  # one tree per request: parent [B, N]
+            rank = sibling_rank(parent[b])
+            kids = [[c for c in range(N) if parent[b, c] == n] for n in range(N)]
         for n in range(N):
             ks = kids[n]
             toks = rng.integers(0, V, size=len(ks) + 1)
