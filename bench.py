@@ -282,7 +282,8 @@ class Step:
         if w.accept == "greedy":
             self.greedy = W.greedy_inputs(w, parent, device=dev)
         elif w.accept == "sample":
-            self.sample = W.sample_chain_inputs(w, device=dev)
+            self.sample = (W.sample_tree_inputs(w, parent, device=dev) if w.sample_tree
+                           else W.sample_chain_inputs(w, device=dev))
         cols = n if self.sample is None else self.sample["p"].shape[1]
         self.acc_out = torch.empty(B, cols, dtype=torch.int32, device=dev)
         self.acc_n = torch.empty(B, dtype=torch.int32, device=dev)
@@ -527,7 +528,9 @@ def run_reference(args, world, rank):
     req_paths = request_paths(w)
     parent = (np.stack([OT.build_tree(p)[0] for p in req_paths]) if w.dynamic else OT.build_tree(w.paths())[0])
     greedy = W.greedy_inputs(w, parent, device="cpu") if w.accept == "greedy" else None
-    sample = W.sample_chain_inputs(w, device="cpu") if w.accept == "sample" else None
+    sample = None
+    if w.accept == "sample":
+        sample = W.sample_tree_inputs(w, parent, device="cpu") if w.sample_tree else W.sample_chain_inputs(w, device="cpu")
     inp_cpu, g, s = cpu_inputs(w, inp, greedy, sample)
     lens = inp_cpu["seq_lens"]
     order = sample_order(lens)

@@ -97,6 +97,7 @@ class Workload:
     vocab: int = 0
     sample_max_draft: int = 4
     dynamic: bool = False      # one tree per request (dynamic_rank_paths)
+    sample_tree: bool = False  # "sample" on the attention tree (sample_tree_inputs), else on chains
     notes: str = field(default="", compare=False)
 
     def paths(self):
@@ -141,6 +142,10 @@ WORKLOADS = {
                  (0.45, 0.2, 0.12, 0.08, 0.06, 0.04, 0.03, 0.02), 64, 6, 6,
                  accept="greedy", vocab=32000, dynamic=True,
                  notes="the 64-request workload with one best-first tree per request"),
+        Workload("b64_l1k_8k_n64_sample", 64, 32, 8, 128, "bf16", ("uniform", 1024, 8192), 16,
+                 (0.45, 0.2, 0.12, 0.08, 0.06, 0.04, 0.03, 0.02), 64, 6, 7,
+                 accept="sample", vocab=32000, sample_tree=True,
+                 notes="the 64-request workload verified stochastically on its tree (i.i.d. siblings)"),
     ]
 }
 
@@ -296,6 +301,45 @@ def sample_chain_inputs(w: Workload, device="cpu", B=None, V=None, max_draft=Non
         "p": p.float().contiguous(), "q": q.float().contiguous(), "tokens": tokens,
         "n_nodes": torch.from_numpy(num_draft + 1).to(device),
         "parent": torch.from_numpy(parent).to(device),
+        "u_accept": torch.from_numpy(u_accept).to(device),
+        "u_final": torch.from_numpy(u_final).to(device),
+    }
+
+
+def sample_tree_inputs(w: Workload, parent, device="cpu", B=None, V=None, noise_std=0.5,
+                       logit_std=math.sqrt(2.0)):
+    """Tree verifier inputs with i.i.d. siblings: p = softmax(logits),
+    q = softmax(logits + noise) per node, and every child's token drawn on
+    its own from its parent's q row (siblings may repeat, as when a drafter
+    samples several candidates with replacement).
+
+    parent int [N] (shared) or [B, N].  Returns p, q [B, N, V] float32, tokens
+    [B, N] int32 (column 0 unused), n_nodes [B] = N, parent as given (int32),
+    u_accept [B, N] and u_final [B] float32 U[0, 1).
+    """
+    B = w.B if B is None else B
+    V = w.vocab if V is None else V
+    par = np.asarray(parent, dtype=np.int64)
+    N = par.shape[-1]
+    g = _gen(w.seed * 1000 + 37, device)
+    logits = torch.randn(B, N, V, generator=g, device=device) * logit_std
+    p = torch.softmax(logits, dim=-1)
+    logits += torch.randn(B, N, V, generator=g, device=device) * noise_std
+    q = torch.softmax(logits, dim=-1)
+    del logits
+    tokens = torch.zeros(B, N, dtype=torch.int32, device=device)
+    if N > 1:
+        pb = np.broadcast_to(par, (B, N))[:, 1:]
+        rows = q[torch.arange(B, device=device)[:, None], torch.from_numpy(np.ascontiguousarray(pb)).to(device)]
+        draws = torch.multinomial(rows.reshape(B * (N - 1), V), 1, generator=g).reshape(B, N - 1)
+        tokens[:, 1:] = draws.to(torch.int32)
+    rng = np.random.default_rng(w.seed * 1000 + 41)
+    u_accept = rng.random((B, N), dtype=np.float32)
+    u_final = rng.random(B, dtype=np.float32)
+    return {
+        "p": p.contiguous(), "q": q.contiguous(), "tokens": tokens,
+        "n_nodes": torch.full((B,), N, dtype=torch.int32, device=device),
+        "parent": torch.from_numpy(np.ascontiguousarray(par.astype(np.int32))).to(device),
         "u_accept": torch.from_numpy(u_accept).to(device),
         "u_final": torch.from_numpy(u_final).to(device),
     }

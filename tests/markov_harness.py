@@ -38,8 +38,33 @@ def draft_round(parent, state0, qt, rng):
     return tokens, state
 
 
-def generate(verify, pt, qt, parent, n_seq, n_tokens, seed, batch=None):
-    """Sequences of ``n_tokens`` tokens from repeated draft/verify rounds."""
+def processed(table, temperature=1.0, top_p=1.0):
+    """A sampler's processing of probability rows: temperature (p^(1/T),
+    renormalised -- softmax(logits / T) of the same logits), then top-p (keep
+    the most probable tokens, highest first and ties by lower index, up to
+    and including the one where the kept mass first reaches top_p; the rest
+    set to zero and the kept mass renormalised).  Returns float32 rows."""
+    t = np.asarray(table, dtype=np.float64) ** (1.0 / temperature)
+    t /= t.sum(axis=-1, keepdims=True)
+    order = np.argsort(-t, axis=-1, kind="stable")
+    sorted_t = np.take_along_axis(t, order, axis=-1)
+    before = np.cumsum(sorted_t, axis=-1) - sorted_t    # mass ahead of each token
+    keep_sorted = before < top_p
+    keep = np.zeros_like(keep_sorted)
+    np.put_along_axis(keep, order, keep_sorted, axis=-1)
+    t = np.where(keep, t, 0.0)
+    t /= t.sum(axis=-1, keepdims=True)
+    return t.astype(np.float32)
+
+
+def generate(verify, pt, qt, parent, n_seq, n_tokens, seed, batch=None, pt_verify=None, qt_verify=None):
+    """Sequences of ``n_tokens`` tokens from repeated draft/verify rounds.
+
+    The drafter samples from ``qt``; the verifier is handed ``pt_verify`` and
+    ``qt_verify`` (default: ``pt`` and ``qt``), so a test can give it rows
+    that differ from the ones actually sampled."""
+    pt_v = pt if pt_verify is None else pt_verify
+    qt_v = qt if qt_verify is None else qt_verify
     V = pt.shape[1]
     start = V
     parent = np.asarray(parent)
@@ -53,8 +78,8 @@ def generate(verify, pt, qt, parent, n_seq, n_tokens, seed, batch=None):
         if active.size == 0:
             break
         tokens, state = draft_round(parent, last[active], qt, rng)
-        p = pt[state].astype(np.float32)
-        q = qt[state].astype(np.float32)
+        p = pt_v[state].astype(np.float32)
+        q = qt_v[state].astype(np.float32)
         n_nodes = np.full(active.size, N, dtype=np.int32)
         u_accept = rng.random((active.size, N), dtype=np.float32)
         u_final = rng.random(active.size, dtype=np.float32)
@@ -85,6 +110,27 @@ def chi_square(seqs, pt):
         expect[cell] = pr
     expect *= seqs.shape[0]
     return float(((counts - expect) ** 2 / expect).sum())
+
+
+def chi_square_support(seqs, pt):
+    """Chi-square over the cells the target can produce, for targets with
+    zero entries: returns (statistic, degrees of freedom, sequences that fell
+    in a zero-probability cell)."""
+    V = pt.shape[1]
+    n_tokens = seqs.shape[1]
+    counts = np.zeros((V,) * n_tokens)
+    np.add.at(counts, tuple(seqs.T), 1)
+    expect = np.zeros_like(counts)
+    for cell in itertools.product(range(V), repeat=n_tokens):
+        pr, prev = 1.0, V
+        for t in cell:
+            pr *= float(pt[prev, t])
+            prev = t
+        expect[cell] = pr
+    expect *= seqs.shape[0]
+    live = expect > 0
+    stat = float(((counts[live] - expect[live]) ** 2 / expect[live]).sum())
+    return stat, int(live.sum()) - 1, int(counts[~live].sum())
 
 
 def chain_adapter(verify_chain, **kw):

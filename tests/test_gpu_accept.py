@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from markov_harness import chi_square, generate
+from markov_harness import chi_square, chi_square_support, generate, processed
 from oracle import accept as OA
 from oracle import tree as OT
 from speculative_decoding_tree_attn_gb300 import capi
@@ -93,6 +93,22 @@ def test_sample_full_workload_bit_exact():
     np.testing.assert_array_equal(res[1].cpu().numpy(), n_c)
 
 
+def test_sample_tree_full_workload_bit_exact():
+    """B=64 requests verified stochastically on the 64-node tree over a
+    32000-token vocabulary, siblings drawn i.i.d. from their parent's q."""
+    w = W.WORKLOADS["b64_l1k_8k_n64_sample"]
+    parent, *_ = OT.build_tree(w.paths())
+    s = W.sample_tree_inputs(w, parent, device="cuda")
+    res = capi.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
+                                     n_nodes=s["n_nodes"])
+    c = {k: v.cpu().numpy() for k, v in s.items()}
+    ref = OA.tree_accept_sample(c["p"], c["q"], c["tokens"], c["parent"], c["n_nodes"], c["u_accept"], c["u_final"])
+    _cmp(res, *ref)
+    # walks leave the root's level and end both by rejection and at leaves
+    n = res[1].cpu().numpy()
+    assert n.mean() > 2.0 and n.min() >= 1
+
+
 @pytest.mark.parametrize("V", [4, 33, 1000, 4096])
 def test_sample_trees_with_sibling_levels(V):
     """Trees with up to 5 siblings per node: several residual levels per node."""
@@ -151,3 +167,17 @@ def test_gpu_tree_lossless_chi_square(verifier_facts):
     pt, qt = W.markov_tables(V, 22)
     seqs = generate(_gpu_verify, pt, qt, parent, 200_000, n_tok, 131)
     assert chi_square(seqs, pt) < thr
+
+
+def test_gpu_sample_processed_target_lossless(verifier_facts):
+    """Temperature / top-p processed target and drafter rows: the GPU walk's
+    output follows the processed target."""
+    scipy_stats = pytest.importorskip("scipy.stats")
+    f = verifier_facts
+    V, n_tok = int(f["chi2_vocab"][0][0]), int(f["chi2_tokens"][0][0])
+    parent, *_ = OT.build_tree([(0,), (1,), (2,), (0, 0), (2, 0)])
+    pt, qt = W.markov_tables(V, 22)
+    pp, qp = processed(pt, 0.8, 0.9), processed(qt, 1.3, 0.95)
+    seqs = generate(_gpu_verify, pp, qp, parent, 100_000, n_tok, 132)
+    stat, df, outside = chi_square_support(seqs, pp)
+    assert outside == 0 and stat < scipy_stats.chi2.ppf(0.999, df)

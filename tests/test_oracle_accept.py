@@ -6,7 +6,11 @@ decoding of a deterministic target.  Stochastic: the sampling page's 2.533
 acceptance check and its 2.19 no-bonus figure, the chi-square losslessness
 test with its negative controls, the page's small checks (p = q, zero drafts,
 empty batch, one-hot target), an exact-rational brute force of the fixed-point
-row sampler, and agreement of the tree walk with the chain verifier.
+row sampler, and agreement of the tree walk with the chain verifier.  The
+sampling page's processed-distribution note: with temperature / top-p
+applied to p (and q as the drafter sampled it) the walk is lossless with
+respect to the processed target, and handing it unprocessed rows shows up as
+bias.
 """
 
 import math
@@ -19,7 +23,7 @@ from oracle import accept as A
 from oracle import tree as T
 from speculative_decoding_tree_attn_gb300 import workloads as W
 
-from markov_harness import chain_adapter, chi_square, generate
+from markov_harness import chain_adapter, chi_square, chi_square_support, generate, processed
 
 
 def page_tree():
@@ -326,3 +330,55 @@ def test_tree_siblings_against_raw_target_fail(verifier_facts):
         return out, n_out
     seqs = generate(verify, pt, qt, parent, 40_000, n_tok, 23)
     assert chi_square(seqs, pt) > thr
+
+
+# ---------------------------------------------------------------- processed distributions
+
+def test_processing_helper():
+    """The harness's sampler processing: identity at T = 1, top_p = 1; the
+    softmax(logits / T) form; a hand-worked top-p cut."""
+    rng = np.random.default_rng(24)
+    t = rng.dirichlet(np.ones(6), size=5)
+    np.testing.assert_allclose(processed(t), t, rtol=1e-6)
+    logits = rng.standard_normal((3, 8))
+    e = np.exp(logits / 0.6)
+    np.testing.assert_allclose(processed(np.exp(logits) / np.exp(logits).sum(-1, keepdims=True), 0.6),
+                               e / e.sum(-1, keepdims=True), rtol=1e-5)
+    np.testing.assert_allclose(processed(np.array([[0.15, 0.5, 0.05, 0.3]]), 1.0, 0.8), [[0, 0.625, 0, 0.375]],
+                               rtol=1e-6)
+    np.testing.assert_allclose(processed(np.array([[0.15, 0.5, 0.05, 0.3]]), 1.0, 0.81),
+                               [[0.15 / 0.95, 0.5 / 0.95, 0, 0.3 / 0.95]], rtol=1e-6)
+
+
+def _processed_tables(V):
+    pt, qt = W.markov_tables(V, 22)
+    # the target samples at T = 0.8 with top-p 0.9; the drafter at its own T = 1.3, top-p 0.95
+    return pt, qt, processed(pt, 0.8, 0.9), processed(qt, 1.3, 0.95)
+
+
+def _tree_verify(p, q, tokens, par, n_nodes, ua, uf):
+    out, n_out, _ = A.tree_accept_sample(p, q, tokens, par, n_nodes, ua, uf)
+    return out, n_out
+
+
+def test_processed_target_lossless(verifier_facts):
+    scipy_stats = pytest.importorskip("scipy.stats")
+    V, _, n_tok, _, _ = _markov_facts(verifier_facts)
+    parent, *_ = T.build_tree(TREES["three_iid_siblings"])
+    pt, qt, pp, qp = _processed_tables(V)
+    seqs = generate(_tree_verify, pp, qp, parent, 40_000, n_tok, 23)
+    stat, df, outside = chi_square_support(seqs, pp)
+    assert outside == 0 and df < V ** n_tok - 1       # top-p removed some cells
+    assert stat < scipy_stats.chi2.ppf(0.999, df)
+
+
+@pytest.mark.parametrize("wrong", ["raw_p", "raw_q"])
+def test_mismatched_processing_is_bias(verifier_facts, wrong):
+    scipy_stats = pytest.importorskip("scipy.stats")
+    V, _, n_tok, _, _ = _markov_facts(verifier_facts)
+    parent, *_ = T.build_tree(TREES["three_iid_siblings"])
+    pt, qt, pp, qp = _processed_tables(V)
+    kw = {"pt_verify": pt} if wrong == "raw_p" else {"qt_verify": qt}
+    seqs = generate(_tree_verify, pp, qp, parent, 40_000, n_tok, 23, **kw)
+    stat, df, outside = chi_square_support(seqs, pp)
+    assert stat > scipy_stats.chi2.ppf(0.999, df) or outside > 0
