@@ -70,6 +70,12 @@ extern "C" {
  * rounding; for testing the second merge route. */
 #define TV_ATTN_PUBLISH_ALL 4
 
+/* Kernel selection of tv_tree_accept_sample. */
+#define TV_SAMPLE_AUTO 0        /* cluster kernel when every request's cluster is resident at once */
+#define TV_SAMPLE_CLUSTER 1     /* one 8-CTA cluster per request, level weights in shared memory;
+                                   TV_ERR_UNSUPPORTED when V > 136,512                            */
+#define TV_SAMPLE_SINGLE_CTA 2  /* one CTA per request, rows streamed, weights recomputed per pass */
+
 /* Description of the last failure on this thread ("" if none). */
 const char* tv_last_error(void);
 
@@ -312,13 +318,20 @@ int tv_tree_accept_greedy(const float* logits, const int32_t* target_argmax,
  * u_final   device float32 [B]: uniform of the replacement / bonus draw.
  * out, n_out, path, out_cols, status: as in tv_tree_accept_greedy.  Tokens
  * outside [0, V) are skipped and flagged TV_DEV_BAD_TOKEN.
+ * flags     TV_SAMPLE_*: both kernels give bit-identical results.  The
+ *           cluster kernel splits each row over 8 CTAs and keeps the current
+ *           level's weights and q in shared memory (12 bytes per vocabulary
+ *           entry), so repeated rejections at a node cost one shared-memory
+ *           pass each; TV_SAMPLE_AUTO uses it when all B clusters fit on the
+ *           device at once, else the single-CTA kernel.  Unknown flags give
+ *           TV_ERR_INVALID_ARG.
  */
 int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,
                           const int32_t* parent, int64_t parent_bstride,
                           const int32_t* n_nodes, const float* u_accept,
                           const float* u_final, int32_t B, int32_t N, int32_t V,
                           int32_t* out, int32_t* n_out, int32_t* path, int32_t out_cols,
-                          int32_t* status, void* stream);
+                          int32_t flags, int32_t* status, void* stream);
 
 /*
  * tv_kv_commit -- device, asynchronous.  Copies the accepted path's tree K/V

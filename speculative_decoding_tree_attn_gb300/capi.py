@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libtreeverify.so")
 TV_F32, TV_BF16 = 0, 1
 TV_ATTN_AUTO, TV_ATTN_SIMT, TV_ATTN_TCGEN05 = 0, 1, 2
 TV_ATTN_PUBLISH_ALL = 4
+TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA = 0, 1, 2
 TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 STATUS_NAMES = {0: "TV_OK", -1: "TV_ERR_INVALID_ARG", -2: "TV_ERR_MISSING_PARENT", -3: "TV_ERR_TOO_MANY_NODES",
                 -4: "TV_ERR_UNSUPPORTED", -5: "TV_ERR_WORKSPACE", -6: "TV_ERR_CUDA"}
@@ -43,7 +44,7 @@ SIGNATURES = {
     "tv_tree_attn_static_workspace_bytes": (ctypes.c_size_t, []),
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
-                                             _P, _P]),
+                                             _I32, _P, _P]),
     "tv_kv_commit": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
                                     _I32, _I32, _P, _P]),
 }
@@ -272,8 +273,9 @@ def tv_tree_accept_greedy(tokens, parent, *, logits=None, target_argmax=None, n_
 
 
 def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=None, out_cols=None, out=None,
-                          n_out=None, path=None, status=None, stream=None):
-    """Stochastic walk; returns (out [B, out_cols], n_out [B], path [B, out_cols])."""
+                          n_out=None, path=None, flags=0, status=None, stream=None):
+    """Stochastic walk; returns (out [B, out_cols], n_out [B], path [B, out_cols]).
+    flags: TV_SAMPLE_AUTO / TV_SAMPLE_CLUSTER / TV_SAMPLE_SINGLE_CTA."""
     _dev(p, "p", (torch.float32,))
     _dev(q, "q", (torch.float32,))
     _dev(tokens, "tokens", (torch.int32,))
@@ -287,7 +289,7 @@ def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=No
     _check("tv_tree_accept_sample",
            lib().tv_tree_accept_sample(_ptr(p), _ptr(q), _ptr(tokens), _ptr(parent), bstride, _ptr(n_nodes),
                                        _ptr(u_accept), _ptr(u_final), B, N, V, _ptr(out), _ptr(n_out), _ptr(path),
-                                       out_cols, _ptr(status), _stream(stream)))
+                                       out_cols, int(flags), _ptr(status), _stream(stream)))
     return out, n_out, path
 
 

@@ -1,4 +1,6 @@
-// Tree acceptance on the device: one CTA of 1024 threads per request.
+// Tree acceptance on the device: one thread-block cluster per request (one
+// CTA per request for target choices given directly, and for stochastic
+// verification over vocabularies too large for the cluster's shared memory).
 //
 // Greedy ("Build the tree attention mask that verifies a draft tree in one
 // pass", "The mask."; "Encode branch histories in masks and positions"): from
@@ -23,12 +25,16 @@
 //   level m >= 1       : accept iff fl64(fl64(u * q(x)) * W_m) < w_m(x)
 //   final draw         : min(#{x : prefix_sum(w)(x) < ceil(fl64(u_final * W))}, V - 1)
 //
-// A pass over a level's row leaves the weight total of every 128-element
-// chunk in shared memory, so the draw re-reads only the chunk that holds the
-// crossing.
+// The cluster sampler keeps each CTA's vocabulary slice of the current
+// level's weights in shared memory; the single-CTA sampler streams the row
+// and leaves the weight total of every chunk in shared memory, so its draw
+// re-reads only the chunk that holds the crossing.
 #include <cooperative_groups.h>
 
 #include <climits>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.h"
 
@@ -43,8 +49,22 @@ __device__ __forceinline__ unsigned long long gtimer() {
   return t;
 }
 #define TV_SAMPLE_T(k) do { if (threadIdx.x == 0 && blockIdx.x < 4096) g_sample_t[blockIdx.x][k] = gtimer(); } while (0)
+// Cluster sampler, per request (rank 0, thread 0): start, end, passes, pass
+// compute time, exchange time, node-entry time, final-draw time, nodes.
+__device__ unsigned long long g_sc_t[4096][8];
+#define TV_SC_DECL unsigned long long sc_tr[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sc_t0 = 0
+#define TV_SC_MARK() do { sc_t0 = gtimer(); } while (0)
+#define TV_SC_ADD(k) do { const unsigned long long t_ = gtimer(); sc_tr[k] += t_ - sc_t0; sc_t0 = t_; } while (0)
+#define TV_SC_SET(k, v) do { sc_tr[k] = (v); } while (0)
+#define TV_SC_STORE(b) do { if (threadIdx.x == 0 && rank == 0 && (b) < 4096) \
+    for (int i_ = 0; i_ < 8; ++i_) g_sc_t[b][i_] = sc_tr[i_]; } while (0)
 #else
 #define TV_SAMPLE_T(k) do { } while (0)
+#define TV_SC_DECL do { } while (0)
+#define TV_SC_MARK() do { } while (0)
+#define TV_SC_ADD(k) do { } while (0)
+#define TV_SC_SET(k, v) do { } while (0)
+#define TV_SC_STORE(b) do { } while (0)
 #endif
 
 constexpr int kThreads = 1024;
@@ -753,6 +773,327 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
   finish_walk(o, b, k);
 }
 
+// ------------------------------------------------------ stochastic, cluster
+
+// The same walk with the vocabulary cut into kScCtas slices, one per CTA of a
+// thread-block cluster.  Each CTA keeps its slice of the current level's
+// weights w_m (uint64) and of q (float32) in shared memory, so a residual
+// pass after the first rejection at a node reads only shared memory and costs
+// O(1) per element, where the single-CTA kernel recomputes w_m from p and q
+// in O(m).  Slice totals are exchanged through distributed shared memory with
+// one cluster barrier per pass; every CTA takes the same accept decisions
+// from the same p(x), q(x) and totals, so all CTAs of a cluster follow one
+// control flow.
+constexpr int kScCtas = 8;
+constexpr int kScThreads = 256;
+constexpr int kScWarps = kScThreads / 32;
+constexpr int kScBatch = 4;                          // float4 of p (and q) a thread requests together
+constexpr size_t kScMaxDyn = 200 * 1024;             // shared memory for the slice state, at most
+
+// Slice length (elements, a multiple of 4) of a V-element row.
+inline int sc_slice(int V) { return (int)((tv::ceil_div(V, kScCtas) + 3) / 4 * 4); }
+
+__device__ __forceinline__ uint64_t sc_block_sum(uint64_t v, uint64_t* s_red) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  uint64_t t = 0;
+#pragma unroll
+  for (int i = 0; i < kScWarps; ++i) t += s_red[i];
+  __syncthreads();
+  return t;
+}
+
+// Level 0 (w = P) or level 1 (w = max(0, P - Q), and q kept) of the slice
+// [lo, lo + len) of a row, read from global memory into shared memory.
+// Returns this thread's part of the slice total.
+__device__ uint64_t sc_fill(const float* __restrict__ prow, const float* __restrict__ qrow, int lo, int len,
+                            bool vec, int level, uint64_t* w, float* qs) {
+  uint64_t acc = 0;
+  if (vec) {  // lo and len are multiples of 4, the row is 16-byte aligned
+    const float4* p4 = reinterpret_cast<const float4*>(prow + lo);
+    const float4* q4 = reinterpret_cast<const float4*>(qrow + lo);
+    const int n4 = len / 4;
+    for (int base = threadIdx.x; base < n4; base += kScBatch * kScThreads) {
+      float4 pv[kScBatch], qv[kScBatch];
+#pragma unroll
+      for (int j = 0; j < kScBatch; ++j) {
+        const int i = base + j * kScThreads;
+        pv[j] = qv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n4) {
+          pv[j] = __ldg(p4 + i);
+          if (level) qv[j] = __ldg(q4 + i);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kScBatch; ++j) {
+        const int i = base + j * kScThreads;
+        if (i >= n4) break;
+        const float ps[4] = {pv[j].x, pv[j].y, pv[j].z, pv[j].w};
+        const float qq[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+        uint64_t wv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int64_t P = fix40(ps[t]);
+          const int64_t Q = level ? fix40(qq[t]) : 0;
+          wv[t] = (uint64_t)(P > Q ? P - Q : 0);
+          acc += wv[t];
+        }
+        reinterpret_cast<ulonglong2*>(w)[2 * i] = make_ulonglong2(wv[0], wv[1]);
+        reinterpret_cast<ulonglong2*>(w)[2 * i + 1] = make_ulonglong2(wv[2], wv[3]);
+        if (level) reinterpret_cast<float4*>(qs)[i] = qv[j];
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < len; i += kScThreads) {
+      const int64_t P = fix40(__ldg(prow + lo + i));
+      float qx = 0.f;
+      if (level) qx = __ldg(qrow + lo + i);
+      const int64_t Q = level ? fix40(qx) : 0;
+      const uint64_t v = (uint64_t)(P > Q ? P - Q : 0);
+      w[i] = v;
+      if (level) qs[i] = qx;
+      acc += v;
+    }
+  }
+  return acc;
+}
+
+// Level m -> m + 1 in place (m >= 1): w = max(0, w - floor((W_m * Q + 2^39) / 2^40)).
+// With Q = H * 2^20 + L (the parts of fix40) the rounded product is
+// floor((W_m * H + floor((W_m * L + 2^39) / 2^20)) / 2^20), exactly (nested
+// floors of an integer plus a fraction), and both products fit in 64 bits:
+// W_m <= sum P <= 2^41 for rows summing to at most 2, H <= 2^21, L <= 2^20.
+// A weight that is already 0 stays 0.
+__device__ uint64_t sc_residual(int len, uint64_t Wm, uint64_t* w, const float* qs) {
+  uint64_t acc = 0;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < len; i += kScThreads) {
+    const uint64_t wv = w[i];
+    if (wv == 0) continue;
+    int32_t H, L;
+    fix40_parts(qs[i], H, L);
+    const uint64_t sub = (Wm * (uint64_t)H + ((Wm * (uint64_t)L + (1ull << 39)) >> 20)) >> 20;
+    const uint64_t v = wv > sub ? wv - sub : 0;
+    w[i] = v;
+    acc += v;
+  }
+  return acc;
+}
+
+// Publishes this CTA's slice total in slot `rank` of every CTA's s_tot[par]
+// and returns the cluster total.  s_tot is double-buffered by pass parity: a
+// CTA writes buffer par again only after the next pass's barrier, which every
+// CTA reaches after reading this pass's totals.
+__device__ uint64_t sc_exchange(cooperative_groups::cluster_group& cl, uint64_t mine,
+                                uint64_t (*s_tot)[kScCtas], int par, int rank) {
+  if (threadIdx.x < kScCtas) *cl.map_shared_rank(&s_tot[par][rank], (unsigned)threadIdx.x) = mine;
+  cl.sync();
+  uint64_t t = 0;
+#pragma unroll
+  for (int r = 0; r < kScCtas; ++r) t += s_tot[par][r];
+  return t;
+}
+
+__global__ void __launch_bounds__(kScThreads)
+    sample_cluster_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                          const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent, int64_t pstride,
+                          const int32_t* __restrict__ n_nodes, const float* __restrict__ u_accept,
+                          const float* __restrict__ u_final, int N, int V, int Ls, AcceptOut o) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
+  __shared__ uint64_t S[TV_MAX_NODES + 1];
+  __shared__ uint64_t s_tot[2][kScCtas];
+  __shared__ uint64_t s_lev[kScCtas];  // slice totals of the current level
+  __shared__ uint64_t s_red[kScWarps];
+  __shared__ int s_kid[TV_MAX_NODES];  // the current node's children in index order
+  __shared__ float s_kp[TV_MAX_NODES], s_kq[TV_MAX_NODES], s_ku[TV_MAX_NODES];  // their p(x), q(x), u
+  __shared__ int s_nk, s_x, s_flag;
+  __shared__ uint64_t s_thr;
+  extern __shared__ __align__(16) uint64_t sc_dyn[];
+  uint64_t* w = sc_dyn;
+  float* qs = reinterpret_cast<float*>(sc_dyn + Ls);
+  const int rank = (int)cl.block_rank();
+  const int b = blockIdx.x / kScCtas;
+  load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
+  if (threadIdx.x == 0) s_x = V - 1;  // read by rank 0 after the draw's barrier
+  __syncthreads();
+  const int n = clamp_nodes(n_nodes, b, N);
+  const int lo = min(rank * Ls, V), len = min(V - lo, Ls);
+  const bool vec = (V % 4 == 0) && (((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q)) & 15) == 0);
+  int node = 0, k = 0, pass = 0;
+  TV_SC_DECL;
+  TV_SC_MARK();
+  TV_SC_SET(0, sc_t0);
+  while (true) {
+    const float* prow = p + ((int64_t)b * N + node) * V;
+    const float* qrow = q + ((int64_t)b * N + node) * V;
+    int m = 0;
+    uint64_t Wm = 0;  // total of the current level (valid for m >= 1)
+    TV_SC_MARK();
+    TV_SC_SET(7, sc_tr[7] + 1);
+    if (threadIdx.x == 0) S[0] = 1ull << 40;
+    if (threadIdx.x < 32) {
+      // list the node's children with the row values their tests read, all
+      // loads in flight together
+      const int lane = threadIdx.x;
+      int cnt = 0;
+      for (int base = node + 1; base < n; base += 32) {
+        const int c = base + lane;
+        const bool is = c < n && s_par[c] == node;
+        const unsigned bal = __ballot_sync(0xffffffffu, is);
+        if (is) {
+          const int j = cnt + __popc(bal & ((1u << lane) - 1u));
+          const int x = s_tok[c];
+          const bool in_v = x >= 0 && x < V;
+          s_kid[j] = c;
+          s_kp[j] = in_v ? prow[x] : 0.f;
+          s_kq[j] = in_v ? qrow[x] : 0.f;
+          s_ku[j] = u_accept[(int64_t)b * N + c];
+        }
+        cnt += __popc(bal);
+      }
+      if (lane == 0) s_nk = cnt;
+    }
+    __syncthreads();
+    TV_SC_ADD(5);
+    const int nk = s_nk;
+    int taken = -1;
+    for (int j = 0; j < nk; ++j) {
+      const int c = s_kid[j], x = s_tok[c];
+      if (x < 0 || x >= V) {
+        if (rank == 0 && threadIdx.x == 0 && o.status) atomicOr(o.status, TV_DEV_BAD_TOKEN);
+        continue;
+      }
+      // one thread decides (double precision is slow here) and shares it;
+      // the pass after a rejection synchronises before s_flag is written again
+      if (threadIdx.x == 0) {
+        const float px = s_kp[j], qx = s_kq[j];
+        const double uq = __dmul_rn((double)s_ku[j], (double)qx);
+        s_flag = m == 0 ? uq < (double)px : __dmul_rn(uq, (double)Wm) < (double)level_weight(px, qx, S, m);
+      }
+      __syncthreads();
+      if (s_flag) { taken = c; break; }
+      // rejected: the target moves to the residual of the current level
+      TV_SC_MARK();
+      const uint64_t part = m == 0 ? sc_fill(prow, qrow, lo, len, vec, 1, w, qs) : sc_residual(len, Wm, w, qs);
+      TV_SC_ADD(3);
+      const uint64_t Wn = sc_exchange(cl, sc_block_sum(part, s_red), s_tot, pass & 1, rank);
+      TV_SC_ADD(4);
+      ++pass;
+      if (Wn > 0) {
+        ++m;
+        Wm = Wn;
+        if (threadIdx.x == 0) S[m] = Wn;
+        if (threadIdx.x < kScCtas) s_lev[threadIdx.x] = s_tot[(pass - 1) & 1][threadIdx.x];
+      } else if (m >= 1) {
+        // the level is kept: rebuild its weights, overwritten by the pass
+        for (int i = threadIdx.x; i < len; i += kScThreads)
+          w[i] = (uint64_t)level_weight(__ldg(prow + lo + i), __ldg(qrow + lo + i), S, m);
+      }
+      __syncthreads();
+    }
+    if (taken >= 0) {
+      if (rank == 0) emit(o, b, k, s_tok[taken], node);
+      ++k;
+      if (k == o.out_cols) {
+        if (rank == 0 && threadIdx.x == 0 && o.status) atomicOr(o.status, TV_DEV_OUT_OVERFLOW);
+        break;
+      }
+      node = taken;
+      continue;
+    }
+    // replacement (after rejections) or bonus (leaf / all children absent)
+    TV_SC_MARK();
+    if (m == 0) {
+      const uint64_t part = sc_fill(prow, qrow, lo, len, vec, 0, w, qs);
+      Wm = sc_exchange(cl, sc_block_sum(part, s_red), s_tot, pass & 1, rank);
+      if (threadIdx.x < kScCtas) s_lev[threadIdx.x] = s_tot[pass & 1][threadIdx.x];
+      ++pass;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) s_thr = (uint64_t)ceil(__dmul_rn((double)u_final[b], (double)Wm));
+    __syncthreads();
+    const uint64_t thr = s_thr;
+    uint64_t E = 0;  // weight of the slices before this one
+    for (int r = 0; r < rank; ++r) E += s_lev[r];
+    const uint64_t T = s_lev[rank];
+    if (thr == 0) {
+      if (rank == 0 && threadIdx.x == 0) s_x = 0;
+    } else if (T > 0 && E < thr && thr <= E + T) {
+      // the crossing lies in this slice: block scan over contiguous segments
+      const uint64_t t = thr - E;
+      const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+      const int seg = (len + kScThreads - 1) / kScThreads;
+      const int a = min((int)threadIdx.x * seg, len), e = min(a + seg, len);
+      uint64_t mine = 0;
+      for (int i = a; i < e; ++i) mine += w[i];
+      uint64_t incl = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint64_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (lane == 31) s_red[warp] = incl;
+      __syncthreads();
+      uint64_t ex = incl - mine;
+      for (int i = 0; i < warp; ++i) ex += s_red[i];
+      if (mine > 0 && ex < t && t <= ex + mine) {
+        uint64_t run = ex;
+        for (int i = a; i < e; ++i) {
+          run += w[i];
+          if (run >= t) {
+            *cl.map_shared_rank(&s_x, 0u) = lo + i;
+            break;
+          }
+        }
+      }
+    }
+    cl.sync();  // the crossing is in rank 0's s_x
+    TV_SC_ADD(6);
+    if (rank == 0) {
+      int x = s_x;
+      if (x > V - 1) x = V - 1;
+      emit(o, b, k, x, node);
+    }
+    ++k;
+    break;
+  }
+  cl.sync();  // no CTA leaves while a peer may still write to its shared memory
+  if (rank == 0) finish_walk(o, b, k);
+  TV_SC_SET(2, pass);
+  TV_SC_MARK();
+  TV_SC_SET(1, sc_t0);
+  TV_SC_STORE(b);
+}
+
+// Clusters of sample_cluster_kernel resident on the current device at once
+// for a launch configuration (cached per device and shared-memory size).
+int sc_capacity(const cudaLaunchConfig_t& cfg, int* out) {
+  static std::mutex mu;
+  static std::map<std::pair<int, size_t>, int> cache;
+  int dev = 0;
+  TV_CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(dev, cfg.dynamicSmemBytes);
+  const auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return TV_OK;
+  }
+  TV_CUDA_TRY(cudaFuncSetAttribute(sample_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScMaxDyn));
+  cudaLaunchConfig_t c = cfg;
+  c.gridDim = dim3(kScCtas);
+  int n = 0;
+  TV_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, sample_cluster_kernel, &c));
+  cache[key] = n;
+  *out = n;
+  return TV_OK;
+}
+
 int check_accept_args(int B, int N, int V, const void* tokens, const void* parent, int64_t pstride,
                       const void* out, const void* n_out, int out_cols) {
   if (B < 0 || N < 1 || N > TV_MAX_NODES || V < 1 || pstride < 0 || out_cols < 1)
@@ -765,6 +1106,10 @@ int check_accept_args(int B, int N, int V, const void* tokens, const void* paren
 }  // namespace
 
 #ifdef TV_TC_TRACE
+extern "C" int tv_debug_sc_times(void* dst, size_t bytes) {
+  const size_t n = sizeof(g_sc_t) < bytes ? sizeof(g_sc_t) : bytes;
+  return cudaMemcpyFromSymbol(dst, g_sc_t, n) == cudaSuccess ? 0 : -1;
+}
 extern "C" int tv_debug_sample_times(void* dst, size_t bytes) {
   const size_t n = sizeof(g_sample_t) < bytes ? sizeof(g_sample_t) : bytes;
   return cudaMemcpyFromSymbol(dst, g_sample_t, n) == cudaSuccess ? 0 : -1;
@@ -797,14 +1142,48 @@ extern "C" int tv_tree_accept_greedy(const float* logits, const int32_t* target_
 extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens, const int32_t* parent,
                                      int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept,
                                      const float* u_final, int32_t B, int32_t N, int32_t V, int32_t* out,
-                                     int32_t* n_out, int32_t* path, int32_t out_cols, int32_t* status,
-                                     void* stream) {
+                                     int32_t* n_out, int32_t* path, int32_t out_cols, int32_t flags,
+                                     int32_t* status, void* stream) {
   tv::clear_error();
   int st = check_accept_args(B, N, V, tokens, parent, parent_bstride, out, n_out, out_cols);
   if (st) return st;
+  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_SINGLE_CTA)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: unknown flags %d", flags);
   if (B == 0) return TV_OK;
   if (!p || !q || !u_accept || !u_final) return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: null pointer");
   AcceptOut o{out, n_out, path, out_cols, status};
+  const int Ls = sc_slice(V);
+  const size_t dyn = (size_t)Ls * (sizeof(uint64_t) + sizeof(float));
+  bool cluster = false;
+  if (flags != TV_SAMPLE_SINGLE_CTA && dyn <= kScMaxDyn && B <= INT_MAX / kScCtas) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kScCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kScThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = (cudaStream_t)stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int capacity = 0;  // (also sets the kernel's shared-memory limit)
+    st = sc_capacity(cfg, &capacity);
+    if (st) return st;
+    // automatic: clusters only when the whole batch is resident at once
+    cluster = flags == TV_SAMPLE_CLUSTER || B <= capacity;
+    if (cluster) {
+      cfg.gridDim = dim3((unsigned)(B * kScCtas));
+      cudaError_t e = cudaLaunchKernelEx(&cfg, sample_cluster_kernel, p, q, tokens, parent, parent_bstride, n_nodes,
+                                         u_accept, u_final, (int)N, (int)V, Ls, o);
+      if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel");
+      return TV_OK;
+    }
+  } else if (flags == TV_SAMPLE_CLUSTER) {
+    return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_accept_sample: the cluster kernel needs V <= %d (V=%d, B=%d)",
+                    kScCtas * (int)(kScMaxDyn / 12 / 4 * 4), V, B);
+  }
+  // one CTA per request, rows streamed and w_m recomputed per pass
   constexpr size_t kDyn = sizeof(float4) * 2 * kStreamStages * (kStageElems / 4) + sizeof(uint64_t) * 2 * kMaxChunks;
   cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDyn);
   if (e != cudaSuccess) return tv::cuda_fail(e, "cudaFuncSetAttribute(sample_kernel)");

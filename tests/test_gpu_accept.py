@@ -78,12 +78,16 @@ def test_greedy_overflow_flag():
     assert status.item() == capi.TV_DEV_OUT_OVERFLOW and n_out.item() == 3
 
 
-def test_sample_full_workload_bit_exact():
+KERNELS = {"auto": 0, "cluster": 1, "single_cta": 2}
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_sample_full_workload_bit_exact(kernel):
     """B=256 chains over a 128000-token vocabulary, ragged num_draft ~ U{0..4}."""
     w = W.WORKLOADS["b256_l2k_4k_n10_sample"]
     s = W.sample_chain_inputs(w, device="cuda")
     res = capi.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
-                                     n_nodes=s["n_nodes"])
+                                     n_nodes=s["n_nodes"], flags=KERNELS[kernel])
     c = {k: v.cpu().numpy() for k, v in s.items()}
     ref = OA.tree_accept_sample(c["p"], c["q"], c["tokens"], c["parent"], c["n_nodes"], c["u_accept"], c["u_final"])
     _cmp(res, *ref)
@@ -93,14 +97,15 @@ def test_sample_full_workload_bit_exact():
     np.testing.assert_array_equal(res[1].cpu().numpy(), n_c)
 
 
-def test_sample_tree_full_workload_bit_exact():
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_sample_tree_full_workload_bit_exact(kernel):
     """B=64 requests verified stochastically on the 64-node tree over a
     32000-token vocabulary, siblings drawn i.i.d. from their parent's q."""
     w = W.WORKLOADS["b64_l1k_8k_n64_sample"]
     parent, *_ = OT.build_tree(w.paths())
     s = W.sample_tree_inputs(w, parent, device="cuda")
     res = capi.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
-                                     n_nodes=s["n_nodes"])
+                                     n_nodes=s["n_nodes"], flags=KERNELS[kernel])
     c = {k: v.cpu().numpy() for k, v in s.items()}
     ref = OA.tree_accept_sample(c["p"], c["q"], c["tokens"], c["parent"], c["n_nodes"], c["u_accept"], c["u_final"])
     _cmp(res, *ref)
@@ -109,11 +114,14 @@ def test_sample_tree_full_workload_bit_exact():
     assert n.mean() > 2.0 and n.min() >= 1
 
 
-@pytest.mark.parametrize("V", [4, 33, 1000, 4096])
-def test_sample_trees_with_sibling_levels(V):
-    """Trees with up to 5 siblings per node: several residual levels per node."""
+@pytest.mark.parametrize("V,B,kernel", [(V, 200, k) for V in (4, 33, 1000, 4096) for k in ("cluster", "single_cta")]
+                         + [(160000, 12, "auto"), (160001, 12, "auto")])
+def test_sample_trees_with_sibling_levels(V, B, kernel):
+    """Trees with up to 5 siblings per node: several residual levels per node,
+    on both kernels.  Vocabularies above 136,512 run the single-CTA kernel
+    (aligned rows streamed through shared memory, odd V read directly)."""
     rng = np.random.default_rng(120 + V)
-    B, N = 200, 16
+    N = 16
     paths = [(0,), (1,), (2,), (3,), (4,), (0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (4, 0), (0, 0, 0), (0, 0, 1),
              (0, 1, 0), (1, 0, 0)]
     parent, *_ = OT.build_tree(paths)
@@ -130,8 +138,38 @@ def test_sample_trees_with_sibling_levels(V):
     uf = rng.random(B, dtype=np.float32)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     res = capi.tv_tree_accept_sample(t(p), t(q), t(tokens), t(parent.astype(np.int32)), t(ua), t(uf),
-                                     n_nodes=t(n_nodes))
+                                     n_nodes=t(n_nodes), flags=KERNELS[kernel])
     _cmp(res, *OA.tree_accept_sample(p, q, tokens, parent, n_nodes, ua, uf))
+    if V > 136512:
+        with pytest.raises(capi.TVError, match="UNSUPPORTED"):
+            capi.tv_tree_accept_sample(t(p), t(q), t(tokens), t(parent.astype(np.int32)), t(ua), t(uf),
+                                       flags=capi.TV_SAMPLE_CLUSTER)
+
+
+@pytest.mark.parametrize("V,kernel", [(4096, "cluster"), (4096, "single_cta"), (160000, "auto")])
+def test_sample_kept_level_after_empty_residual(V, kernel):
+    """A rejection whose residual pass leaves no mass keeps the level (the
+    p = q guard) and the final draw still uses that level's weights: q is
+    one-hot at token t and p puts 1.5 on t (rows may sum to 2), the children
+    carry tokens with q = 0, so the second and third rejections find an
+    empty residual."""
+    t = V * 3 // 4 + 1
+    B, N = 2, 4
+    parent = np.array([-1, 0, 0, 0], dtype=np.int32)
+    p = np.zeros((B, N, V), dtype=np.float32)
+    q = np.zeros((B, N, V), dtype=np.float32)
+    p[:, :, t] = 1.5
+    q[:, :, t] = 1.0
+    tokens = np.array([[0, 7, 7, 9]] * B, dtype=np.int32)
+    ua = np.full((B, N), 0.5, dtype=np.float32)
+    uf = np.array([0.3, 0.9], dtype=np.float32)
+    n_nodes = np.full(B, N, dtype=np.int32)
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    res = capi.tv_tree_accept_sample(tt(p), tt(q), tt(tokens), tt(parent), tt(ua), tt(uf), n_nodes=tt(n_nodes),
+                                     flags=KERNELS[kernel])
+    ref = OA.tree_accept_sample(p, q, tokens, parent, n_nodes, ua, uf)
+    _cmp(res, *ref)
+    assert (ref[1] == 1).all() and (ref[0][:, 0] == t).all()
 
 
 def test_sample_bad_token_flag():
@@ -144,10 +182,10 @@ def test_sample_bad_token_flag():
     assert status.item() == capi.TV_DEV_BAD_TOKEN and n_out.item() == 1
 
 
-def _gpu_verify(p, q, tokens, parent, n_nodes, ua, uf):
+def _gpu_verify(p, q, tokens, parent, n_nodes, ua, uf, flags=0):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     out, n_out, _ = capi.tv_tree_accept_sample(t(p), t(q), t(tokens.astype(np.int32)), t(parent.astype(np.int32)),
-                                               t(ua), t(uf), n_nodes=t(n_nodes.astype(np.int32)))
+                                               t(ua), t(uf), n_nodes=t(n_nodes.astype(np.int32)), flags=flags)
     return out.cpu().numpy(), n_out.cpu().numpy()
 
 
@@ -160,12 +198,14 @@ def test_gpu_chain_lossless_chi_square(verifier_facts):
     assert chi_square(seqs, pt) < thr
 
 
-def test_gpu_tree_lossless_chi_square(verifier_facts):
+@pytest.mark.parametrize("kernel", ["cluster", "single_cta"])
+def test_gpu_tree_lossless_chi_square(verifier_facts, kernel):
     f = verifier_facts
     V, n_tok, thr = int(f["chi2_vocab"][0][0]), int(f["chi2_tokens"][0][0]), float(f["chi2_threshold"][0][0])
     parent, *_ = OT.build_tree([(0,), (1,), (2,), (0, 0), (2, 0)])
     pt, qt = W.markov_tables(V, 22)
-    seqs = generate(_gpu_verify, pt, qt, parent, 200_000, n_tok, 131)
+    verify = lambda *a: _gpu_verify(*a, flags=KERNELS[kernel])
+    seqs = generate(verify, pt, qt, parent, 200_000, n_tok, 131)
     assert chi_square(seqs, pt) < thr
 
 

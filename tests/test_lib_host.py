@@ -82,5 +82,8 @@ def test_device_entry_points_reject_bad_sizes_on_host():
     assert h.tv_rope_apply(None, None, None, None, 10, 1, 1, 1, 1, 60, 1, None, None) == -1
     assert h.tv_tree_accept_greedy(None, None, None, None, 0, None, 1, 65, 10, None, None, None, 4, None, None) == -1
     assert h.tv_tree_accept_sample(None, None, None, None, 0, None, None, None, 0, 10, 10, None, None, None, 4,
-                                   None, None) == 0
+                                   0, None, None) == 0
     assert b"bad sizes" in h.tv_last_error() or h.tv_last_error() == b""
+    assert h.tv_tree_accept_sample(None, None, None, None, 0, None, None, None, 0, 10, 10, None, None, None, 4,
+                                   3, None, None) == -1
+    assert b"unknown flags" in h.tv_last_error()
