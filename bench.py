@@ -170,10 +170,13 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def attention_bytes(w, lens, N, esize):
+def attention_bytes(w, lens, N, esize, counts=None):
+    """Algorithmic bytes of one attention call: prefix K+V, then the tree K+V
+    and Q+O rows of the nodes present (all N, or n_b per ragged request)."""
+    nodes = w.B * N if counts is None else int(np.sum(counts))
     kv = int(np.sum(lens)) * w.Hkv * w.D * 2 * esize
-    tree = w.B * N * w.Hkv * w.D * 2 * esize
-    qo = 2 * w.B * N * w.Hq * w.D * esize
+    tree = nodes * w.Hkv * w.D * 2 * esize
+    qo = 2 * nodes * w.Hq * w.D * esize
     return kv + tree + qo
 
 
@@ -185,21 +188,24 @@ def request_paths(w):
     return W.dynamic_rank_paths(w) if w.dynamic else [w.paths()] * w.B
 
 
-def oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, requests):
-    """The oracle on a list of requests (all nodes, all heads) plus acceptance."""
+def oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, requests, counts):
+    """The oracle on a list of requests (every present node, all heads) plus
+    acceptance."""
     from oracle import accept as OA
     from oracle import attention as OAt
     from oracle import tree as OT
 
     for b in requests:
         parent, depth, rows, _ = OT.build_tree(req_paths[b])
-        OT.tree_mask_batch(parent[None], inp_cpu["seq_lens"][b:b + 1])
+        n_b = counts[b:b + 1]
+        OT.tree_mask_batch(parent[None], inp_cpu["seq_lens"][b:b + 1], n_b)
         sl = slice(b, b + 1)
         OAt.tree_attention(inp_cpu["q"][sl], inp_cpu["k_cache"], inp_cpu["v_cache"], inp_cpu["block_table"][sl],
-                           inp_cpu["seq_lens"][sl], inp_cpu["k_tree"][sl], inp_cpu["v_tree"][sl], parent)
+                           inp_cpu["seq_lens"][sl], inp_cpu["k_tree"][sl], inp_cpu["v_tree"][sl], parent,
+                           nodes=[(0, i) for i in range(int(n_b[0]))], n_nodes=n_b)
         if greedy is not None:
             am = OA.argmax_rows(greedy["logits"][b])
-            OA.tree_accept_greedy(am[None], greedy["tokens"][sl], parent)
+            OA.tree_accept_greedy(am[None], greedy["tokens"][sl], parent, n_b)
         if sample is not None:
             OA.tree_accept_sample(sample["p"][sl], sample["q"][sl], sample["tokens"][sl], sample["parent"],
                                   sample["n_nodes"][sl], sample["u_accept"][sl], sample["u_final"][sl])
@@ -228,17 +234,17 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def time_oracle(w, inp_cpu, req_paths, greedy, sample, seconds, order):
+def time_oracle(w, inp_cpu, req_paths, greedy, sample, seconds, order, counts):
     """Times the oracle request by request until `seconds` elapse; returns
     (nodes/s, requests used, elapsed)."""
     done, t0 = [], time.perf_counter()
     for b in order:
-        oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, [b])
+        oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, [b], counts)
         done.append(int(b))
         if time.perf_counter() - t0 >= seconds:
             break
     el = time.perf_counter() - t0
-    return len(done) * w.n_nodes / el, done, el
+    return int(np.sum(counts[done])) / el, done, el
 
 
 def sample_order(lens, seed=0):
@@ -289,7 +295,9 @@ class Step:
         self.acc_n = torch.empty(B, dtype=torch.int32, device=dev)
         self.acc_path = torch.empty(B, cols, dtype=torch.int32, device=dev)
         self.esize = 2 if dt == torch.bfloat16 else 4
-        self.attn_bytes = attention_bytes(w, self.lens, n, self.esize)
+        self.counts = W.node_counts(w)  # nodes present per request (all n unless ragged)
+        self.n_nodes = torch.from_numpy(self.counts).to(dev) if w.ragged else None
+        self.attn_bytes = attention_bytes(w, self.lens, n, self.esize, self.counts)
         # tree_mask, rope_apply, the attention kernel(s), the acceptance kernel;
         # the tcgen05 path is one kernel (plus a counter memset), the CUDA-core
         # path plan + attention + combine
@@ -311,7 +319,8 @@ class Step:
 
     def run(self, ev_attn=None):
         c, i = self.capi, self.inp
-        c.tv_tree_mask(self.parent, self.seq_lens, mask=self.mask, depth=self.depth, pos=self.pos)
+        c.tv_tree_mask(self.parent, self.seq_lens, mask=self.mask, depth=self.depth, pos=self.pos,
+                       n_nodes=self.n_nodes)
         c.tv_rope_apply(i["q"], i["k_tree"], self.pos, self.table)
         if ev_attn:
             ev_attn[0].record()
@@ -319,7 +328,8 @@ class Step:
         if ev_attn:
             ev_attn[1].record()
         if self.greedy is not None:
-            c.tv_tree_accept_greedy(self.greedy["tokens"], self.parent, logits=self.greedy["logits"], out=self.acc_out,
+            c.tv_tree_accept_greedy(self.greedy["tokens"], self.parent, logits=self.greedy["logits"],
+                                    n_nodes=self.n_nodes, out=self.acc_out,
                                     n_out=self.acc_n, path=self.acc_path)
         elif self.sample is not None:
             s = self.sample
@@ -334,7 +344,7 @@ class Step:
         par_all = self.parent.cpu().numpy().reshape(-1, self.N)
         chains = []
         for b in range(self.w.B):
-            par = par_all[b % par_all.shape[0]]
+            par = par_all[b % par_all.shape[0]][:int(self.counts[b])]
             depth = np.zeros(par.size, dtype=np.int64)
             for i in range(1, par.size):
                 depth[i] = depth[par[i]] + 1
@@ -426,7 +436,7 @@ def run_ours(args, world, rank, local):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
         torch.distributed.barrier()
-    nodes = w.B * st.N
+    nodes = int(np.sum(st.counts))
     value = world * nodes * args.steps / (total_ms / 1e3)
 
     # end to end through the public API: pinned host inputs in, accepted tokens out
@@ -492,7 +502,8 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp_cpu, g, s = cpu_inputs(w, st.inp, st.greedy, st.sample)
-        nps, used, el = time_oracle(w, inp_cpu, st.req_paths, g, s, args.cpu_seconds, sample_order(st.lens))
+        nps, used, el = time_oracle(w, inp_cpu, st.req_paths, g, s, args.cpu_seconds, sample_order(st.lens),
+                                    st.counts)
         cpu = {"value": nps, "unit": "nodes/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{len(used)} of {w.B} requests (all {st.N} nodes, all {w.Hq} heads, acceptance incl.), "
                          f"prefix lengths {[int(st.lens[b]) for b in used][:6]}..., {el:.1f} s"}
@@ -507,6 +518,7 @@ def run_ours(args, world, rank, local):
             "config": {"workload": w.name, "B": w.B, "N": st.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab,
                        "tree": "one per request" if w.dynamic else "shared",
+                       "nodes_present": int(np.sum(st.counts)),
                        "l2": ("L2 flushed between steps" if flush is not None
                               else f"inputs larger than L2 ({ws_bytes / 2**30:.2f} GiB per step)"),
                        "kernel_flags": args.flags, "parallelism": f"replicas x{world} (requests sharded)",
@@ -533,17 +545,18 @@ def run_reference(args, world, rank):
         sample = W.sample_tree_inputs(w, parent, device="cpu") if w.sample_tree else W.sample_chain_inputs(w, device="cpu")
     inp_cpu, g, s = cpu_inputs(w, inp, greedy, sample)
     lens = inp_cpu["seq_lens"]
+    counts = W.node_counts(w)
     order = sample_order(lens)
     for k in range(args.warmup):
-        oracle_sample_run(w, inp_cpu, req_paths, g, s, [order[k % len(order)]])
+        oracle_sample_run(w, inp_cpu, req_paths, g, s, [order[k % len(order)]], counts)
     t0 = time.perf_counter()
     used = []
     for k in range(args.steps):
         b = order[k % len(order)]
-        oracle_sample_run(w, inp_cpu, req_paths, g, s, [b])
+        oracle_sample_run(w, inp_cpu, req_paths, g, s, [b], counts)
         used.append(b)
     el = time.perf_counter() - t0
-    value = args.steps * w.n_nodes / el
+    value = int(np.sum(counts[used])) / el
     cores = blas_threads()
     line = {
         "impl": "reference",

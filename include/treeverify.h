@@ -118,14 +118,20 @@ int tv_tree_build(const int32_t* ranks, const int32_t* offsets, int32_t n_paths,
  * parent    device int32 [B, N] with row stride parent_bstride elements
  *           (0 = one tree shared by all requests).
  * seq_lens  device int32 [B]: prefix length L_b (tokens already cached).
+ * n_nodes   device int32 [B] (nullable = N): ragged trees in a bucket of N
+ *           ("What interviewers probe next": graph capture needs a fixed
+ *           tree shape per batch bucket).  Request b holds nodes
+ *           0 .. n_b - 1 (n_b clamped to [1, N]); nodes i >= n_b are absent:
+ *           mask 0, depth 0, pos -1, parent[b, i] not read.
  * mask      device uint64 [B, N] out; depth, pos device int32 [B, N] out
- *           (pos = L_b + depth).  A request whose parent row is not a
- *           parent-before-child tree gets zero rows and TV_DEV_BAD_TOPOLOGY.
+ *           (pos = L_b + depth).  A request whose parent row (its first n_b
+ *           entries) is not a parent-before-child tree gets zero rows and
+ *           TV_DEV_BAD_TOPOLOGY.
  * status    device int32 (nullable), see TV_DEV_*.
  */
 int tv_tree_mask(const int32_t* parent, int64_t parent_bstride, const int32_t* seq_lens,
-                 int32_t B, int32_t N, uint64_t* mask, int32_t* depth, int32_t* pos,
-                 int32_t* status, void* stream);
+                 const int32_t* n_nodes, int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
+                 int32_t* pos, int32_t* status, void* stream);
 
 /*
  * tv_rope_table -- device, asynchronous.  Fills the rotary table used by
@@ -149,7 +155,8 @@ int tv_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base
  * pos     device int32 [B, N] (from tv_tree_mask).
  * cos_sin device float32 [max_pos, 2, D/2] from tv_rope_table.
  * A position outside [0, max_pos) leaves the row untouched and sets
- * TV_DEV_BAD_POSITION.  D in {16, 32, 64, 128, 256}; B*N*(Hq+Hkv)*D/16 < 2^31
+ * TV_DEV_BAD_POSITION, except -1 (an absent node of a ragged tree), which
+ * leaves it untouched silently.  D in {16, 32, 64, 128, 256}; B*N*(Hq+Hkv)*D/16 < 2^31
  * (else TV_ERR_UNSUPPORTED).
  */
 int tv_rope_apply(void* q, void* k_tree, const int32_t* pos, const float* cos_sin,
@@ -175,7 +182,9 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  * per-node ancestor rows.  Output row (b, i, h) is
  *   softmax(scale * q . K^T) V  over keys = prefix 0..L_b-1 of request b
  *   (KV head h / (Hq/Hkv)) followed by the tree nodes j with bit j of
- *   mask[b, i] set.
+ *   mask[b, i] set.  A row whose key set is empty (L_b = 0 and a zero mask
+ *   row, i.e. an absent node) is written as zeros with lse = -inf; an absent
+ *   node with L_b > 0 attends to the prefix only.
  * q and k_tree must already be rotated (tv_rope_apply); the cached prefix
  * keys are stored rotated.
  *

@@ -26,6 +26,13 @@ softmax scale defaults to ``1/sqrt(D)``; the root's K/V is tree row 0 (it is
 the last accepted token, not yet in the cache); the paged cache is laid out
 ``[num_blocks, Hkv, block_size, D]`` and position t of request b lives in
 block ``block_table[b, t // block_size]``, slot ``t % block_size``.
+
+Ragged trees ("Build the tree attention mask ...", "What interviewers probe
+next": a fixed tree shape per batch bucket): with ``n_nodes`` request b holds
+nodes 0 .. n_b - 1 and a node i >= n_b is absent.  An absent node has no
+position and no tree keys: its query is taken as given (not rotated) and
+attends to the prefix alone; with an empty prefix it has no keys at all and
+its row is zero with log-normaliser -inf.
 """
 
 from __future__ import annotations
@@ -63,7 +70,10 @@ def gather_prefix(cache, block_row, prefix_len):
 
 
 def _softmax_attend(qh, keys, vals, scale):
-    """Ordinary attention of query rows qh [G, D] over keys/vals [T, D]."""
+    """Ordinary attention of query rows qh [G, D] over keys/vals [T, D]; an
+    empty key set gives zero rows and log-normaliser -inf."""
+    if keys.shape[0] == 0:
+        return np.zeros((qh.shape[0], vals.shape[-1])), np.full(qh.shape[0], -np.inf)
     s = (qh @ keys.T) * scale
     m = s.max(axis=1, keepdims=True)
     e = np.exp(s - m)
@@ -73,14 +83,15 @@ def _softmax_attend(qh, keys, vals, scale):
 
 def tree_attention(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree,
                    parent, *, rope_base=10000.0, scale=None, nodes=None,
-                   mutant=None):
+                   mutant=None, n_nodes=None):
     """Per-node path attention (see module docstring).
 
     Shapes: q [B, N, Hq, D]; k_tree, v_tree [B, N, Hkv, D] (q and k_tree NOT
     yet rotated); caches [num_blocks, Hkv, block_size, D]; block_table
     [B, max_blocks]; seq_lens [B]; parent [N] (one tree for all requests) or
     [B, N].  ``nodes`` optionally lists the (b, i) pairs to compute (others
-    stay NaN).  Returns (out [B, N, Hq, D] f64, lse [B, N, Hq] f64, natural
+    stay NaN).  ``n_nodes`` [B] (optional): ragged trees, nodes >= n_nodes[b]
+    absent (module docstring).  Returns (out [B, N, Hq, D] f64, lse [B, N, Hq] f64, natural
     log of the softmax normaliser).
 
     ``mutant`` exists only for the negative-control tests and models the two
@@ -109,8 +120,16 @@ def tree_attention(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree,
         L = int(seq_lens[b])
         pk = gather_prefix(k_cache, block_table[b], L)
         pv = gather_prefix(v_cache, block_table[b], L)
-        dep = depth_of(par)
+        n_b = N if n_nodes is None else min(max(int(n_nodes[b]), 1), N)
+        dep = depth_of(par[:n_b])
         for i in node_list:
+            if i >= n_b:  # absent: the prefix alone, query as given
+                qi = np.asarray(q[b, i], dtype=np.float64)
+                for kvh in range(Hkv):
+                    o, l = _softmax_attend(qi[kvh * G:(kvh + 1) * G], pk[:, kvh], pv[:, kvh], scale)
+                    out[b, i, kvh * G:(kvh + 1) * G] = o
+                    lse[b, i, kvh * G:(kvh + 1) * G] = l
+                continue
             if mutant == "causal_flat":
                 chain = list(range(i + 1))
                 key_pos = L + dep[chain]

@@ -136,12 +136,19 @@ def path_to_root(parent, i):
     return chain[::-1]
 
 
-def tree_mask_batch(parent, seq_lens):
+def tree_mask_batch(parent, seq_lens, n_nodes=None):
     """Batched structure for per-request parent arrays.
 
     ``parent`` is int [B, N]; returns (rows uint64 [B, N], depth int [B, N],
     pos int [B, N], ok bool [B]).  A request whose parent row fails
     :func:`check_topology` gets ``ok = False`` and zero rows / depth / pos.
+
+    Ragged trees in a bucket of N ("Build the tree attention mask ...",
+    "What interviewers probe next": CUDA graph capture keeps a fixed tree
+    shape per batch bucket): with ``n_nodes`` request b is the tree of its
+    first n_b = clamp(n_nodes[b], 1, N) nodes and the others are absent, with
+    row 0, depth 0 and position -1 (no position: nothing rotates or attends
+    to them).
     """
     parent = np.asarray(parent)
     B, N = parent.shape
@@ -150,12 +157,14 @@ def tree_mask_batch(parent, seq_lens):
     pos = np.zeros((B, N), dtype=np.int64)
     ok = np.ones(B, dtype=bool)
     for b in range(B):
+        n = N if n_nodes is None else min(max(int(n_nodes[b]), 1), N)
+        pos[b, n:] = -1
         try:
-            r = ancestor_rows(parent[b])
+            r = ancestor_rows(parent[b, :n])
         except TopologyError:
             ok[b] = False
             continue
-        rows[b] = np.array(r, dtype=np.uint64)
-        depth[b] = depth_of(parent[b])
-        pos[b] = positions(depth[b], seq_lens[b])
+        rows[b, :n] = np.array(r, dtype=np.uint64)
+        depth[b, :n] = depth_of(parent[b, :n])
+        pos[b, :n] = positions(depth[b, :n], seq_lens[b])
     return rows, depth, pos, ok

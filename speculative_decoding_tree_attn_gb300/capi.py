@@ -33,7 +33,7 @@ SIGNATURES = {
     "tv_last_error": (ctypes.c_char_p, []),
     "tv_version": (ctypes.c_int, []),
     "tv_tree_build": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P, _P, _P]),
-    "tv_tree_mask": (ctypes.c_int, [_P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P]),
+    "tv_tree_mask": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _P]),
     "tv_rope_table": (ctypes.c_int, [_P, _I32, _I32, _D, _P]),
     "tv_rope_apply": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "tv_tree_attn_workspace_size": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
@@ -130,11 +130,14 @@ def tv_tree_build(paths, max_nodes=64):
     return parent[:k].copy(), depth[:k].copy(), mask[:k].copy(), p2n[:len(paths)].copy(), k
 
 
-def tv_tree_mask(parent, seq_lens, status=None, mask=None, depth=None, pos=None, stream=None):
-    """parent int32 [N] (shared) or [B, N]; seq_lens int32 [B] -> (mask int64 [B, N]
+def tv_tree_mask(parent, seq_lens, status=None, mask=None, depth=None, pos=None, stream=None, n_nodes=None):
+    """parent int32 [N] (shared) or [B, N]; seq_lens int32 [B]; n_nodes int32 [B]
+    (optional, ragged trees: nodes >= n_nodes[b] absent) -> (mask int64 [B, N]
     holding the uint64 rows, depth int32 [B, N], pos int32 [B, N])."""
     _dev(parent, "parent", (torch.int32,))
     _dev(seq_lens, "seq_lens", (torch.int32,))
+    if n_nodes is not None:
+        _dev(n_nodes, "n_nodes", (torch.int32,))
     B = seq_lens.numel()
     N = parent.shape[-1]
     bstride = 0 if parent.dim() == 1 else parent.stride(0)
@@ -142,8 +145,8 @@ def tv_tree_mask(parent, seq_lens, status=None, mask=None, depth=None, pos=None,
     mask = torch.empty(B, N, dtype=torch.int64, device=dev) if mask is None else mask
     depth = torch.empty(B, N, dtype=torch.int32, device=dev) if depth is None else depth
     pos = torch.empty(B, N, dtype=torch.int32, device=dev) if pos is None else pos
-    _check("tv_tree_mask", lib().tv_tree_mask(_ptr(parent), bstride, _ptr(seq_lens), B, N, _ptr(mask), _ptr(depth),
-                                              _ptr(pos), _ptr(status), _stream(stream)))
+    _check("tv_tree_mask", lib().tv_tree_mask(_ptr(parent), bstride, _ptr(seq_lens), _ptr(n_nodes), B, N, _ptr(mask),
+                                              _ptr(depth), _ptr(pos), _ptr(status), _stream(stream)))
     return mask, depth, pos
 
 

@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(AttnParams p
     for (int rr = 0; rr < RPW; ++rr) {
       const int r = warp * RPW + rr, gr = rg * kSimtRows + r;
       if (gr >= p.R) continue;
-      const float inv = 1.f / l[rr];
+      const float inv = l[rr] > 0.f ? 1.f / l[rr] : 0.f;  // no key at all: zero row, lse -inf
       const float lse2 = m[rr] + log2f(l[rr]);
       if (complete) {
         const int i = gr / p.G, h = kvh * p.G + gr % p.G;

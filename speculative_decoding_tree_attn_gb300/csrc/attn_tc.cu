@@ -681,7 +681,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
                                                uint8_t* stage) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   constexpr float kLn2 = 0.69314718055994530942f;
-  const float inv = 1.f / l;
+  const float inv = l > 0.f ? 1.f / l : 0.f;  // no key at all (empty prefix, absent node): zero row
   const float lse2 = m_run + log2f(l);
   const bool complete = (s.a == 0 && s.e == s.n);
   const Pieces pc(sp, s.real_start, s.n);

@@ -88,8 +88,8 @@ __global__ void __launch_bounds__(256) rope_apply_kernel(T* __restrict__ q, T* _
     const int bi = r / heads;
     const int h = r - bi * heads;
     const int32_t p = __ldg(pos + bi);
-    if (p < 0 || p >= max_pos) {
-      if (status && c == 0) atomicOr(status, TV_DEV_BAD_POSITION);
+    if (p < 0 || p >= max_pos) {  // -1: an absent node of a ragged tree, left as it is
+      if (status && c == 0 && p != -1) atomicOr(status, TV_DEV_BAD_POSITION);
       continue;
     }
     T* row = (h < Hq) ? q + ((int64_t)bi * Hq + h) * D : kt + ((int64_t)bi * Hkv + (h - Hq)) * D;

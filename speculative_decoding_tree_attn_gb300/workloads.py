@@ -98,10 +98,23 @@ class Workload:
     sample_max_draft: int = 4
     dynamic: bool = False      # one tree per request (dynamic_rank_paths)
     sample_tree: bool = False  # "sample" on the attention tree (sample_tree_inputs), else on chains
+    ragged: bool = False       # per-request node counts in the bucket of n_nodes (node_counts)
     notes: str = field(default="", compare=False)
 
     def paths(self):
         return best_first_paths(self.rank_probs, self.n_nodes, self.max_depth)
+
+
+def node_counts(w: Workload, B=None):
+    """Nodes per request: n_nodes for all, or for a ragged workload a seeded
+    draw from U{ceil(N/4) .. N} (each request keeps the first n_b nodes of its
+    tree, a tree itself since parents precede children)."""
+    B = w.B if B is None else B
+    N = w.n_nodes
+    if not w.ragged:
+        return np.full(B, N, dtype=np.int32)
+    rng = np.random.default_rng(w.seed * 1000 + 43)
+    return rng.integers(max(1, (N + 3) // 4), N + 1, size=B).astype(np.int32)
 
 
 def dynamic_rank_paths(w: Workload, B=None):
@@ -142,6 +155,10 @@ WORKLOADS = {
                  (0.45, 0.2, 0.12, 0.08, 0.06, 0.04, 0.03, 0.02), 64, 6, 6,
                  accept="greedy", vocab=32000, dynamic=True,
                  notes="the 64-request workload with one best-first tree per request"),
+        Workload("b64_l1k_8k_n64_ragged", 64, 32, 8, 128, "bf16", ("uniform", 1024, 8192), 16,
+                 (0.45, 0.2, 0.12, 0.08, 0.06, 0.04, 0.03, 0.02), 64, 6, 8,
+                 accept="greedy", vocab=32000, dynamic=True, ragged=True,
+                 notes="one best-first tree per request, n_b ~ U{16..64} nodes in the bucket of 64"),
         Workload("b64_l1k_8k_n64_sample", 64, 32, 8, 128, "bf16", ("uniform", 1024, 8192), 16,
                  (0.45, 0.2, 0.12, 0.08, 0.06, 0.04, 0.03, 0.02), 64, 6, 7,
                  accept="sample", vocab=32000, sample_tree=True,

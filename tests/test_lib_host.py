@@ -77,8 +77,8 @@ def test_tree_build_errors():
 
 def test_device_entry_points_reject_bad_sizes_on_host():
     h = capi.lib()
-    assert h.tv_tree_mask(None, 0, None, 1, 65, None, None, None, None, None) == -1
-    assert h.tv_tree_mask(None, 0, None, 0, 10, None, None, None, None, None) == 0
+    assert h.tv_tree_mask(None, 0, None, None, 1, 65, None, None, None, None, None) == -1
+    assert h.tv_tree_mask(None, 0, None, None, 0, 10, None, None, None, None, None) == 0
     assert h.tv_rope_apply(None, None, None, None, 10, 1, 1, 1, 1, 60, 1, None, None) == -1
     assert h.tv_tree_accept_greedy(None, None, None, None, 0, None, 1, 65, 10, None, None, None, 4, None, None) == -1
     assert h.tv_tree_accept_sample(None, None, None, None, 0, None, None, None, 0, 10, 10, None, None, None, 4,

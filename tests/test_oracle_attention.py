@@ -158,3 +158,35 @@ def test_negative_controls_fail_bf16_tolerance(mutant, L):
     bad, _ = A.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
                               inp["seq_lens"], inp["k_tree"], inp["v_tree"], parent, mutant=mutant)
     assert np.abs(good - bad).max() > 10 * 2e-2
+
+
+def test_ragged_absent_nodes_and_empty_key_set():
+    """Absent nodes of a ragged tree: the prefix alone, with the query as
+    given; with an empty prefix no key at all -- a zero row and lse -inf.
+    Valid rows equal the truncated tree's rows."""
+    rng = np.random.default_rng(78)
+    N, Hq, Hkv, D, bs = 6, 4, 2, 8, 4
+    parent = np.array([-1, 0, 0, 1, 1, 3])
+    for L in (0, 7):
+        nb = max((L + bs - 1) // bs, 1)
+        kc = rng.standard_normal((nb, Hkv, bs, D))
+        vc = rng.standard_normal((nb, Hkv, bs, D))
+        q = rng.standard_normal((1, N, Hq, D))
+        kt = rng.standard_normal((1, N, Hkv, D))
+        vt = rng.standard_normal((1, N, Hkv, D))
+        table = np.arange(nb)[None]
+        out, lse = A.tree_attention(q, kc, vc, table, np.array([L]), kt, vt, parent, n_nodes=[4])
+        full, flse = A.tree_attention(q[:, :4], kc, vc, table, np.array([L]), kt[:, :4], vt[:, :4], parent[:4])
+        np.testing.assert_array_equal(out[0, :4], full[0])
+        np.testing.assert_array_equal(lse[0, :4], flse[0])
+        if L == 0:
+            assert (out[0, 4:] == 0).all() and np.isneginf(lse[0, 4:]).all()
+        else:
+            # prefix-only softmax of the unrotated query, written out directly
+            keys = kc[0, :, :L] if nb == 1 else np.concatenate([kc[j] for j in range(nb)], axis=1)[:, :L]
+            vals = vc[0, :, :L] if nb == 1 else np.concatenate([vc[j] for j in range(nb)], axis=1)[:, :L]
+            for i in (4, 5):
+                for h in range(Hq):
+                    s = keys[h // 2] @ q[0, i, h] / np.sqrt(D)
+                    e = np.exp(s - s.max())
+                    np.testing.assert_allclose(out[0, i, h], e @ vals[h // 2] / e.sum(), rtol=1e-12, atol=1e-12)

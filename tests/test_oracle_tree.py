@@ -112,3 +112,30 @@ def test_path_to_root():
     assert T.path_to_root(parent, 9) == [0, 1, 3, 6, 9]
     assert T.path_to_root(parent, 5) == [0, 2, 5]
     assert T.path_to_root(parent, 0) == [0]
+
+
+def test_ragged_mask_equals_truncated_trees():
+    """Ragged trees in a bucket: a request's valid rows are those of its tree
+    alone (its first n_b nodes), absent rows are 0 with position -1, and the
+    parent entries of absent nodes are never read."""
+    rng = np.random.default_rng(77)
+    N, B = 20, 12
+    par = np.stack([T.build_tree(W.random_rank_paths(N, 5, rng))[0] for _ in range(B)])
+    n = rng.integers(1, N + 1, size=B)
+    n[0], n[1] = 1, N
+    lens = rng.integers(0, 500, size=B)
+    garbage = par.copy()
+    for b in range(B):
+        garbage[b, n[b]:] = 999
+    rows, depth, pos, ok = T.tree_mask_batch(garbage, lens, n)
+    assert ok.all()
+    for b in range(B):
+        r1, d1, p1, ok1 = T.tree_mask_batch(par[b:b + 1, :n[b]], lens[b:b + 1])
+        assert ok1.all()
+        np.testing.assert_array_equal(rows[b, :n[b]], r1[0])
+        np.testing.assert_array_equal(pos[b, :n[b]], p1[0])
+        assert (rows[b, n[b]:] == 0).all() and (pos[b, n[b]:] == -1).all() and (depth[b, n[b]:] == 0).all()
+    # a bad parent among the valid nodes is still caught
+    bad = garbage.copy()
+    bad[1, 5] = 7
+    assert not T.tree_mask_batch(bad, lens, n)[3][1]
