@@ -71,10 +71,14 @@ extern "C" {
 #define TV_ATTN_PUBLISH_ALL 4
 
 /* Kernel selection of tv_tree_accept_sample. */
-#define TV_SAMPLE_AUTO 0        /* cluster kernel when every request's cluster is resident at once */
+#define TV_SAMPLE_AUTO 0        /* TV_SAMPLE_CLUSTER when every request's cluster is resident at
+                                   once, else TV_SAMPLE_STREAM with the largest cluster size that
+                                   keeps them all resident, else TV_SAMPLE_SINGLE_CTA            */
 #define TV_SAMPLE_CLUSTER 1     /* one 8-CTA cluster per request, level weights in shared memory;
                                    TV_ERR_UNSUPPORTED when V > 136,512                            */
 #define TV_SAMPLE_SINGLE_CTA 2  /* one CTA per request, rows streamed, weights recomputed per pass */
+#define TV_SAMPLE_STREAM 3      /* clusters of 1-8 CTAs per request streaming their row slices, only
+                                   chunk totals kept; TV_ERR_UNSUPPORTED when V > 1,048,576         */
 
 /* Description of the last failure on this thread ("" if none). */
 const char* tv_last_error(void);
@@ -327,12 +331,13 @@ int tv_tree_accept_greedy(const float* logits, const int32_t* target_argmax,
  * u_final   device float32 [B]: uniform of the replacement / bonus draw.
  * out, n_out, path, out_cols, status: as in tv_tree_accept_greedy.  Tokens
  * outside [0, V) are skipped and flagged TV_DEV_BAD_TOKEN.
- * flags     TV_SAMPLE_*: both kernels give bit-identical results.  The
+ * flags     TV_SAMPLE_*: every kernel gives bit-identical results.  The
  *           cluster kernel splits each row over 8 CTAs and keeps the current
  *           level's weights and q in shared memory (12 bytes per vocabulary
  *           entry), so repeated rejections at a node cost one shared-memory
- *           pass each; TV_SAMPLE_AUTO uses it when all B clusters fit on the
- *           device at once, else the single-CTA kernel.  Unknown flags give
+ *           pass each.  The streaming clusters re-read their slice from
+ *           memory at every pass and keep only 256-element chunk totals, so
+ *           large batches stay resident.  Unknown flags give
  *           TV_ERR_INVALID_ARG.
  */
 int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,

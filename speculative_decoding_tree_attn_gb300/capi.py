@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libtreeverify.so")
 TV_F32, TV_BF16 = 0, 1
 TV_ATTN_AUTO, TV_ATTN_SIMT, TV_ATTN_TCGEN05 = 0, 1, 2
 TV_ATTN_PUBLISH_ALL = 4
-TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA = 0, 1, 2
+TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA, TV_SAMPLE_STREAM = 0, 1, 2, 3
 TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 STATUS_NAMES = {0: "TV_OK", -1: "TV_ERR_INVALID_ARG", -2: "TV_ERR_MISSING_PARENT", -3: "TV_ERR_TOO_MANY_NODES",
                 -4: "TV_ERR_UNSUPPORTED", -5: "TV_ERR_WORKSPACE", -6: "TV_ERR_CUDA"}
@@ -278,7 +278,7 @@ def tv_tree_accept_greedy(tokens, parent, *, logits=None, target_argmax=None, n_
 def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=None, out_cols=None, out=None,
                           n_out=None, path=None, flags=0, status=None, stream=None):
     """Stochastic walk; returns (out [B, out_cols], n_out [B], path [B, out_cols]).
-    flags: TV_SAMPLE_AUTO / TV_SAMPLE_CLUSTER / TV_SAMPLE_SINGLE_CTA."""
+    flags: TV_SAMPLE_AUTO / TV_SAMPLE_CLUSTER / TV_SAMPLE_SINGLE_CTA / TV_SAMPLE_STREAM."""
     _dev(p, "p", (torch.float32,))
     _dev(q, "q", (torch.float32,))
     _dev(tokens, "tokens", (torch.int32,))

@@ -34,6 +34,7 @@
 #include <climits>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "common.h"
@@ -491,7 +492,7 @@ __device__ uint64_t row_pass(const RowView& r, const uint64_t* S, int m, uint64_
 // registers could hold.  Stage = kStageElems elements of p (and q), one
 // 256-element chunk per warp.  Needs 16-byte aligned rows, V % 4 == 0 and
 // 256-element chunks (k == 2).
-constexpr int kStreamStages = 2;
+constexpr int kStreamStages = 2;  // (a third stage measured no faster: the pass is issue-bound)
 constexpr int kChunkElems = 256;                  // a chunk: two float4 per lane of one warp
 constexpr int kStageElems = kChunkElems * kSampleWarps;  // 4096: one chunk per warp and stage
 static_assert(kStageElems % (4 * kSampleThreads) == 0, "whole float4 copies per thread");
@@ -687,10 +688,9 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
   __shared__ uint64_t S[TV_MAX_NODES + 1];
   __shared__ uint64_t s_red[kSampleWarps], s_base;
-  extern __shared__ float4 dsm[];  // stream ring, then the chunk totals of the current / next level
+  extern __shared__ float4 dsm[];  // stream ring, then the chunk totals of the current level
   float4* ring = dsm;
-  uint64_t* cs_cur = reinterpret_cast<uint64_t*>(dsm + 2 * kStreamStages * (kStageElems / 4));
-  uint64_t* cs_tmp = cs_cur + kMaxChunks;
+  uint64_t* cs = reinterpret_cast<uint64_t*>(dsm + 2 * kStreamStages * (kStageElems / 4));
   __shared__ int s_flag, s_idx, s_chunk;
   const int b = blockIdx.x;
   TV_SAMPLE_T(0);
@@ -736,14 +736,15 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
       if (ok) { taken = c; break; }
       // rejected: the target moves to the residual of the current level
       TV_SAMPLE_T(6);
-      const uint64_t Wn = pass(row, m + 1, cs_tmp);
+      const uint64_t Wn = pass(row, m + 1, cs);
       TV_SAMPLE_T(7);
       if (Wn > 0) {
         ++m;
         Wm = Wn;
         if (threadIdx.x == 0) S[m] = Wn;
-        for (int c = threadIdx.x; c < nc; c += blockDim.x) cs_cur[c] = cs_tmp[c];
         __syncthreads();
+      } else if (m >= 1) {
+        pass(row, m, cs);  // the level is kept: its chunk totals again (level 0's are rebuilt at the draw)
       }
     }
     if (taken >= 0) {
@@ -758,11 +759,11 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
     }
     // replacement (after rejections) or bonus (leaf / all children absent)
     TV_SAMPLE_T(2);
-    if (m == 0) Wm = pass(row, 0, cs_cur);
+    if (m == 0) Wm = pass(row, 0, cs);
     TV_SAMPLE_T(3);
     const double t = __dmul_rn((double)u_final[b], (double)Wm);
     const uint64_t thr = (uint64_t)ceil(t);
-    int x = find_crossing(row, S, m, cs_cur, thr, s_red, &s_chunk, &s_base, &s_idx);
+    int x = find_crossing(row, S, m, cs, thr, s_red, &s_chunk, &s_base, &s_idx);
     TV_SAMPLE_T(4);
     if (x > V - 1) x = V - 1;
     emit(o, b, k, x, node);
@@ -790,8 +791,8 @@ constexpr int kScWarps = kScThreads / 32;
 constexpr int kScBatch = 4;                          // float4 of p (and q) a thread requests together
 constexpr size_t kScMaxDyn = 200 * 1024;             // shared memory for the slice state, at most
 
-// Slice length (elements, a multiple of 4) of a V-element row.
-inline int sc_slice(int V) { return (int)((tv::ceil_div(V, kScCtas) + 3) / 4 * 4); }
+// Slice length (elements, a multiple of 4) of a V-element row cut over csize CTAs.
+inline int sc_slice(int V, int csize) { return (int)((tv::ceil_div(V, csize) + 3) / 4 * 4); }
 
 __device__ __forceinline__ uint64_t sc_block_sum(uint64_t v, uint64_t* s_red) {
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
@@ -888,16 +889,78 @@ __device__ uint64_t sc_residual(int len, uint64_t Wm, uint64_t* w, const float* 
 // CTA writes buffer par again only after the next pass's barrier, which every
 // CTA reaches after reading this pass's totals.
 __device__ uint64_t sc_exchange(cooperative_groups::cluster_group& cl, uint64_t mine,
-                                uint64_t (*s_tot)[kScCtas], int par, int rank) {
-  if (threadIdx.x < kScCtas) *cl.map_shared_rank(&s_tot[par][rank], (unsigned)threadIdx.x) = mine;
+                                uint64_t (*s_tot)[kScCtas], int par, int rank, int nct) {
+  if ((int)threadIdx.x < nct) *cl.map_shared_rank(&s_tot[par][rank], (unsigned)threadIdx.x) = mine;
   cl.sync();
   uint64_t t = 0;
-#pragma unroll
-  for (int r = 0; r < kScCtas; ++r) t += s_tot[par][r];
+  for (int r = 0; r < nct; ++r) t += s_tot[par][r];
   return t;
 }
 
-__global__ void __launch_bounds__(kScThreads)
+// The stateless variant's pass at a level: the CTA's slice [lo, lo + len) in
+// 256-element chunks read from global memory (two chunks per warp in
+// flight), each chunk's weight total into cs[] for the draw; returns this
+// thread's part of the slice total.  Levels 0 and 1 sum the fixed-point
+// images in 32-bit parts (add_weights4); deeper levels recompute each weight
+// from p and q (level_weight), O(level) per element.
+constexpr int kScChunk = 256;
+constexpr int kScMaxChunks = 2 * kScThreads;  // chunk totals one block scan covers (find_crossing)
+
+__device__ uint64_t sc_stream(const float* __restrict__ prow, const float* __restrict__ qrow, int lo, int len,
+                              bool vec, int level, const uint64_t* S, uint64_t* cs, int nch) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const RowView r{prow + lo, qrow + lo, len, kScChunk / 128, nch, vec};
+  for (int c0 = warp; c0 < nch; c0 += 2 * kScWarps) {
+    float4 pv[2][2], qv[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = c0 + j * kScWarps;
+        load4(r, c < nch ? c * kScChunk + 128 * h + 4 * lane : len, level, pv[j][h], qv[j][h]);
+      }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int c = c0 + j * kScWarps;
+      uint64_t v;
+      if (level <= 1) {
+        int32_t hh = 0, ll = 0;
+        add_weights4(pv[j][0], qv[j][0], level, hh, ll);
+        add_weights4(pv[j][1], qv[j][1], level, hh, ll);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+          hh += __shfl_xor_sync(0xffffffffu, hh, off);
+          ll += __shfl_xor_sync(0xffffffffu, ll, off);
+        }
+        v = (uint64_t)(((int64_t)hh << 20) + ll);
+      } else {
+        uint64_t acc = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          int64_t wv[4];
+          weights4(r, c < nch ? c * kScChunk + 128 * h + 4 * lane : len, pv[j][h], qv[j][h], S, level, wv);
+          acc += (uint64_t)(wv[0] + wv[1] + wv[2] + wv[3]);
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        v = acc;
+      }
+      if (lane == 0 && c < nch) cs[c] = v;
+    }
+  }
+  __syncthreads();
+  uint64_t t = 0;
+  for (int c = threadIdx.x; c < nch; c += kScThreads) t += cs[c];
+  return t;
+}
+
+// kState: the slice's weights and q kept in shared memory (one pass from
+// global memory per node, later levels from shared memory); otherwise every
+// pass streams the slice from global memory and only chunk totals are kept
+// (a small footprint, so many requests are resident at once).  The cluster
+// size (1 to 8) is a launch parameter.
+template <bool kState>
+__global__ void __launch_bounds__(kScThreads, 4)
     sample_cluster_kernel(const float* __restrict__ p, const float* __restrict__ q,
                           const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent, int64_t pstride,
                           const int32_t* __restrict__ n_nodes, const float* __restrict__ u_accept,
@@ -911,18 +974,21 @@ __global__ void __launch_bounds__(kScThreads)
   __shared__ uint64_t s_red[kScWarps];
   __shared__ int s_kid[TV_MAX_NODES];  // the current node's children in index order
   __shared__ float s_kp[TV_MAX_NODES], s_kq[TV_MAX_NODES], s_ku[TV_MAX_NODES];  // their p(x), q(x), u
-  __shared__ int s_nk, s_x, s_flag;
-  __shared__ uint64_t s_thr;
+  __shared__ int s_nk, s_x, s_flag, s_chunk, s_idx;
+  __shared__ uint64_t s_thr, s_base;
   extern __shared__ __align__(16) uint64_t sc_dyn[];
-  uint64_t* w = sc_dyn;
-  float* qs = reinterpret_cast<float*>(sc_dyn + Ls);
+  uint64_t* w = sc_dyn;                                // kState: level weights of the slice
+  float* qs = reinterpret_cast<float*>(sc_dyn + Ls);   // kState: q of the slice
+  uint64_t* cs = sc_dyn;                               // otherwise: chunk totals
   const int rank = (int)cl.block_rank();
-  const int b = blockIdx.x / kScCtas;
+  const int nct = (int)cl.num_blocks();
+  const int b = blockIdx.x / nct;
   load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
   if (threadIdx.x == 0) s_x = V - 1;  // read by rank 0 after the draw's barrier
   __syncthreads();
   const int n = clamp_nodes(n_nodes, b, N);
   const int lo = min(rank * Ls, V), len = min(V - lo, Ls);
+  const int nch = (len + kScChunk - 1) / kScChunk;
   const bool vec = (V % 4 == 0) && (((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q)) & 15) == 0);
   int node = 0, k = 0, pass = 0;
   TV_SC_DECL;
@@ -979,20 +1045,26 @@ __global__ void __launch_bounds__(kScThreads)
       if (s_flag) { taken = c; break; }
       // rejected: the target moves to the residual of the current level
       TV_SC_MARK();
-      const uint64_t part = m == 0 ? sc_fill(prow, qrow, lo, len, vec, 1, w, qs) : sc_residual(len, Wm, w, qs);
+      uint64_t part;
+      if constexpr (kState) part = m == 0 ? sc_fill(prow, qrow, lo, len, vec, 1, w, qs) : sc_residual(len, Wm, w, qs);
+      else part = sc_stream(prow, qrow, lo, len, vec, m + 1, S, cs, nch);
       TV_SC_ADD(3);
-      const uint64_t Wn = sc_exchange(cl, sc_block_sum(part, s_red), s_tot, pass & 1, rank);
+      const uint64_t Wn = sc_exchange(cl, sc_block_sum(part, s_red), s_tot, pass & 1, rank, nct);
       TV_SC_ADD(4);
       ++pass;
       if (Wn > 0) {
         ++m;
         Wm = Wn;
         if (threadIdx.x == 0) S[m] = Wn;
-        if (threadIdx.x < kScCtas) s_lev[threadIdx.x] = s_tot[(pass - 1) & 1][threadIdx.x];
+        if (threadIdx.x < nct) s_lev[threadIdx.x] = s_tot[(pass - 1) & 1][threadIdx.x];
       } else if (m >= 1) {
-        // the level is kept: rebuild its weights, overwritten by the pass
-        for (int i = threadIdx.x; i < len; i += kScThreads)
-          w[i] = (uint64_t)level_weight(__ldg(prow + lo + i), __ldg(qrow + lo + i), S, m);
+        // the level is kept: rebuild what the pass overwrote
+        if constexpr (kState) {
+          for (int i = threadIdx.x; i < len; i += kScThreads)
+            w[i] = (uint64_t)level_weight(__ldg(prow + lo + i), __ldg(qrow + lo + i), S, m);
+        } else {
+          sc_stream(prow, qrow, lo, len, vec, m, S, cs, nch);
+        }
       }
       __syncthreads();
     }
@@ -1009,9 +1081,11 @@ __global__ void __launch_bounds__(kScThreads)
     // replacement (after rejections) or bonus (leaf / all children absent)
     TV_SC_MARK();
     if (m == 0) {
-      const uint64_t part = sc_fill(prow, qrow, lo, len, vec, 0, w, qs);
-      Wm = sc_exchange(cl, sc_block_sum(part, s_red), s_tot, pass & 1, rank);
-      if (threadIdx.x < kScCtas) s_lev[threadIdx.x] = s_tot[pass & 1][threadIdx.x];
+      uint64_t part;
+      if constexpr (kState) part = sc_fill(prow, qrow, lo, len, vec, 0, w, qs);
+      else part = sc_stream(prow, qrow, lo, len, vec, 0, S, cs, nch);
+      Wm = sc_exchange(cl, sc_block_sum(part, s_red), s_tot, pass & 1, rank, nct);
+      if (threadIdx.x < nct) s_lev[threadIdx.x] = s_tot[pass & 1][threadIdx.x];
       ++pass;
       __syncthreads();
     }
@@ -1023,7 +1097,13 @@ __global__ void __launch_bounds__(kScThreads)
     const uint64_t T = s_lev[rank];
     if (thr == 0) {
       if (rank == 0 && threadIdx.x == 0) s_x = 0;
-    } else if (T > 0 && E < thr && thr <= E + T) {
+    } else if (!kState && T > 0 && E < thr && thr <= E + T) {
+      // the crossing lies in this slice: find its chunk from the totals, then
+      // the element, re-reading that chunk
+      const RowView r{prow + lo, qrow + lo, len, kScChunk / 128, nch, vec};
+      const int x = find_crossing(r, S, m, cs, thr - E, s_red, &s_chunk, &s_base, &s_idx);
+      if (threadIdx.x == 0 && x < len) *cl.map_shared_rank(&s_x, 0u) = lo + x;
+    } else if (kState && T > 0 && E < thr && thr <= E + T) {
       // the crossing lies in this slice: block scan over contiguous segments
       const uint64_t t = thr - E;
       const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
@@ -1070,29 +1150,49 @@ __global__ void __launch_bounds__(kScThreads)
   TV_SC_STORE(b);
 }
 
-// Clusters of sample_cluster_kernel resident on the current device at once
-// for a launch configuration (cached per device and shared-memory size).
+// Clusters of a sampler kernel resident on the current device at once for a
+// launch configuration (cached per device, kernel, cluster size and shared
+// memory).  Also raises the kernel's dynamic shared-memory limit.
+template <bool kState>
 int sc_capacity(const cudaLaunchConfig_t& cfg, int* out) {
   static std::mutex mu;
-  static std::map<std::pair<int, size_t>, int> cache;
+  static std::map<std::tuple<int, size_t, unsigned>, int> cache;
   int dev = 0;
   TV_CUDA_TRY(cudaGetDevice(&dev));
+  const unsigned csize = cfg.attrs[0].val.clusterDim.x;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(dev, cfg.dynamicSmemBytes);
+  const auto key = std::make_tuple(dev, cfg.dynamicSmemBytes, csize);
   const auto it = cache.find(key);
   if (it != cache.end()) {
     *out = it->second;
     return TV_OK;
   }
-  TV_CUDA_TRY(cudaFuncSetAttribute(sample_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScMaxDyn));
+  TV_CUDA_TRY(cudaFuncSetAttribute(sample_cluster_kernel<kState>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kScMaxDyn));
   cudaLaunchConfig_t c = cfg;
-  c.gridDim = dim3(kScCtas);
+  c.gridDim = dim3(csize);
   int n = 0;
-  TV_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, sample_cluster_kernel, &c));
+  TV_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, sample_cluster_kernel<kState>, &c));
   cache[key] = n;
   *out = n;
   return TV_OK;
 }
+
+struct ScLaunch {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  ScLaunch(int csize, size_t dyn, void* stream) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kScThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = (cudaStream_t)stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
 
 int check_accept_args(int B, int N, int V, const void* tokens, const void* parent, int64_t pstride,
                       const void* out, const void* n_out, int out_cols) {
@@ -1147,44 +1247,62 @@ extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32
   tv::clear_error();
   int st = check_accept_args(B, N, V, tokens, parent, parent_bstride, out, n_out, out_cols);
   if (st) return st;
-  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_SINGLE_CTA)
+  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_STREAM)
     return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: unknown flags %d", flags);
   if (B == 0) return TV_OK;
   if (!p || !q || !u_accept || !u_final) return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: null pointer");
   AcceptOut o{out, n_out, path, out_cols, status};
-  const int Ls = sc_slice(V);
-  const size_t dyn = (size_t)Ls * (sizeof(uint64_t) + sizeof(float));
-  bool cluster = false;
-  if (flags != TV_SAMPLE_SINGLE_CTA && dyn <= kScMaxDyn && B <= INT_MAX / kScCtas) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kScCtas;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kScThreads);
-    cfg.dynamicSmemBytes = dyn;
-    cfg.stream = (cudaStream_t)stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int capacity = 0;  // (also sets the kernel's shared-memory limit)
-    st = sc_capacity(cfg, &capacity);
+  if (B > INT_MAX / kScCtas && flags != TV_SAMPLE_SINGLE_CTA)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: B=%d too large", B);
+  // 1. one 8-CTA cluster per request keeping the level weights on chip, when
+  //    every request's cluster is resident at once (or when asked for)
+  const int Ls8 = sc_slice(V, kScCtas);
+  const size_t dyn_state = (size_t)Ls8 * (sizeof(uint64_t) + sizeof(float));
+  if ((flags == TV_SAMPLE_AUTO || flags == TV_SAMPLE_CLUSTER) && dyn_state <= kScMaxDyn) {
+    ScLaunch L(kScCtas, dyn_state, stream);
+    int capacity = 0;
+    st = sc_capacity<true>(L.cfg, &capacity);
     if (st) return st;
-    // automatic: clusters only when the whole batch is resident at once
-    cluster = flags == TV_SAMPLE_CLUSTER || B <= capacity;
-    if (cluster) {
-      cfg.gridDim = dim3((unsigned)(B * kScCtas));
-      cudaError_t e = cudaLaunchKernelEx(&cfg, sample_cluster_kernel, p, q, tokens, parent, parent_bstride, n_nodes,
-                                         u_accept, u_final, (int)N, (int)V, Ls, o);
-      if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel");
+    if (flags == TV_SAMPLE_CLUSTER || B <= capacity) {
+      L.cfg.gridDim = dim3((unsigned)(B * kScCtas));
+      cudaError_t e = cudaLaunchKernelEx(&L.cfg, sample_cluster_kernel<true>, p, q, tokens, parent, parent_bstride,
+                                         n_nodes, u_accept, u_final, (int)N, (int)V, Ls8, o);
+      if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel<state>");
       return TV_OK;
     }
   } else if (flags == TV_SAMPLE_CLUSTER) {
-    return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_accept_sample: the cluster kernel needs V <= %d (V=%d, B=%d)",
-                    kScCtas * (int)(kScMaxDyn / 12 / 4 * 4), V, B);
+    return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_accept_sample: the cluster kernel needs V <= %d (V=%d)",
+                    kScCtas * (int)(kScMaxDyn / 12 / 4 * 4), V);
+  }
+  // 2. streaming clusters: the largest cluster (8, 4, 2 or 1 CTAs) with which
+  //    all B requests are resident at once, each slice within one block scan
+  //    of chunk totals
+  if (flags == TV_SAMPLE_AUTO || flags == TV_SAMPLE_STREAM) {
+    const size_t dyn = sizeof(uint64_t) * kScMaxChunks;
+    int pick = 0;
+    for (int csize = kScCtas; csize >= 1; csize /= 2) {
+      if ((int64_t)sc_slice(V, csize) > (int64_t)kScMaxChunks * kScChunk) break;  // slice too long
+      ScLaunch L(csize, dyn, stream);
+      int capacity = 0;
+      st = sc_capacity<false>(L.cfg, &capacity);
+      if (st) return st;
+      pick = csize;
+      if (B <= capacity) break;
+    }
+    if (pick > 0) {
+      ScLaunch L(pick, dyn, stream);
+      L.cfg.gridDim = dim3((unsigned)(B * pick));
+      cudaError_t e = cudaLaunchKernelEx(&L.cfg, sample_cluster_kernel<false>, p, q, tokens, parent, parent_bstride,
+                                         n_nodes, u_accept, u_final, (int)N, (int)V, sc_slice(V, pick), o);
+      if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel<stream>");
+      return TV_OK;
+    }
+    if (flags == TV_SAMPLE_STREAM)
+      return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_accept_sample: V=%d too large for the streaming clusters", V);
   }
   // one CTA per request, rows streamed and w_m recomputed per pass
-  constexpr size_t kDyn = sizeof(float4) * 2 * kStreamStages * (kStageElems / 4) + sizeof(uint64_t) * 2 * kMaxChunks;
+  constexpr size_t kDyn = sizeof(float4) * 2 * kStreamStages * (kStageElems / 4) + sizeof(uint64_t) * kMaxChunks;
+  static_assert(2 * (kDyn + 2048 + 1024) <= 228 * 1024, "two CTAs per SM");
   cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDyn);
   if (e != cudaSuccess) return tv::cuda_fail(e, "cudaFuncSetAttribute(sample_kernel)");
   sample_kernel<<<B, kSampleThreads, kDyn, (cudaStream_t)stream>>>(p, q, tokens, parent, parent_bstride, n_nodes, u_accept,

@@ -78,7 +78,7 @@ def test_greedy_overflow_flag():
     assert status.item() == capi.TV_DEV_OUT_OVERFLOW and n_out.item() == 3
 
 
-KERNELS = {"auto": 0, "cluster": 1, "single_cta": 2}
+KERNELS = {"auto": 0, "cluster": 1, "single_cta": 2, "stream": 3}
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -114,12 +114,13 @@ def test_sample_tree_full_workload_bit_exact(kernel):
     assert n.mean() > 2.0 and n.min() >= 1
 
 
-@pytest.mark.parametrize("V,B,kernel", [(V, 200, k) for V in (4, 33, 1000, 4096) for k in ("cluster", "single_cta")]
-                         + [(160000, 12, "auto"), (160001, 12, "auto")])
+@pytest.mark.parametrize("V,B,kernel",
+                         [(V, 200, k) for V in (4, 33, 1000, 4096) for k in ("cluster", "single_cta", "stream")]
+                         + [(V, 12, k) for V in (160000, 160001) for k in ("auto", "single_cta")])
 def test_sample_trees_with_sibling_levels(V, B, kernel):
     """Trees with up to 5 siblings per node: several residual levels per node,
-    on both kernels.  Vocabularies above 136,512 run the single-CTA kernel
-    (aligned rows streamed through shared memory, odd V read directly)."""
+    on every kernel.  Vocabularies above 136,512 have no on-chip-state
+    cluster kernel (aligned rows and odd V both)."""
     rng = np.random.default_rng(120 + V)
     N = 16
     paths = [(0,), (1,), (2,), (3,), (4,), (0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (4, 0), (0, 0, 0), (0, 0, 1),
@@ -146,7 +147,8 @@ def test_sample_trees_with_sibling_levels(V, B, kernel):
                                        flags=capi.TV_SAMPLE_CLUSTER)
 
 
-@pytest.mark.parametrize("V,kernel", [(4096, "cluster"), (4096, "single_cta"), (160000, "auto")])
+@pytest.mark.parametrize("V,kernel", [(4096, "cluster"), (4096, "single_cta"), (4096, "stream"), (160000, "auto"),
+                                      (160000, "single_cta")])
 def test_sample_kept_level_after_empty_residual(V, kernel):
     """A rejection whose residual pass leaves no mass keeps the level (the
     p = q guard) and the final draw still uses that level's weights: q is
@@ -198,7 +200,7 @@ def test_gpu_chain_lossless_chi_square(verifier_facts):
     assert chi_square(seqs, pt) < thr
 
 
-@pytest.mark.parametrize("kernel", ["cluster", "single_cta"])
+@pytest.mark.parametrize("kernel", ["cluster", "single_cta", "stream"])
 def test_gpu_tree_lossless_chi_square(verifier_facts, kernel):
     f = verifier_facts
     V, n_tok, thr = int(f["chi2_vocab"][0][0]), int(f["chi2_tokens"][0][0]), float(f["chi2_threshold"][0][0])

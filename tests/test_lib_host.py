@@ -85,5 +85,5 @@ def test_device_entry_points_reject_bad_sizes_on_host():
                                    0, None, None) == 0
     assert b"bad sizes" in h.tv_last_error() or h.tv_last_error() == b""
     assert h.tv_tree_accept_sample(None, None, None, None, 0, None, None, None, 0, 10, 10, None, None, None, 4,
-                                   3, None, None) == -1
+                                   4, None, None) == -1
     assert b"unknown flags" in h.tv_last_error()
