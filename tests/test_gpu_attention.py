@@ -110,6 +110,23 @@ def test_row_groups_and_gqa_widths(G, N):
             _check_all(inp, paths, BF16_TOL, flags, num_ctas)
 
 
+@pytest.mark.parametrize("bs", [1, 8, 32, 48, 128, 256])
+def test_cache_block_sizes(bs):
+    """Paged caches with other block sizes: the tcgen05 kernel takes multiples
+    of 16 that divide 64 or that 64 divides (one TMA box per block, or a block
+    spanning tiles); the others run the CUDA-core kernel (automatic choice)."""
+    rng = np.random.default_rng(140 + bs)
+    N = 26
+    paths = W.random_rank_paths(N, 5, rng)
+    w = _workload(3, 8, 2, 128, "bf16", bs, N, 141 + bs)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[bs * 3 + 5, 1, 700])
+    tc = tc_available(8, 2, N, bs=bs)
+    assert tc == (bs % 16 == 0 and (64 % bs == 0 or bs % 64 == 0))
+    for flags in [capi.TV_ATTN_AUTO, capi.TV_ATTN_SIMT] + ([capi.TV_ATTN_TCGEN05] if tc else []):
+        for num_ctas in (0, 7):
+            _check_all(inp, paths, BF16_TOL, flags, num_ctas)
+
+
 @pytest.mark.parametrize("D", [64, 256])
 def test_other_head_dims_simt(D):
     rng = np.random.default_rng(95 + D)
