@@ -63,6 +63,10 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flags", type=int, default=0, help="tree attention kernel selection (0 auto, 1 CUDA-core, 2 tcgen05)")
     ap.add_argument("--num-ctas", type=int, default=0)
+    ap.add_argument("--rope", default="auto", choices=["auto", "fused", "separate"],
+                    help="fused: tree-key RoPE inside the mask kernel and Q RoPE inside the attention kernel's Q load; "
+                         "separate: tv_tree_mask + tv_rope_apply + tv_tree_attn_verify; auto: fused where it "
+                         "measured faster (the one-M-tile kernel, G*N <= 128, with B*Hkv >= 2 x SMs), else separate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
@@ -273,7 +277,7 @@ def sample_order(lens, seed=0):
 # --------------------------------------------------------------------------- GPU step
 
 class Step:
-    def __init__(self, w, dev, flags, num_ctas):
+    def __init__(self, w, dev, flags, num_ctas, rope="fused"):
         from speculative_decoding_tree_attn_gb300 import capi
         self.capi, self.w, self.dev = capi, w, dev
         self.paths = w.paths()
@@ -298,8 +302,14 @@ class Step:
         self.out = torch.empty_like(self.inp["q"])
         dt = self.inp["q"].dtype
         self.flags, self.num_ctas = flags, num_ctas
+        # auto: fused where it measured faster -- the one-M-tile kernel with
+        # enough (request, KV head) units for two busy CTAs per SM
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.fused_rope = rope == "fused" or (rope == "auto" and (w.Hq // w.Hkv) * n <= 128
+                                              and B * w.Hkv >= 2 * sms)
+        ws_flags = flags | (capi.TV_ATTN_ROPE_Q if self.fused_rope else 0)
         self.ws = capi.alloc_workspace(capi.tv_tree_attn_workspace_size(B, n, w.Hq, w.Hkv, w.D, dt, w.block_size,
-                                                                         num_ctas, flags), dev)
+                                                                         num_ctas, ws_flags), dev)
         self.greedy = self.sample = None
         if w.accept == "greedy":
             self.greedy = W.greedy_inputs(w, parent, device=dev)
@@ -321,23 +331,33 @@ class Step:
         if flags == capi.TV_ATTN_AUTO:
             try:
                 capi.tv_tree_attn_workspace_size(B, n, w.Hq, w.Hkv, w.D, dt, w.block_size, num_ctas,
-                                                 capi.TV_ATTN_TCGEN05)
+                                                 capi.TV_ATTN_TCGEN05 | (ws_flags & capi.TV_ATTN_ROPE_Q))
                 uses_tc = True
             except capi.TVError:
                 uses_tc = False
-        self.launches = 2 + (1 if uses_tc else 3) + (1 if w.accept != "none" else 0)
+        # mask (+ rope), the attention kernel(s), the acceptance kernel
+        self.launches = (1 if self.fused_rope else 2) + (1 if uses_tc else 3) + (1 if w.accept != "none" else 0)
 
     def run_attn(self):
         i = self.inp
-        self.capi.tv_tree_attn_verify(i["q"], i["k_cache"], i["v_cache"], i["block_table"], self.seq_lens,
-                                      i["k_tree"], i["v_tree"], self.mask, out=self.out, workspace=self.ws,
-                                      num_ctas=self.num_ctas, flags=self.flags)
+        if self.fused_rope:
+            self.capi.tv_tree_attn_verify_rope(i["q"], i["k_cache"], i["v_cache"], i["block_table"], self.seq_lens,
+                                               i["k_tree"], i["v_tree"], self.mask, self.table, out=self.out,
+                                               workspace=self.ws, num_ctas=self.num_ctas, flags=self.flags)
+        else:
+            self.capi.tv_tree_attn_verify(i["q"], i["k_cache"], i["v_cache"], i["block_table"], self.seq_lens,
+                                          i["k_tree"], i["v_tree"], self.mask, out=self.out, workspace=self.ws,
+                                          num_ctas=self.num_ctas, flags=self.flags)
 
     def run(self, ev_attn=None):
         c, i = self.capi, self.inp
-        c.tv_tree_mask(self.parent, self.seq_lens, mask=self.mask, depth=self.depth, pos=self.pos,
-                       n_nodes=self.n_nodes)
-        c.tv_rope_apply(i["q"], i["k_tree"], self.pos, self.table)
+        if self.fused_rope:  # mask + tree-key rotation in one kernel; Q is rotated inside the attention kernel
+            c.tv_tree_prepare(self.parent, self.seq_lens, i["k_tree"], self.table, n_nodes=self.n_nodes,
+                              mask=self.mask, depth=self.depth, pos=self.pos)
+        else:
+            c.tv_tree_mask(self.parent, self.seq_lens, mask=self.mask, depth=self.depth, pos=self.pos,
+                           n_nodes=self.n_nodes)
+            c.tv_rope_apply(i["q"], i["k_tree"], self.pos, self.table)
         if ev_attn:
             ev_attn[0].record()
         self.run_attn()
@@ -392,7 +412,7 @@ class Step:
 def run_ours(args, world, rank, local):
     w = rank_workload(W.WORKLOADS[args.workload], rank)
     dev = torch.device("cuda", torch.cuda.current_device())
-    st = Step(w, dev, args.flags, args.num_ctas)
+    st = Step(w, dev, args.flags, args.num_ctas, args.rope)
     ws_bytes = st.attn_bytes + sum(t.numel() * t.element_size() for t in st.per_step_inputs().values())
     flush = None
     if ws_bytes < 2 * L2_BYTES:
@@ -506,7 +526,8 @@ def run_ours(args, world, rank, local):
     achieved = st.attn_bytes / (attn_mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": "tv_tree_attn_verify (tcgen05: counter memset + one persistent kernel)",
+                "kernel": ("tv_tree_attn_verify_rope" if st.fused_rope else "tv_tree_attn_verify")
+                          + " (tcgen05: counter memset + one persistent kernel)",
                 "algorithmic_bytes_per_call": int(st.attn_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
                 "attn_ms_mean": round(attn_mean_ms, 4)}
 
@@ -533,7 +554,8 @@ def run_ours(args, world, rank, local):
                        "l2": ("L2 flushed between steps" if flush is not None
                               else f"inputs larger than L2 ({ws_bytes / 2**30:.2f} GiB per step)"),
                        "kernel_flags": args.flags, "parallelism": f"dp{world}: one batch of {w.B} requests per GPU, no collective on the data path",
-                       "timing": "eager calls" if args.eager else "CUDA graph replays of the step"},
+                       "timing": "eager calls" if args.eager else "CUDA graph replays of the step",
+                       "rope": "fused" if st.fused_rope else "separate"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": st.launches * args.steps,
             "kv_commit": commit,

@@ -69,6 +69,10 @@ extern "C" {
  * never directly from the finishing CTA's accumulator.  Same results up to
  * rounding; for testing the second merge route. */
 #define TV_ATTN_PUBLISH_ALL 4
+/* Workspace query for tv_tree_attn_verify_rope (Q rotated while it is
+ * loaded; the tensor-core kernel then needs Hq/Hkv in {4, 8, 16}).  Not a
+ * flag of tv_tree_attn_verify itself. */
+#define TV_ATTN_ROPE_Q 8
 
 /* Kernel selection of tv_tree_accept_sample. */
 #define TV_SAMPLE_AUTO 0        /* TV_SAMPLE_CLUSTER when every request's cluster is resident at
@@ -136,6 +140,26 @@ int tv_tree_build(const int32_t* ranks, const int32_t* offsets, int32_t n_paths,
 int tv_tree_mask(const int32_t* parent, int64_t parent_bstride, const int32_t* seq_lens,
                  const int32_t* n_nodes, int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
                  int32_t* pos, int32_t* status, void* stream);
+
+/*
+ * tv_tree_prepare -- device, asynchronous.  tv_tree_mask and the rotation of
+ * the tree keys in one launch: the same mask, depth and pos as tv_tree_mask,
+ * and k_tree rotated in place at pos exactly as tv_rope_apply would (same
+ * bits).  Used with tv_tree_attn_verify_rope, which rotates Q itself, the
+ * step needs no separate RoPE kernel.
+ *
+ * parent, parent_bstride, seq_lens, n_nodes, mask, depth, pos: as in
+ *           tv_tree_mask.
+ * k_tree    device [B, N, Hkv, head_dim] (dtype), rotated in place (NULL: only
+ *           the mask part).  head_dim in {16, 32, 64, 128, 256}.
+ * cos_sin   device float32 [max_pos, 2, head_dim/2] from tv_rope_table.
+ * A position outside [0, max_pos) other than -1 leaves the row untouched and
+ * sets TV_DEV_BAD_POSITION; -1 (absent node) leaves it silently.
+ */
+int tv_tree_prepare(const int32_t* parent, int64_t parent_bstride, const int32_t* seq_lens,
+                    const int32_t* n_nodes, int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
+                    int32_t* pos, void* k_tree, int32_t Hkv, int32_t head_dim, int32_t dtype,
+                    const float* cos_sin, int32_t max_pos, int32_t* status, void* stream);
 
 /*
  * tv_rope_table -- device, asynchronous.  Fills the rotary table used by
@@ -236,6 +260,33 @@ int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                         int32_t dtype, float scale, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, int32_t num_ctas,
                         int32_t flags, int32_t* status, void* stream);
+
+/*
+ * tv_tree_attn_verify_rope -- device, asynchronous.  tv_tree_attn_verify with
+ * RoPE of the queries fused into the kernels' Q load ("Build the tree
+ * attention mask ...", "What interviewers probe next": a node is rotated at
+ * its depth position; the separate rope step is one read and write of Q the
+ * fused load saves).  q is given unrotated and is not modified; each row is
+ * rotated at L_b + depth, depth = popcount(mask row) - 1, with the table
+ * cos_sin [max_pos, 2, head_dim/2] and exactly the arithmetic and rounding of
+ * tv_rope_apply, so the outputs have the same bits as tv_rope_apply followed
+ * by tv_tree_attn_verify.  k_tree must already be rotated (tv_tree_prepare,
+ * or tv_rope_apply with q = NULL).  A zero mask row (absent node) is not
+ * rotated; a position >= max_pos leaves the row unrotated and sets
+ * TV_DEV_BAD_POSITION.  Workspace: tv_tree_attn_workspace_size with flags |
+ * TV_ATTN_ROPE_Q (the tensor-core kernel takes Hq/Hkv in {4, 8, 16} here; the
+ * CUDA-core kernel any).  Other arguments as in tv_tree_attn_verify.
+ */
+int tv_tree_attn_verify_rope(const void* q, const void* k_cache, const void* v_cache,
+                             int64_t num_blocks, int32_t block_size,
+                             const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* seq_lens, const void* k_tree, const void* v_tree,
+                             const uint64_t* mask, int64_t mask_bstride,
+                             const float* cos_sin, int32_t max_pos,
+                             int32_t B, int32_t N, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                             int32_t dtype, float scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, int32_t num_ctas,
+                             int32_t flags, int32_t* status, void* stream);
 
 /*
  * tv_tree_attn_verify_static -- device, asynchronous; allocation-free variant

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libtreeverify.so")
 TV_F32, TV_BF16 = 0, 1
 TV_ATTN_AUTO, TV_ATTN_SIMT, TV_ATTN_TCGEN05 = 0, 1, 2
 TV_ATTN_PUBLISH_ALL = 4
+TV_ATTN_ROPE_Q = 8
 TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA, TV_SAMPLE_STREAM = 0, 1, 2, 3
 TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 STATUS_NAMES = {0: "TV_OK", -1: "TV_ERR_INVALID_ARG", -2: "TV_ERR_MISSING_PARENT", -3: "TV_ERR_TOO_MANY_NODES",
@@ -42,6 +43,11 @@ SIGNATURES = {
     "tv_tree_attn_verify_static": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _I64, _I32,
                                                   _I32, _I32, _I32, _I32, _I32, _F, _P, _P, _I32, _I32, _P, _P]),
     "tv_tree_attn_static_workspace_bytes": (ctypes.c_size_t, []),
+    "tv_tree_attn_verify_rope": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _I64, _P, _I32,
+                                                _I32, _I32, _I32, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _I32, _I32,
+                                                _P, _P]),
+    "tv_tree_prepare": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _P, _I32,
+                                       _P, _P]),
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
                                              _I32, _P, _P]),
@@ -210,6 +216,66 @@ def tv_tree_attn_verify(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tr
                                      _ptr(workspace), workspace.numel(), num_ctas, flags, _ptr(status),
                                      _stream(stream)))
     return out
+
+
+def tv_tree_attn_verify_rope(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, mask, cos_sin, *,
+                             scale=None, out=None, lse=None, workspace=None, num_ctas=0, flags=0, status=None,
+                             stream=None):
+    """Tree attention with Q rotated as it is loaded (q unrotated and left as
+    it is; k_tree already rotated); returns out [B, N, Hq, D], the same bits as
+    tv_rope_apply followed by tv_tree_attn_verify."""
+    dts = (torch.float32, torch.bfloat16)
+    _dev(q, "q", dts)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_tree", k_tree), ("v_tree", v_tree)):
+        _dev(t, name, (q.dtype,))
+    _dev(block_table, "block_table", (torch.int32,))
+    _dev(seq_lens, "seq_lens", (torch.int32,))
+    _dev(mask, "mask", (torch.int64,))
+    _dev(cos_sin, "cos_sin", (torch.float32,))
+    B, N, Hq, D = q.shape
+    Hkv = k_tree.shape[2]
+    num_blocks, _, block_size, _ = k_cache.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(tv_tree_attn_workspace_size(B, N, Hq, Hkv, D, q.dtype, block_size, num_ctas,
+                                                                flags | TV_ATTN_ROPE_Q), q.device)
+    mstride = 0 if mask.dim() == 1 else mask.stride(0)
+    _check("tv_tree_attn_verify_rope",
+           lib().tv_tree_attn_verify_rope(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, block_size,
+                                          _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(k_tree),
+                                          _ptr(v_tree), _ptr(mask), mstride, _ptr(cos_sin), cos_sin.shape[0], B, N,
+                                          Hq, Hkv, D, _code(q.dtype), scale, _ptr(out), _ptr(lse), _ptr(workspace),
+                                          workspace.numel(), num_ctas, flags, _ptr(status), _stream(stream)))
+    return out
+
+
+def tv_tree_prepare(parent, seq_lens, k_tree=None, cos_sin=None, *, n_nodes=None, status=None, mask=None,
+                    depth=None, pos=None, stream=None):
+    """tv_tree_mask plus the rotation of k_tree [B, N, Hkv, D] in place at pos,
+    in one launch; returns (mask, depth, pos) like tv_tree_mask."""
+    _dev(parent, "parent", (torch.int32,))
+    _dev(seq_lens, "seq_lens", (torch.int32,))
+    if n_nodes is not None:
+        _dev(n_nodes, "n_nodes", (torch.int32,))
+    B = seq_lens.numel()
+    N = parent.shape[-1]
+    bstride = 0 if parent.dim() == 1 else parent.stride(0)
+    dev = seq_lens.device
+    mask = torch.empty(B, N, dtype=torch.int64, device=dev) if mask is None else mask
+    depth = torch.empty(B, N, dtype=torch.int32, device=dev) if depth is None else depth
+    pos = torch.empty(B, N, dtype=torch.int32, device=dev) if pos is None else pos
+    Hkv = D = dt = max_pos = 0
+    if k_tree is not None:
+        _dev(k_tree, "k_tree", (torch.float32, torch.bfloat16))
+        _dev(cos_sin, "cos_sin", (torch.float32,))
+        Hkv, D, dt, max_pos = k_tree.shape[2], k_tree.shape[3], _code(k_tree.dtype), cos_sin.shape[0]
+    _check("tv_tree_prepare",
+           lib().tv_tree_prepare(_ptr(parent), bstride, _ptr(seq_lens), _ptr(n_nodes), B, N, _ptr(mask),
+                                 _ptr(depth), _ptr(pos), _ptr(k_tree), Hkv, D, dt, _ptr(cos_sin), max_pos,
+                                 _ptr(status), _stream(stream)))
+    return mask, depth, pos
 
 
 def tv_tree_attn_static_workspace_bytes():

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "attn_common.cuh"
+#include "rope_math.cuh"
 #include "attn_tc.h"
 
 namespace tv {
@@ -134,7 +135,25 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(AttnParams p
       float v = 0.f;
       if (gr < p.R) {
         const int i = gr / p.G, h = kvh * p.G + gr % p.G;
-        v = to_f32(q[(((int64_t)b * p.N + i) * p.Hq + h) * D + d]);
+        const T* qrow = q + (((int64_t)b * p.N + i) * p.Hq + h) * D;
+        v = to_f32(qrow[d]);
+        if (p.rope_cs) {
+          // rotate at L_b + depth (depth from the ancestor row), the
+          // arithmetic and rounding of tv_rope_apply; an absent node (row 0)
+          // or a position past the table stays as it is
+          const uint64_t mr = p.mask[(int64_t)b * p.mask_bstride + i];
+          const int ps = mr ? p.seq_lens[b] + __popcll(mr) - 1 : -1;
+          if (ps >= 0 && ps < p.rope_max_pos) {
+            constexpr int half = D / 2;
+            const int k = d % half;
+            float y1, y2;
+            rope_pair(to_f32(qrow[k]), to_f32(qrow[k + half]), p.rope_cs[(int64_t)ps * D + k],
+                      p.rope_cs[(int64_t)ps * D + half + k], y1, y2);
+            v = to_f32(from_f32<T>(d < half ? y1 : y2));
+          } else if (ps >= p.rope_max_pos && d == 0 && p.status) {
+            atomicOr(p.status, TV_DEV_BAD_POSITION);
+          }
+        }
       }
       Qs[idx] = v;
     }
@@ -381,6 +400,8 @@ void layout_workspace(AttnConfig* cfg, int D) {
 
 int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size, int num_ctas, int flags,
                 AttnConfig* cfg) {
+  const bool rope = (flags & TV_ATTN_ROPE_Q) != 0;
+  flags &= ~TV_ATTN_ROPE_Q;
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Hq % Hkv)
     return fail(TV_ERR_INVALID_ARG, "tree attention: bad sizes B=%d N=%d Hq=%d Hkv=%d", B, N, Hq, Hkv);
   if (D != 64 && D != 128 && D != 256)
@@ -394,10 +415,10 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
   int st = current_device_info(&dev);
   if (st) return st;
   const int G = Hq / Hkv, R = G * N;
-  const bool tc_ok = tc_supported(dev, dtype, D, R, G, block_size);
+  const bool tc_ok = tc_supported(dev, dtype, D, R, G, block_size, rope);
   if (sel == TV_ATTN_TCGEN05 && !tc_ok)
     return fail(TV_ERR_UNSUPPORTED, "tcgen05 tree attention: %s (sm_%d%d, opt-in smem %zu B)",
-                tc_unsupported_reason(dev, dtype, D, R, G, block_size), dev.cc_major, dev.cc_minor,
+                tc_unsupported_reason(dev, dtype, D, R, G, block_size, rope), dev.cc_major, dev.cc_minor,
                 dev.max_smem_optin);
   cfg->tc = (sel == TV_ATTN_TCGEN05) || (sel == TV_ATTN_AUTO && tc_ok);
   int per_sm = 1;
@@ -451,15 +472,15 @@ extern "C" int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int
   return TV_OK;
 }
 
-extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
-                                   int32_t block_size, const int32_t* block_table, int32_t max_blocks,
-                                   const int32_t* seq_lens, const void* k_tree, const void* v_tree,
-                                   const uint64_t* mask, int64_t mask_bstride, int32_t B, int32_t N, int32_t Hq,
-                                   int32_t Hkv, int32_t head_dim, int32_t dtype, float scale, void* out, float* lse,
-                                   void* workspace, size_t workspace_bytes, int32_t num_ctas, int32_t flags,
-                                   int32_t* status, void* stream) {
-  using namespace tv;
-  clear_error();
+namespace tv {
+namespace {
+
+int verify_impl(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks, int32_t block_size,
+                const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens, const void* k_tree,
+                const void* v_tree, const uint64_t* mask, int64_t mask_bstride, int32_t B, int32_t N, int32_t Hq,
+                int32_t Hkv, int32_t head_dim, int32_t dtype, float scale, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, int32_t num_ctas, int32_t flags, const float* rope_cs, int32_t rope_max_pos,
+                int32_t* status, void* stream) {
   AttnConfig cfg;
   int st = attn_config(B, N, Hq, Hkv, head_dim, dtype, block_size, num_ctas, flags, &cfg);
   if (st) return st;
@@ -486,6 +507,9 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
   p.R = p.G * N; p.RPG = cfg.RPG; p.RG = cfg.RG; p.U = cfg.U; p.BLK = cfg.BLK; p.P = cfg.P;
   p.unit_cost = cfg.tc ? tc_unit_cost(cfg.RPG) : 0;
   p.direct_merge = (flags & TV_ATTN_PUBLISH_ALL) ? 0 : 1;
+  p.rope_cs = rope_cs;
+  p.rope_max_pos = rope_max_pos;
+  p.status = status;
   // tile indices of the plan are 32-bit
   const int64_t unit_tiles_max = ((int64_t)max_blocks * block_size + cfg.BLK - 1) / cfg.BLK + 1 + p.unit_cost;
   if ((int64_t)cfg.U * unit_tiles_max >= (int64_t(1) << 31))
@@ -503,6 +527,40 @@ extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const voi
   if ((st = launch_plan(p, s))) return st;
   if ((st = simt_dispatch(p, dtype, s, nullptr))) return st;
   return launch_combine(p, dtype, s);
+}
+
+}  // namespace
+}  // namespace tv
+
+extern "C" int tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                                   int32_t block_size, const int32_t* block_table, int32_t max_blocks,
+                                   const int32_t* seq_lens, const void* k_tree, const void* v_tree,
+                                   const uint64_t* mask, int64_t mask_bstride, int32_t B, int32_t N, int32_t Hq,
+                                   int32_t Hkv, int32_t head_dim, int32_t dtype, float scale, void* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, int32_t num_ctas, int32_t flags,
+                                   int32_t* status, void* stream) {
+  tv::clear_error();
+  if (flags & TV_ATTN_ROPE_Q)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify: TV_ATTN_ROPE_Q belongs to tv_tree_attn_verify_rope");
+  return tv::verify_impl(q, k_cache, v_cache, num_blocks, block_size, block_table, max_blocks, seq_lens, k_tree,
+                         v_tree, mask, mask_bstride, B, N, Hq, Hkv, head_dim, dtype, scale, out, lse, workspace,
+                         workspace_bytes, num_ctas, flags, nullptr, 0, status, stream);
+}
+
+extern "C" int tv_tree_attn_verify_rope(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                                        int32_t block_size, const int32_t* block_table, int32_t max_blocks,
+                                        const int32_t* seq_lens, const void* k_tree, const void* v_tree,
+                                        const uint64_t* mask, int64_t mask_bstride, const float* cos_sin,
+                                        int32_t max_pos, int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
+                                        int32_t head_dim, int32_t dtype, float scale, void* out, float* lse,
+                                        void* workspace, size_t workspace_bytes, int32_t num_ctas, int32_t flags,
+                                        int32_t* status, void* stream) {
+  tv::clear_error();
+  if (B > 0 && (!cos_sin || max_pos < 1))
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify_rope: needs the rotary table");
+  return tv::verify_impl(q, k_cache, v_cache, num_blocks, block_size, block_table, max_blocks, seq_lens, k_tree,
+                         v_tree, mask, mask_bstride, B, N, Hq, Hkv, head_dim, dtype, scale, out, lse, workspace,
+                         workspace_bytes, num_ctas, flags | TV_ATTN_ROPE_Q, cos_sin, max_pos, status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -61,6 +61,10 @@ struct AttnParams {
   int P;    // persistent CTAs
   int unit_cost;  // extra virtual tiles charged per unit (its fixed start/finish cost)
   int direct_merge;  // tcgen05: the last piece may merge straight from its accumulator
+  const float* rope_cs;  // non-null: Q arrives unrotated and is rotated as it is loaded, at
+                         // L_b + depth (depth from the ancestor row), with this cos/sin table
+  int rope_max_pos;      // rows of rope_cs
+  int32_t* status;       // device status word (nullable), TV_DEV_* bits
   float scale_log2;  // softmax scale * log2(e)
 };
 

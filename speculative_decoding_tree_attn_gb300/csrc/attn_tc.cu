@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "attn_tc.h"
+#include "rope_math.cuh"
 
 #ifdef TV_TC_TRACE
 // Development aid: clock64 stamps of pipeline events of CTA 0, one slot per
@@ -353,6 +354,76 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ------------------------------------------------------------ fused RoPE of Q
+
+// Position of a row from its ancestor row: L + depth with depth = popcount - 1
+// (the row holds the node and its ancestors); an absent node (row 0) has none.
+__device__ __forceinline__ int row_pos(uint64_t mrow, int L) { return mrow ? L + __popcll(mrow) - 1 : -1; }
+
+// Rotate-half RoPE of one whole bf16 query row (q[c] = elements 8c .. 8c+7) at
+// position pos, with the float32 arithmetic and bf16 rounding of
+// tv_rope_apply, so the rotated row has the same bits.  The G consecutive
+// lanes holding the G heads of one node share the position: lane j of the
+// group loads the cosines and sines of frequencies [j * 64 / G, (j+1) * 64 / G)
+// of the table row and the others read them by shuffles (every lane of the
+// warp takes part).  pos outside [0, max_pos) leaves the row as it is (-1:
+// an absent node; otherwise TV_DEV_BAD_POSITION).
+template <int G>
+__device__ __forceinline__ void rope_row_group(uint4 (&q)[16], const float* __restrict__ cs, int pos, int max_pos,
+                                               int32_t* status, int lane) {
+  constexpr int kPer = 64 / G;
+  static_assert(kPer % 4 == 0, "whole float4 table loads per lane");
+  const int j = lane % G, base = lane - j;
+  const bool inb = pos >= 0 && pos < max_pos;
+  if (pos >= max_pos && j == 0 && status) atomicOr(status, TV_DEV_BAD_POSITION);
+  float c[kPer], sn[kPer];
+#pragma unroll
+  for (int v = 0; v < kPer; ++v) c[v] = sn[v] = 0.f;
+  if (inb) {
+    const float4* c4 = reinterpret_cast<const float4*>(cs + (int64_t)pos * kD + j * kPer);
+    const float4* s4 = reinterpret_cast<const float4*>(cs + (int64_t)pos * kD + kD / 2 + j * kPer);
+#pragma unroll
+    for (int v = 0; v < kPer / 4; ++v) {
+      const float4 a = __ldg(c4 + v), b = __ldg(s4 + v);
+      c[4 * v] = a.x; c[4 * v + 1] = a.y; c[4 * v + 2] = a.z; c[4 * v + 3] = a.w;
+      sn[4 * v] = b.x; sn[4 * v + 1] = b.y; sn[4 * v + 2] = b.z; sn[4 * v + 3] = b.w;
+    }
+  }
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const uint32_t lo[4] = {q[ch].x, q[ch].y, q[ch].z, q[ch].w};
+    const uint32_t hi[4] = {q[ch + 8].x, q[ch + 8].y, q[ch + 8].z, q[ch + 8].w};
+    uint32_t olo[4], ohi[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int k0 = 8 * ch + 2 * w, k1 = k0 + 1;
+      const float c0 = __shfl_sync(0xffffffffu, c[k0 % kPer], base + k0 / kPer);
+      const float s0 = __shfl_sync(0xffffffffu, sn[k0 % kPer], base + k0 / kPer);
+      const float c1 = __shfl_sync(0xffffffffu, c[k1 % kPer], base + k1 / kPer);
+      const float s1 = __shfl_sync(0xffffffffu, sn[k1 % kPer], base + k1 / kPer);
+      float y1a, y2a, y1b, y2b;
+      rope_pair(__uint_as_float(lo[w] << 16), __uint_as_float(hi[w] << 16), c0, s0, y1a, y2a);
+      rope_pair(__uint_as_float(lo[w] & 0xffff0000u), __uint_as_float(hi[w] & 0xffff0000u), c1, s1, y1b, y2b);
+      olo[w] = pack_bf16(y1a, y1b);
+      ohi[w] = pack_bf16(y2a, y2b);
+    }
+    if (inb) {
+      q[ch] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+      q[ch + 8] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+    }
+  }
+}
+
+// The G of the launch (4, 8 or 16: the fused path needs whole power-of-two
+// lane groups of at least four).
+__device__ __forceinline__ void rope_row(uint4 (&q)[16], const AttnParams& p, int pos, int32_t* status, int lane) {
+  switch (p.G) {
+    case 4: rope_row_group<4>(q, p.rope_cs, pos, p.rope_max_pos, status, lane); break;
+    case 8: rope_row_group<8>(q, p.rope_cs, pos, p.rope_max_pos, status, lane); break;
+    default: rope_row_group<16>(q, p.rope_cs, pos, p.rope_max_pos, status, lane); break;
+  }
 }
 
 // ---------------------------------------------------------------- work walk
@@ -902,7 +973,7 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePla
 
 // ---------------------------------------------------------------- the kernel
 
-template <int M>
+template <int M, bool kRope>
 __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
     attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
   using C = Cfg<M>;
@@ -1034,7 +1105,27 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       const uint64_t mrow = valid_row ? p.mask[(int64_t)s.b * p.mask_bstride + node] : 1ull;
       // this row of Q into TMEM (the previous unit's MMAs are complete: its
       // epilogue waited for the last O update)
-      {
+      if constexpr (kRope) {
+        // the whole row, rotated at the node's position, then into TMEM
+        const uint4* src = reinterpret_cast<const uint4*>(q + orow * kD);
+        uint4 qr[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) qr[c] = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        rope_row(qr, p, valid_row ? row_pos(mrow, s.L) : -1, status, lane);
+#pragma unroll
+        for (int c = 0; c < kD / 64; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = qr[c * 8 + j];
+            r[4 * j] = v.x; r[4 * j + 1] = v.y; r[4 * j + 2] = v.z; r[4 * j + 3] = v.w;
+          }
+          tmem_st32(tQ + c * 32, r);
+        }
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&bars.q_full);
+      } else {
         const uint4* src = reinterpret_cast<const uint4*>(q + orow * kD);
 #pragma unroll
         for (int c = 0; c < kD / 64; ++c) {
@@ -1177,6 +1268,7 @@ struct PairCfg {
   static constexpr int kSoftmaxWarp0 = 8;
 };
 
+template <bool kRope>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
   using C = PairCfg;
@@ -1339,6 +1431,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       mrow_next = r.valid ? __ldg(reinterpret_cast<const unsigned long long*>(p.mask) +
                                   (int64_t)sg.b * p.mask_bstride + r.node)
                           : 1ull;
+      if constexpr (kRope) rope_row(qreg, p, r.valid ? row_pos(mrow_next, sg.L) : -1, status, lane);
     };
     // Q row into its operand slot: M tile 0 into TMEM, M tile 1 into the
     // swizzled shared tile; then tell the S issuers.
@@ -1524,19 +1617,32 @@ int encode(EncodeTiled fn, CUtensorMap* map, const void* ptr, int rank, const cu
   return TV_OK;
 }
 
-template <int M>
+template <int M, bool kRope>
 int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
   using C = Cfg<M>;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_tc_kernel<M, kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_kernel)");
-  attn_tc_kernel<M><<<p.P, C::kThreads, C::kSmem, stream>>>(p, maps, status);
+  attn_tc_kernel<M, kRope><<<p.P, C::kThreads, C::kSmem, stream>>>(p, maps, status);
   TV_LAUNCH_CHECK("attn_tc_kernel");
+  return TV_OK;
+}
+
+template <bool kRope>
+int launch_pair(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_tc_pair_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
+  attn_tc_pair_kernel<kRope><<<p.P, PairCfg::kThreads, PairCfg::kSmem, stream>>>(p, maps, status);
+  TV_LAUNCH_CHECK("attn_tc_pair_kernel");
   return TV_OK;
 }
 
 }  // namespace
 
-const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size) {
+const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size,
+                                  bool rope) {
+  if (rope && G != 4 && G != 8 && G != 16) return "Q rotated while loading needs Hq/Hkv in {4, 8, 16}";
   if (dev.cc_major != 10) return "device is not sm_10x";
   if (dtype != TV_BF16) return "dtype is not bf16";
   if (head_dim != kD) return "head_dim is not 128";
@@ -1548,8 +1654,8 @@ const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim
   return nullptr;
 }
 
-bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size) {
-  return tc_unsupported_reason(dev, dtype, head_dim, rows, G, block_size) == nullptr;
+bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size, bool rope) {
+  return tc_unsupported_reason(dev, dtype, head_dim, rows, G, block_size, rope) == nullptr;
 }
 
 int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
@@ -1603,12 +1709,9 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
     if ((st = encode(fn, &maps.kt, p.k_tree, 4, dims, strides, box, "k_tree"))) return st;
     if ((st = encode(fn, &maps.vt, p.v_tree, 4, dims, strides, box, "v_tree"))) return st;
   }
-  if (p.RPG <= 128) return launch_m<1>(p, maps, status, stream);
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
-  attn_tc_pair_kernel<<<p.P, PairCfg::kThreads, PairCfg::kSmem, stream>>>(p, maps, status);
-  TV_LAUNCH_CHECK("attn_tc_pair_kernel");
-  return TV_OK;
+  if (p.RPG <= 128)
+    return p.rope_cs ? launch_m<1, true>(p, maps, status, stream) : launch_m<1, false>(p, maps, status, stream);
+  return p.rope_cs ? launch_pair<true>(p, maps, status, stream) : launch_pair<false>(p, maps, status, stream);
 }
 
 }  // namespace tv

@@ -11,11 +11,13 @@ constexpr int kTcMaxRows = 256;  // two 128-row M tiles per CTA (more rows: row 
 
 // True when the tensor-core kernel can run this shape on this device:
 // bf16, head_dim 128, rows = G * N <= 512, G divides 128, block_size a
-// multiple of 16 that divides 64 or is a multiple of 64.
-bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size);
+// multiple of 16 that divides 64 or is a multiple of 64; with rope (Q rotated
+// as it is loaded) also G in {4, 8, 16}.
+bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size, bool rope);
 
 // Why the shape is rejected (nullptr when it is supported).
-const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size);
+const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size,
+                                  bool rope);
 
 // Rows per unit for `rows` = G * N query rows per KV head (128 or 256).
 int tc_rows_per_unit(int rows);

@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "common.h"
+#include "rope_math.cuh"
 
 namespace {
 
@@ -33,42 +34,6 @@ __global__ void rope_table_kernel(float* __restrict__ cs, int max_pos, int D, do
     cs[(int64_t)p * D + half + k] = (float)s;
   }
 }
-
-template <typename T>
-struct Vec8;  // eight consecutive elements, one 16- or 32-byte access
-
-template <>
-struct Vec8<__nv_bfloat16> {
-  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
-    uint4 raw = *reinterpret_cast<const uint4*>(p);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 f = __bfloat1622float2(h[i]);
-      v[2 * i] = f.x;
-      v[2 * i + 1] = f.y;
-    }
-  }
-  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[8]) {
-    uint4 raw;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-    *reinterpret_cast<uint4*>(p) = raw;
-  }
-};
-
-template <>
-struct Vec8<float> {
-  static __device__ __forceinline__ void load(const float* p, float (&v)[8]) {
-    float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-  static __device__ __forceinline__ void store(float* p, const float (&v)[8]) {
-    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-  }
-};
 
 // One thread rotates 8 pairs (elements k..k+7 and k+D/2..k+D/2+7) of one row.
 // Rows are enumerated as (b, i, head) with the Hq query heads first, then the
@@ -102,10 +67,7 @@ __global__ void __launch_bounds__(256) rope_apply_kernel(T* __restrict__ q, T* _
     Vec8<float>::load(sinr, si);
     float y1[8], y2[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      y1[e] = x1[e] * co[e] - x2[e] * si[e];
-      y2[e] = x2[e] * co[e] + x1[e] * si[e];
-    }
+    for (int e = 0; e < 8; ++e) rope_pair(x1[e], x2[e], co[e], si[e], y1[e], y2[e]);
     Vec8<T>::store(row + c * 8, y1);
     Vec8<T>::store(row + half + c * 8, y2);
   }

@@ -14,21 +14,23 @@
 // n_nodes, request b holds nodes 0 .. n_b - 1 of the bucket's N; the others
 // are absent -- mask row 0, depth 0, position -1 -- and their parents are not
 // read.
+#include <algorithm>
+
 #include "common.h"
+#include "rope_math.cuh"
 
 namespace {
 
-__global__ void tree_mask_kernel(const int32_t* __restrict__ parent, int64_t pstride,
-                                 const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ n_nodes,
-                                 int B, int N, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
-                                 int32_t* __restrict__ pos, int32_t* __restrict__ status) {
-  const int warps_per_block = blockDim.x / 32;
-  const int b = blockIdx.x * warps_per_block + threadIdx.x / 32;
+// Rows, depths and positions of request b, computed by one warp (lane l owns
+// nodes l and l + 32) and written to mask/depth/pos at row b; positions also
+// to s_pos when given.  Returns false (rows zeroed, status flagged) for a
+// request whose first n parents are not a parent-before-child tree.
+__device__ void request_rows(const int32_t* __restrict__ parent, int64_t pstride,
+                             const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ n_nodes, int b,
+                             int N, int32_t* sp, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
+                             int32_t* __restrict__ pos, int32_t* s_pos, int32_t* __restrict__ status) {
   const int lane = threadIdx.x % 32;
-  if (b >= B) return;
   const int32_t* par = parent + (int64_t)b * pstride;
-  __shared__ int32_t s_par[8][TV_MAX_NODES];
-  int32_t* sp = s_par[threadIdx.x / 32];
   int n = N;
   if (n_nodes) n = min(max(n_nodes[b], 1), N);
 
@@ -48,9 +50,12 @@ __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, int64_t pst
     int32_t d = 0;
     const int64_t o = (int64_t)b * N + i;
     if (i >= n) {  // absent node
-      mask[o] = 0;
-      depth[o] = 0;
-      pos[o] = -1;
+      if (mask) {
+        mask[o] = 0;
+        depth[o] = 0;
+        pos[o] = -1;
+      }
+      if (s_pos) s_pos[i] = -1;
       continue;
     }
     if (ok) {
@@ -62,12 +67,82 @@ __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, int64_t pst
         ++d;
       }
     }
-    mask[o] = row;
-    depth[o] = ok ? d : 0;
-    pos[o] = ok ? L + d : 0;
+    if (mask) {
+      mask[o] = row;
+      depth[o] = ok ? d : 0;
+      pos[o] = ok ? L + d : 0;
+    }
+    if (s_pos) s_pos[i] = ok ? L + d : -1;
   }
-  if (!ok && lane == 0 && status)
+  if (!ok && lane == 0 && status && mask)
     atomicOr(status, (topo_ok ? 0 : TV_DEV_BAD_TOPOLOGY) | (L < 0 ? TV_DEV_BAD_POSITION : 0));
+}
+
+__global__ void tree_mask_kernel(const int32_t* __restrict__ parent, int64_t pstride,
+                                 const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ n_nodes,
+                                 int B, int N, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
+                                 int32_t* __restrict__ pos, int32_t* __restrict__ status) {
+  const int warps_per_block = blockDim.x / 32;
+  const int b = blockIdx.x * warps_per_block + threadIdx.x / 32;
+  if (b >= B) return;
+  __shared__ int32_t s_par[8][TV_MAX_NODES];
+  request_rows(parent, pstride, seq_lens, n_nodes, b, N, s_par[threadIdx.x / 32], mask, depth, pos, nullptr,
+               status);
+}
+
+// The mask kernel and the rotation of the tree keys in one launch: CTA
+// (b, y) rebuilds request b's positions in shared memory (CTA (b, 0) also
+// writes mask, depth and pos) and rotates its share of request b's tree-key
+// rows in place at those positions, with the arithmetic of tv_rope_apply.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) tree_prepare_kernel(
+    const int32_t* __restrict__ parent, int64_t pstride, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ n_nodes, int N, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
+    int32_t* __restrict__ pos, T* __restrict__ kt, int Hkv, const float* __restrict__ cs, int max_pos,
+    int32_t* __restrict__ status) {
+  constexpr int half = D / 2;
+  constexpr int chunks = half / 8;
+  __shared__ int32_t s_par[TV_MAX_NODES], s_pos[TV_MAX_NODES];
+  const int b = blockIdx.x;
+  if (threadIdx.x < 32)
+    request_rows(parent, pstride, seq_lens, n_nodes, b, N, s_par, blockIdx.y == 0 ? mask : nullptr, depth, pos,
+                 s_pos, status);
+  __syncthreads();
+  if (!kt) return;
+  const int items = N * Hkv * chunks;
+  for (int t = blockIdx.y * blockDim.x + threadIdx.x; t < items; t += gridDim.y * blockDim.x) {
+    const int c = t % chunks;
+    const int r = t / chunks;  // (node, head) row of request b
+    const int i = r / Hkv;
+    const int32_t p = s_pos[i];
+    if (p < 0 || p >= max_pos) {  // -1: an absent node (or a bad tree), left as it is
+      if (status && c == 0 && p != -1) atomicOr(status, TV_DEV_BAD_POSITION);
+      continue;
+    }
+    T* row = kt + ((int64_t)b * N * Hkv + r) * D;
+    const float* cosr = cs + (int64_t)p * D + c * 8;
+    float x1[8], x2[8], co[8], si[8], y1[8], y2[8];
+    Vec8<T>::load(row + c * 8, x1);
+    Vec8<T>::load(row + half + c * 8, x2);
+    Vec8<float>::load(cosr, co);
+    Vec8<float>::load(cosr + half, si);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rope_pair(x1[e], x2[e], co[e], si[e], y1[e], y2[e]);
+    Vec8<T>::store(row + c * 8, y1);
+    Vec8<T>::store(row + half + c * 8, y2);
+  }
+}
+
+template <typename T, int D>
+int launch_prepare(const int32_t* parent, int64_t pstride, const int32_t* seq_lens, const int32_t* n_nodes, int B,
+                   int N, uint64_t* mask, int32_t* depth, int32_t* pos, void* kt, int Hkv, const float* cs,
+                   int max_pos, int32_t* status, cudaStream_t stream) {
+  const int items = N * Hkv * (D / 16);
+  const int ys = kt ? (int)std::min<int64_t>(tv::ceil_div(items, 256 * 4), 16) : 1;
+  tree_prepare_kernel<T, D><<<dim3(B, ys), 256, 0, stream>>>(parent, pstride, seq_lens, n_nodes, N, mask, depth,
+                                                              pos, static_cast<T*>(kt), Hkv, cs, max_pos, status);
+  TV_LAUNCH_CHECK("tree_prepare_kernel");
+  return TV_OK;
 }
 
 }  // namespace
@@ -88,4 +163,34 @@ extern "C" int tv_tree_mask(const int32_t* parent, int64_t parent_bstride, const
                                                                  mask, depth, pos, status);
   TV_LAUNCH_CHECK("tree_mask_kernel");
   return TV_OK;
+}
+
+extern "C" int tv_tree_prepare(const int32_t* parent, int64_t parent_bstride, const int32_t* seq_lens,
+                               const int32_t* n_nodes, int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
+                               int32_t* pos, void* k_tree, int32_t Hkv, int32_t head_dim, int32_t dtype,
+                               const float* cos_sin, int32_t max_pos, int32_t* status, void* stream) {
+  tv::clear_error();
+  if (B < 0 || N < 1 || N > TV_MAX_NODES || parent_bstride < 0 || max_pos < 0)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_prepare: bad sizes B=%d N=%d stride=%lld max_pos=%d", B, N,
+                    (long long)parent_bstride, max_pos);
+  if (k_tree && (Hkv < 1 || !cos_sin || (dtype != TV_F32 && dtype != TV_BF16)))
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_prepare: tree keys need Hkv >= 1, a table and dtype f32/bf16");
+  if (k_tree && (int64_t)B * N * Hkv * head_dim >= (int64_t(1) << 40))
+    return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_prepare: tree keys too large");
+  if (B == 0) return TV_OK;
+  if (!parent || !seq_lens || !mask || !depth || !pos)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_prepare: null pointer");
+  cudaStream_t s = (cudaStream_t)stream;
+#define TV_PREP(T, D) return launch_prepare<T, D>(parent, parent_bstride, seq_lens, n_nodes, B, N, mask, depth, pos, \
+                                                  k_tree, Hkv, cos_sin, max_pos, status, s)
+  if (!k_tree) TV_PREP(float, 128);
+  switch (head_dim) {
+    case 16: if (dtype == TV_BF16) TV_PREP(__nv_bfloat16, 16); TV_PREP(float, 16);
+    case 32: if (dtype == TV_BF16) TV_PREP(__nv_bfloat16, 32); TV_PREP(float, 32);
+    case 64: if (dtype == TV_BF16) TV_PREP(__nv_bfloat16, 64); TV_PREP(float, 64);
+    case 128: if (dtype == TV_BF16) TV_PREP(__nv_bfloat16, 128); TV_PREP(float, 128);
+    case 256: if (dtype == TV_BF16) TV_PREP(__nv_bfloat16, 256); TV_PREP(float, 256);
+    default: return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_prepare: head_dim %d not in {16, 32, 64, 128, 256}", head_dim);
+  }
+#undef TV_PREP
 }
