@@ -51,7 +51,7 @@ from speculative_decoding_tree_attn_gb300 import workloads as W  # noqa: E402
 DEFAULT_WORKLOAD = "b64_l1k_8k_n64_greedy"
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS = 6800.0
-ATTN_SOURCES = ["attn.cu", "attn_tc.cu", "attn_common.cuh", "attn_tc.h"]
+ATTN_SOURCES = ["attn.cu", "attn_tc.cu", "attn_common.cuh", "attn_tc.h", "rope_math.cuh"]
 
 
 def parse_args():
