@@ -52,6 +52,8 @@ extern "C" {
 #define TV_DEV_OUT_OVERFLOW 4   /* walk longer than out_cols: truncated       */
 #define TV_DEV_BAD_POSITION 8   /* prefix length < 0 or position >= max_pos   */
 #define TV_DEV_TIMEOUT 16       /* a pipeline wait in a kernel exceeded 2 s     */
+#define TV_DEV_BAD_BLOCK 32     /* a block-table entry a prefix position uses is outside
+                                   [0, num_blocks): those keys and values read as zeros */
 
 /* ---- element types ------------------------------------------------------ */
 #define TV_F32 0
@@ -222,7 +224,9 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  *            t % block_size.  Slots >= L_b of a used block must hold finite
  *            values (they are read and weighted by exactly zero).
  * block_table device int32 [B, max_blocks]; entries >= ceil(L_b/block_size)
- *            are never read.
+ *            are never read; an entry that is read but lies outside
+ *            [0, num_blocks) reads as zero keys and values and sets
+ *            TV_DEV_BAD_BLOCK.
  * seq_lens   device int32 [B], 0 <= L_b <= max_blocks * block_size.
  * k_tree,    device [B, N, Hkv, D] (dtype): node K/V (node 0 = root).
  * v_tree

@@ -25,6 +25,7 @@ TV_ATTN_PUBLISH_ALL = 4
 TV_ATTN_ROPE_Q = 8
 TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA, TV_SAMPLE_STREAM = 0, 1, 2, 3
 TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
+TV_DEV_BAD_BLOCK = 32
 STATUS_NAMES = {0: "TV_OK", -1: "TV_ERR_INVALID_ARG", -2: "TV_ERR_MISSING_PARENT", -3: "TV_ERR_TOO_MANY_NODES",
                 -4: "TV_ERR_UNSUPPORTED", -5: "TV_ERR_WORKSPACE", -6: "TV_ERR_CUDA"}
 

@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(AttnParams p
               const int64_t o = ((blk * p.Hkv + kvh) * p.block_size + t % p.block_size) * D + d;
               kv = to_f32(kc[o]);
               vv = to_f32(vc[o]);
+            } else if (d == 0 && p.status) {
+              atomicOr(p.status, TV_DEV_BAD_BLOCK);
             }
           }
         }

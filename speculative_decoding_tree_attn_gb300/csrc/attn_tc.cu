@@ -939,7 +939,10 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePla
                    &bars.kv_full[stage]);
         } else if (j < 4 * nsub) {
           int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
-          if (blk < 0 || blk >= p.num_blocks) y = rows_total;  // out of range: TMA fills zeros
+          if (blk < 0 || blk >= p.num_blocks) {  // out of range: TMA fills zeros
+            y = rows_total;
+            if (status) atomicOr(status, TV_DEV_BAD_BLOCK);
+          }
           tma_2d_stream((is_v ? dv : dk) + h * kKVHalfBytes + sub * br * 128, is_v ? &maps.vc : &maps.kc, h * 64,
                         (int)y, &bars.kv_full[stage], pol);
         }

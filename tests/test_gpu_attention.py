@@ -110,6 +110,42 @@ def test_row_groups_and_gqa_widths(G, N):
             _check_all(inp, paths, BF16_TOL, flags, num_ctas)
 
 
+@pytest.mark.parametrize("flags", KERNELS)
+def test_bad_block_table_entries_read_as_zeros(flags):
+    """Block-table entries outside [0, num_blocks) (one past the end, one
+    negative) are never dereferenced: those positions read as zero keys and
+    values, and TV_DEV_BAD_BLOCK is set.  Checked against the oracle run on
+    the same table with the bad entries pointing at an all-zero block."""
+    paths = W.PAGE_TREE_PATHS
+    w = _workload(3, 8, 2, 128, "bf16", 16, 10, 151)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[40, 100, 70])
+    nb = inp["k_cache"].shape[0]
+    bad = inp["block_table"].clone()
+    bad[0, 1] = nb + 3
+    bad[1, 0] = -1
+    bad[2, 4] = nb
+    inp_bad = dict(inp, block_table=bad)
+    parent, *_ = capi.tv_tree_build(paths)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mask, _, pos = capi.tv_tree_mask(torch.from_numpy(parent).cuda(), inp["seq_lens"], status=status)
+    table = capi.tv_rope_table(200, 128, device="cuda")
+    q, kt = inp["q"].clone(), inp["k_tree"].clone()
+    capi.tv_rope_apply(q, kt, pos, table, status=status)
+    out = capi.tv_tree_attn_verify(q, inp["k_cache"], inp["v_cache"], bad, inp["seq_lens"], kt, inp["v_tree"], mask,
+                                   flags=flags, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == capi.TV_DEV_BAD_BLOCK
+    # the oracle's view: one zero block appended, the bad entries pointing at it
+    zero = torch.zeros_like(inp["k_cache"][:1])
+    fixed = bad.clone()
+    fixed[(fixed < 0) | (fixed >= nb)] = nb
+    inp_ref = dict(inp, k_cache=torch.cat([inp["k_cache"], zero]), v_cache=torch.cat([inp["v_cache"], zero]),
+                   block_table=fixed)
+    pairs = [(b, i) for b in range(3) for i in range(10)]
+    ref = oracle_rows(inp_ref, paths, pairs)
+    assert max_err(out, ref, pairs) <= BF16_TOL
+
+
 @pytest.mark.parametrize("bs", [1, 8, 32, 48, 128, 256])
 def test_cache_block_sizes(bs):
     """Paged caches with other block sizes: the tcgen05 kernel takes multiples
