@@ -223,3 +223,45 @@ def test_gpu_sample_processed_target_lossless(verifier_facts):
     seqs = generate(_gpu_verify, pp, qp, parent, 100_000, n_tok, 132)
     stat, df, outside = chi_square_support(seqs, pp)
     assert outside == 0 and stat < scipy_stats.chi2.ppf(0.999, df)
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_sample_edge_shapes(kernel):
+    """A one-token vocabulary (every draw is token 0), a root-only tree (the
+    bonus draw only) and a large batch (2048 requests), on every kernel."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    rng = np.random.default_rng(140)
+    cases = []
+    B, N = 5, 4
+    cases.append((np.ones((B, N, 1), np.float32), np.ones((B, N, 1), np.float32), np.zeros((B, N), np.int32),
+                  np.arange(-1, N - 1, dtype=np.int32)))
+    B, N, V = 7, 1, 300
+    p = rng.dirichlet(np.ones(V), size=(B, N)).astype(np.float32)
+    cases.append((p, p.copy(), np.zeros((B, N), np.int32), np.array([-1], np.int32)))
+    B, N, V = 2048, 4, 1000
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, N)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, size=(B, N)).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    cases.append((p, q, tok, np.array([-1, 0, 0, 1], np.int32)))
+    for p, q, tok, par in cases:
+        B, N, V = p.shape
+        n_nodes = rng.integers(1, N + 1, size=B).astype(np.int32)
+        ua = rng.random((B, N), dtype=np.float32)
+        uf = rng.random(B, dtype=np.float32)
+        res = capi.tv_tree_accept_sample(t(p), t(q), t(tok), t(par), t(ua), t(uf), n_nodes=t(n_nodes),
+                                         flags=KERNELS[kernel])
+        _cmp(res, *OA.tree_accept_sample(p, q, tok, par, n_nodes, ua, uf))
+        if V == 1:
+            assert (res[0].cpu().numpy()[:, 0] == 0).all()
+
+
+def test_greedy_edge_shapes():
+    """Root-only trees, a one-token vocabulary and a large batch."""
+    rng = np.random.default_rng(141)
+    for B, N, V in ((9, 1, 500), (6, 5, 1), (4096, 3, 64)):
+        parent = np.arange(-1, N - 1, dtype=np.int32)
+        tokens = rng.integers(0, V, size=(B, N)).astype(np.int32)
+        logits = rng.standard_normal((B, N, V)).astype(np.float32)
+        par = torch.from_numpy(parent).cuda()
+        res = capi.tv_tree_accept_greedy(torch.from_numpy(tokens).cuda(), par, logits=torch.from_numpy(logits).cuda())
+        _cmp(res, *OA.tree_accept_greedy(OA.argmax_rows(logits), tokens, parent))
