@@ -363,6 +363,41 @@ def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=No
     return out, n_out, path
 
 
+def verify_chain(draft, q, p, num_draft, u, u_final, *, flags=0, status=None, stream=None):
+    """The verifier page's chain interface on top of tv_tree_accept_sample.
+
+    draft int32 [B, K] (draft j drawn from q[:, j]); q float32 [B, K, V]; p
+    float32 [B, K + 1, V] (the target after each prefix, the last row for the
+    bonus); num_draft int32 [B] (ragged); u float32 [B, K] (one uniform per
+    test); u_final float32 [B].  Returns (out int32 [B, K + 1] -1 padded,
+    n_out int32 [B] = accepted + 1).  Only marshalling: the chain is a tree
+    whose node j + 1 is draft j (node 0 the last accepted token), node j's q
+    row is q[:, j] (a zero row for the last node, which has no children)."""
+    B, K = draft.shape
+    V = p.shape[-1]
+    dev = p.device
+    tokens = torch.zeros(B, K + 1, dtype=torch.int32, device=dev)
+    tokens[:, 1:] = draft.to(torch.int32)
+    q_nodes = torch.zeros(B, K + 1, V, dtype=torch.float32, device=dev)
+    q_nodes[:, :K] = q
+    u_nodes = torch.zeros(B, K + 1, dtype=torch.float32, device=dev)
+    u_nodes[:, 1:] = u
+    parent = torch.arange(-1, K, dtype=torch.int32, device=dev)
+    n_nodes = (num_draft.to(torch.int32) + 1).contiguous()
+    out, n_out, _ = tv_tree_accept_sample(p.contiguous(), q_nodes, tokens, parent, u_nodes, u_final.contiguous(),
+                                          n_nodes=n_nodes, flags=flags, status=status, stream=stream)
+    return out, n_out
+
+
+def accept_greedy(parent, tokens, target_argmax, *, n_nodes=None, status=None, stream=None):
+    """The mask page's accept_greedy(parent, tokens, target_argmax) on top of
+    tv_tree_accept_greedy: parent int32 [N] or [B, N], tokens int32 [B, N],
+    target_argmax int32 [B, N] (the target's choice after each node).  Returns
+    (out, n_out, path) like tv_tree_accept_greedy."""
+    return tv_tree_accept_greedy(tokens, parent, target_argmax=target_argmax, n_nodes=n_nodes, status=status,
+                                 stream=stream)
+
+
 def tv_kv_commit(k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, path, n_out, *, new_seq_lens=None,
                  status=None, stream=None):
     """Copy the accepted path's tree K/V rows into the paged cache (in place);

@@ -265,3 +265,28 @@ def test_greedy_edge_shapes():
         par = torch.from_numpy(parent).cuda()
         res = capi.tv_tree_accept_greedy(torch.from_numpy(tokens).cuda(), par, logits=torch.from_numpy(logits).cuda())
         _cmp(res, *OA.tree_accept_greedy(OA.argmax_rows(logits), tokens, parent))
+
+
+def test_page_interfaces():
+    """The pages' own call shapes: the chain verifier verify(draft, q, p,
+    num_draft, u, u_final) and accept_greedy(parent, tokens, target_argmax),
+    against the oracle."""
+    rng = np.random.default_rng(142)
+    B, K, V = 300, 5, 700
+    p = rng.dirichlet(np.ones(V) * 0.4, size=(B, K + 1)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.4, size=(B, K)).astype(np.float32)
+    q[:30] = p[:30, :K]
+    draft = np.stack([[rng.choice(V, p=q[b, j] / q[b, j].sum()) for j in range(K)] for b in range(B)]).astype(np.int32)
+    nd = rng.integers(0, K + 1, size=B).astype(np.int32)
+    u = rng.random((B, K), dtype=np.float32)
+    uf = rng.random(B, dtype=np.float32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out, n_out = capi.verify_chain(t(draft), t(q), t(p), t(nd), t(u), t(uf))
+    r_out, r_n = OA.verify_chain(draft, q, p, nd, u, uf)
+    np.testing.assert_array_equal(n_out.cpu().numpy(), r_n)
+    np.testing.assert_array_equal(out.cpu().numpy(), r_out)
+    parent, *_ = OT.build_tree(W.PAGE_TREE_PATHS)
+    tokens = rng.integers(0, 4, size=(B, parent.size)).astype(np.int32)
+    am = rng.integers(0, 4, size=(B, parent.size)).astype(np.int32)
+    res = capi.accept_greedy(t(parent.astype(np.int32)), t(tokens), t(am))
+    _cmp(res, *OA.tree_accept_greedy(am, tokens, parent))
