@@ -1,6 +1,7 @@
 // Tree attention: the plan and combine kernels, the CUDA-core (FP32 FFMA)
-// kernel, and the tv_tree_attn_verify entry point that dispatches between the
-// CUDA-core kernel and the tcgen05 kernel of attn_tc.cu.
+// kernel, and the tv_tree_attn_verify / tv_tree_attn_verify_rope entry points
+// that dispatch between the CUDA-core kernel and the tcgen05 kernel of
+// attn_tc.cu (the _rope variant rotates each query row as it is loaded).
 //
 // What is computed ("Tree Verification", "Tree Attention"; "Build the tree
 // attention mask that verifies a draft tree in one pass", "The mask."): each

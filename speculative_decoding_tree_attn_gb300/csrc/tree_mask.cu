@@ -1,4 +1,6 @@
-// tv_tree_mask: batched ancestor rows, depths and position ids on the device.
+// tv_tree_mask: batched ancestor rows, depths and position ids on the device;
+// tv_tree_prepare: the same plus the rotation of the tree keys at those
+// positions, in one launch.
 //
 // "Build the tree attention mask that verifies a draft tree in one pass",
 // "The mask.": node i sees itself and its ancestors; its position id is the
