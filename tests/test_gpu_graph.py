@@ -70,3 +70,29 @@ def test_graph_replay_matches_direct_calls(name):
             k = int(st["n"][b].item())
             assert torch.equal(got["acc"][b, :k], st["acc"][b, :k])
             assert torch.equal(got["path"][b, :k], st["path"][b, :k])
+
+
+def test_sampler_captured_on_first_call():
+    """The stochastic walk's first call for a shape (its kernel choice queries
+    the device's cluster capacity) may itself be inside a CUDA-graph capture;
+    the replay equals a direct call."""
+    import numpy as np
+    rng = np.random.default_rng(160)
+    B, N, V = 37, 6, 777  # a vocabulary no other test uses: nothing cached for it yet
+    parent = torch.tensor([-1, 0, 0, 1, 1, 2], dtype=torch.int32, device="cuda")
+    p = torch.from_numpy(rng.dirichlet(np.ones(V), size=(B, N)).astype(np.float32)).cuda()
+    q = torch.from_numpy(rng.dirichlet(np.ones(V), size=(B, N)).astype(np.float32)).cuda()
+    tok = torch.from_numpy(rng.integers(0, V, size=(B, N)).astype(np.int32)).cuda()
+    ua = torch.from_numpy(rng.random((B, N), dtype=np.float32)).cuda()
+    uf = torch.from_numpy(rng.random(B, dtype=np.float32)).cuda()
+    out = torch.empty(B, N, dtype=torch.int32, device="cuda")
+    n_out = torch.empty(B, dtype=torch.int32, device="cuda")
+    path = torch.empty(B, N, dtype=torch.int32, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        capi.tv_tree_accept_sample(p, q, tok, parent, ua, uf, out=out, n_out=n_out, path=path)
+    graph.replay()
+    torch.cuda.synchronize()
+    ref = capi.tv_tree_accept_sample(p, q, tok, parent, ua, uf)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref[0]) and torch.equal(n_out, ref[1]) and torch.equal(path, ref[2])
