@@ -65,7 +65,7 @@ def parse_args():
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--rope", default="auto", choices=["auto", "fused", "separate"],
                     help="fused: tree-key RoPE inside the mask kernel and Q RoPE inside the attention kernel's Q load; "
-                         "separate: tv_tree_mask + tv_rope_apply + tv_tree_attn_verify; auto: fused where it "
+                         "separate: tv_tree_prepare rotating Q and the tree keys, then tv_tree_attn_verify; auto: fused where it "
                          "measured faster (the one-M-tile kernel, G*N <= 128, with B*Hkv >= 2 x SMs), else separate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -335,8 +335,8 @@ class Step:
                 uses_tc = True
             except capi.TVError:
                 uses_tc = False
-        # mask (+ rope), the attention kernel(s), the acceptance kernel
-        self.launches = (1 if self.fused_rope else 2) + (1 if uses_tc else 3) + (1 if w.accept != "none" else 0)
+        # mask + rope, the attention kernel(s), the acceptance kernel
+        self.launches = 1 + (1 if uses_tc else 3) + (1 if w.accept != "none" else 0)
 
     def run_attn(self):
         i = self.inp
@@ -354,10 +354,9 @@ class Step:
         if self.fused_rope:  # mask + tree-key rotation in one kernel; Q is rotated inside the attention kernel
             c.tv_tree_prepare(self.parent, self.seq_lens, i["k_tree"], self.table, n_nodes=self.n_nodes,
                               mask=self.mask, depth=self.depth, pos=self.pos)
-        else:
-            c.tv_tree_mask(self.parent, self.seq_lens, mask=self.mask, depth=self.depth, pos=self.pos,
-                           n_nodes=self.n_nodes)
-            c.tv_rope_apply(i["q"], i["k_tree"], self.pos, self.table)
+        else:  # mask + rotation of the queries and tree keys in one kernel, before the attention kernel
+            c.tv_tree_prepare(self.parent, self.seq_lens, i["k_tree"], self.table, q=i["q"], n_nodes=self.n_nodes,
+                              mask=self.mask, depth=self.depth, pos=self.pos)
         if ev_attn:
             ev_attn[0].record()
         self.run_attn()

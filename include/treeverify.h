@@ -144,24 +144,27 @@ int tv_tree_mask(const int32_t* parent, int64_t parent_bstride, const int32_t* s
                  int32_t* pos, int32_t* status, void* stream);
 
 /*
- * tv_tree_prepare -- device, asynchronous.  tv_tree_mask and the rotation of
- * the tree keys in one launch: the same mask, depth and pos as tv_tree_mask,
- * and k_tree rotated in place at pos exactly as tv_rope_apply would (same
- * bits).  Used with tv_tree_attn_verify_rope, which rotates Q itself, the
- * step needs no separate RoPE kernel.
+ * tv_tree_prepare -- device, asynchronous.  tv_tree_mask and RoPE in one
+ * launch: the same mask, depth and pos as tv_tree_mask, and the queries
+ * and/or tree keys rotated in place at pos exactly as tv_rope_apply would
+ * (same bits).  With q = NULL only the tree keys are rotated (the step then
+ * uses tv_tree_attn_verify_rope, which rotates Q as it loads it); with both,
+ * it replaces tv_tree_mask + tv_rope_apply.
  *
  * parent, parent_bstride, seq_lens, n_nodes, mask, depth, pos: as in
  *           tv_tree_mask.
- * k_tree    device [B, N, Hkv, head_dim] (dtype), rotated in place (NULL: only
- *           the mask part).  head_dim in {16, 32, 64, 128, 256}.
+ * q         device [B, N, Hq, head_dim] (dtype), rotated in place (nullable).
+ * k_tree    device [B, N, Hkv, head_dim] (dtype), rotated in place
+ *           (nullable; both NULL: only the mask part).  head_dim in
+ *           {16, 32, 64, 128, 256}.
  * cos_sin   device float32 [max_pos, 2, head_dim/2] from tv_rope_table.
  * A position outside [0, max_pos) other than -1 leaves the row untouched and
  * sets TV_DEV_BAD_POSITION; -1 (absent node) leaves it silently.
  */
 int tv_tree_prepare(const int32_t* parent, int64_t parent_bstride, const int32_t* seq_lens,
                     const int32_t* n_nodes, int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
-                    int32_t* pos, void* k_tree, int32_t Hkv, int32_t head_dim, int32_t dtype,
-                    const float* cos_sin, int32_t max_pos, int32_t* status, void* stream);
+                    int32_t* pos, void* q, int32_t Hq, void* k_tree, int32_t Hkv, int32_t head_dim,
+                    int32_t dtype, const float* cos_sin, int32_t max_pos, int32_t* status, void* stream);
 
 /*
  * tv_rope_table -- device, asynchronous.  Fills the rotary table used by

@@ -47,8 +47,8 @@ SIGNATURES = {
     "tv_tree_attn_verify_rope": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _I64, _P, _I32,
                                                 _I32, _I32, _I32, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _I32, _I32,
                                                 _P, _P]),
-    "tv_tree_prepare": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _P, _I32,
-                                       _P, _P]),
+    "tv_tree_prepare": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                       _P, _I32, _P, _P]),
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
                                              _I32, _P, _P]),
@@ -252,10 +252,11 @@ def tv_tree_attn_verify_rope(q, k_cache, v_cache, block_table, seq_lens, k_tree,
     return out
 
 
-def tv_tree_prepare(parent, seq_lens, k_tree=None, cos_sin=None, *, n_nodes=None, status=None, mask=None,
+def tv_tree_prepare(parent, seq_lens, k_tree=None, cos_sin=None, *, q=None, n_nodes=None, status=None, mask=None,
                     depth=None, pos=None, stream=None):
-    """tv_tree_mask plus the rotation of k_tree [B, N, Hkv, D] in place at pos,
-    in one launch; returns (mask, depth, pos) like tv_tree_mask."""
+    """tv_tree_mask plus the rotation of k_tree [B, N, Hkv, D] and/or q
+    [B, N, Hq, D] in place at pos, in one launch; returns (mask, depth, pos)
+    like tv_tree_mask."""
     _dev(parent, "parent", (torch.int32,))
     _dev(seq_lens, "seq_lens", (torch.int32,))
     if n_nodes is not None:
@@ -267,15 +268,20 @@ def tv_tree_prepare(parent, seq_lens, k_tree=None, cos_sin=None, *, n_nodes=None
     mask = torch.empty(B, N, dtype=torch.int64, device=dev) if mask is None else mask
     depth = torch.empty(B, N, dtype=torch.int32, device=dev) if depth is None else depth
     pos = torch.empty(B, N, dtype=torch.int32, device=dev) if pos is None else pos
-    Hkv = D = dt = max_pos = 0
+    Hq = Hkv = D = dt = max_pos = 0
+    for t, nm in ((q, "q"), (k_tree, "k_tree")):
+        if t is not None:
+            _dev(t, nm, (torch.float32, torch.bfloat16))
+            _dev(cos_sin, "cos_sin", (torch.float32,))
+            D, dt, max_pos = t.shape[3], _code(t.dtype), cos_sin.shape[0]
+    if q is not None:
+        Hq = q.shape[2]
     if k_tree is not None:
-        _dev(k_tree, "k_tree", (torch.float32, torch.bfloat16))
-        _dev(cos_sin, "cos_sin", (torch.float32,))
-        Hkv, D, dt, max_pos = k_tree.shape[2], k_tree.shape[3], _code(k_tree.dtype), cos_sin.shape[0]
+        Hkv = k_tree.shape[2]
     _check("tv_tree_prepare",
            lib().tv_tree_prepare(_ptr(parent), bstride, _ptr(seq_lens), _ptr(n_nodes), B, N, _ptr(mask),
-                                 _ptr(depth), _ptr(pos), _ptr(k_tree), Hkv, D, dt, _ptr(cos_sin), max_pos,
-                                 _ptr(status), _stream(stream)))
+                                 _ptr(depth), _ptr(pos), _ptr(q), Hq, _ptr(k_tree), Hkv, D, dt, _ptr(cos_sin),
+                                 max_pos, _ptr(status), _stream(stream)))
     return mask, depth, pos
 
 

@@ -1,6 +1,6 @@
 // tv_tree_mask: batched ancestor rows, depths and position ids on the device;
-// tv_tree_prepare: the same plus the rotation of the tree keys at those
-// positions, in one launch.
+// tv_tree_prepare: the same plus the rotation of the queries and/or tree keys
+// at those positions, in one launch.
 //
 // "Build the tree attention mask that verifies a draft tree in one pass",
 // "The mask.": node i sees itself and its ancestors; its position id is the
@@ -92,16 +92,18 @@ __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, int64_t pst
                status);
 }
 
-// The mask kernel and the rotation of the tree keys in one launch: CTA
-// (b, y) rebuilds request b's positions in shared memory (CTA (b, 0) also
-// writes mask, depth and pos) and rotates its share of request b's tree-key
-// rows in place at those positions, with the arithmetic of tv_rope_apply.
+// The mask kernel and RoPE in one launch: CTA (b, y) rebuilds request b's
+// positions in shared memory (CTA (b, 0) also writes mask, depth and pos) and
+// rotates its share of request b's query rows (when q is given) and tree-key
+// rows (when k_tree is given) in place at those positions, with the
+// arithmetic of tv_rope_apply.  Rows run node by node, the Hq query heads of
+// a node first, then its Hkv tree-key heads.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) tree_prepare_kernel(
     const int32_t* __restrict__ parent, int64_t pstride, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ n_nodes, int N, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
-    int32_t* __restrict__ pos, T* __restrict__ kt, int Hkv, const float* __restrict__ cs, int max_pos,
-    int32_t* __restrict__ status) {
+    int32_t* __restrict__ pos, T* __restrict__ q, int Hq, T* __restrict__ kt, int Hkv, const float* __restrict__ cs,
+    int max_pos, int32_t* __restrict__ status) {
   constexpr int half = D / 2;
   constexpr int chunks = half / 8;
   __shared__ int32_t s_par[TV_MAX_NODES], s_pos[TV_MAX_NODES];
@@ -110,18 +112,18 @@ __global__ void __launch_bounds__(256) tree_prepare_kernel(
     request_rows(parent, pstride, seq_lens, n_nodes, b, N, s_par, blockIdx.y == 0 ? mask : nullptr, depth, pos,
                  s_pos, status);
   __syncthreads();
-  if (!kt) return;
-  const int items = N * Hkv * chunks;
+  const int hq = q ? Hq : 0, hk = kt ? Hkv : 0, heads = hq + hk;
+  const int items = N * heads * chunks;
   for (int t = blockIdx.y * blockDim.x + threadIdx.x; t < items; t += gridDim.y * blockDim.x) {
     const int c = t % chunks;
     const int r = t / chunks;  // (node, head) row of request b
-    const int i = r / Hkv;
+    const int i = r / heads, h = r - i * heads;
     const int32_t p = s_pos[i];
     if (p < 0 || p >= max_pos) {  // -1: an absent node (or a bad tree), left as it is
       if (status && c == 0 && p != -1) atomicOr(status, TV_DEV_BAD_POSITION);
       continue;
     }
-    T* row = kt + ((int64_t)b * N * Hkv + r) * D;
+    T* row = h < hq ? q + (((int64_t)b * N + i) * Hq + h) * D : kt + (((int64_t)b * N + i) * Hkv + (h - hq)) * D;
     const float* cosr = cs + (int64_t)p * D + c * 8;
     float x1[8], x2[8], co[8], si[8], y1[8], y2[8];
     Vec8<T>::load(row + c * 8, x1);
@@ -137,12 +139,14 @@ __global__ void __launch_bounds__(256) tree_prepare_kernel(
 
 template <typename T, int D>
 int launch_prepare(const int32_t* parent, int64_t pstride, const int32_t* seq_lens, const int32_t* n_nodes, int B,
-                   int N, uint64_t* mask, int32_t* depth, int32_t* pos, void* kt, int Hkv, const float* cs,
-                   int max_pos, int32_t* status, cudaStream_t stream) {
-  const int items = N * Hkv * (D / 16);
-  const int ys = kt ? (int)std::min<int64_t>(tv::ceil_div(items, 256 * 4), 16) : 1;
+                   int N, uint64_t* mask, int32_t* depth, int32_t* pos, void* q, int Hq, void* kt, int Hkv,
+                   const float* cs, int max_pos, int32_t* status, cudaStream_t stream) {
+  const int heads = (q ? Hq : 0) + (kt ? Hkv : 0);
+  const int items = N * heads * (D / 16);
+  const int ys = heads ? (int)std::min<int64_t>(tv::ceil_div(items, 256 * 4), 32) : 1;
   tree_prepare_kernel<T, D><<<dim3(B, ys), 256, 0, stream>>>(parent, pstride, seq_lens, n_nodes, N, mask, depth,
-                                                              pos, static_cast<T*>(kt), Hkv, cs, max_pos, status);
+                                                              pos, static_cast<T*>(q), Hq, static_cast<T*>(kt), Hkv,
+                                                              cs, max_pos, status);
   TV_LAUNCH_CHECK("tree_prepare_kernel");
   return TV_OK;
 }
@@ -169,23 +173,24 @@ extern "C" int tv_tree_mask(const int32_t* parent, int64_t parent_bstride, const
 
 extern "C" int tv_tree_prepare(const int32_t* parent, int64_t parent_bstride, const int32_t* seq_lens,
                                const int32_t* n_nodes, int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
-                               int32_t* pos, void* k_tree, int32_t Hkv, int32_t head_dim, int32_t dtype,
-                               const float* cos_sin, int32_t max_pos, int32_t* status, void* stream) {
+                               int32_t* pos, void* q, int32_t Hq, void* k_tree, int32_t Hkv, int32_t head_dim,
+                               int32_t dtype, const float* cos_sin, int32_t max_pos, int32_t* status, void* stream) {
   tv::clear_error();
   if (B < 0 || N < 1 || N > TV_MAX_NODES || parent_bstride < 0 || max_pos < 0)
     return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_prepare: bad sizes B=%d N=%d stride=%lld max_pos=%d", B, N,
                     (long long)parent_bstride, max_pos);
-  if (k_tree && (Hkv < 1 || !cos_sin || (dtype != TV_F32 && dtype != TV_BF16)))
-    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_prepare: tree keys need Hkv >= 1, a table and dtype f32/bf16");
-  if (k_tree && (int64_t)B * N * Hkv * head_dim >= (int64_t(1) << 40))
-    return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_prepare: tree keys too large");
+  const bool rot = q || k_tree;
+  if (rot && ((q && Hq < 1) || (k_tree && Hkv < 1) || !cos_sin || (dtype != TV_F32 && dtype != TV_BF16)))
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_prepare: rotation needs Hq/Hkv >= 1, a table and dtype f32/bf16");
+  if (rot && (int64_t)B * N * ((q ? Hq : 0) + (k_tree ? Hkv : 0)) * head_dim >= (int64_t(1) << 40))
+    return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_prepare: rows too large");
   if (B == 0) return TV_OK;
   if (!parent || !seq_lens || !mask || !depth || !pos)
     return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_prepare: null pointer");
   cudaStream_t s = (cudaStream_t)stream;
 #define TV_PREP(T, D) return launch_prepare<T, D>(parent, parent_bstride, seq_lens, n_nodes, B, N, mask, depth, pos, \
-                                                  k_tree, Hkv, cos_sin, max_pos, status, s)
-  if (!k_tree) TV_PREP(float, 128);
+                                                  q, Hq, k_tree, Hkv, cos_sin, max_pos, status, s)
+  if (!rot) TV_PREP(float, 128);
   switch (head_dim) {
     case 16: if (dtype == TV_BF16) TV_PREP(__nv_bfloat16, 16); TV_PREP(float, 16);
     case 32: if (dtype == TV_BF16) TV_PREP(__nv_bfloat16, 32); TV_PREP(float, 32);

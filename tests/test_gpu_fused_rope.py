@@ -1,7 +1,7 @@
 """RoPE fused into the attention kernels' Q load (tv_tree_attn_verify_rope)
-and into the mask kernel for the tree keys (tv_tree_prepare): both must give
-the same bits as the separate path tv_tree_mask -> tv_rope_apply ->
-tv_tree_attn_verify (one rotation formula, float32, bf16 rounding), on both
+and into the mask kernel (tv_tree_prepare, for the tree keys alone or for Q
+and the tree keys): each must give the same bits as the separate path
+tv_tree_mask -> tv_rope_apply -> tv_tree_attn_verify (one rotation formula, float32, bf16 rounding), on both
 attention kernels, for every GQA width the fused tensor-core path takes, with
 ragged trees, empty prefixes and positions past the table; and the fused path
 against the oracle at full size."""
@@ -120,3 +120,44 @@ def test_fused_full_size(name):
     pairs = [(bb, i) for bb in bs for i in (0, w.n_nodes // 2, w.n_nodes - 1)]
     ref = oracle_rows(inp, w.paths(), pairs)
     assert max_err(b, ref, pairs) <= BF16_TOL
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("ragged", [None, [5, 26, 13, 1]])
+def test_prepare_with_q_equals_mask_then_rope(dtype, ragged):
+    """tv_tree_prepare rotating Q and the tree keys is tv_tree_mask followed by
+    tv_rope_apply, bit for bit, including absent nodes (left untouched)."""
+    w, par, inp, nn = _case(32, 8, 26, [0, 3, 700, 1500], 417, dtype=dtype, ragged=ragged)
+    table = capi.tv_rope_table(1600, 128, device="cuda")
+    a = _separate(inp, par, table, nn, capi.TV_ATTN_AUTO)
+    q, kt = inp["q"].clone(), inp["k_tree"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m, d, p = capi.tv_tree_prepare(par, inp["seq_lens"], kt, table, q=q, n_nodes=nn, status=status)
+    sq = inp["q"].clone()
+    capi.tv_rope_apply(sq, None, a[2][2], table)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and int(a[4].item()) == 0
+    for x, y in zip((m, d, p), a[2]):
+        assert torch.equal(x, y)
+    assert torch.equal(kt, a[3]) and torch.equal(q, sq)
+    # Q alone
+    q2 = inp["q"].clone()
+    capi.tv_tree_prepare(par, inp["seq_lens"], None, table, q=q2, n_nodes=nn)
+    torch.cuda.synchronize()
+    assert torch.equal(q2, sq)
+
+
+def test_prepare_with_q_past_the_table_flags():
+    """A position past the table leaves those Q rows as they are and sets
+    TV_DEV_BAD_POSITION; rows inside the table are still rotated."""
+    w, par, inp, _ = _case(32, 8, 26, [0, 590], 418)
+    table = capi.tv_rope_table(593, 128, device="cuda")  # request 1's positions 590.. run past row 592
+    q = inp["q"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, _, pos = capi.tv_tree_prepare(par, inp["seq_lens"], None, table, q=q, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & capi.TV_DEV_BAD_POSITION
+    bad = (pos >= 593).cpu()
+    assert bad.any() and not bad.all()
+    assert torch.equal(q.cpu()[bad], inp["q"].cpu()[bad])
+    assert not torch.equal(q.cpu()[~bad], inp["q"].cpu()[~bad])
