@@ -746,7 +746,71 @@ __device__ __forceinline__ void staged_merge(const AttnParams& p, const Pieces& 
   if (active && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
 }
 
-template <bool kStage>
+// Direct merge of a split unit's row with exactly one other piece, at the
+// slice's last segment of the two-M-tile kernel: the other piece's row is
+// copied by cp.async into the idle K/V ring (16-byte chunk k of row r at
+// (k * 128 + (r & 127)) * 16, so a warp's 32 rows read 512 consecutive bytes)
+// while its log2-sum-exp loads, then combined with this CTA's O from TMEM in
+// piece order with the arithmetic of piece_stats / accum_pieces, so the row
+// matches the other merge routes bit for bit.  Warp-collective (TMEM reads);
+// `active` lanes merge their row.
+__device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pieces& pc, float lse2, float inv,
+                                                  int row, int rl, int64_t orow, uint32_t tO, uint8_t* stage,
+                                                  bool active) {
+  constexpr float kLn2 = 0.69314718055994530942f;
+  const bool self_first = (int)blockIdx.x == pc.c0;
+  const int64_t so = pc.slot(self_first ? pc.c1 : pc.c0) * p.RPG + row;
+  const uint32_t dst = smem_u32(stage) + rl * 16;
+  float lo = 0.f;
+  if (active) {
+    const float* src = p.part_o + so * kD;
+#pragma unroll
+    for (int j = 0; j < kD / 4; ++j)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + j * 2048), "l"(src + 4 * j) : "memory");
+    lo = __ldcg(p.part_lse + so);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  const float l0 = self_first ? lse2 : lo, l1 = self_first ? lo : lse2;
+  float mx = -INFINITY;
+  mx = fmaxf(mx, l0);
+  mx = fmaxf(mx, l1);
+  float z = 0.f;
+  z += exp2f(l0 - mx);
+  z += exp2f(l1 - mx);
+  const float zinv = 1.f / z;
+  const float w0 = exp2f(l0 - mx) * zinv, w1 = exp2f(l1 - mx) * zinv;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  const uint8_t* srow = stage + rl * 16;
+#pragma unroll 1
+  for (int c = 0; c < kD; c += 16) {
+    uint32_t r[16];
+    __syncwarp();
+    tmem_ld16(tO + c, r);
+    tmem_ld_wait();
+    if (!active) continue;
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 o = *reinterpret_cast<const float4*>(srow + ((c >> 2) + j) * 2048);
+      const float ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float mine = __uint_as_float(r[4 * j + e]) * inv;
+        const float a = fmaf(w0, self_first ? mine : ov[e], 0.f);
+        acc[4 * j + e] = fmaf(w1, self_first ? ov[e] : mine, a);
+      }
+    }
+    store_bf16_16(out + orow * kD + c, acc);
+  }
+  __syncwarp();
+  if (active && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+}
+
+// kStage: 0 no staging; 1 merges at the slice's last segment may stage
+// through `stage` (staged_merge); 2 only a direct merge with one other piece
+// stages (staged_pair_merge).
+template <int kStage>
 __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
                                                bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
                                                uint8_t* stage) {
@@ -762,11 +826,18 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   bool direct = false;
   float mx = lse2, z = 1.f;
   const int rl = row & 127;
-  const bool staged = kStage && stage != nullptr && !complete && pc.c1 - pc.c0 < kStagePieces && pc.T >= pc.P;
+  const bool staged = kStage == 1 && stage != nullptr && !complete && pc.c1 - pc.c0 < kStagePieces && pc.T >= pc.P;
   if (!complete && valid_row && p.direct_merge) direct = ld_acquire_u32(ctr) + mine == (uint32_t)s.n;
-  if constexpr (kStage) {
+  if constexpr (kStage == 1) {
     if (staged && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
       staged_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
+      return 1;
+    }
+  }
+  if constexpr (kStage == 2) {
+    const bool pair = stage != nullptr && pc.c1 - pc.c0 == 1 && pc.T >= pc.P;
+    if (pair && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
+      staged_pair_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
       return 1;
     }
   }
@@ -803,7 +874,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
     if (valid_row && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
     return complete ? 0 : 1;
   }
-  if constexpr (kStage) {
+  if constexpr (kStage == 1) {
     if (staged) {
       bool last = false;
       if (valid_row) {
@@ -835,8 +906,9 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   return 3;
 }
 
-// kStage: merges at the slice's last segment may stage through `stage`.
-template <bool kStage>
+// kStage (as in finish_row_impl): how merges at the slice's last segment may
+// stage through `stage`.
+template <int kStage>
 __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
                                            bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
                                            uint8_t* stage) {
@@ -1225,7 +1297,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       Segment s_ahead;
       // after the slice's last tile the K/V ring is idle: merges stage through it
       uint8_t* stage = ahead.next(p, s_ahead) ? nullptr : smem_raw + (base - raw) + C::kOffK;
-      finish_row<true>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
+      finish_row<1>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
       fence_before();
     }
   }
@@ -1270,6 +1342,7 @@ struct PairCfg {
   static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
   static constexpr int kSoftmaxWarp0 = 8;
 };
+static_assert(PairCfg::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 
 template <bool kRope>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -1571,8 +1644,22 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
       if (!ok) break;
       fence_after();
+      // After the slice's last tile the K/V ring goes idle once both M tiles'
+      // last P.V products have completed (the last stage's empty barrier
+      // counts one commit from each O issuer, and each commit covers that
+      // issuer's earlier products; the S products completed before their
+      // softmax).  A direct merge with one other piece then stages that
+      // piece's rows through it, M tile m in its own 64 KB (the K half of the
+      // ring for m = 0, the V half for 1).
+      uint8_t* stage = nullptr;
+      if (!have_next) {
+        ok = mbar_wait_warp(&bars.kv_empty[(g - 1) % C::kStages], ((g - 1) / C::kStages) & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        stage = smem_raw + (base - raw) + (m == 0 ? C::kOffK : C::kOffV);
+      }
       if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
-      finish_row<false>(p, sp, s, row, valid_row, orow, tO, m_run, l, nullptr);
+      finish_row<2>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
       fence_before();
       if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       s = s_next;
