@@ -71,6 +71,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--oracle-single-core", default=None, metavar="LENS",
+                    help="internal (run by the cpu_baseline leg with one BLAS/OpenMP thread): time the oracle on "
+                         "requests of these comma-separated prefix lengths and print one JSON line")
     return ap.parse_args()
 
 
@@ -537,7 +540,9 @@ def run_ours(args, world, rank, local):
                                     st.counts)
         cpu = {"value": nps, "unit": "nodes/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{len(used)} of {w.B} requests (all {st.N} nodes, all {w.Hq} heads, acceptance incl.), "
-                         f"prefix lengths {[int(st.lens[b]) for b in used][:6]}..., {el:.1f} s"}
+                         f"prefix lengths {[int(st.lens[b]) for b in used][:6]}..., {el:.1f} s",
+               "single_core": oracle_single_core(w, [int(st.lens[b]) for b in used[:6]],
+                                                 min(8.0, args.cpu_seconds))}
 
     if rank == 0:
         line = {
@@ -563,11 +568,10 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line))
 
 
-def run_reference(args, world, rank):
-    if rank != 0:
-        return
-    w = W.WORKLOADS[args.workload]
-    inp = W.attention_inputs(w, device="cpu")
+def cpu_workload(w, seq_lens=None):
+    """The workload's inputs generated on the CPU (the recipe's generators on
+    the CPU device), as the oracle takes them."""
+    inp = W.attention_inputs(w, device="cpu", seq_lens=seq_lens)
     from oracle import tree as OT
     req_paths = request_paths(w)
     parent = (np.stack([OT.build_tree(p)[0] for p in req_paths]) if w.dynamic else OT.build_tree(w.paths())[0])
@@ -576,8 +580,43 @@ def run_reference(args, world, rank):
     if w.accept == "sample":
         sample = W.sample_tree_inputs(w, parent, device="cpu") if w.sample_tree else W.sample_chain_inputs(w, device="cpu")
     inp_cpu, g, s = cpu_inputs(w, inp, greedy, sample)
+    return inp_cpu, g, s, req_paths, W.node_counts(w)
+
+
+def run_oracle_single_core(args):
+    """One-core oracle timing (the parent starts this process with one BLAS and
+    OpenMP thread): requests of the given prefix lengths, generated on the CPU
+    with the workload's recipe, timed one by one until --cpu-seconds."""
+    lens = np.array([int(x) for x in args.oracle_single_core.split(",")], dtype=np.int32)
+    w = dataclasses.replace(W.WORKLOADS[args.workload], B=len(lens))
+    inp_cpu, g, s, req_paths, counts = cpu_workload(w, seq_lens=lens)
+    nps, used, el = time_oracle(w, inp_cpu, req_paths, g, s, args.cpu_seconds, list(range(len(lens))), counts)
+    print(json.dumps({"value": nps, "requests": len(used), "seconds": round(el, 2), "threads": blas_threads()}))
+
+
+def oracle_single_core(w, lens, seconds):
+    """cpu_baseline's one-core figure: run_oracle_single_core in a child
+    process with the thread counts pinned to 1."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "LOCAL_WORLD_SIZE")}
+    env.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--workload", w.name, "--cpu-seconds", str(seconds),
+           "--oracle-single-core", ",".join(str(int(x)) for x in lens)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+        out = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+    return {"value": out["value"], "unit": "nodes/s", "cores": out["threads"],
+            "sample": f"{out['requests']} requests of prefix lengths {list(map(int, lens))[:out['requests']]}, "
+                      f"inputs regenerated on the CPU with the same recipe, {out['seconds']} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    inp_cpu, g, s, req_paths, counts = cpu_workload(w)
     lens = inp_cpu["seq_lens"]
-    counts = W.node_counts(w)
     order = sample_order(lens)
     for k in range(args.warmup):
         oracle_sample_run(w, inp_cpu, req_paths, g, s, [order[k % len(order)]], counts)
@@ -609,6 +648,9 @@ def run_reference(args, world, rank):
 
 def main():
     args = parse_args()
+    if args.oracle_single_core:
+        run_oracle_single_core(args)
+        return
     world, rank, local = dist_setup(args)
     try:
         if args.impl == "reference":
