@@ -218,6 +218,21 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(const float* __restric
 constexpr int kGreedyCtas = 8;
 constexpr int kGreedyThreads = 256;
 
+// Orderable key of a float (no NaN): key(a) > key(b) exactly when a > b, and
+// -0 and +0 share a key, as they compare equal.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.f));  // -0 + 0 = +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Warp argmax of (key, index) pairs: the largest key, the lowest index among
+// equal keys (the order of `better`); every lane gets the result.
+__device__ __forceinline__ void warp_argmax_key(uint32_t& key, uint32_t& idx) {
+  const uint32_t km = __reduce_max_sync(0xffffffffu, key);
+  idx = __reduce_min_sync(0xffffffffu, key == km ? idx : 0xffffffffu);
+  key = km;
+}
+
 __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThreads)
     greedy_cluster_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tokens,
                           const int32_t* __restrict__ parent, int64_t pstride, const int32_t* __restrict__ n_nodes,
@@ -225,15 +240,11 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
-  __shared__ float s_v[kGreedyThreads / 32];
-  __shared__ int s_i[kGreedyThreads / 32];
-  __shared__ float s_res_v[2];  // this CTA's slice result, by step parity (read by the peers)
-  __shared__ int s_res_i[2];
-  __shared__ int s_choice, s_best;
+  __shared__ uint32_t s_key[kGreedyThreads / 32], s_idx[kGreedyThreads / 32];
+  __shared__ uint32_t s_res_key[2], s_res_idx[2];  // this CTA's slice result, by step parity (read by the peers)
+  __shared__ int s_choice, s_next;
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / kGreedyCtas;
-  load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
-  __syncthreads();
   const int n = clamp_nodes(n_nodes, b, N);
   const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
   int seg = (V + kGreedyCtas - 1) / kGreedyCtas;
@@ -246,17 +257,20 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
     float bv = -INFINITY;
     int bi = INT_MAX;
     if (vec) {
-      // kBatch float4 per thread requested together, then compared
+      // kBatch float4 per thread requested together, then compared; the
+      // first batch of the root row goes out before the tree is loaded
       constexpr int kBatch = 4;
       const float4* r4 = reinterpret_cast<const float4*>(row) + lo / 4;
       const int n4 = (hi - lo) / 4;
-      for (int base = threadIdx.x; base < n4; base += kBatch * kGreedyThreads) {
+      for (int base = threadIdx.x; base < n4 || (step == 0 && base == (int)threadIdx.x);
+           base += kBatch * kGreedyThreads) {
         float4 x[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int t = base + u * kGreedyThreads;
           if (t < n4) x[u] = __ldg(r4 + t);
         }
+        if (step == 0 && base == (int)threadIdx.x) load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           if (base + u * kGreedyThreads >= n4) break;
@@ -268,52 +282,51 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
         }
       }
     } else {
+      if (step == 0) load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
       for (int i = lo + threadIdx.x; i < hi; i += kGreedyThreads) {
         const float x = __ldg(row + i);
         if (better(x, i, bv, bi)) { bv = x; bi = i; }
       }
     }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == 0) { s_v[warp] = bv; s_i[warp] = bi; }
-    __syncthreads();
+    uint32_t key = order_key(bv), idx = (uint32_t)bi;
+    warp_argmax_key(key, idx);
+    if (lane == 0) { s_key[warp] = key; s_idx[warp] = idx; }
+    __syncthreads();  // also publishes the tree rows at step 0
     const int par = step & 1;
     if (warp == 0) {
-      bv = lane < kGreedyThreads / 32 ? s_v[lane] : -INFINITY;
-      bi = lane < kGreedyThreads / 32 ? s_i[lane] : INT_MAX;
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if (lane == 0) { s_res_v[par] = bv; s_res_i[par] = bi; }
+      key = lane < kGreedyThreads / 32 ? s_key[lane] : 0u;
+      idx = lane < kGreedyThreads / 32 ? s_idx[lane] : 0xffffffffu;
+      warp_argmax_key(key, idx);
+      if (lane == 0) { s_res_key[par] = key; s_res_idx[par] = idx; }
     }
     cluster.sync();  // every slice result of this step is visible cluster-wide
     if (warp == 0) {
-      bv = -INFINITY;
-      bi = INT_MAX;
+      key = 0u;
+      idx = 0xffffffffu;
       if (lane < kGreedyCtas) {
-        bv = *cluster.map_shared_rank(&s_res_v[par], lane);
-        bi = *cluster.map_shared_rank(&s_res_i[par], lane);
+        key = *cluster.map_shared_rank(&s_res_key[par], lane);
+        idx = *cluster.map_shared_rank(&s_res_idx[par], lane);
       }
+      warp_argmax_key(key, idx);
+      const int choice = (int)idx;
+      // lowest-index valid child of `node` carrying the choice (children
+      // follow their parent and N <= 64: two 32-node windows)
+      int nxt = INT_MAX;
 #pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      for (int w0 = 1; w0 <= 33; w0 += 32) {
+        const int c = node + w0 + lane;
+        const unsigned hit = __ballot_sync(0xffffffffu, c < n && s_par[c] == node && s_tok[c] == choice);
+        if (hit && nxt == INT_MAX) nxt = node + w0 + __ffs(hit) - 1;
       }
-      if (lane == 0) s_choice = bi;
+      if (lane == 0) {
+        s_choice = choice;
+        s_next = nxt;
+      }
     }
     __syncthreads();
-    const int choice = s_choice;
+    const int choice = s_choice, nxt = s_next;
     if (rank == 0) emit(o, b, k, choice, node);
     ++k;
-    const int nxt = find_child(s_par, s_tok, node, n, choice, &s_best);
     if (nxt == INT_MAX) break;
     if (k == o.out_cols) {
       if (rank == 0 && threadIdx.x == 0 && o.status) atomicOr(o.status, TV_DEV_OUT_OVERFLOW);
