@@ -87,3 +87,30 @@ def test_device_entry_points_reject_bad_sizes_on_host():
     assert h.tv_tree_accept_sample(None, None, None, None, 0, None, None, None, 0, 10, 10, None, None, None, 4,
                                    4, None, None) == -1
     assert b"unknown flags" in h.tv_last_error()
+
+
+def test_tree_prepare_rejects_bad_arguments_on_host():
+    """tv_tree_prepare checks its sizes, rotation arguments and head_dim
+    before any launch (fake non-null pointers are never touched)."""
+    import ctypes
+    h = capi.lib()
+    fake = ctypes.c_void_p(256)
+    tb = fake  # stands for every device buffer
+    # N past the 64-node limit; B = 0 is a no-op
+    assert h.tv_tree_prepare(None, 0, None, None, 1, 65, None, None, None, None, 0, None, 0, 128, 1, None, 16,
+                             None, None) == -1
+    assert b"bad sizes" in h.tv_last_error()
+    assert h.tv_tree_prepare(None, 0, None, None, 0, 10, None, None, None, None, 0, None, 0, 128, 1, None, 16,
+                             None, None) == 0
+    # Q given without query heads, or without a table
+    assert h.tv_tree_prepare(tb, 10, tb, None, 2, 10, tb, tb, tb, fake, 0, None, 0, 128, 1, tb, 16, None,
+                             None) == -1
+    assert b"rotation needs" in h.tv_last_error()
+    assert h.tv_tree_prepare(tb, 10, tb, None, 2, 10, tb, tb, tb, fake, 4, fake, 2, 128, 1, None, 16, None,
+                             None) == -1
+    assert b"rotation needs" in h.tv_last_error()
+    # a head_dim the rotation does not take
+    assert h.tv_tree_prepare(tb, 10, tb, None, 2, 10, tb, tb, tb, fake, 4, fake, 2, 48, 1, tb, 16, None,
+                             None) == -4  # TV_ERR_UNSUPPORTED
+    assert b"head_dim 48" in h.tv_last_error()
+
