@@ -366,6 +366,10 @@ class Step:
         self.run_attn()
         if ev_attn:
             ev_attn[1].record()
+        self.run_accept()
+
+    def run_accept(self):
+        c = self.capi
         if self.greedy is not None:
             c.tv_tree_accept_greedy(self.greedy["tokens"], self.parent, logits=self.greedy["logits"],
                                     n_nodes=self.n_nodes, out=self.acc_out,
@@ -552,6 +556,33 @@ def run_ours(args, world, rank, local):
         moved = rows * w.Hkv * w.D * st.esize * 2 * 2  # K and V rows, read and written
         commit = {"us_per_call": round(us, 2), "rows": rows, "bytes": moved, "gbs": round(moved / (us * 1e-6) / 1e9, 1)}
 
+    # the acceptance call alone (graph replays, L2 flushed before each): the
+    # lazy greedy walk reads one logits row per emitted token
+    accept = None
+    if graphs and (st.greedy is not None or st.sample is not None):
+        g_acc = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_acc):
+            st.run_accept()
+        fl = flush if flush is not None else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        evc = []
+        for k in range(args.warmup + args.steps):
+            fl.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g_acc.replay()
+            b.record()
+            if k >= args.warmup:
+                evc.append((a, b))
+        torch.cuda.synchronize()
+        us = statistics.mean(a.elapsed_time(b) for a, b in evc) * 1e3
+        emitted = int(st.acc_n.sum().item())
+        accept = {"call": "tv_tree_accept_greedy" if st.greedy is not None else "tv_tree_accept_sample",
+                  "us_per_call": round(us, 2), "tokens_out": emitted}
+        if st.greedy is not None:
+            rows_b = emitted * w.vocab * 4
+            accept.update(bytes_read=rows_b, all_rows_bytes=w.B * st.N * w.vocab * 4,
+                          gbs=round(rows_b / (us * 1e-6) / 1e9, 1))
+
     peak, peak_kind = measured_hbm_peak()
     attn_mean_ms = statistics.mean(attn_ms)
     achieved = st.attn_bytes / (attn_mean_ms / 1e3) / 1e9
@@ -591,7 +622,7 @@ def run_ours(args, world, rank, local):
                        "rope": "fused" if st.fused_rope else "separate"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": st.launches * args.steps,
-            "kv_commit": commit,
+            "kv_commit": commit, "accept": accept,
             "kv_read_gbs": round(achieved, 1), "kv_read_frac_of_peak": round(achieved / peak, 4),
         }
         print(json.dumps(line))
