@@ -1344,7 +1344,17 @@ struct PairCfg {
 };
 static_assert(PairCfg::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 
-template <bool kRope>
+// M tile 1 of a unit holds no valid row: the unit is the last row group of
+// a (request, KV head) with at most 128 rows left.
+__device__ __forceinline__ bool m1_idle(const AttnParams& p, const Segment& s) {
+  return p.R - s.rg * p.RPG <= 128;
+}
+
+// kSkip: units whose M tile 1 is idle (m1_idle) run M tile 0 alone -- no S_1
+// or P_1.V products and no softmax for M tile 1; its issuers and softmax warps
+// only keep the K/V ring and the query barrier in step.  Their own barriers
+// (s_full/s_free/p_full/o_done of M tile 1) then count products, not tiles.
+template <bool kRope, bool kSkip>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
   using C = PairCfg;
@@ -1396,7 +1406,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBlk, false);
       const uint32_t dS = tmem + C::col_s(m);
-      uint32_t g = 0;
+      uint32_t g = 0, g1 = 0;  // tiles of the ring; with kSkip, S products of this M tile
+      uint32_t& gm = kSkip ? g1 : g;
       int seg_i = 0;
       bool ok = true;
       Walk walk(sp);
@@ -1405,12 +1416,19 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
         if (!ok) break;
         fence_after();
+        if constexpr (kSkip) {
+          if (m == 1 && m1_idle(p, s)) {
+            g += s.e - s.a;
+            ++seg_i;
+            continue;
+          }
+        }
         if (m == 0) TV_TRACE(3, g);
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
           if (m == 0) TV_TRACE(29, g);
-          if (ok && g > 0) ok = mbar_wait(&bars.s_free[m], (g - 1) & 1, &bars, status);
+          if (ok && gm > 0) ok = mbar_wait(&bars.s_free[m], (gm - 1) & 1, &bars, status);
           if (!ok) break;
           fence_after();
           if (m == 0) TV_TRACE(30, g);
@@ -1431,6 +1449,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
             }
           }
           mma_commit(&bars.s_full[m]);
+          if constexpr (kSkip) ++g1;
           if (m == 0) TV_TRACE(2, g);
         }
         ++seg_i;
@@ -1443,14 +1462,22 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(128, kD, true);
       const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
-      uint32_t g = 0;
+      uint32_t g = 0, g1 = 0;  // tiles of the ring; with kSkip, P.V products of this M tile
+      uint32_t& gm = kSkip ? g1 : g;
       bool ok = true;
       Walk walk(sp);
       Segment s;
       while (ok && walk.next(p, s)) {
+        const bool idle = kSkip && m == 1 && m1_idle(p, s);
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
           const int stage = g % C::kStages;
-          ok = mbar_wait(&bars.p_full[m], g & 1, &bars, status);
+          if (idle) {  // no product: release the stage once its load has landed
+            ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+            if (!ok) break;
+            mma_commit(&bars.kv_empty[stage]);
+            continue;
+          }
+          ok = mbar_wait(&bars.p_full[m], gm & 1, &bars, status);
           if (ok) ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
           if (!ok) break;
           fence_after();
@@ -1461,6 +1488,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           for (int kk = 1; kk < kBlk / 16; ++kk) mma_ts<true>(dO, aP + kk * 8, vlo + kk * (2048 >> 4), hi, idO);
           mma_commit(&bars.o_done[m]);
           mma_commit(&bars.kv_empty[stage]);
+          if constexpr (kSkip) ++g1;
           if (m == 0) TV_TRACE(4, g);
         }
       }
@@ -1475,7 +1503,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = lane_addr + C::col_s(m), tP = lane_addr + C::col_p(m), tO = lane_addr + C::col_o(m);
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    uint32_t g = 0;
+    uint32_t g = 0, g1 = 0;  // tiles of the ring; with kSkip, tiles this M tile computed
+    uint32_t& gm = kSkip ? g1 : g;
+    uint32_t useg = 0;  // with kSkip: units of the slice walked so far
     bool ok = true;
     Walk walk(sp);
     Segment s;
@@ -1546,15 +1576,34 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         tv::trace::g_cta_time[blockIdx.x][2] = ++n_segs_traced;
       }
 #endif
+      if constexpr (kSkip) {
+        if (m == 1 && m1_idle(p, s)) {  // nothing to compute: count the ring, place the next Q
+          g += s.e - s.a;
+          // the next unit's arrivals on q_full wait until this unit's phase has
+          // completed (M tile 0 may still be placing this unit's Q)
+          ok = mbar_wait_warp(&bars.q_full, useg & 1, &bars, status);
+          if (!ok) break;
+          ++useg;
+          Segment s_next;
+          const bool have_next = walk.next(p, s_next);
+          if (have_next) {
+            fetch_q(s_next);
+            place_q();
+          }
+          s = s_next;
+          have = have_next;
+          continue;
+        }
+      }
       const RowOf rid = row_of(s);
       const bool valid_row = rid.valid;
       const int64_t orow = rid.orow;
       const uint64_t mrow = mrow_next;
       float m_run = -INFINITY, l = 0.f;
       const int n_seg = s.e - s.a;
-      for (int k = 0; k < n_seg; ++k, ++g) {
+      for (int k = 0; k < n_seg; ++k, ++g, ++g1) {
         const int t = s.a + k;
-        ok = mbar_wait_warp(&bars.s_full[m], g & 1, &bars, status);
+        ok = mbar_wait_warp(&bars.s_full[m], gm & 1, &bars, status);
         if (!ok) break;
         fence_after();
         if (rl == 0) TV_TRACE(6 + 4 * m, g);
@@ -1603,7 +1652,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         const float sum0 = sum_f32x2(add_f32x2(acc0, acc1)), sum1 = 0.f;
         if (k > 0) {
           // P_m(g-1) consumed and O_m holds tiles < g
-          ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
+          ok = mbar_wait_warp(&bars.o_done[m], (gm - 1) & 1, &bars, status);
           if (!ok) break;
           fence_after();
           if (__any_sync(0xffffffffu, grow)) {
@@ -1641,7 +1690,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         place_q();
       }
       if (m == 0 && rl == 0) TV_TRACE(15, g - 1);
-      ok = mbar_wait_warp(&bars.o_done[m], (g - 1) & 1, &bars, status);
+      ok = mbar_wait_warp(&bars.o_done[m], (gm - 1) & 1, &bars, status);
       if (!ok) break;
       fence_after();
       // After the slice's last tile the K/V ring goes idle once both M tiles'
@@ -1662,6 +1711,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       finish_row<2>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
       fence_before();
       if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
+      if constexpr (kSkip) ++useg;
       s = s_next;
       have = have_next;
     }
@@ -1718,12 +1768,12 @@ int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStrea
   return TV_OK;
 }
 
-template <bool kRope>
+template <bool kRope, bool kSkip>
 int launch_pair(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_tc_pair_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PairCfg::kSmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
-  attn_tc_pair_kernel<kRope><<<p.P, PairCfg::kThreads, PairCfg::kSmem, stream>>>(p, maps, status);
+  attn_tc_pair_kernel<kRope, kSkip><<<p.P, PairCfg::kThreads, PairCfg::kSmem, stream>>>(p, maps, status);
   TV_LAUNCH_CHECK("attn_tc_pair_kernel");
   return TV_OK;
 }
@@ -1801,7 +1851,11 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
   }
   if (p.RPG <= 128)
     return p.rope_cs ? launch_m<1, true>(p, maps, status, stream) : launch_m<1, false>(p, maps, status, stream);
-  return p.rope_cs ? launch_pair<true>(p, maps, status, stream) : launch_pair<false>(p, maps, status, stream);
+  if (p.rope_cs) return launch_pair<true, false>(p, maps, status, stream);
+  // a last row group of at most 128 rows leaves M tile 1 idle: skip it
+  const int tail = p.R % p.RPG;
+  if (p.R > p.RPG && tail > 0 && tail <= 128) return launch_pair<false, true>(p, maps, status, stream);
+  return launch_pair<false, false>(p, maps, status, stream);
 }
 
 }  // namespace tv

@@ -187,7 +187,7 @@ def test_mask_sensitive_tree_keys_dominate():
         _check_all(inp, paths, BF16_TOL, flags)
 
 
-@pytest.mark.parametrize("G,N", [(4, 26), (4, 64)])
+@pytest.mark.parametrize("G,N", [(4, 26), (4, 64), (8, 33)])
 def test_split_unit_merge_routes(G, N):
     """Units cut into many pieces (long prefixes, wide grids, grids wider than
     the plan so that some slices are empty).  The tensor-core kernel merges a
