@@ -113,6 +113,7 @@ struct Bars {
   uint64_t o_done[2];
   uint64_t s_free[2];
   uint64_t q_full;
+  uint64_t sh_stat, sh_read;  // shared units (two-M-tile kernel): M tile 1's part posted / read
   uint32_t tmem_base;
   int abort;
 };
@@ -1344,22 +1345,34 @@ struct PairCfg {
 };
 static_assert(PairCfg::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 
-// M tile 1 of a unit holds no valid row: the unit is the last row group of
-// a (request, KV head) with at most 128 rows left.
-__device__ __forceinline__ bool m1_idle(const AttnParams& p, const Segment& s) {
+// The unit is the last row group of a (request, KV head) with at most 128
+// rows left, so one M tile holds all its rows.
+__device__ __forceinline__ bool shared_unit(const AttnParams& p, const Segment& s) {
   return p.R - s.rg * p.RPG <= 128;
 }
 
-// kSkip: units whose M tile 1 is idle (m1_idle) run M tile 0 alone -- no S_1
-// or P_1.V products and no softmax for M tile 1; its issuers and softmax warps
-// only keep the K/V ring and the query barrier in step.  Their own barriers
-// (s_full/s_free/p_full/o_done of M tile 1) then count products, not tiles.
+// kSkip: a shared unit (shared_unit) has its rows in both M tiles, and the
+// key tiles go to the M tile sh_owner names, each M tile with its own running
+// max and sum; at the unit's end M tile 1 posts its (max, sum) through shared
+// memory, and M tile 0 merges M tile 1's accumulator into its own (same TMEM
+// lanes; a part without keys adds nothing) and finishes the rows.  The
+// per-M-tile barriers (s_full/s_free/p_full/o_done) then count that M tile's
+// products, not the ring's tiles.
+//
+// kSplitKeys: the two M tiles take the even and the odd key tiles.  On the
+// 264-row shape (33 nodes, G = 8) that measured slower than M tile 0 taking
+// every tile (0.715 against 0.690 ms): its shared units are bound by the
+// second read of their K/V, not by one M tile's chain.  So M tile 0 computes
+// shared units alone and M tile 1's part is empty.
+constexpr bool kSplitKeys = false;
+__device__ __forceinline__ int sh_owner(int t) { return kSplitKeys ? (t & 1) : 0; }
 template <bool kRope, bool kSkip>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
   using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
+  __shared__ float s_sh[kSkip ? 256 : 1];  // shared units: M tile 1's running max and sum per row
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t sK = base + C::kOffK, sV = base + C::kOffV, sQ1 = base + C::kOffQ1;
@@ -1383,6 +1396,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       mbar_init(&bars.o_done[m], 1);
     }
     mbar_init(&bars.q_full, 256);
+    mbar_init(&bars.sh_stat, 128);
+    mbar_init(&bars.sh_read, 128);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1416,15 +1431,10 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
         if (!ok) break;
         fence_after();
-        if constexpr (kSkip) {
-          if (m == 1 && m1_idle(p, s)) {
-            g += s.e - s.a;
-            ++seg_i;
-            continue;
-          }
-        }
+        const bool sh = kSkip && shared_unit(p, s);
         if (m == 0) TV_TRACE(3, g);
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
+          if (sh && sh_owner(t) != m) continue;  // the other M tile's tile
           const int stage = g % C::kStages;
           ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
           if (m == 0) TV_TRACE(29, g);
@@ -1468,10 +1478,11 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       Walk walk(sp);
       Segment s;
       while (ok && walk.next(p, s)) {
-        const bool idle = kSkip && m == 1 && m1_idle(p, s);
+        const bool sh = kSkip && shared_unit(p, s);
+        bool started = false;  // with kSkip: this M tile has a product in this unit
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
           const int stage = g % C::kStages;
-          if (idle) {  // no product: release the stage once its load has landed
+          if (sh && sh_owner(t) != m) {  // the other M tile's tile: release this share once it has landed
             ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
             if (!ok) break;
             mma_commit(&bars.kv_empty[stage]);
@@ -1482,8 +1493,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           if (!ok) break;
           fence_after();
           const uint32_t vlo = desc_lo(sV + stage * kKVTileBytes, kKVHalfBytes);
-          if (t > s.a) mma_ts<true>(dO, aP, vlo, hi, idO);
+          if (kSkip ? started : t > s.a) mma_ts<true>(dO, aP, vlo, hi, idO);
           else mma_ts<false>(dO, aP, vlo, hi, idO);
+          started = true;
 #pragma unroll
           for (int kk = 1; kk < kBlk / 16; ++kk) mma_ts<true>(dO, aP + kk * 8, vlo + kk * (2048 >> 4), hi, idO);
           mma_commit(&bars.o_done[m]);
@@ -1505,7 +1517,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
     uint32_t g = 0, g1 = 0;  // tiles of the ring; with kSkip, tiles this M tile computed
     uint32_t& gm = kSkip ? g1 : g;
-    uint32_t useg = 0;  // with kSkip: units of the slice walked so far
+    uint32_t useg = 0, shi = 0;  // with kSkip: units of the slice walked so far; shared units
     bool ok = true;
     Walk walk(sp);
     Segment s;
@@ -1521,7 +1533,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     };
     auto row_of = [&](const Segment& sg) {
       RowOf r;
-      const int unit_row = sg.rg * p.RPG + row;
+      const int unit_row = sg.rg * p.RPG + ((kSkip && shared_unit(p, sg)) ? rl : row);
       r.valid = unit_row < p.R;
       r.node = r.valid ? unit_row / p.G : 0;
       r.orow = ((int64_t)sg.b * p.N + r.node) * p.Hq + sg.kvh * p.G + unit_row % p.G;
@@ -1576,33 +1588,17 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         tv::trace::g_cta_time[blockIdx.x][2] = ++n_segs_traced;
       }
 #endif
-      if constexpr (kSkip) {
-        if (m == 1 && m1_idle(p, s)) {  // nothing to compute: count the ring, place the next Q
-          g += s.e - s.a;
-          // the next unit's arrivals on q_full wait until this unit's phase has
-          // completed (M tile 0 may still be placing this unit's Q)
-          ok = mbar_wait_warp(&bars.q_full, useg & 1, &bars, status);
-          if (!ok) break;
-          ++useg;
-          Segment s_next;
-          const bool have_next = walk.next(p, s_next);
-          if (have_next) {
-            fetch_q(s_next);
-            place_q();
-          }
-          s = s_next;
-          have = have_next;
-          continue;
-        }
-      }
+      const bool sh = kSkip && shared_unit(p, s);
       const RowOf rid = row_of(s);
       const bool valid_row = rid.valid;
       const int64_t orow = rid.orow;
       const uint64_t mrow = mrow_next;
       float m_run = -INFINITY, l = 0.f;
       const int n_seg = s.e - s.a;
-      for (int k = 0; k < n_seg; ++k, ++g, ++g1) {
+      int kk = 0;  // with kSkip: tiles this M tile computed in this unit
+      for (int k = 0; k < n_seg; ++k, ++g) {
         const int t = s.a + k;
+        if (sh && sh_owner(t) != m) continue;  // the other M tile's tile
         ok = mbar_wait_warp(&bars.s_full[m], gm & 1, &bars, status);
         if (!ok) break;
         fence_after();
@@ -1650,7 +1646,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           pk[c] = pack_bf16(e0, e1);
         }
         const float sum0 = sum_f32x2(add_f32x2(acc0, acc1)), sum1 = 0.f;
-        if (k > 0) {
+        if ((kSkip ? kk : k) > 0) {
           // P_m(g-1) consumed and O_m holds tiles < g
           ok = mbar_wait_warp(&bars.o_done[m], (gm - 1) & 1, &bars, status);
           if (!ok) break;
@@ -1678,8 +1674,16 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         fence_before();
         mbar_arrive(&bars.p_full[m]);
         if (rl == 0) TV_TRACE(9 + 4 * m, g);
+        if constexpr (kSkip) {
+          ++kk;
+          ++g1;
+        }
       }
       if (!ok) break;
+      if (sh) {  // this unit's query phase completes before the next unit's arrivals go out
+        ok = mbar_wait_warp(&bars.q_full, useg & 1, &bars, status);
+        if (!ok) break;
+      }
       // The next unit's Q goes in first (its S_m MMAs then run during this
       // epilogue): this unit's S_m MMAs have all completed -- the softmax has
       // read every S_m tile -- and its rows are warm in L2.
@@ -1690,9 +1694,56 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         place_q();
       }
       if (m == 0 && rl == 0) TV_TRACE(15, g - 1);
-      ok = mbar_wait_warp(&bars.o_done[m], (gm - 1) & 1, &bars, status);
-      if (!ok) break;
-      fence_after();
+      if (!sh || kk > 0) {
+        ok = mbar_wait_warp(&bars.o_done[m], (gm - 1) & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+      }
+      if constexpr (kSkip) {
+        if (sh) {
+          if (m == 1) {  // post this M tile's (max, sum); its accumulator stays until M tile 0 has read it
+            s_sh[rl] = m_run;
+            s_sh[128 + rl] = kk > 0 ? l : 0.f;
+            fence_before();
+            mbar_arrive(&bars.sh_stat);
+            ok = mbar_wait_warp(&bars.sh_read, shi & 1, &bars, status);
+            if (!ok) break;
+            ++shi;
+            ++useg;
+            s = s_next;
+            have = have_next;
+            continue;
+          }
+          ok = mbar_wait_warp(&bars.sh_stat, shi & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          ++shi;
+          // O = O_0 2^(m_0 - m) + O_1 2^(m_1 - m), l likewise, m = max (a part
+          // without keys -- no tile, or every key masked -- adds nothing)
+          const float m1v = s_sh[rl], l1v = s_sh[128 + rl];
+          const bool h0 = kk > 0 && l > 0.f, h1 = l1v > 0.f;
+          const float mm = h0 ? (h1 ? fmaxf(m_run, m1v) : m_run) : (h1 ? m1v : m_run);
+          const float a0 = h0 ? exp2f(m_run - mm) : 0.f, a1 = h1 ? exp2f(m1v - mm) : 0.f;
+          const uint32_t tO1 = lane_addr + C::col_o(1);
+#pragma unroll 1
+          for (int c = 0; c < kD; c += 32) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tO + c, r0);
+            tmem_ld32(tO1 + c, r1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              r0[j] = __float_as_uint((h0 ? __uint_as_float(r0[j]) * a0 : 0.f) +
+                                      (h1 ? __uint_as_float(r1[j]) * a1 : 0.f));
+            tmem_st32(tO + c, r0);
+          }
+          tmem_st_wait();
+          l = (h0 ? l * a0 : 0.f) + (h1 ? l1v * a1 : 0.f);
+          m_run = mm;
+          fence_before();
+          mbar_arrive(&bars.sh_read);  // M tile 1's accumulator is free again
+        }
+      }
       // After the slice's last tile the K/V ring goes idle once both M tiles'
       // last P.V products have completed (the last stage's empty barrier
       // counts one commit from each O issuer, and each commit covers that
@@ -1790,7 +1841,9 @@ const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim
   if (G < 1 || 128 % G) return "Hq/Hkv does not divide 128";
   if (block_size % 16 || !(kBlk % block_size == 0 || block_size % kBlk == 0))
     return "block_size is not a multiple of 16 that divides or is divisible by 64";
-  if (dev.max_smem_optin < (size_t)PairCfg::kSmem + sizeof(Bars)) return "not enough opt-in shared memory";
+  // dynamic ring + barriers + the shared-unit statistics + the slice plan
+  if (dev.max_smem_optin < (size_t)PairCfg::kSmem + sizeof(Bars) + 256 * sizeof(float) + 64)
+    return "not enough opt-in shared memory";
   return nullptr;
 }
 
