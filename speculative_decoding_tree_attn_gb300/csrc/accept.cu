@@ -233,6 +233,48 @@ __device__ __forceinline__ void warp_argmax_key(uint32_t& key, uint32_t& idx) {
   key = km;
 }
 
+// One-way exchange of the slice results: each CTA stores its packed result
+// into slot [rank] of every peer's shared memory with st.async, which counts
+// the 8 bytes against the peer's mbarrier for that step parity; a CTA waits
+// on its own mbarrier (armed for 8 results per step) instead of a cluster
+// barrier.  Waits are bounded (TV_DEV_TIMEOUT).
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void gx_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(bar)) : "memory");
+}
+__device__ __forceinline__ void gx_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void gx_send(uint64_t* slot, uint64_t* bar, unsigned peer, uint64_t v) {
+  uint32_t rs, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"((uint32_t)__cvta_generic_to_shared(slot)), "r"(peer));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(peer));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u64 [%0], %1, [%2];" ::"r"(rs), "l"(v), "r"(rb)
+               : "memory");
+}
+// true once the phase of the given parity has completed; false after about 2 s
+__device__ __forceinline__ bool gx_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+  const uint64_t t0 = gtime();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(a), "r"(parity)
+                 : "memory");
+    if (done) return true;
+    if ((it & 255u) == 255u && gtime() - t0 > 2000000000ull) return false;
+  }
+}
+
 __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThreads)
     greedy_cluster_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tokens,
                           const int32_t* __restrict__ parent, int64_t pstride, const int32_t* __restrict__ n_nodes,
@@ -241,9 +283,16 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
   __shared__ uint32_t s_key[kGreedyThreads / 32], s_idx[kGreedyThreads / 32];
-  __shared__ uint32_t s_res_key[2], s_res_idx[2];  // this CTA's slice result, by step parity (read by the peers)
+  __shared__ uint64_t s_slot[2][kGreedyCtas];  // the CTAs' packed slice results, by step parity
+  __shared__ uint64_t s_bar[2];                 // their arrival, by step parity
   __shared__ int s_choice, s_next;
   const int rank = (int)cluster.block_rank();
+  if (threadIdx.x == 0) {
+    gx_init(&s_bar[0]);
+    gx_init(&s_bar[1]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  cluster.sync();  // every CTA's barriers are initialised before any result is sent
   const int b = blockIdx.x / kGreedyCtas;
   const int n = clamp_nodes(n_nodes, b, N);
   const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
@@ -297,18 +346,21 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
       key = lane < kGreedyThreads / 32 ? s_key[lane] : 0u;
       idx = lane < kGreedyThreads / 32 ? s_idx[lane] : 0xffffffffu;
       warp_argmax_key(key, idx);
-      if (lane == 0) { s_res_key[par] = key; s_res_idx[par] = idx; }
-    }
-    cluster.sync();  // every slice result of this step is visible cluster-wide
-    if (warp == 0) {
-      key = 0u;
-      idx = 0xffffffffu;
-      if (lane < kGreedyCtas) {
-        key = *cluster.map_shared_rank(&s_res_key[par], lane);
-        idx = *cluster.map_shared_rank(&s_res_idx[par], lane);
+      // (key, ~index) packed: the largest value is the largest key, then the lowest index
+      if (lane == 0) gx_expect(&s_bar[par], 8u * kGreedyCtas);
+      __syncwarp();
+      if (lane < kGreedyCtas)
+        gx_send(&s_slot[par][rank], &s_bar[par], (unsigned)lane, ((uint64_t)key << 32) | (uint64_t)(~idx));
+      const bool late = __any_sync(0xffffffffu, !gx_wait(&s_bar[par], (step >> 1) & 1));
+      if (late && lane == 0 && o.status) atomicOr(o.status, TV_DEV_TIMEOUT);
+      uint64_t v = lane < kGreedyCtas ? s_slot[par][lane] : 0ull;
+#pragma unroll
+      for (int off = 4; off; off >>= 1) {
+        const uint64_t w = __shfl_xor_sync(0xffffffffu, v, off);
+        v = w > v ? w : v;
       }
-      warp_argmax_key(key, idx);
-      const int choice = (int)idx;
+      v = __shfl_sync(0xffffffffu, v, 0);
+      const int choice = (int)(~(uint32_t)v);
       // lowest-index valid child of `node` carrying the choice (children
       // follow their parent and N <= 64: two 32-node windows)
       int nxt = INT_MAX;
@@ -320,7 +372,7 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
       }
       if (lane == 0) {
         s_choice = choice;
-        s_next = nxt;
+        s_next = late ? INT_MAX : nxt;  // a peer's result never came: end the walk
       }
     }
     __syncthreads();
@@ -334,7 +386,7 @@ __global__ void __cluster_dims__(kGreedyCtas, 1, 1) __launch_bounds__(kGreedyThr
     }
     node = nxt;
   }
-  cluster.sync();  // no CTA leaves while a peer may still read its slice result
+  cluster.sync();  // no CTA leaves while a peer's result may still be on its way to it
   if (rank == 0) finish_walk(o, b, k);
 }
 
