@@ -60,30 +60,47 @@ def rope(x, pos, base=10000.0):
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
+def gather_prefix_heads(cache, block_row, prefix_len):
+    """Prefix rows 0..L-1 of one request from a paged cache, per KV head ->
+    [Hkv, L, D] f64: position t is slot t % block_size of block
+    block_row[t // block_size] (whole blocks are gathered, then cut at L)."""
+    nb, Hkv, block_size, D = cache.shape
+    L = int(prefix_len)
+    used = -(-L // block_size)
+    blocks = np.asarray(block_row)[:used]
+    x = np.asarray(cache[blocks], dtype=np.float64)                      # [used, Hkv, bs, D]
+    return np.ascontiguousarray(x.transpose(1, 0, 2, 3).reshape(Hkv, used * block_size, D)[:, :L])
+
+
 def gather_prefix(cache, block_row, prefix_len):
     """Prefix rows 0..L-1 of one request from a paged cache -> [L, Hkv, D] f64."""
-    block_size = cache.shape[2]
-    t = np.arange(int(prefix_len))
-    blocks = np.asarray(block_row)[t // block_size]
-    slots = t % block_size
-    return np.asarray(cache[blocks, :, slots, :], dtype=np.float64)
+    return gather_prefix_heads(cache, block_row, prefix_len).transpose(1, 0, 2)
 
 
-def _softmax_attend(qh, keys, vals, scale):
-    """Ordinary attention of query rows qh [G, D] over keys/vals [T, D]; an
-    empty key set gives zero rows and log-normaliser -inf."""
-    if keys.shape[0] == 0:
-        return np.zeros((qh.shape[0], vals.shape[-1])), np.full(qh.shape[0], -np.inf)
-    s = (qh @ keys.T) * scale
+def _softmax_attend(qh, key_parts, val_parts, scale):
+    """Ordinary attention of query rows qh [G, D] over the key set made of
+    ``key_parts`` (a list of [T_k, D] arrays laid end to end, values
+    likewise): one score row over all keys, one softmax, and the weighted sum
+    of the values taken part by part (the same sum, reassociated, so that the
+    long prefix is never copied next to each node's path).  An empty key set
+    gives zero rows and log-normaliser -inf."""
+    if sum(k.shape[0] for k in key_parts) == 0:
+        return np.zeros((qh.shape[0], val_parts[0].shape[-1])), np.full(qh.shape[0], -np.inf)
+    s = np.concatenate([qh @ k.T for k in key_parts], axis=1) * scale
     m = s.max(axis=1, keepdims=True)
     e = np.exp(s - m)
     z = e.sum(axis=1, keepdims=True)
-    return (e @ vals) / z, (m + np.log(z))[:, 0]
+    o = np.zeros((qh.shape[0], val_parts[0].shape[-1]))
+    start = 0
+    for v in val_parts:
+        o += e[:, start:start + v.shape[0]] @ v
+        start += v.shape[0]
+    return o / z, (m + np.log(z))[:, 0]
 
 
 def tree_attention(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree,
                    parent, *, rope_base=10000.0, scale=None, nodes=None,
-                   mutant=None, n_nodes=None):
+                   mutant=None, n_nodes=None, rotate=True):
     """Per-node path attention (see module docstring).
 
     Shapes: q [B, N, Hq, D]; k_tree, v_tree [B, N, Hkv, D] (q and k_tree NOT
@@ -93,6 +110,12 @@ def tree_attention(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree,
     stay NaN).  ``n_nodes`` [B] (optional): ragged trees, nodes >= n_nodes[b]
     absent (module docstring).  Returns (out [B, N, Hq, D] f64, lse [B, N, Hq] f64, natural
     log of the softmax normaliser).
+
+    ``rotate=False`` takes ``q`` and ``k_tree`` as already rotated (each node
+    at its own position L + depth): the same per-path attention with the
+    RoPE step left out.  It lets a test give the attention kernel alone the
+    rotated rows, so that its output is compared without the rounding of a
+    separate rotation in the input precision.
 
     ``mutant`` exists only for the negative-control tests and models the two
     mistakes the mask page lists: ``"causal_flat"`` lets node i see every
@@ -118,15 +141,16 @@ def tree_attention(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree,
     for b, node_list in want.items():
         par = parent[b] if parent.ndim == 2 else parent
         L = int(seq_lens[b])
-        pk = gather_prefix(k_cache, block_table[b], L)
-        pv = gather_prefix(v_cache, block_table[b], L)
+        # prefix keys and values of each KV head, [L, D] contiguous
+        pk = gather_prefix_heads(k_cache, block_table[b], L)
+        pv = gather_prefix_heads(v_cache, block_table[b], L)
         n_b = N if n_nodes is None else min(max(int(n_nodes[b]), 1), N)
         dep = depth_of(par[:n_b])
         for i in node_list:
             if i >= n_b:  # absent: the prefix alone, query as given
                 qi = np.asarray(q[b, i], dtype=np.float64)
                 for kvh in range(Hkv):
-                    o, l = _softmax_attend(qi[kvh * G:(kvh + 1) * G], pk[:, kvh], pv[:, kvh], scale)
+                    o, l = _softmax_attend(qi[kvh * G:(kvh + 1) * G], [pk[kvh]], [pv[kvh]], scale)
                     out[b, i, kvh * G:(kvh + 1) * G] = o
                     lse[b, i, kvh * G:(kvh + 1) * G] = l
                 continue
@@ -144,13 +168,15 @@ def tree_attention(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree,
                 q_pos = L + len(chain) - 1
             else:
                 raise ValueError(mutant)
-            kt = rope(np.asarray(k_tree[b, chain], dtype=np.float64),
-                      np.asarray(key_pos)[:, None], rope_base)
-            keys = np.concatenate([pk, kt], axis=0)
-            vals = np.concatenate([pv, np.asarray(v_tree[b, chain], dtype=np.float64)], axis=0)
-            qi = rope(np.asarray(q[b, i], dtype=np.float64), q_pos, rope_base)
+            kt = np.asarray(k_tree[b, chain], dtype=np.float64)
+            qi = np.asarray(q[b, i], dtype=np.float64)
+            if rotate:
+                kt = rope(kt, np.asarray(key_pos)[:, None], rope_base)
+                qi = rope(qi, q_pos, rope_base)
+            vt = np.asarray(v_tree[b, chain], dtype=np.float64)
             for kvh in range(Hkv):
-                o, l = _softmax_attend(qi[kvh * G:(kvh + 1) * G], keys[:, kvh], vals[:, kvh], scale)
+                # keys: the prefix, then the root-to-node path
+                o, l = _softmax_attend(qi[kvh * G:(kvh + 1) * G], [pk[kvh], kt[:, kvh]], [pv[kvh], vt[:, kvh]], scale)
                 out[b, i, kvh * G:(kvh + 1) * G] = o
                 lse[b, i, kvh * G:(kvh + 1) * G] = l
     return out, lse

@@ -11,6 +11,9 @@ is pinned here against other formulations:
 * a general tree equals ONE masked pass over [prefix | all nodes] with the
   ancestor mask and depth positions (the "Tree Verification" correctness
   condition), computed with torch's masked scaled_dot_product_attention;
+* with ``rotate=False`` (queries and tree keys given already rotated) a
+  general tree is the same one masked pass with no rotation at all, and
+  rotating the inputs first at L + depth reproduces the default;
 * permuting the physical blocks of the paged cache changes nothing;
 * the two mistakes the mask page lists (causal mask over flattened nodes,
   sequential positions) move outputs by far more than the bf16 tolerance, so
@@ -133,6 +136,60 @@ def test_tree_equals_one_masked_pass(seed):
         s = np.where(full[None], s, -np.inf)
         ref_lse = torch.logsumexp(torch.from_numpy(s), dim=-1).numpy()
         np.testing.assert_allclose(lse[b].transpose(1, 0), ref_lse, rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("seed", [15, 16])
+def test_prerotated_inputs_are_one_masked_pass_without_rope(seed):
+    rng = np.random.default_rng(seed)
+    N = int(rng.integers(2, 40))
+    paths = W.random_rank_paths(N, 6, rng)
+    parent, depth, rows, _ = T.build_tree(paths)
+    Hq, Hkv, D = 6, 2, 32
+    lens = [int(x) for x in rng.integers(0, 50, size=2)]
+    inp = _case(2, N, Hq, Hkv, D, lens, 8, seed)
+    out, lse = A.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                inp["seq_lens"], inp["k_tree"], inp["v_tree"], parent, rotate=False)
+    tm = T.dense_mask(rows, N)
+    G = Hq // Hkv
+    for b in range(2):
+        L = lens[b]
+        pk = A.gather_prefix(inp["k_cache"], inp["block_table"][b], L)
+        pv = A.gather_prefix(inp["v_cache"], inp["block_table"][b], L)
+        keys = np.concatenate([pk, np.asarray(inp["k_tree"][b], dtype=np.float64)], 0)
+        vals = np.concatenate([pv, np.asarray(inp["v_tree"][b], dtype=np.float64)], 0)
+        qs = np.asarray(inp["q"][b], dtype=np.float64).transpose(1, 0, 2)
+        full = np.concatenate([np.ones((N, L), dtype=bool), tm], 1)
+        kh = np.repeat(keys.transpose(1, 0, 2), G, 0)
+        vh = np.repeat(vals.transpose(1, 0, 2), G, 0)
+        np.testing.assert_allclose(out[b].transpose(1, 0, 2), _sdpa(qs, kh, vh, mask=full), rtol=0, atol=1e-11)
+        s = np.einsum("hnd,htd->hnt", qs, kh) / np.sqrt(D)
+        ref_lse = torch.logsumexp(torch.from_numpy(np.where(full[None], s, -np.inf)), dim=-1).numpy()
+        np.testing.assert_allclose(lse[b].transpose(1, 0), ref_lse, rtol=0, atol=1e-11)
+    # rotating q and the tree keys at L + depth first gives the default mode
+    pos = np.stack([T.positions(depth, L) for L in lens])                         # [B, N]
+    q_rot = A.rope(inp["q"], pos[:, :, None])
+    kt_rot = A.rope(inp["k_tree"], pos[:, :, None])
+    out2, lse2 = A.tree_attention(q_rot, inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"],
+                                  kt_rot, inp["v_tree"], parent, rotate=False)
+    out1, lse1 = A.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"],
+                                  inp["k_tree"], inp["v_tree"], parent)
+    np.testing.assert_allclose(out2, out1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse1, rtol=0, atol=1e-12)
+
+
+def test_gather_prefix_position_by_position():
+    """Prefix position t is slot t % block_size of block block_table[t // block_size]."""
+    rng = np.random.default_rng(21)
+    nb, Hkv, bs, D = 9, 3, 4, 5
+    cache = rng.standard_normal((nb, Hkv, bs, D))
+    row = rng.permutation(nb)
+    for L in (0, 1, 3, 4, 5, 17, 36):
+        got = A.gather_prefix(cache, row, L)
+        assert got.shape == (L, Hkv, D)
+        for t in range(L):
+            assert np.array_equal(got[t], cache[row[t // bs], :, t % bs, :])
+        heads = A.gather_prefix_heads(cache, row, L)
+        assert np.array_equal(heads, got.transpose(1, 0, 2))
 
 
 def test_block_permutation_invariance():
