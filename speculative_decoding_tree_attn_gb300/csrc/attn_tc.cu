@@ -114,6 +114,7 @@ struct Bars {
   uint64_t s_free[2];
   uint64_t q_full;
   uint64_t sh_stat, sh_read;  // shared units (two-M-tile kernel): M tile 1's part posted / read
+  uint64_t tail_sync;         // tail rows (two-M-tile kernel): the four producer warps' end-of-unit exchange
   uint32_t tmem_base;
   int abort;
 };
@@ -1312,6 +1313,372 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
   }
 }
 
+// ---------------------------------------------------------------- tail rows of the two-M-tile kernel
+//
+// When a (request, KV head) has R = G * N rows just above the 256 that two
+// 128-row M tiles hold (the long-context shape: 33 nodes x 8 heads = 264), a
+// second row group would stream the unit's whole K/V a second time for a few
+// rows, and a third M tile costs as much tensor time as a full one and does
+// not fit in TMEM.  The rows 256 .. R - 1 (at most kTailRows) are instead
+// computed from the K/V tiles already in the stage ring by two warps of
+// their own (the kernel's producer warps 2 and 3; warps 0 and 1 issue all
+// TMA boxes), with warp-level bf16 MMAs (mma.sync m16n8k16, fp32
+// accumulation) in transposed form, so that the tail rows sit on the MMA's
+// 8-wide N side and nothing is padded:
+//   S^T [16 keys x 8 rows]  = K[16 keys x 128] Q_tail^T
+//   O_w^T [128 x 8 rows]   += V[16 keys x 128]^T P^T
+// Tail warp w takes keys 32w .. 32w + 31 of every tile (two 16-key blocks)
+// and keeps its own running maximum and sum over them; the two parts are
+// merged once per unit, in warp order, and the rows are written (or, for a
+// split unit, published and merged) with the same arithmetic as the other
+// rows' memory merge.  A tail warp frees a stage with its own arrival on the
+// stage's empty barrier once its reads of the stage are done, so the ring
+// waits for the tail as it waits for the P V products; the tail warps lag the
+// TMA stream by at most the ring's depth and never hold up a TMA issue.
+constexpr int kTailRows = 8;
+constexpr int kTailWarps = 2;
+constexpr int kTailKeys = kBlk / kTailWarps;  // keys of a tile per tail warp (two 16-key blocks)
+
+struct TailSmem {
+  float m[kTailWarps][kTailRows];                      // per warp at the unit's end: running maximum (log2)
+  float l[kTailWarps][kTailRows];                      //   ... and the sum of its keys' weights
+  float o[kTailWarps][kTailRows][kD];                  //   ... and its unnormalised rows
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// d += A[16 x 16] B[16 x 8], bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held as one 32-bit fragment
+// per lane (row lane / 4, columns 2 (lane % 4), + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// One tail warp's share of the tail rows of the unit in progress.  Lane
+// (g = lane / 4, t = lane % 4) holds, in MMA fragment order: Q of tail row g
+// (the B operand of S^T: d = 16 ks + 2t, +1 and + 8, + 9), and the scores,
+// weights and O^T entries of tail rows 2t and 2t + 1 for keys (or head
+// dimensions) g and g + 8 of each 16-wide block.
+struct TailRowsState {
+  uint32_t qb[8][2];
+  uint64_t mr[2];  // ancestor rows of tail rows 2t, 2t + 1
+  float m_run[2], l[2];
+  float o[8][4];   // O^T block mb: (d 16mb + g, row 2t), (.., row 2t + 1), (d 16mb + g + 8, row 2t), (.., 2t + 1)
+};
+
+// Loads Q of the segment's tail rows (rotated here when Q arrives unrotated)
+// and the tail rows' ancestor rows, and clears the running state.
+template <bool kRope>
+__device__ __forceinline__ void tail_begin(const AttnParams& p, const Segment& s, TailRowsState& ts, int lane,
+                                           int32_t* status) {
+  const int g = lane >> 2, tq = lane & 3;
+  const int ur = kTcMaxRows + g;  // unit row of this lane's Q operand column
+  const bool v = ur < p.R;
+  const int node = v ? ur / p.G : 0;
+  const int64_t orow = ((int64_t)s.b * p.N + node) * p.Hq + s.kvh * p.G + ur % p.G;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.q) + orow * kD);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    ts.qb[ks][0] = v ? __ldg(src + 8 * ks + tq) : 0u;
+    ts.qb[ks][1] = v ? __ldg(src + 8 * ks + tq + 4) : 0u;
+  }
+  const unsigned long long* mrows =
+      reinterpret_cast<const unsigned long long*>(p.mask) + (int64_t)s.b * p.mask_bstride;
+  if constexpr (kRope) {
+    // rotate-half at the node's position with tv_rope_apply's float32
+    // arithmetic and bf16 rounding: element d pairs with d + 64, i.e. word
+    // ks with word ks + 4 of the same lane
+    const int pos = v ? row_pos(__ldg(mrows + node), s.L) : -1;
+    if (pos >= p.rope_max_pos && tq == 0 && status) atomicOr(status, TV_DEV_BAD_POSITION);
+    if (pos >= 0 && pos < p.rope_max_pos) {
+      const float* cs = p.rope_cs + (int64_t)pos * kD;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+        for (int wd = 0; wd < 2; ++wd) {
+          const int k0 = 16 * ks + 2 * tq + 8 * wd;  // frequency of the word's low element
+          const uint32_t lo = ts.qb[ks][wd], hi = ts.qb[ks + 4][wd];
+          float a0, b0, a1, b1;
+          rope_pair(__uint_as_float(lo << 16), __uint_as_float(hi << 16), __ldg(cs + k0), __ldg(cs + kD / 2 + k0), a0,
+                    b0);
+          rope_pair(__uint_as_float(lo & 0xffff0000u), __uint_as_float(hi & 0xffff0000u), __ldg(cs + k0 + 1),
+                    __ldg(cs + kD / 2 + k0 + 1), a1, b1);
+          ts.qb[ks][wd] = pack_bf16(a0, a1);
+          ts.qb[ks + 4][wd] = pack_bf16(b0, b1);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int r = kTcMaxRows + 2 * tq + j;
+    ts.mr[j] = r < p.R ? __ldg(mrows + r / p.G) : 0ull;
+    ts.m_run[j] = -INFINITY;
+    ts.l[j] = 0.f;
+  }
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ts.o[mb][e] = 0.f;
+}
+
+// Tile t of the segment from the stage at kb (K) / vb (V): S^T of this
+// warp's 32 keys, online softmax over them, O^T += V^T P^T.
+__device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s, int t, uint32_t kb, uint32_t vb,
+                                          TailRowsState& ts, int w, int lane) {
+  const int g = lane >> 2, tq = lane & 3, i8 = lane >> 3;
+  // S^T per 16-key block: A = K rows x 16 head dims per step, by ldmatrix:
+  // matrices (keys 0-7 | 8-15) x (dims 0-7 | 8-15) of the step, lane
+  // i8 * 8 + r addressing row r of matrix i8; four accumulators per block
+  // (steps ks, ks + 4 chained) so that MMA latency overlaps
+  float sv[2][4];
+  {
+    float acc[2][4][4];
+#pragma unroll
+    for (int kb2 = 0; kb2 < 2; ++kb2)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[kb2][c][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int kb2 = 0; kb2 < 2; ++kb2) {
+        const int key = kTailKeys * w + 16 * kb2 + (lane & 7) + 8 * (i8 & 1);
+        uint32_t a[4];
+        ldsm_x4(kb + key * 128 + (ks >> 2) * kKVHalfBytes + (((2 * (ks & 3) + (i8 >> 1)) ^ (key & 7)) << 4), a);
+        mma_m16n8k16(acc[kb2][ks & 3], a, ts.qb[ks][0], ts.qb[ks][1]);
+      }
+    }
+#pragma unroll
+    for (int kb2 = 0; kb2 < 2; ++kb2)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sv[kb2][e] = (acc[kb2][0][e] + acc[kb2][1][e]) + (acc[kb2][2][e] + acc[kb2][3][e]);
+  }
+  // sv[kb2]: (key k, row 2t), (k, 2t + 1), (k + 8, 2t), (k + 8, 2t + 1), k = 32w + 16 kb2 + g
+#pragma unroll
+  for (int kb2 = 0; kb2 < 2; ++kb2) {
+    const int k0 = kTailKeys * w + 16 * kb2 + g, k1 = k0 + 8;
+    if (t == s.n - 1) {
+      if (!(k0 < p.N && ((ts.mr[0] >> k0) & 1ull))) sv[kb2][0] = -INFINITY;
+      if (!(k0 < p.N && ((ts.mr[1] >> k0) & 1ull))) sv[kb2][1] = -INFINITY;
+      if (!(k1 < p.N && ((ts.mr[0] >> k1) & 1ull))) sv[kb2][2] = -INFINITY;
+      if (!(k1 < p.N && ((ts.mr[1] >> k1) & 1ull))) sv[kb2][3] = -INFINITY;
+    } else {
+      const int lim = s.L - t * kBlk;
+      if (k0 >= lim) sv[kb2][0] = sv[kb2][1] = -INFINITY;
+      if (k1 >= lim) sv[kb2][2] = sv[kb2][3] = -INFINITY;
+    }
+  }
+  float mx[2] = {fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2])),
+                 fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]))};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
+    mx[j] *= p.scale_log2;
+  }
+  float m_use[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float m_new = fmaxf(ts.m_run[j], mx[j]);
+    if (m_new > ts.m_run[j] + kRescaleThreshold) {
+      const float al = exp2f(ts.m_run[j] - m_new);
+      ts.l[j] *= al;
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        ts.o[mb][j] *= al;
+        ts.o[mb][2 + j] *= al;
+      }
+      ts.m_run[j] = m_new;
+    }
+    m_use[j] = ts.m_run[j] == -INFINITY ? 0.f : ts.m_run[j];
+  }
+  float pv[2][4];
+#pragma unroll
+  for (int kb2 = 0; kb2 < 2; ++kb2)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pv[kb2][e] = fast_exp2(fmaf(sv[kb2][e], p.scale_log2, -m_use[e & 1]));
+  ts.l[0] += (pv[0][0] + pv[0][2]) + (pv[1][0] + pv[1][2]);
+  ts.l[1] += (pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]);
+  // P^T as the B operand of O^T: the weights of (key g | g + 8, rows 2t,
+  // 2t + 1), packed as bf16 pairs, are 8x8 fragments of P[key][row];
+  // movmatrix transposes them in registers to P[row g][keys 2t, 2t + 1]
+  // (resp. 8 + 2t, 9 + 2t), the B fragment layout
+  uint32_t bp[2][2];
+#pragma unroll
+  for (int kb2 = 0; kb2 < 2; ++kb2) {
+    bp[kb2][0] = movmatrix_trans(pack_bf16(pv[kb2][0], pv[kb2][1]));
+    bp[kb2][1] = movmatrix_trans(pack_bf16(pv[kb2][2], pv[kb2][3]));
+  }
+  // O^T: A = V^T (16 head dims x 16 keys) by transposing ldmatrix of the V
+  // rows: matrices (dims 0-7 | 8-15) x (keys 0-7 | 8-15)
+#pragma unroll
+  for (int kb2 = 0; kb2 < 2; ++kb2) {
+    const int key = kTailKeys * w + 16 * kb2 + (lane & 7) + 8 * (i8 >> 1);
+    const uint32_t row = vb + key * 128;
+    const int sw = key & 7;
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      uint32_t a[4];
+      ldsm_x4_trans(row + (mb >> 2) * kKVHalfBytes + (((2 * (mb & 3) + (i8 & 1)) ^ sw) << 4), a);
+      mma_m16n8k16(ts.o[mb], a, bp[kb2][0], bp[kb2][1]);
+    }
+  }
+}
+
+// End of a segment: the tail warps' parts are merged (warp order) and the
+// tail rows written; a split unit publishes its part and the piece that
+// completes the rows' arrival counts merges them from memory, with the
+// arithmetic of the other rows' memory merge.  Collective over the tail
+// warps (two passes of the tail_sync barrier).
+__device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& sp, const Segment& s, TailRowsState& ts,
+                                         TailSmem* sm, Bars& bars, uint32_t& tb, int w, int lane, int32_t* status) {
+  constexpr float kLn2 = 0.69314718055994530942f;
+  constexpr int kThreadsPerRow = 32 * kTailWarps / kTailRows;
+  constexpr int kCols = kD / kThreadsPerRow;  // head dims per thread in the merge
+  static_assert(kCols == 16, "the merge below handles 16 head dims per thread");
+  const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) ts.l[j] += __shfl_xor_sync(0xffffffffu, ts.l[j], off);
+  if (g == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      sm->m[w][2 * tq + j] = ts.m_run[j];
+      sm->l[w][2 * tq + j] = ts.l[j];
+    }
+  }
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sm->o[w][2 * tq + (e & 1)][16 * mb + g + 8 * (e >> 1)] = ts.o[mb][e];
+  mbar_arrive(&bars.tail_sync);
+  if (!mbar_wait_warp(&bars.tail_sync, tb & 1, &bars, status)) return false;
+  ++tb;
+  // thread i of the tail warps: tail row i / 8, head dims (i % 8) * 16 .. + 15
+  const int i = w * 32 + lane;
+  const int r = i / kThreadsPerRow, d0 = (i % kThreadsPerRow) * kCols;
+  const int ur = kTcMaxRows + r;
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kTailWarps; ++q) M = fmaxf(M, sm->m[q][r]);
+  float a[kTailWarps], l = 0.f;
+#pragma unroll
+  for (int q = 0; q < kTailWarps; ++q) {
+    a[q] = M == -INFINITY ? 0.f : exp2f(sm->m[q][r] - M);
+    l = fmaf(a[q], sm->l[q][r], l);
+  }
+  float v[kCols];
+#pragma unroll
+  for (int j = 0; j < kCols; ++j) {
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kTailWarps; ++q) acc = fmaf(a[q], sm->o[q][r][d0 + j], acc);
+    v[j] = acc;
+  }
+  // the scratch may be reused once every tail thread has read it
+  mbar_arrive(&bars.tail_sync);
+  const float inv = l > 0.f ? 1.f / l : 0.f;  // no key at all: zero row
+#pragma unroll
+  for (int j = 0; j < kCols; ++j) v[j] *= inv;
+  const float lse2 = M + log2f(l);
+  const bool valid = ur < p.R;
+  const int node = valid ? ur / p.G : 0;
+  const int64_t orow = ((int64_t)s.b * p.N + node) * p.Hq + s.kvh * p.G + ur % p.G;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  const bool lead = (lane % kThreadsPerRow) == 0;
+  if (s.a == 0 && s.e == s.n) {
+    if (valid) {
+      store_bf16_16(out + orow * kD + d0, v);
+      if (lead && p.lse) p.lse[orow] = lse2 * kLn2;
+    }
+  } else {
+    const Pieces pc(sp, s.real_start, s.n);
+    const uint32_t mine = (uint32_t)(s.e - s.a);
+    const int64_t srow = pc.slot(blockIdx.x) * p.RPG + ur;
+    if (valid) {
+      float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + d0);
+#pragma unroll
+      for (int j = 0; j < kCols / 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      if (lead) p.part_lse[srow] = lse2;
+    }
+    __threadfence();
+    __syncwarp();
+    bool last = false;
+    if (valid && lead) last = atom_add_acq_rel(p.arrive + (int64_t)pc.c0 * p.RPG + ur, mine) + mine == (uint32_t)s.n;
+    last = __shfl_sync(0xffffffffu, last, lane & ~(kThreadsPerRow - 1));
+    if (last) {
+      __threadfence();
+      float mx, z;
+      piece_stats<false>(p, pc, -1, 0.f, ur, mx, z);
+      float acc[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
+      accum_pieces<false>(acc, p, pc, -1, acc, 0.f, ur, d0, mx, 1.f / z);
+      store_bf16_16(out + orow * kD + d0, acc);
+      if (lead && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+    }
+  }
+  const bool ok = mbar_wait_warp(&bars.tail_sync, tb & 1, &bars, status);
+  ++tb;
+  return ok;
+}
+
+// A tail warp's loop: every tile of the CTA's slice, in ring order, after
+// the TMA producers' loads land; the stage is freed after the warp's reads.
+template <int kStages, bool kRope>
+__device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& sp, Bars& bars, uint32_t sK, uint32_t sV,
+                                         TailSmem* tsm, int w, int lane, int32_t* status) {
+  uint32_t g = 0, tb = 0;
+  bool ok = true;
+  Walk walk(sp);
+  Segment s;
+  TailRowsState ts;
+  while (ok && walk.next(p, s)) {
+    tail_begin<kRope>(p, s, ts, lane, status);
+    for (int t = s.a; t < s.e; ++t, ++g) {
+      const int stage = g % kStages;
+      ok = mbar_wait_warp(&bars.kv_full[stage], (g / kStages) & 1, &bars, status);
+      if (!ok) break;
+      tail_tile(p, s, t, sK + stage * kKVTileBytes, sV + stage * kKVTileBytes, ts, w, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.kv_empty[stage]);
+    }
+    if (!ok) break;
+    ok = tail_end(p, sp, s, ts, tsm, bars, tb, w, lane, status);
+  }
+}
+
 // ---------------------------------------------------------------- two M tiles (up to 256 rows)
 //
 // Every operand placement is chosen so that no single resource is on the
@@ -1323,11 +1690,16 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
 //  * TMEM (512 columns) holds S_0 S_1 P_0 P_1 Q_0 O_0 O_1 = 64+64+32+32+64+128+128;
 //    Q_1 therefore stays in shared memory (S_1 = Q_1 K^T reads both operands
 //    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
-struct PairCfg {
-  static constexpr int kStages = 6;
-  // Warps 0-3 issue TMA, 4-7 issue MMAs (S_0, S_1, PV_0, PV_1), 8-15 are the
-  // two softmax warpgroups: warp w runs on sub-partition w % 4, so each
-  // sub-partition carries one producer, one issuer and two softmax warps.
+template <bool kTail>
+struct PairCfgT {
+  // Five K/V stages (measured 1-3 % faster than six on the 64-request and
+  // long-context shapes); the shared memory left holds the tail rows'
+  // end-of-unit scratch.
+  static constexpr int kStages = 5;
+  // Warps 0-3 issue TMA (and, with tail rows, compute them), 4-7 issue MMAs
+  // (S_0, S_1, PV_0, PV_1), 8-15 are the two softmax warpgroups: warp w runs
+  // on sub-partition w % 4, so each sub-partition carries one producer, one
+  // issuer and two softmax warps.
   static constexpr int kProducers = 4;
   static constexpr int kThreads = 32 * 16;
   static constexpr int kAllocWarp = 4;
@@ -1335,7 +1707,8 @@ struct PairCfg {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
   static constexpr int kOffQ1 = kOffV + kStages * kKVTileBytes;  // 2 halves x 128 rows x 128 B
-  static constexpr int kBytes = kOffQ1 + 2 * 128 * 128;
+  static constexpr int kOffTail = kOffQ1 + 2 * 128 * 128;
+  static constexpr int kBytes = kOffTail + (kTail ? (int)sizeof(TailSmem) : 0);
   static constexpr int kSmem = kBytes + 1024;
   static constexpr uint32_t col_s(int m) { return m * 64; }
   static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
@@ -1343,6 +1716,9 @@ struct PairCfg {
   static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
   static constexpr int kSoftmaxWarp0 = 8;
 };
+using PairCfg = PairCfgT<false>;
+static_assert(PairCfgT<true>::kSmem <= 227 * 1024 - 1024, "the tail variant fits the opt-in shared memory");
+static_assert(PairCfgT<true>::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 static_assert(PairCfg::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 
 // The unit is the last row group of a (request, KV head) with at most 128
@@ -1366,10 +1742,11 @@ __device__ __forceinline__ bool shared_unit(const AttnParams& p, const Segment& 
 // shared units alone and M tile 1's part is empty.
 constexpr bool kSplitKeys = false;
 __device__ __forceinline__ int sh_owner(int t) { return kSplitKeys ? (t & 1) : 0; }
-template <bool kRope, bool kSkip>
+template <bool kRope, bool kSkip, bool kTail>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
-  using C = PairCfg;
+  using C = PairCfgT<kTail>;
+  static_assert(!(kSkip && kTail), "tail rows replace the second row group");
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   __shared__ float s_sh[kSkip ? 256 : 1];  // shared units: M tile 1's running max and sum per row
@@ -1387,7 +1764,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 2);  // one commit from each O issuer
+      mbar_init(&bars.kv_empty[s], kTail ? 2 + kTailWarps : 2);  // one commit from each O issuer (+ the tail warps)
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(&bars.s_full[m], 1);
@@ -1398,6 +1775,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     mbar_init(&bars.q_full, 256);
     mbar_init(&bars.sh_stat, 128);
     mbar_init(&bars.sh_read, 128);
+    mbar_init(&bars.tail_sync, 32 * kTailWarps);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1414,7 +1792,17 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   constexpr uint32_t hi = desc_hi(1024);
 
   if (warp < C::kProducers) {
-    run_producer<C::kStages, C::kProducers>(p, sp, maps, bars, sK, sV, lane, status, warp);
+    if constexpr (kTail) {
+      // warps 0-1 issue every TMA box; warps 2-3 compute the tail rows
+      if (warp < C::kProducers - kTailWarps) {
+        run_producer<C::kStages, C::kProducers - kTailWarps>(p, sp, maps, bars, sK, sV, lane, status, warp);
+      } else {
+        TailSmem* tsm = reinterpret_cast<TailSmem*>(smem_raw + (base - raw) + C::kOffTail);
+        run_tail<C::kStages, kRope>(p, sp, bars, sK, sV, tsm, warp - (C::kProducers - kTailWarps), lane, status);
+      }
+    } else {
+      run_producer<C::kStages, C::kProducers>(p, sp, maps, bars, sK, sV, lane, status, warp);
+    }
   } else if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ S_m = Q_m K^T issuer
     const int m = warp - 4;
@@ -1819,12 +2207,13 @@ int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStrea
   return TV_OK;
 }
 
-template <bool kRope, bool kSkip>
+template <bool kRope, bool kSkip, bool kTail>
 int launch_pair(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PairCfg::kSmem);
+  constexpr int smem = PairCfgT<kTail>::kSmem;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip, kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
-  attn_tc_pair_kernel<kRope, kSkip><<<p.P, PairCfg::kThreads, PairCfg::kSmem, stream>>>(p, maps, status);
+  attn_tc_pair_kernel<kRope, kSkip, kTail><<<p.P, PairCfg::kThreads, smem, stream>>>(p, maps, status);
   TV_LAUNCH_CHECK("attn_tc_pair_kernel");
   return TV_OK;
 }
@@ -1842,7 +2231,7 @@ const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim
   if (block_size % 16 || !(kBlk % block_size == 0 || block_size % kBlk == 0))
     return "block_size is not a multiple of 16 that divides or is divisible by 64";
   // dynamic ring + barriers + the shared-unit statistics + the slice plan
-  if (dev.max_smem_optin < (size_t)PairCfg::kSmem + sizeof(Bars) + 256 * sizeof(float) + 64)
+  if (dev.max_smem_optin < (size_t)PairCfgT<true>::kSmem + sizeof(Bars) + 256 * sizeof(float) + 64)
     return "not enough opt-in shared memory";
   return nullptr;
 }
@@ -1851,7 +2240,12 @@ bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int 
   return tc_unsupported_reason(dev, dtype, head_dim, rows, G, block_size, rope) == nullptr;
 }
 
-int tc_rows_per_unit(int rows) { return rows <= 128 ? 128 : 256; }
+int tc_rows_per_unit(int rows) {
+  if (rows <= 128) return 128;
+  if (rows <= kTcMaxRows) return kTcMaxRows;
+  // up to kTailRows rows past the two M tiles: one unit holds them all (tail rows)
+  return rows <= kTcMaxRows + kTailRows ? rows : kTcMaxRows;
+}
 
 int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : 1; }
 
@@ -1904,11 +2298,15 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
   }
   if (p.RPG <= 128)
     return p.rope_cs ? launch_m<1, true>(p, maps, status, stream) : launch_m<1, false>(p, maps, status, stream);
-  if (p.rope_cs) return launch_pair<true, false>(p, maps, status, stream);
+  // rows past the two M tiles computed beside them (tc_rows_per_unit gave the unit all R rows)
+  if (p.RPG > kTcMaxRows)
+    return p.rope_cs ? launch_pair<true, false, true>(p, maps, status, stream)
+                     : launch_pair<false, false, true>(p, maps, status, stream);
+  if (p.rope_cs) return launch_pair<true, false, false>(p, maps, status, stream);
   // a last row group of at most 128 rows leaves M tile 1 idle: skip it
   const int tail = p.R % p.RPG;
-  if (p.R > p.RPG && tail > 0 && tail <= 128) return launch_pair<false, true>(p, maps, status, stream);
-  return launch_pair<false, false>(p, maps, status, stream);
+  if (p.R > p.RPG && tail > 0 && tail <= 128) return launch_pair<false, true, false>(p, maps, status, stream);
+  return launch_pair<false, false, false>(p, maps, status, stream);
 }
 
 }  // namespace tv

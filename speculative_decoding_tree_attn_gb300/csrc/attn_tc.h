@@ -19,7 +19,9 @@ bool tc_supported(const DeviceInfo& dev, int dtype, int head_dim, int rows, int 
 const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size,
                                   bool rope);
 
-// Rows per unit for `rows` = G * N query rows per KV head (128 or 256).
+// Rows per unit for `rows` = G * N query rows per KV head: 128, 256, or all
+// of them when they exceed 256 by at most 8 (those tail rows are computed
+// beside the two M tiles, so the unit's K/V is read once).
 int tc_rows_per_unit(int rows);
 
 // Resident CTAs per SM the kernel is built for at this row count.
