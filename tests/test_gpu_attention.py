@@ -1,18 +1,24 @@
 """GPU parity of the tree-attention path (tree_build -> tree_mask -> rope_apply
 -> tree_attn_verify) against the float64 per-path oracle.
 
-Tolerances are the ones fixed for this path: max-abs 1e-4 for float32 inputs
-and 2e-2 for bf16 inputs (float32 accumulation).  Both kernels are covered:
-the CUDA-core kernel for every shape, the tcgen05 kernel for the shapes it
-accepts.  Small cases compare every output; the full-size workloads compare
-sampled requests (shortest and longest prefix included) in the launch
-configuration the bench times."""
+Output tolerances are the ones fixed for this path: max-abs 1e-4 for float32
+inputs and 2e-2 for bf16 inputs (float32 accumulation).  Every case is run
+twice: the whole path, whose log-sum-exp is held to the bound the input-
+precision rounding of the rotated rows allows (gpu_helpers.lse_pipeline_bound),
+and the attention kernel alone on rows the oracle rotated, whose log-sum-exp
+is held to the kernel's own float32 error (gpu_helpers.LSE_TOL).  Both
+kernels are covered: the CUDA-core kernel for every shape, the tcgen05 kernel
+for the shapes it accepts.  Small cases compare every output; the full-size
+workloads compare every node of several requests (shortest and longest
+prefix and split units included) in the launch configuration the bench
+times."""
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import BF16_TOL, F32_TOL, gpu_pipeline, max_err, oracle_rows, to_np
+from gpu_helpers import (BF16_TOL, F32_TOL, LSE_TOL, check_lse_within, gpu_attention, gpu_pipeline, lse_err,
+                         lse_pipeline_bound, max_err, oracle_rows, prerotated, to_np)
 from oracle import tree as OT
 from speculative_decoding_tree_attn_gb300 import capi
 from speculative_decoding_tree_attn_gb300 import workloads as W
@@ -34,16 +40,23 @@ def _workload(B, Hq, Hkv, D, dtype, bs, N, seed):
     return W.Workload("case", B, Hq, Hkv, D, dtype, ("fixed", 0), bs, (0.7, 0.15), N, 8, seed)
 
 
-def _check_all(inp, paths, tol, flags, num_ctas=0):
+def _check_all(inp, paths, tol, flags, num_ctas=0, pairs=None):
+    """The whole path and the kernel alone (module docstring) on `pairs`
+    (default: every node of every request)."""
     B, N = inp["q"].shape[:2]
-    pairs = [(b, i) for b in range(B) for i in range(N)]
+    pairs = [(b, i) for b in range(B) for i in range(N)] if pairs is None else pairs
     out, lse = gpu_pipeline(inp, paths, flags=flags, num_ctas=num_ctas, want_lse=True)
     ref = oracle_rows(inp, paths, pairs)
     err = max_err(out, ref, pairs)
     assert err <= tol, err
-    lse_g = to_np(lse)
-    lerr = max(float(np.abs(lse_g[b, i] - ref[(b, i)][1]).max()) for b, i in pairs)
-    assert lerr <= 20 * tol, lerr
+    check_lse_within(lse, ref, pairs, lse_pipeline_bound(inp, pairs))
+    rot = prerotated(inp, paths)
+    out_k, lse_k = gpu_attention(rot, paths, flags=flags, num_ctas=num_ctas)
+    ref_k = oracle_rows(rot, paths, pairs, rotate=False)
+    err_k = max_err(out_k, ref_k, pairs)
+    assert err_k <= tol, err_k
+    lerr = lse_err(lse_k, ref_k, pairs)
+    assert lerr <= LSE_TOL[inp["q"].dtype], lerr
     return out
 
 
@@ -193,7 +206,9 @@ def test_split_unit_merge_routes(G, N):
     the plan so that some slices are empty).  The tensor-core kernel merges a
     split row either in the last piece straight from its accumulator, or from
     every piece's published partial (forced by TV_ATTN_PUBLISH_ALL); both
-    routes must match the oracle and each other bit for bit."""
+    routes must match the oracle (outputs, and the log-sum-exp at the
+    kernel's own error on pre-rotated rows, where a wrong merge weight would
+    show) and each other bit for bit."""
     if not tc_available(2 * G, 2, N):
         pytest.skip("tensor-core kernel unavailable for this shape")
     rng = np.random.default_rng(140 + G + N)
@@ -201,18 +216,24 @@ def test_split_unit_merge_routes(G, N):
     for lens, grids in (([3000, 70, 1500], (2, 7, 40, 152)), ([70, 0, 10], (300,))):
         w = _workload(3, 2 * G, 2, 128, "bf16", 16, N, 141 + N)
         inp = W.attention_inputs(w, device="cuda", seq_lens=lens)
+        rot = prerotated(inp, paths)
         pairs = [(b, i) for b in range(3) for i in range(N)]
         ref = oracle_rows(inp, paths, pairs)
+        ref_k = oracle_rows(rot, paths, pairs, rotate=False)
+        bound = lse_pipeline_bound(inp, pairs)
         for num_ctas in grids:
             res = []
             for extra in (0, capi.TV_ATTN_PUBLISH_ALL):
-                out, lse = gpu_pipeline(inp, paths, flags=capi.TV_ATTN_TCGEN05 | extra, num_ctas=num_ctas,
-                                        want_lse=True)
+                flags = capi.TV_ATTN_TCGEN05 | extra
+                out, lse = gpu_pipeline(inp, paths, flags=flags, num_ctas=num_ctas, want_lse=True)
                 assert max_err(out, ref, pairs) <= BF16_TOL, (lens, num_ctas, extra)
-                lse_g = to_np(lse)
-                assert max(float(np.abs(lse_g[b, i] - ref[(b, i)][1]).max()) for b, i in pairs) <= 20 * BF16_TOL
-                res.append((out, lse))
-            assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1]), (lens, num_ctas)
+                check_lse_within(lse, ref, pairs, bound)
+                out_k, lse_k = gpu_attention(rot, paths, flags=flags, num_ctas=num_ctas)
+                assert max_err(out_k, ref_k, pairs) <= BF16_TOL, (lens, num_ctas, extra)
+                assert lse_err(lse_k, ref_k, pairs) <= LSE_TOL[torch.bfloat16], (lens, num_ctas, extra)
+                res.append((out, lse, out_k, lse_k))
+            for a, b in zip(res[0], res[1]):
+                assert torch.equal(a, b), (lens, num_ctas)
 
 
 def test_deterministic_and_kernel_agreement():
@@ -243,20 +264,49 @@ def test_workspace_errors():
 FULL = ["gqa_b8_l512_2048_n26", "b64_l1k_8k_n64_greedy", "long_b16_l32k_n33", "b256_l2k_4k_n10_sample"]
 
 
+def _split_requests(lens, w, P):
+    """Requests with a unit whose real tiles are cut by a slice boundary of
+    the tensor-core plan (P slices of equal tile counts over the units laid
+    end to end, each unit's virtual start tiles first), as the kernel derives
+    it."""
+    rows = (w.Hq // w.Hkv) * w.n_nodes
+    cost = 3 if rows <= 128 else 8
+    tiles = [(int(L) + 63) // 64 + 1 + cost for L in lens]
+    T = sum(t * w.Hkv for t in tiles)
+    P = max(1, min(P, (T + 11) // 12))
+    bounds = {c * T // P for c in range(1, P)}
+    out, start = set(), 0
+    for b, t in enumerate(tiles):
+        for _ in range(w.Hkv):
+            if any(start + cost < x < start + t for x in bounds):
+                out.add(b)
+            start += t
+    return sorted(out)
+
+
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
+def test_full_size_all_nodes_of_sampled_requests(name):
     """Full workloads in the bench's launch configuration (auto kernel, one
-    wave); sampled requests incl. the shortest and longest prefix."""
+    wave): every node and head of several requests -- the shortest and the
+    longest prefix, requests with a unit split across CTAs, random others --
+    on the whole path and on the kernel alone (module docstring)."""
     w = W.WORKLOADS[name]
     inp = W.attention_inputs(w, device="cuda")
     paths = w.paths()
-    out, _ = gpu_pipeline(inp, paths)
     lens = inp["seq_lens"].cpu().numpy()
     rng = np.random.default_rng(100)
-    bs = sorted({int(lens.argmin()), int(lens.argmax()), *rng.integers(0, w.B, size=2).tolist()})
-    N = w.n_nodes
-    nodes = sorted({0, N - 1, *rng.integers(0, N, size=3).tolist()})
-    pairs = [(b, i) for b in bs for i in nodes]
-    ref = oracle_rows(inp, paths, pairs)
-    assert max_err(out, ref, pairs) <= BF16_TOL
-    assert torch.isfinite(out.float()).all()
+    n_req = 5 if w.prefix[0] == "fixed" and w.prefix[1] >= 16384 else 8
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = (w.Hq // w.Hkv) * w.n_nodes
+    split = _split_requests(lens, w, sms * (2 if rows <= 128 else 1))
+    bs = [int(lens.argmin()), int(lens.argmax())]
+    bs += [b for b in split[:2] if b not in bs]
+    for b in rng.permutation(w.B).tolist():
+        if len(bs) >= n_req:
+            break
+        if b not in bs:
+            bs.append(int(b))
+    if w.B > 2:
+        assert any(b in split for b in bs), "no request with a split unit sampled"
+    pairs = [(b, i) for b in sorted(bs) for i in range(w.n_nodes)]
+    _check_all(inp, paths, BF16_TOL, capi.TV_ATTN_AUTO, pairs=pairs)

@@ -65,8 +65,13 @@ def test_rope_table_matches_oracle():
     np.testing.assert_allclose(cs[pos, 1], np.sin(ang), rtol=0, atol=1.2e-7)
 
 
-@pytest.mark.parametrize("dtype,tol", [(torch.float32, 2e-6), (torch.bfloat16, 2e-2)])
-def test_rope_apply_matches_oracle(dtype, tol):
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_rope_apply_matches_oracle(dtype):
+    """Each rotated element is the exact rotation rounded to the input
+    precision: |gpu - oracle| <= u |oracle| (u = 2^-8 for bf16, 2^-24 for
+    float32) plus the float32 rotation's own error, at most 2^-21 of the
+    pair's magnitude |x1| + |x2| (two products of a float32 table entry,
+    itself within 2^-24, and one rounded sum)."""
     g = torch.Generator(device="cuda").manual_seed(41)
     B, N, Hq, Hkv, D = 3, 7, 8, 2, 128
     q = torch.randn(B, N, Hq, D, device="cuda", generator=g).to(dtype)
@@ -78,8 +83,14 @@ def test_rope_apply_matches_oracle(dtype, tol):
     P = pos.cpu().numpy()
     ref_q = OA.rope(q.float().cpu().numpy(), P[..., None])
     ref_k = OA.rope(kt.float().cpu().numpy(), P[..., None])
-    np.testing.assert_allclose(q2.float().cpu().numpy(), ref_q, rtol=0, atol=tol * 4)
-    np.testing.assert_allclose(k2.float().cpu().numpy(), ref_k, rtol=0, atol=tol * 4)
+    u = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -24
+    for x, got, ref in ((q, q2, ref_q), (kt, k2, ref_k)):
+        x = x.double().cpu().numpy()
+        half = x.shape[-1] // 2
+        pair = np.abs(x[..., :half]) + np.abs(x[..., half:])
+        bound = u * np.abs(ref) + 2.0 ** -21 * np.concatenate([pair, pair], axis=-1)
+        err = np.abs(got.double().cpu().numpy() - ref)
+        assert (err <= bound).all(), float((err - bound).max())
 
 
 def test_rope_apply_bad_position_flag():
