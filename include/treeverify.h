@@ -312,7 +312,9 @@ int tv_tree_attn_verify_rope(const void* q, const void* k_cache, const void* v_c
  *            shape whose plan alone does not fit, returns TV_ERR_WORKSPACE.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  The call allocates nothing (no cudaMalloc / cudaFree).  Every call
+ * capture.  After a cudaDeviceReset the next call looks the address up again
+ * (the device's context has changed), so make that call outside a capture
+ * too.  The call allocates nothing (no cudaMalloc / cudaFree).  Every call
  * uses the same array, so calls that can overlap on the GPU (different
  * streams, or graphs replayed concurrently) race and must be serialised by the
  * caller; the array needs no clearing between calls (everything read is
@@ -420,15 +422,19 @@ int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,
  *                   blocks for positions up to L_b + n_out[b] - 1.
  * seq_lens          device int32 [B]: L_b (read).
  * new_seq_lens      device int32 [B] out (nullable, must not alias
- *                   seq_lens): L_b + n_out[b].
+ *                   seq_lens): L_b + n_out[b], or L_b + j when step j is the
+ *                   first that cannot be committed (below).
  * k_tree, v_tree    device [B, N, Hkv, D] (dtype).
  * path              device int32 [B, path_cols]: the accepted path as
  *                   tv_tree_accept_* return it (node indices, root first).
  * n_out             device int32 [B]: path length per request (values are
  *                   clamped to [0, path_cols]).
- * A node index outside [0, N) is skipped and flags TV_DEV_BAD_TOPOLOGY; a
- * position beyond the block table, or a table entry outside
- * [0, num_blocks), is skipped and flags TV_DEV_OUT_OVERFLOW.  D * element
+ * The first path step whose node index is outside [0, N) (TV_DEV_BAD_TOPOLOGY)
+ * or whose position is beyond the block table or maps to a table entry
+ * outside [0, num_blocks) (TV_DEV_OUT_OVERFLOW) ends the commit: the steps
+ * before it are copied, nothing from it on, and new_seq_lens counts only
+ * the copied steps, so the next step never treats unwritten slots as
+ * prefix.  D * element
  * size must be a multiple of 16 bytes and the K/V buffers 16-byte aligned.
  * No page defines a separate entry point: it is the copy the mask page's
  * serving loop performs after acceptance.

@@ -20,6 +20,12 @@ j, i.e. at position ``L_b + j``.  Committing copies tree row
 stores them rotated at ``L_b + depth``, which is their cache position).
 The token emitted after the last path node has no K/V yet: it is the next
 step's root.
+
+The pages define no failure; the library's reading (``stop_at_bad=True``):
+a path step that cannot be committed -- a node outside the tree, a
+position without a block in the table (or a table entry outside the
+cache) -- ends the committed prefix there, so the prefix length never counts
+a slot that was not written.
 """
 
 from __future__ import annotations
@@ -27,13 +33,14 @@ from __future__ import annotations
 import numpy as np
 
 
-def commit_path(k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, path, n_out):
+def commit_path(k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, path, n_out, stop_at_bad=False):
     """Returns (k_cache', v_cache', seq_lens') with the accepted rows copied in.
 
     k_cache, v_cache [num_blocks, Hkv, block_size, D]; block_table
     [B, max_blocks]; seq_lens [B]; k_tree, v_tree [B, N, Hkv, D]; path
     [B, cols] node indices; n_out [B].  Raises if a position does not fit the
-    block table.
+    block table, unless ``stop_at_bad``: then the first step that cannot be
+    committed ends the request's commit (module docstring).
     """
     kc = np.array(k_cache, copy=True)
     vc = np.array(v_cache, copy=True)
@@ -41,13 +48,18 @@ def commit_path(k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, path, n
     bs = kc.shape[2]
     for b in range(lens.size):
         L = int(seq_lens[b])
+        done = int(n_out[b])
         for j in range(int(n_out[b])):
             node = int(path[b, j])
             t = L + j
+            fits = t // bs < block_table.shape[1] and 0 <= int(block_table[b, t // bs]) < kc.shape[0]
+            if stop_at_bad and not (0 <= node < k_tree.shape[1] and fits):
+                done = j
+                break
             if t // bs >= block_table.shape[1]:
                 raise ValueError(f"request {b}: position {t} beyond its block table")
             blk = int(block_table[b, t // bs])
             kc[blk, :, t % bs, :] = k_tree[b, node]
             vc[blk, :, t % bs, :] = v_tree[b, node]
-        lens[b] = L + int(n_out[b])
+        lens[b] = L + done
     return kc, vc, lens

@@ -8,6 +8,10 @@
 // cache position L_b + j; its tree K/V rows (every KV head, stored rotated at
 // that position) are copied into block block_table[b, (L_b + j) / block_size],
 // slot (L_b + j) % block_size, and the prefix length becomes L_b + n_out[b].
+// A path step that cannot be committed (a node outside the tree, a position
+// without a valid block) ends the committed prefix there: the steps before it
+// are copied, the prefix length becomes L_b + (that step's index), and the
+// step's reason is flagged; nothing past it is written.
 //
 // Pure copy work: one CTA per request, its threads over the 16-byte chunks of
 // the request's (path step, KV head) rows of K and of V; consecutive threads
@@ -30,9 +34,28 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(char* __restrict__ kc, c
   const int b = blockIdx.x;
   const int chunks = row_bytes / 16;
   const int L = seq_lens[b];
-  int n = n_out[b];
-  n = n < 0 ? 0 : (n > path_cols ? path_cols : n);
-  if (new_lens && threadIdx.x == 0) new_lens[b] = L + n;
+  __shared__ int s_n;
+  if (threadIdx.x == 0) {
+    // the committed prefix ends at the first step that cannot be committed
+    int n = n_out[b];
+    n = n < 0 ? 0 : (n > path_cols ? path_cols : n);
+    for (int j = 0; j < n; ++j) {
+      const int node = path[(int64_t)b * path_cols + j];
+      const int64_t col = ((int64_t)L + j) / bs;
+      const int64_t blk = (L >= 0 && col < max_blocks) ? table[(int64_t)b * max_blocks + col] : -1;
+      const int bad = (node < 0 || node >= N) ? TV_DEV_BAD_TOPOLOGY
+                                               : ((blk < 0 || blk >= num_blocks) ? TV_DEV_OUT_OVERFLOW : 0);
+      if (bad) {
+        if (status) atomicOr(status, bad);
+        n = j;
+        break;
+      }
+    }
+    s_n = n;
+    if (new_lens) new_lens[b] = L + n;
+  }
+  __syncthreads();
+  const int n = s_n;
   const int per_row = Hkv * chunks;
   for (int t = threadIdx.x; t < n * per_row; t += blockDim.x) {
     const int j = t / per_row;
@@ -40,17 +63,8 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(char* __restrict__ kc, c
     const int h = r / chunks;
     const int c = r - h * chunks;
     const int node = path[(int64_t)b * path_cols + j];
-    if (node < 0 || node >= N) {
-      if (status && r == 0) atomicOr(status, TV_DEV_BAD_TOPOLOGY);
-      continue;
-    }
     const int64_t pos = (int64_t)L + j;
-    const int64_t col = pos / bs;
-    const int64_t blk = (L >= 0 && col < max_blocks) ? table[(int64_t)b * max_blocks + col] : -1;
-    if (blk < 0 || blk >= num_blocks) {
-      if (status && r == 0) atomicOr(status, TV_DEV_OUT_OVERFLOW);
-      continue;
-    }
+    const int64_t blk = table[(int64_t)b * max_blocks + pos / bs];  // checked above for every step < n
     const int64_t src = (((int64_t)b * N + node) * Hkv + h) * row_bytes + c * 16;
     const int64_t dst = ((blk * Hkv + h) * bs + pos % bs) * row_bytes + c * 16;
     *reinterpret_cast<uint4*>(kc + dst) = *reinterpret_cast<const uint4*>(kt + src);

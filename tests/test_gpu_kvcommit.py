@@ -75,15 +75,28 @@ def test_commit_block_edges_and_shapes(dtype, bs, Hkv, D):
     assert torch.equal(vc.float().cpu(), torch.from_numpy(ovc).float())
 
 
-def test_commit_flags_bad_nodes_and_overflow():
-    w = W.Workload("case", 2, 2, 1, 64, "f32", ("fixed", 0), 16, (0.7, 0.15), 6, 3, 420)
-    inp = W.attention_inputs(w, device="cuda", seq_lens=[14, 3], reserve=2)
+def test_commit_stops_at_the_first_step_it_cannot_commit():
+    """A bad node or a position without a block ends the commit there: the
+    steps before it are copied, nothing after, and the new prefix length
+    counts only the copied steps (bit for bit against the oracle's
+    stop_at_bad reading)."""
+    w = W.Workload("case", 3, 2, 1, 64, "f32", ("fixed", 0), 16, (0.7, 0.15), 6, 3, 420)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[14, 3, 5], reserve=2)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    # request 0: 5 rows from 14 reach position 18, past its 1-block table width; request 1: node 9 >= N
-    path = np.array([[0, 1, 2, 3, 4], [0, 9, -1, -1, -1]])
-    kc, vc, lens = _gpu_commit(inp, path, np.array([5, 2]), status=status)
-    assert int(status.item()) & capi.TV_DEV_OUT_OVERFLOW and int(status.item()) & capi.TV_DEV_BAD_TOPOLOGY
-    np.testing.assert_array_equal(lens.cpu().numpy(), [19, 5])
+    # request 0: 5 rows from 14 reach position 16, past its 1-block table
+    # width (step 2); request 1: node 9 >= N at step 1, then a valid node;
+    # request 2: a negative node at step 2
+    path = np.array([[0, 1, 2, 3, 4], [0, 9, 1, -1, -1], [0, 1, -3, 2, -1]])
+    n_out = np.array([5, 3, 4])
+    kc, vc, lens = _gpu_commit(inp, path, n_out, status=status)
+    assert int(status.item()) == capi.TV_DEV_OUT_OVERFLOW | capi.TV_DEV_BAD_TOPOLOGY
+    okc, ovc, olens = OK.commit_path(to_np(inp["k_cache"]), to_np(inp["v_cache"]), inp["block_table"].cpu().numpy(),
+                                     inp["seq_lens"].cpu().numpy(), to_np(inp["k_tree"]), to_np(inp["v_tree"]),
+                                     path, n_out, stop_at_bad=True)
+    np.testing.assert_array_equal(olens, [16, 4, 7])
+    np.testing.assert_array_equal(lens.cpu().numpy(), olens)
+    assert torch.equal(kc.float().cpu(), torch.from_numpy(okc).float())
+    assert torch.equal(vc.float().cpu(), torch.from_numpy(ovc).float())
 
 
 @pytest.mark.parametrize("name", ["gqa_b8_l512_2048_n26", "tiny_b1_f32"])

@@ -99,3 +99,31 @@ def test_commit_leaves_other_slots_and_rejects_overflow():
     lens_far = np.array([3, 8])
     with pytest.raises(ValueError):
         OK.commit_path(kc, vc, table, lens_far, kt, vt, too_long, np.array([2, 5]))
+
+
+def test_stop_at_bad_equals_the_commit_of_the_path_before_it():
+    """With stop_at_bad, a path whose step j cannot be committed (bad node,
+    or a position past the block table) commits exactly what the same path
+    cut to its first j steps commits."""
+    rng = np.random.default_rng(311)
+    parent, depth, rows, _ = OT.build_tree(PAGE_PATHS)
+    N = parent.size
+    lens = np.array([3, 7, 5])
+    q, kc, vc, table, kt, vt = _inputs(rng, 3, N, 2, 1, 8, 4, lens, reserve=2)
+    path = np.array([[0, 2, N + 4, 5], [0, 1, 3, -1], [0, 1, 3, 6]])
+    n_out = np.array([4, 4, 4])
+    lens_far = np.array([3, 7, 10])  # request 2: positions 10..13 reach table column 3, past its width
+    got = OK.commit_path(kc, vc, table, lens_far, kt, vt, path, n_out, stop_at_bad=True)
+    cut = []
+    for b in range(3):
+        j = 0
+        while j < n_out[b]:
+            t = lens_far[b] + j
+            if not (0 <= path[b, j] < N) or t // 4 >= table.shape[1]:
+                break
+            j += 1
+        cut.append(j)
+    assert cut == [2, 3, 2]
+    ref = OK.commit_path(kc, vc, table, lens_far, kt, vt, path, np.array(cut))
+    for a, r in zip(got, ref):
+        np.testing.assert_array_equal(a, r)
