@@ -10,6 +10,7 @@
 // ancestor row (itself and its ancestors) -- the [prefix all true | tree
 // mask] step mask, with the tree part taken as per-node bit rows.  Online
 // softmax in the log2 domain with float32 accumulation.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -585,21 +586,52 @@ namespace {
 constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;  // 32 MiB per device
 __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-// Device address of g_static_workspace for the current device, looked up once
-// per device (the host-side name is only a stand-in for the device array).
+// Identity of the current CUDA context (cuCtxGetId through the runtime's
+// driver entry-point query), 0 when it cannot be had.  A device reset tears
+// the primary context down and loads the module again, possibly at another
+// address, and the new context has a new identity.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS) return id;
+  return 0;
+}
+
+// Device address of g_static_workspace for the current device (the host-side
+// name is only a stand-in for the device array), looked up once per device
+// with that device current, and again if the device's context was replaced
+// since (after a cudaDeviceReset the old address would be stale).
 int static_workspace_ptr(void** out) {
   static std::mutex mu;
   static void* cached[64] = {};
+  static unsigned long long cached_ctx[64] = {};
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(TV_ERR_UNSUPPORTED, "device id %d out of range", dev);
   std::lock_guard<std::mutex> lock(mu);
-  if (!cached[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!cached[dev] || (ctx != 0 && ctx != cached_ctx[dev])) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_workspace);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_static_workspace)");
     cached[dev] = ptr;
+    cached_ctx[dev] = ctx != 0 ? ctx : current_context_id();
   }
   *out = cached[dev];
   return TV_OK;
