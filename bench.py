@@ -70,11 +70,17 @@ def parse_args():
                          "measured faster (the one-M-tile kernel, G*N <= 128, with B*Hkv >= 2 x SMs), else separate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other target configurations after the headline")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--oracle-single-core", default=None, metavar="LENS",
                     help="internal (run by the cpu_baseline leg with one BLAS/OpenMP thread): time the oracle on "
                          "requests of these comma-separated prefix lengths and print one JSON line")
+    ap.add_argument("--oracle-worker", action="store_true",
+                    help="internal: with --oracle-single-core, build the inputs, run --warmup requests, print "
+                         "'ready', wait for a line on stdin, then time the requests in turn (cycling) for "
+                         "--cpu-seconds, or for exactly --steps requests when --cpu-seconds is 0")
     return ap.parse_args()
 
 
@@ -258,14 +264,20 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def time_oracle(w, inp_cpu, req_paths, greedy, sample, seconds, order, counts):
-    """Times the oracle request by request until `seconds` elapse; returns
+def time_oracle(w, inp_cpu, req_paths, greedy, sample, seconds, order, counts, cycle=False, max_requests=None):
+    """Times the oracle request by request until `seconds` elapse (or
+    max_requests are done); with `cycle` the order repeats.  Returns
     (nodes/s, requests used, elapsed)."""
     done, t0 = [], time.perf_counter()
-    for b in order:
-        oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, [b], counts)
-        done.append(int(b))
-        if time.perf_counter() - t0 >= seconds:
+    while True:
+        for b in order:
+            oracle_sample_run(w, inp_cpu, req_paths, greedy, sample, [b], counts)
+            done.append(int(b))
+            if (max_requests is not None and len(done) >= max_requests) or \
+                    (max_requests is None and time.perf_counter() - t0 >= seconds):
+                el = time.perf_counter() - t0
+                return int(np.sum(counts[done])) / el, done, el
+        if not cycle:
             break
     el = time.perf_counter() - t0
     return int(np.sum(counts[done])) / el, done, el
@@ -427,20 +439,24 @@ class Step:
         return t
 
 
-def run_ours(args, world, rank, local):
-    w = rank_workload(W.WORKLOADS[args.workload], rank)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    st = Step(w, dev, args.flags, args.num_ctas, args.rope)
+def l2_flush_buffer(st, dev):
+    """A buffer larger than L2 to overwrite between timed iterations when a
+    step's data would otherwise stay in L2 (None when it cannot)."""
     ws_bytes = st.attn_bytes + sum(t.numel() * t.element_size() for t in st.per_step_inputs().values())
-    flush = None
-    if ws_bytes < 2 * L2_BYTES:
-        flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev) if ws_bytes < 2 * L2_BYTES else None
+    return flush, ws_bytes
+
+
+def measure_step(st, args, flush, world=1):
+    """W warm-up steps, then K timed steps and K timed attention calls (CUDA
+    graph replays unless --eager), CUDA events on the launching stream, SM
+    clocks sampled during the timed region.  Returns (step_ms, attn_ms,
+    clocks, graphs)."""
     for _ in range(args.warmup):
         st.run()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     graphs = None
@@ -484,6 +500,53 @@ def run_ours(args, world, rank, local):
     clocks = sampler.summary()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     attn_ms = [a.elapsed_time(b) for a, b in eva]
+    return step_ms, attn_ms, clocks, graphs
+
+
+def roofline_of(st, w, attn_ms):
+    peak, peak_kind = measured_hbm_peak()
+    attn_mean_ms = statistics.mean(attn_ms)
+    achieved = st.attn_bytes / (attn_mean_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+            "kernel": ("tv_tree_attn_verify_rope" if st.fused_rope else "tv_tree_attn_verify")
+                      + " (tcgen05: counter memset + one persistent kernel)",
+            "algorithmic_bytes_per_call": int(st.attn_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
+            "attn_ms_mean": round(attn_mean_ms, 4)}
+
+
+# Every target configuration, timed after the headline in the same run and
+# reported under "per_config" (the headline workload included, as measured
+# there).
+PER_CONFIG = ["gqa_b8_l512_2048_n26", "b64_l1k_8k_n64_greedy", "long_b16_l32k_n33", "b256_l2k_4k_n10_sample"]
+
+
+def measure_config(name, args, dev):
+    """One workload's attention call and step, measured as the headline is."""
+    w = W.WORKLOADS[name]
+    st = Step(w, dev, args.flags, args.num_ctas, args.rope)
+    flush, ws_bytes = l2_flush_buffer(st, dev)
+    step_ms, attn_ms, clocks, graphs = measure_step(st, args, flush)
+    roof = roofline_of(st, w, attn_ms)
+    nodes = int(np.sum(st.counts))
+    ms = statistics.mean(step_ms)
+    res = {"attn_ms_mean": roof["attn_ms_mean"], "frac": roof["frac"], "achieved_gbs": roof["achieved"],
+           "algorithmic_bytes": roof["algorithmic_bytes_per_call"], "traffic": roof["traffic"],
+           "ms_per_step": round(ms, 4), "nodes_per_s": nodes / (ms / 1e3), "nodes_per_step": nodes,
+           "accept": w.accept, "rope": "fused" if st.fused_rope else "separate",
+           "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
+           "clocks": clocks}
+    del st, graphs, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, world, rank, local):
+    w = rank_workload(W.WORKLOADS[args.workload], rank)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = Step(w, dev, args.flags, args.num_ctas, args.rope)
+    flush, ws_bytes = l2_flush_buffer(st, dev)
+    step_ms, attn_ms, clocks, graphs = measure_step(st, args, flush, world)
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, world, dev)
     if world > 1:
@@ -583,26 +646,45 @@ def run_ours(args, world, rank, local):
             accept.update(bytes_read=rows_b, all_rows_bytes=w.B * st.N * w.vocab * 4,
                           gbs=round(rows_b / (us * 1e-6) / 1e9, 1))
 
-    peak, peak_kind = measured_hbm_peak()
-    attn_mean_ms = statistics.mean(attn_ms)
-    achieved = st.attn_bytes / (attn_mean_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": ("tv_tree_attn_verify_rope" if st.fused_rope else "tv_tree_attn_verify")
-                          + " (tcgen05: counter memset + one persistent kernel)",
-                "algorithmic_bytes_per_call": int(st.attn_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
-                "attn_ms_mean": round(attn_mean_ms, 4)}
+    roofline = roofline_of(st, w, attn_ms)
+    achieved, peak = roofline["achieved"], roofline["peak"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        inp_cpu, g, s = cpu_inputs(w, st.inp, st.greedy, st.sample)
-        nps, used, el = time_oracle(w, inp_cpu, st.req_paths, g, s, args.cpu_seconds, sample_order(st.lens),
-                                    st.counts)
-        cpu = {"value": nps, "unit": "nodes/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{len(used)} of {w.B} requests (all {st.N} nodes, all {w.Hq} heads, acceptance incl.), "
-                         f"prefix lengths {[int(st.lens[b]) for b in used][:6]}..., {el:.1f} s",
-               "single_core": oracle_single_core(w, [int(st.lens[b]) for b in used[:6]],
-                                                 min(8.0, args.cpu_seconds))}
+        # the oracle on every host core: one single-threaded process per core
+        # (os.cpu_count()), each on a rotation of the workload's prefix
+        # lengths (the shortest and longest first), started together
+        lens_s = [int(st.lens[b]) for b in sample_order(st.lens)[:8]]
+        try:
+            nps, procs, res = oracle_all_cores(w, lens_s, seconds=args.cpu_seconds)
+            cpu = {"value": nps, "unit": "nodes/s", "cores": procs, "kind": "oracle",
+                   "sample": f"{procs} single-threaded processes started together, each timing the oracle "
+                             f"(all nodes and heads of a request, acceptance incl.) on a rotation of prefix "
+                             f"lengths {lens_s} for {args.cpu_seconds:.0f} s: {sum(r['requests'] for r in res)} "
+                             f"requests, {sum(r['nodes'] for r in res)} nodes in "
+                             f"{max(r['seconds'] for r in res):.1f} s (inputs regenerated on the CPU with the "
+                             f"workload's recipe)",
+                   "blas_threads_per_process": 1,
+                   "single_core": oracle_single_core(w, lens_s[:6], min(8.0, args.cpu_seconds))}
+        except (RuntimeError, OSError, subprocess.SubprocessError, ValueError) as e:
+            cpu = {"value": None, "unit": "nodes/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "error": f"{type(e).__name__}: {e}"[:200]}
+
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        del graphs
+        torch.cuda.empty_cache()
+        per_config = {}
+        for name in PER_CONFIG:
+            per_config[name] = (measure_config(name, args, dev) if name != w.name else
+                                {"attn_ms_mean": roofline["attn_ms_mean"], "frac": roofline["frac"],
+                                 "achieved_gbs": roofline["achieved"],
+                                 "algorithmic_bytes": roofline["algorithmic_bytes_per_call"],
+                                 "traffic": roofline["traffic"], "ms_per_step": round(total_ms / args.steps, 4),
+                                 "nodes_per_s": value, "nodes_per_step": nodes, "accept": w.accept,
+                                 "rope": "fused" if st.fused_rope else "separate", "clocks": clocks,
+                                 "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
+                                 "note": "the headline measurement"})
 
     if rank == 0:
         line = {
@@ -624,6 +706,7 @@ def run_ours(args, world, rank, local):
             "gpu_launches": st.launches * args.steps,
             "kv_commit": commit, "accept": accept,
             "kv_read_gbs": round(achieved, 1), "kv_read_frac_of_peak": round(achieved / peak, 4),
+            "per_config": per_config,
         }
         print(json.dumps(line))
 
@@ -646,19 +729,77 @@ def cpu_workload(w, seq_lens=None):
 def run_oracle_single_core(args):
     """One-core oracle timing (the parent starts this process with one BLAS and
     OpenMP thread): requests of the given prefix lengths, generated on the CPU
-    with the workload's recipe, timed one by one until --cpu-seconds."""
+    with the workload's recipe, timed one by one until --cpu-seconds.  With
+    --oracle-worker it is one of several such processes started together
+    (all-core figure, reference arm)."""
     lens = np.array([int(x) for x in args.oracle_single_core.split(",")], dtype=np.int32)
     w = dataclasses.replace(W.WORKLOADS[args.workload], B=len(lens))
     inp_cpu, g, s, req_paths, counts = cpu_workload(w, seq_lens=lens)
-    nps, used, el = time_oracle(w, inp_cpu, req_paths, g, s, args.cpu_seconds, list(range(len(lens))), counts)
-    print(json.dumps({"value": nps, "requests": len(used), "seconds": round(el, 2), "threads": blas_threads()}))
+    order = list(range(len(lens)))
+    if args.oracle_worker:
+        for k in range(args.warmup):
+            oracle_sample_run(w, inp_cpu, req_paths, g, s, [order[k % len(order)]], counts)
+        print("ready", flush=True)
+        sys.stdin.readline()
+        if args.cpu_seconds > 0:
+            nps, used, el = time_oracle(w, inp_cpu, req_paths, g, s, args.cpu_seconds, order, counts, cycle=True)
+        else:
+            nps, used, el = time_oracle(w, inp_cpu, req_paths, g, s, 0, order, counts, cycle=True,
+                                        max_requests=args.steps)
+    else:
+        nps, used, el = time_oracle(w, inp_cpu, req_paths, g, s, args.cpu_seconds, order, counts)
+    print(json.dumps({"value": nps, "requests": len(used), "nodes": int(np.sum(counts[used])),
+                      "seconds": round(el, 3), "threads": blas_threads()}))
+
+
+def one_thread_env():
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "LOCAL_WORLD_SIZE")}
+    env.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    return env
+
+
+def oracle_all_cores(w, lens, seconds=None, steps=None, warmup=0, timeout=900):
+    """One single-threaded oracle process per host core (os.cpu_count()),
+    each on its own rotation of the sampled prefix lengths.  Every process
+    builds its inputs and runs its warm-up requests, then all are released
+    together; each times its requests for `seconds` (cycling), or exactly
+    `steps` requests.  Returns (nodes/s over all processes = total nodes /
+    longest elapsed time, processes, per-process results)."""
+    n = os.cpu_count() or 1
+    cmds = []
+    for k in range(n):
+        mine = [int(lens[(k + j) % len(lens)]) for j in range(min(len(lens), 4))]
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", w.name, "--oracle-single-core",
+               ",".join(map(str, mine)), "--oracle-worker", "--warmup", str(warmup),
+               "--cpu-seconds", str(seconds if seconds is not None else 0), "--steps", str(steps or 1)]
+        cmds.append(cmd)
+    procs = [subprocess.Popen(c, env=one_thread_env(), stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                              stderr=subprocess.DEVNULL, text=True) for c in cmds]
+    try:
+        for pr in procs:  # every process ready (inputs built, warm-up done)
+            line = pr.stdout.readline()
+            if line.strip() != "ready":
+                raise RuntimeError(f"oracle worker did not start ({line.strip()[:80]})")
+        for pr in procs:
+            pr.stdin.write("go\n")
+            pr.stdin.flush()
+        res = []
+        for pr in procs:
+            out, _ = pr.communicate(timeout=timeout)
+            res.append(json.loads(out.strip().splitlines()[-1]))
+    finally:
+        for pr in procs:
+            if pr.poll() is None:
+                pr.kill()
+    nodes = sum(r["nodes"] for r in res)
+    el = max(r["seconds"] for r in res)
+    return nodes / el, n, res
 
 
 def oracle_single_core(w, lens, seconds):
     """cpu_baseline's one-core figure: run_oracle_single_core in a child
     process with the thread counts pinned to 1."""
-    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "LOCAL_WORLD_SIZE")}
-    env.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    env = one_thread_env()
     cmd = [sys.executable, os.path.abspath(__file__), "--workload", w.name, "--cpu-seconds", str(seconds),
            "--oracle-single-core", ",".join(str(int(x)) for x in lens)]
     try:
@@ -672,23 +813,19 @@ def oracle_single_core(w, lens, seconds):
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the oracle on every host core.  One single-threaded
+    process per core (os.cpu_count()) builds its requests' inputs with the
+    workload's recipe and runs --warmup requests; all are then released
+    together and each runs --steps requests, one per step (a step is one
+    request on every core at once).  value = nodes / the longest process
+    time; ms_per_step = that time / steps."""
     if rank != 0:
         return
     w = W.WORKLOADS[args.workload]
-    inp_cpu, g, s, req_paths, counts = cpu_workload(w)
-    lens = inp_cpu["seq_lens"]
-    order = sample_order(lens)
-    for k in range(args.warmup):
-        oracle_sample_run(w, inp_cpu, req_paths, g, s, [order[k % len(order)]], counts)
-    t0 = time.perf_counter()
-    used = []
-    for k in range(args.steps):
-        b = order[k % len(order)]
-        oracle_sample_run(w, inp_cpu, req_paths, g, s, [b], counts)
-        used.append(b)
-    el = time.perf_counter() - t0
-    value = int(np.sum(counts[used])) / el
-    cores = blas_threads()
+    lens = W.prefix_lengths(w)
+    lens_s = [int(lens[b]) for b in sample_order(lens)[:8]]
+    value, procs, res = oracle_all_cores(w, lens_s, steps=args.steps, warmup=args.warmup)
+    el = max(r["seconds"] for r in res)
     line = {
         "impl": "reference",
         "metric": "tree-verify nodes/s and KV-read HBM GB/s (% of GB300 peak), 1 GPU",
@@ -698,9 +835,11 @@ def run_reference(args, world, rank):
         "config": {"workload": w.name, "B": w.B, "N": w.n_nodes, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "prefix": list(w.prefix), "block_size": w.block_size, "accept": w.accept, "vocab": w.vocab,
                    "tree": "one per request" if w.dynamic else "shared"},
-        "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle",
-                         "sample": f"one request per step (all {w.n_nodes} nodes, all heads, acceptance incl.), "
-                                   f"requests {used[:6]}..."},
+        "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": procs, "kind": "oracle",
+                         "blas_threads_per_process": 1,
+                         "sample": f"{procs} single-threaded processes, one request each per step (all "
+                                   f"{w.n_nodes} nodes, all heads, acceptance incl.), prefix lengths {lens_s} in "
+                                   f"rotation; {sum(r['nodes'] for r in res)} nodes in {el:.2f} s"},
         "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

@@ -28,10 +28,23 @@ def test_reference_arm_line_has_the_contract_keys():
     assert d["value"] > 0 and d["unit"] == "nodes/s" and d["higher_is_better"] is True
     assert d["config"]["workload"] == "tiny_b1_f32"
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["sample"]
+    assert cb["cores"] == os.cpu_count() and cb["blas_threads_per_process"] == 1
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_oracle_worker_waits_for_go_and_runs_exact_steps():
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "tiny_b1_f32",
+                        "--oracle-single-core", "32,16", "--oracle-worker", "--warmup", "1", "--cpu-seconds", "0",
+                        "--steps", "3"], input="go\n", capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = r.stdout.splitlines()
+    assert lines[0] == "ready"
+    d = json.loads(lines[-1])
+    assert d["requests"] == 3 and d["nodes"] == 30 and d["threads"] == 1
 
 
 def test_single_core_oracle_timing_line():
