@@ -1671,6 +1671,9 @@ __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& s
       ok = mbar_wait_warp(&bars.kv_full[stage], (g / kStages) & 1, &bars, status);
       if (!ok) break;
       tail_tile(p, s, t, sK + stage * kKVTileBytes, sV + stage * kKVTileBytes, ts, w, lane);
+      // the stage was read through the generic proxy (ldmatrix) and the next
+      // TMA load writes it through the async proxy: order the reads first
+      fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.kv_empty[stage]);
     }

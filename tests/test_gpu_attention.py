@@ -236,6 +236,28 @@ def test_split_unit_merge_routes(G, N):
                 assert torch.equal(a, b), (lens, num_ctas)
 
 
+@pytest.mark.parametrize("G,N,grids", [(8, 33, (2, 3, 7)), (4, 64, (2, 5)), (4, 26, (3,))])
+def test_repeated_calls_bit_identical(G, N, grids):
+    """The same call forty times gives the same bits: every stage of the K/V
+    ring is released only after all of its readers are done with it (a tail
+    row read through the generic proxy without a proxy fence before the
+    release once let the next TMA load overwrite it, here 39 runs in 40)."""
+    if not tc_available(2 * G, 2, N):
+        pytest.skip("tensor-core kernel unavailable for this shape")
+    rng = np.random.default_rng(140 + G + N)
+    paths = W.random_rank_paths(N, 6, rng)
+    w = _workload(3, 2 * G, 2, 128, "bf16", 16, N, 141 + N)
+    inp = prerotated(W.attention_inputs(w, device="cuda", seq_lens=[3000, 70, 1500]), paths)
+    for num_ctas in grids:
+        first = None
+        for _ in range(40):
+            out, lse = gpu_attention(inp, paths, flags=capi.TV_ATTN_TCGEN05, num_ctas=num_ctas)
+            if first is None:
+                first = (out, lse)
+            else:
+                assert torch.equal(out, first[0]) and torch.equal(lse, first[1]), num_ctas
+
+
 def test_deterministic_and_kernel_agreement():
     w = W.WORKLOADS["gqa_b8_l512_2048_n26"]
     inp = W.attention_inputs(w, device="cuda")
