@@ -75,6 +75,11 @@ extern "C" {
  * loaded; the tensor-core kernel then needs Hq/Hkv in {4, 8, 16}).  Not a
  * flag of tv_tree_attn_verify itself. */
 #define TV_ATTN_ROPE_Q 8
+/* Flag bit, tcgen05 kernel only: units of 129-256 rows (G * N) run on CTA
+ * pairs (tcgen05.mma.cta_group::2, each SM loading half of every K/V tile)
+ * instead of one SM per unit.  Same results up to rounding; slower than the
+ * one-SM kernel on the shapes measured so far. */
+#define TV_ATTN_CTA_PAIRS 16
 
 /* Kernel selection of tv_tree_accept_sample. */
 #define TV_SAMPLE_AUTO 0        /* TV_SAMPLE_CLUSTER when every request's cluster is resident at
@@ -243,7 +248,8 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  *            256-byte aligned; its contents on entry are irrelevant (the
  *            tensor-core path clears its arrival counters in it with a
  *            cudaMemsetAsync on `stream`).
- * flags      TV_ATTN_* kernel selection, optionally | TV_ATTN_PUBLISH_ALL.
+ * flags      TV_ATTN_* kernel selection, optionally | TV_ATTN_PUBLISH_ALL
+ *            | TV_ATTN_CTA_PAIRS.
  * num_ctas   persistent grid size (0 = one wave of the current device);
  *            must equal the value given to tv_tree_attn_workspace_size.
  * status     device int32 (nullable): TV_DEV_TIMEOUT if a pipeline wait of

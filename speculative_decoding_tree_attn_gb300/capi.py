@@ -23,6 +23,7 @@ TV_F32, TV_BF16 = 0, 1
 TV_ATTN_AUTO, TV_ATTN_SIMT, TV_ATTN_TCGEN05 = 0, 1, 2
 TV_ATTN_PUBLISH_ALL = 4
 TV_ATTN_ROPE_Q = 8
+TV_ATTN_CTA_PAIRS = 16
 TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA, TV_SAMPLE_STREAM = 0, 1, 2, 3
 TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 TV_DEV_BAD_BLOCK = 32

@@ -384,6 +384,7 @@ int simt_dispatch(const AttnParams& p, int dtype, cudaStream_t stream, int* bloc
 // Shape decisions shared by the workspace query and the launch.
 struct AttnConfig {
   bool tc;
+  bool duo;  // units of 129-256 rows on CTA pairs (P counts pairs)
   int RPG, RG, U, BLK, P;
   int64_t off_arrive, off_part_o, off_part_lse, bytes;
 };
@@ -405,7 +406,8 @@ void layout_workspace(AttnConfig* cfg, int D) {
 int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size, int num_ctas, int flags,
                 AttnConfig* cfg) {
   const bool rope = (flags & TV_ATTN_ROPE_Q) != 0;
-  flags &= ~TV_ATTN_ROPE_Q;
+  const bool pairs = (flags & TV_ATTN_CTA_PAIRS) != 0;
+  flags &= ~(TV_ATTN_ROPE_Q | TV_ATTN_CTA_PAIRS);
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Hq % Hkv)
     return fail(TV_ERR_INVALID_ARG, "tree attention: bad sizes B=%d N=%d Hq=%d Hkv=%d", B, N, Hq, Hkv);
   if (D != 64 && D != 128 && D != 256)
@@ -440,7 +442,8 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
   }
   cfg->RG = (int)ceil_div(R, cfg->RPG);
   cfg->U = B * Hkv * cfg->RG;
-  cfg->P = num_ctas > 0 ? num_ctas : dev.sm_count * per_sm;
+  cfg->duo = cfg->tc && cfg->RPG == kTcMaxRows && pairs;
+  cfg->P = num_ctas > 0 ? num_ctas : (cfg->duo ? tc_duo_pairs(dev) : dev.sm_count * per_sm);
   layout_workspace(cfg, D);
   return TV_OK;
 }
@@ -526,7 +529,7 @@ int verify_impl(const void* q, const void* k_cache, const void* v_cache, int64_t
     // it only needs the arrival counters at zero
     cudaError_t e = cudaMemsetAsync(p.arrive, 0, (size_t)p.P * p.RPG * sizeof(uint32_t), s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(arrival counters)");
-    return launch_attn_tc(p, status, s);
+    return launch_attn_tc(p, status, s, cfg.duo);
   }
   if ((st = launch_plan(p, s))) return st;
   if ((st = simt_dispatch(p, dtype, s, nullptr))) return st;

@@ -108,6 +108,7 @@ struct Cfg {
 struct Bars {
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
+  uint64_t peer_full[8];  // CTA pairs: the odd CTA's half of a tile has landed (even CTA's copy)
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
@@ -436,6 +437,7 @@ struct SlicePlan {
   int us0;  // first (virtual) tile of unit u0
   int u0;
   int P;    // slices the plan is cut into (CTAs from P on have no work)
+  int c;    // this CTA's slice (its CTA index, or its CTA pair's index)
 };
 
 // Fewest tiles a slice gets: a small plan goes to fewer CTAs rather than
@@ -451,7 +453,7 @@ __device__ __forceinline__ int unit_tiles(const AttnParams& p, int b) {
 
 // Warp-collective.  The units of request b are consecutive and all have
 // unit_tiles(b) tiles, so the tile prefix sums are taken over requests.
-__device__ void plan_slice(const AttnParams& p, int lane, SlicePlan& sp) {
+__device__ void plan_slice(const AttnParams& p, int lane, SlicePlan& sp, int c) {
   const int64_t upb = (int64_t)p.Hkv * p.RG;
   long long tot = 0;
   for (int b = lane; b < p.B; b += 32) tot += unit_tiles(p, b);
@@ -460,7 +462,6 @@ __device__ void plan_slice(const AttnParams& p, int lane, SlicePlan& sp) {
   const int T = (int)(tot * upb);  // the host bounds the plan below 2^31 tiles
   int P = (T + TV_MIN_SLICE_TILES - 1) / TV_MIN_SLICE_TILES;
   P = P < 1 ? 1 : (P > p.P ? p.P : P);
-  const int c = blockIdx.x;
   const int t0 = c < P ? (int)cta_start(c, T, P) : T, t1 = c < P ? (int)cta_start(c + 1, T, P) : T;
   int u0 = p.U, us0 = T;
   if (t0 < t1) {
@@ -489,6 +490,7 @@ __device__ void plan_slice(const AttnParams& p, int lane, SlicePlan& sp) {
     }
   }
   if (lane == 0) {
+    sp.c = c;
     sp.T = T;
     sp.P = P;
     sp.t0 = t0;
@@ -554,8 +556,9 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* ptr, uint32_t v) 
 // slots, except c0 when the unit began after the start of its slice (slot 1).
 struct Pieces {
   int T, P, c0, c1;
+  int self;  // this CTA's slice
   bool c0_slot1;
-  __device__ Pieces(const SlicePlan& sp, int real_start, int n_real) : T(sp.T), P(sp.P) {
+  __device__ Pieces(const SlicePlan& sp, int real_start, int n_real) : T(sp.T), P(sp.P), self(sp.c) {
     c0 = (int)cta_of(real_start, T, P);
     c1 = (int)cta_of(real_start + n_real - 1, T, P);
     c0_slot1 = cta_start(c0, T, P) < real_start;
@@ -653,7 +656,7 @@ static_assert(3 * kKVTileBytes * 2 >= kStageBytes, "the single-M-tile ring holds
 __device__ __forceinline__ void staged_merge(const AttnParams& p, const Pieces& pc, float lse2, float inv, int row,
                                              int rl, int64_t orow, uint32_t tO, uint8_t* stage, bool active) {
   constexpr float kLn2 = 0.69314718055994530942f;
-  const int self = blockIdx.x;
+  const int self = pc.self;
   const int np = pc.c1 - pc.c0 + 1;
   float lse[kStagePieces], w[kStagePieces];
   float mx = -INFINITY;
@@ -760,7 +763,7 @@ __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pie
                                                   int row, int rl, int64_t orow, uint32_t tO, uint8_t* stage,
                                                   bool active) {
   constexpr float kLn2 = 0.69314718055994530942f;
-  const bool self_first = (int)blockIdx.x == pc.c0;
+  const bool self_first = pc.self == pc.c0;
   const int64_t so = pc.slot(self_first ? pc.c1 : pc.c0) * p.RPG + row;
   const uint32_t dst = smem_u32(stage) + rl * 16;
   float lo = 0.f;
@@ -822,7 +825,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   const float lse2 = m_run + log2f(l);
   const bool complete = (s.a == 0 && s.e == s.n);
   const Pieces pc(sp, s.real_start, s.n);
-  const int self = blockIdx.x;
+  const int self = pc.self;
   uint32_t* ctr = p.arrive + (int64_t)pc.c0 * p.RPG + row;
   const uint32_t mine = (uint32_t)(s.e - s.a);
   bool direct = false;
@@ -948,11 +951,27 @@ template <int kStages, int kProducers = 1>
 __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePlan& sp, const TcMaps& maps, Bars& bars,
                                              uint32_t sK, uint32_t sV, int lane, int32_t* status, int prod = 0) {
     // ------------------------------------------------------------ TMA producer
+    // The producer shares its sub-partition with busy softmax warps, so the
+    // tile loop is kept short: each lane's box (K or V, column half,
+    // sub-block, its offset in the stage) is fixed for the whole slice, and
+    // block arithmetic uses shifts when the block size is a power of two.
     const int bs = p.block_size;
+    const int lbs = (bs & (bs - 1)) == 0 ? __ffs(bs) - 1 : -1;  // log2(bs) for a power of two
     const int br = bs < kBlk ? bs : kBlk;  // rows per TMA box
     const int nsub = kBlk / br;
     const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
     const uint64_t pol = policy_evict_first();
+    // box j < 4 * nsub: sub-box j / 4, column half (j / 2) % 2, K (even j) or V
+    // (odd j); this warp issues the boxes j = lane * kProducers + prod
+    const int j = lane * kProducers + prod;
+    const int sub = (j >> 2) < nsub ? (j >> 2) : 0;
+    const int h = (j >> 1) & 1;
+    const bool is_v = j & 1;
+    const bool has_box = j < 4 * nsub;
+    const uint32_t dst_base = (is_v ? sV : sK) + h * kKVHalfBytes + sub * br * 128;
+    const CUtensorMap* map = is_v ? &maps.vc : &maps.kc;
+    const CUtensorMap* tmap = is_v ? &maps.vt : &maps.kt;
+    auto div_bs = [&](int x) { return lbs >= 0 ? x >> lbs : x / bs; };
     uint32_t g = 0;
     bool ok = true;
     Walk walk(sp);
@@ -976,49 +995,43 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePla
         if (lane == 0 && prod == 0)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(p.mask + (int64_t)s.b * p.mask_bstride));
       }
-      const int nb = (s.L + bs - 1) / bs;  // valid table entries of request b
+      const int nb = div_bs(s.L + bs - 1);  // valid table entries of request b
       const int32_t* trow = p.block_table + (int64_t)s.b * p.max_blocks;
-      int w0 = (s.a * kBlk) / bs;          // first entry held in `cur`
+      const int64_t head_row = (int64_t)s.kvh * bs;
+      const int last_pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
+      int w0 = div_bs(s.a * kBlk);  // first entry held in `cur`
       int32_t cur = (w0 + lane < nb) ? __ldg(trow + w0 + lane) : 0;
       int32_t nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
       for (int t = s.a; t < s.e && ok; ++t, ++g) {
         const int stage = g % kStages;
         const uint32_t use = g / kStages;
         const bool tree_tile = (t == s.n - 1);
-        if (!tree_tile && (t * kBlk) / bs >= w0 + 32) {
+        if (!tree_tile && div_bs(t * kBlk) >= w0 + 32) {
           w0 += 32;
           cur = nxt;
           nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
         }
-        // box j < 4 * nsub: sub-box j / 4, column half (j / 2) % 2, K (even j) or V (odd j);
-        // this warp issues the boxes j = lane * kProducers + prod, one per lane
-        const int j = lane * kProducers + prod;
-        const int sub = (j >> 2) < nsub ? (j >> 2) : 0;
         int pos = t * kBlk + sub * br;
-        if (pos >= s.L) pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
-        const int rel = pos / bs - w0;
+        if (pos >= s.L) pos = last_pos;
+        const int bi = div_bs(pos);
+        const int rel = bi - w0;
         const int32_t from_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
         const int32_t from_nxt = __shfl_sync(0xffffffffu, nxt, rel & 31);
         const int64_t blk = rel < 32 ? from_cur : from_nxt;
         if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
         if (!ok) break;
-        const uint32_t dk = sK + stage * kKVTileBytes, dv = sV + stage * kKVTileBytes;
         if (prod == 0 && lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
         __syncwarp();
-        const int h = (j >> 1) & 1;
-        const bool is_v = j & 1;
+        const uint32_t dst = dst_base + stage * kKVTileBytes;
         if (tree_tile) {
-          if (j < 4)
-            tma_4d((is_v ? dv : dk) + h * kKVHalfBytes, is_v ? &maps.vt : &maps.kt, h * 64, s.kvh, 0, s.b,
-                   &bars.kv_full[stage]);
-        } else if (j < 4 * nsub) {
-          int64_t y = (blk * p.Hkv + s.kvh) * bs + pos % bs;
+          if (j < 4) tma_4d(dst, tmap, h * 64, s.kvh, 0, s.b, &bars.kv_full[stage]);
+        } else if (has_box) {
+          int64_t y = blk * p.Hkv * bs + head_row + (pos - bi * bs);
           if (blk < 0 || blk >= p.num_blocks) {  // out of range: TMA fills zeros
             y = rows_total;
             if (status) atomicOr(status, TV_DEV_BAD_BLOCK);
           }
-          tma_2d_stream((is_v ? dv : dk) + h * kKVHalfBytes + sub * br * 128, is_v ? &maps.vc : &maps.kc, h * 64,
-                        (int)y, &bars.kv_full[stage], pol);
+          tma_2d_stream(dst, map, h * 64, (int)y, &bars.kv_full[stage], pol);
         }
         __syncwarp();
         if (prod == 0 && lane == 0) TV_TRACE(31, g);
@@ -1063,7 +1076,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
   TV_TRACE_CTA(0);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __shared__ SlicePlan sp;
-  if (warp == 0) plan_slice(p, lane, sp);
+  if (warp == 0) plan_slice(p, lane, sp, blockIdx.x);
   __syncthreads();
   if (sp.t0 >= sp.t1) return;  // empty slice: uniform exit before any setup
   if (threadIdx.x == 0) {
@@ -1625,7 +1638,7 @@ __device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& s
   } else {
     const Pieces pc(sp, s.real_start, s.n);
     const uint32_t mine = (uint32_t)(s.e - s.a);
-    const int64_t srow = pc.slot(blockIdx.x) * p.RPG + ur;
+    const int64_t srow = pc.slot(pc.self) * p.RPG + ur;
     if (valid) {
       float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + d0);
 #pragma unroll
@@ -1761,7 +1774,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   TV_TRACE_CTA(0);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __shared__ SlicePlan sp;
-  if (warp == 0) plan_slice(p, lane, sp);
+  if (warp == 0) plan_slice(p, lane, sp, blockIdx.x);
   __syncthreads();
   if (sp.t0 >= sp.t1) return;
   if (threadIdx.x == 0) {
@@ -2168,6 +2181,585 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA pairs (cta_group::2), up to 256 rows
+//
+// Two SMs share every unit of up to 256 rows: the rows are split 128 / 128
+// between the pair's CTAs (each keeps its rows' S, P, Q and O in its own
+// TMEM), and every MMA is one tcgen05.mma.cta_group::2 with M = 256 issued
+// by the even CTA.  The B operand of an MMA is split between the two CTAs'
+// shared memory along N, so each SM loads half of every K/V tile from HBM:
+//   S = Q K^T   (N = 64 keys):       this CTA holds keys 32r .. 32r + 31;
+//   O += P V    (N = 128 head dims): this CTA holds head dims 64r .. 64r + 63.
+// Per row an SM then has 512 TMEM columns for 128 rows instead of 256, which
+// holds two sets of S, P and O: two softmax warpgroups take the even and the
+// odd key tiles of a unit, each with its own running max, sum and O, merged
+// at the unit's end.  The S product of the next tile is computed while the
+// softmax of the current one runs, and each warpgroup has two tiles' time
+// for its softmax.  TMEM columns: S_A 0-63, S_B 64-127, P_A 128-159,
+// P_B 160-191, Q 192-255 (the A operand of S, "TS" form), O_A 256-383,
+// O_B 384-511.
+//
+// Barriers: each CTA's loads complete on its own kv_full barrier; the odd
+// CTA forwards that completion to the even CTA's peer_full barrier, so the
+// issuing thread knows both halves of a tile have landed.  MMA completions
+// are committed to both CTAs' barriers at once (multicast); the softmax
+// warps of both CTAs arrive on the even CTA's s_free / p_full / q_full
+// barriers (one arrival per warp, through the cluster's shared memory).
+struct DuoCfg {
+  static constexpr int kStages = 8;
+  static constexpr int kKHalfBytes = 32 * 128;  // 32 keys x 64 head dims
+  static constexpr int kKBytes = 2 * kKHalfBytes;
+  static constexpr int kVBytes = kBlk * 128;     // 64 keys x 64 head dims
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kStages * kKBytes;
+  static constexpr int kBytes = kOffV + kStages * kVBytes;
+  static constexpr int kSmem = kBytes + 1024;
+  // warps 0-3: TMA (boxes dealt round-robin: one warp issues a box only
+  // about every 150 cycles and then stalls); warps 4 / 5: S_A / S_B issuers
+  // (even CTA), warp 4 of the odd CTA forwards its loads' completion; warp
+  // 6: P V issuer (even CTA) and TMEM allocation; warp 7 idle; warps 8-11 /
+  // 12-15: softmax warpgroups A (even tiles) / B (odd tiles).
+  static constexpr int kThreads = 32 * 16;
+  static constexpr int kProducers = 4;
+  static constexpr int kAllocWarp = 6;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t col_s(int x) { return x * 64; }
+  static constexpr uint32_t col_p(int x) { return 128 + x * 32; }
+  static constexpr uint32_t kColQ = 192;
+  static constexpr uint32_t col_o(int x) { return 256 + x * 128; }
+  static constexpr int kSoftmaxWarp0 = 8;
+};
+static_assert(DuoCfg::kStages * DuoCfg::kKBytes >= 128 * kD * 4, "the K ring holds one M tile's staged rows");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Arrival on the even CTA's copy of a barrier (remote for the odd CTA).  The
+// remote arrival is relaxed: a release at cluster scope stalls the arriving
+// warp for about a thousand cycles, and the operations it would order have
+// completed already (tcgen05.wait::ld / ::st precede every such arrival, and
+// the MMAs that consume the data are issued after it is observed).
+__device__ __forceinline__ void mbar_arrive_leader(uint64_t* bar, uint32_t rank) {
+  if (rank == 0) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+  } else {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(smem_u32(bar)));
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+  }
+}
+
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for barriers that other CTAs of the cluster arrive on.
+__device__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, Bars* bars, int32_t* status) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*(volatile int*)&bars->abort) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *(volatile int*)&bars->abort = 1;
+        if (status) atomicOr(status, TV_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mma2(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)acc)
+      : "memory");
+}
+
+// Completion of the issuing thread's earlier MMAs, signalled on the barrier
+// at this offset in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit2(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+struct DuoMaps {
+  CUtensorMap kc, vc, kt, vt;  // K boxes of 32 (or block_size) rows, V boxes of 64 (or block_size) rows
+};
+
+// TMA producer of one CTA of the pair: this CTA's 32 keys (both head-dim
+// halves) and this CTA's head-dim half of all 64 keys of every tile.  The
+// producer shares its sub-partition with busy softmax warps, so the tile loop
+// is kept short: each lane's box (which half, which sub-block, its offset in
+// the tile and in the stage) is fixed for the whole slice, and block
+// arithmetic uses shifts when the block size is a power of two.
+template <int kStages, int kProducers>
+__device__ __forceinline__ void duo_producer(const AttnParams& p, const SlicePlan& sp, const DuoMaps& maps, Bars& bars,
+                                             uint32_t sK, uint32_t sV, uint32_t rank, int lane, int32_t* status,
+                                             int prod) {
+  using C = DuoCfg;
+  const int bs = p.block_size;
+  const int lbs = (bs & (bs - 1)) == 0 ? __ffs(bs) - 1 : -1;  // log2(bs) for a power of two
+  const int brk = bs < 32 ? bs : 32, nk = 32 / brk;        // K boxes per head-dim half
+  const int brv = bs < kBlk ? bs : kBlk, nv = kBlk / brv;  // V boxes
+  const int64_t rows_total = (int64_t)p.num_blocks * p.Hkv * bs;
+  const uint64_t pol = policy_evict_first();
+  // this lane's box j (j < 2 nk: K, half j / nk, sub-box j % nk; then V
+  // sub-box j - 2 nk): dealt round-robin over the producer warps
+  const int j = lane * kProducers + prod;
+  const bool is_k = j < 2 * nk;
+  const bool has_box = j < 2 * nk + nv;
+  const int sub = is_k ? j % nk : j - 2 * nk;
+  const int h = is_k ? j / nk : (int)rank;
+  const int br = is_k ? brk : brv;
+  const int off = is_k ? (int)rank * 32 + sub * brk : sub * brv;  // key offset of the box in the tile
+  const uint32_t dst_off = is_k ? (uint32_t)(h * C::kKHalfBytes + sub * brk * 128) : (uint32_t)(sub * brv * 128);
+  const uint32_t dst_base = is_k ? sK : sV;
+  const uint32_t dst_stride = is_k ? C::kKBytes : C::kVBytes;
+  const CUtensorMap* map = is_k ? &maps.kc : &maps.vc;
+  auto div_bs = [&](int x) { return lbs >= 0 ? x >> lbs : x / bs; };
+  uint32_t g = 0;
+  bool ok = true;
+  Walk walk(sp);
+  Segment s;
+  while (ok && walk.next(p, s)) {
+    {
+      const int rows = p.R - s.rg * p.RPG < p.RPG ? p.R - s.rg * p.RPG : p.RPG;
+      const char* qb = static_cast<const char*>(p.q);
+      for (int r = lane * kProducers + prod; r < 128; r += 32 * kProducers) {
+        const int ur = s.rg * p.RPG + (int)rank * 128 + r;
+        if (ur - s.rg * p.RPG >= rows) break;
+        const int64_t orow = ((int64_t)s.b * p.N + ur / p.G) * p.Hq + s.kvh * p.G + ur % p.G;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + orow * (kD * 2)));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + orow * (kD * 2) + 128));
+      }
+      if (lane == 0 && prod == 0)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.mask + (int64_t)s.b * p.mask_bstride));
+    }
+    const int nb = div_bs(s.L + bs - 1);
+    const int32_t* trow = p.block_table + (int64_t)s.b * p.max_blocks;
+    const int64_t head_row = (int64_t)s.kvh * bs;  // row of (block 0, this KV head) over Hkv * bs rows per block
+    const int last_pos = s.L > 0 ? (s.L - 1) / br * br : 0;  // ragged tail: finite rows, weight 0
+    int w0 = div_bs(s.a * kBlk);
+    int32_t cur = (w0 + lane < nb) ? __ldg(trow + w0 + lane) : 0;
+    int32_t nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
+    for (int t = s.a; t < s.e && ok; ++t, ++g) {
+      const int stage = g % kStages;
+      const uint32_t use = g / kStages;
+      const bool tree_tile = (t == s.n - 1);
+      if (!tree_tile && div_bs(t * kBlk) >= w0 + 32) {
+        w0 += 32;
+        cur = nxt;
+        nxt = (w0 + 32 + lane < nb) ? __ldg(trow + w0 + 32 + lane) : 0;
+      }
+      int pos = t * kBlk + off;
+      if (pos >= s.L) pos = last_pos;
+      const int bi = div_bs(pos);
+      const int rel = bi - w0;
+      const int32_t from_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
+      const int32_t from_nxt = __shfl_sync(0xffffffffu, nxt, rel & 31);
+      const int64_t blk = rel < 32 ? from_cur : from_nxt;
+      if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
+      if (!ok) break;
+      if (lane == 0 && prod == 0) mbar_expect_tx(&bars.kv_full[stage], C::kKBytes + C::kVBytes);
+      __syncwarp();
+      if (tree_tile) {
+        const uint32_t dk = sK + stage * C::kKBytes, dv = sV + stage * C::kVBytes;
+        if (j < 2)
+          tma_4d(j == 0 ? dk : dk + C::kKHalfBytes, &maps.kt, 64 * j, s.kvh, (int)rank * 32, s.b, &bars.kv_full[stage]);
+        else if (j == 2)
+          tma_4d(dv, &maps.vt, 64 * (int)rank, s.kvh, 0, s.b, &bars.kv_full[stage]);
+      } else if (has_box) {
+        int64_t y = blk * p.Hkv * bs + head_row + (pos - bi * bs);
+        if (blk < 0 || blk >= p.num_blocks) {
+          y = rows_total;
+          if (status) atomicOr(status, TV_DEV_BAD_BLOCK);
+        }
+        tma_2d_stream(dst_base + stage * dst_stride + dst_off, map, h * 64, (int)y, &bars.kv_full[stage], pol);
+      }
+      __syncwarp();
+    }
+  }
+  // drain: every load this warp issued has landed before it exits
+  if (lane == 0) {
+    const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0;
+    for (uint32_t i = first; i < g; ++i)
+      mbar_wait(&bars.kv_full[i % kStages], (i / kStages) & 1, &bars, nullptr, false);
+  }
+}
+
+template <bool kRope>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoCfg::kThreads, 1)
+    attn_tc_duo_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ DuoMaps maps, int32_t* status) {
+  using C = DuoCfg;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Bars bars;
+  __shared__ float s_sh[256];  // warpgroup B's running max and sum per row at a unit's end
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sK = base + C::kOffK, sV = base + C::kOffV;
+  const uint32_t rank = cluster_rank();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  __shared__ SlicePlan sp;
+  if (warp == 0) plan_slice(p, lane, sp, blockIdx.x / 2);
+  __syncthreads();
+  if (sp.t0 >= sp.t1) return;  // both CTAs of the pair have the same (empty) slice
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.peer_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.s_full[x], 1);
+      mbar_init(&bars.s_free[x], 8);
+      mbar_init(&bars.p_full[x], 8);
+      mbar_init(&bars.o_done[x], 1);
+    }
+    mbar_init(&bars.q_full, 8);
+    mbar_init(&bars.sh_stat, 4);
+    mbar_init(&bars.sh_read, 4);
+    bars.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == C::kAllocWarp) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  // both CTAs' barriers are initialised (and their TMEM allocated) before any
+  // remote arrival or multicast commit
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  constexpr uint32_t hi = desc_hi(1024);
+
+  if (warp < C::kProducers) {
+    duo_producer<C::kStages, C::kProducers>(p, sp, maps, bars, sK, sV, rank, lane, status, warp);
+  } else if (warp == 4 && rank == 1) {
+    if (lane == 0) {
+      // forwarder: this CTA's half of tile g has landed -> the even CTA's peer_full
+      uint32_t g = 0;
+      bool ok = true;
+      Walk walk(sp);
+      Segment s;
+      while (ok && walk.next(p, s)) {
+        for (int t = s.a; t < s.e && ok; ++t, ++g) {
+          const int stage = g % C::kStages;
+          ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          if (ok) mbar_arrive_leader(&bars.peer_full[stage], 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if ((warp == 4 || warp == 5) && rank == 0) {
+    if (lane == 0) {
+      // S_X = Q K^T for the tiles of warpgroup X (warp 4: the even tiles of a
+      // unit, warp 5: the odd ones)
+      const int x = warp - 4;
+      constexpr uint32_t idS = idesc_bf16(256, kBlk, false);
+      uint32_t g = 0, uses = 0;
+      int seg_i = 0;
+      bool ok = true;
+      Walk walk(sp);
+      Segment s;
+      while (ok && walk.next(p, s)) {
+        ok = mbar_wait_cl(&bars.q_full, seg_i & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        for (int t = s.a; t < s.e && ok; ++t, ++g) {
+          if (((t - s.a) & 1) != x) continue;
+          const int stage = g % C::kStages;
+          ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          if (ok) ok = mbar_wait_cl(&bars.peer_full[stage], (g / C::kStages) & 1, &bars, status);
+          if (ok && uses > 0) ok = mbar_wait_cl(&bars.s_free[x], (uses - 1) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          const uint32_t blo = desc_lo(sK + stage * C::kKBytes, 0);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t b = ((uint64_t)hi << 32) | (blo + (kk / 4) * (C::kKHalfBytes >> 4) + (kk % 4) * 2);
+            mma2(tmem + C::col_s(x), tmem + C::kColQ + kk * 8, b, idS, kk > 0);
+          }
+          mma_commit2(&bars.s_full[x]);
+          ++uses;
+        }
+        ++seg_i;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    if (lane == 0 && rank == 0) {
+      // O_X += P_X V
+      constexpr uint32_t idO = idesc_bf16(256, kD, true);
+      uint32_t g = 0, uses[2] = {0, 0};
+      bool ok = true;
+      Walk walk(sp);
+      Segment s;
+      while (ok && walk.next(p, s)) {
+        for (int t = s.a; t < s.e && ok; ++t, ++g) {
+          const int k = t - s.a, x = k & 1;
+          const int stage = g % C::kStages;
+          ok = mbar_wait_cl(&bars.p_full[x], uses[x] & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          const uint32_t vlo = desc_lo(sV + stage * C::kVBytes, 0);
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma2(tmem + C::col_o(x), tmem + C::col_p(x) + kk * 8, ((uint64_t)hi << 32) | (vlo + kk * (2048 >> 4)), idO,
+                 k >= 2 || kk > 0);
+          mma_commit2(&bars.o_done[x]);
+          mma_commit2(&bars.kv_empty[stage]);
+          ++uses[x];
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + 8) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int x = (warp - C::kSoftmaxWarp0) / 4;  // 0: warpgroup A (even tiles), 1: B (odd tiles)
+    const int quarter = warp % 4;
+    const int rl = quarter * 32 + lane;
+    const int row = (int)rank * 128 + rl;  // row within the unit
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = lane_addr + C::col_s(x), tP = lane_addr + C::col_p(x), tO = lane_addr + C::col_o(x);
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    uint32_t g = 0, uses = 0, useg = 0;
+    bool ok = true;
+    Walk walk(sp);
+    Segment s;
+    struct RowOf {
+      bool valid;
+      int node;
+      int64_t orow;
+    };
+    auto row_of = [&](const Segment& sg) {
+      RowOf r;
+      const int unit_row = sg.rg * p.RPG + row;
+      r.valid = unit_row < p.R;
+      r.node = r.valid ? unit_row / p.G : 0;
+      r.orow = ((int64_t)sg.b * p.N + r.node) * p.Hq + sg.kvh * p.G + unit_row % p.G;
+      return r;
+    };
+    // Q rows of a unit into TMEM (warpgroup A), then the even CTA's q_full
+    auto place_q = [&](const Segment& sg) {
+      const RowOf r = row_of(sg);
+      const uint4* src = reinterpret_cast<const uint4*>(q + r.orow * kD);
+      uint4 qr[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) qr[c] = r.valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      if constexpr (kRope) {
+        const uint64_t mrow = r.valid ? __ldg(reinterpret_cast<const unsigned long long*>(p.mask) +
+                                              (int64_t)sg.b * p.mask_bstride + r.node)
+                                      : 1ull;
+        rope_row(qr, p, r.valid ? row_pos(mrow, sg.L) : -1, status, lane);
+      }
+#pragma unroll
+      for (int c = 0; c < kD / 64; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[4 * j] = qr[c * 8 + j].x; v[4 * j + 1] = qr[c * 8 + j].y;
+          v[4 * j + 2] = qr[c * 8 + j].z; v[4 * j + 3] = qr[c * 8 + j].w;
+        }
+        tmem_st32(lane_addr + C::kColQ + c * 32, v);
+      }
+      tmem_st_wait();
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_leader(&bars.q_full, rank);
+    };
+    bool have = walk.next(p, s);
+    if (have && x == 0) place_q(s);
+    while (ok && have) {
+      const RowOf rid = row_of(s);
+      const uint64_t mrow = rid.valid ? __ldg(reinterpret_cast<const unsigned long long*>(p.mask) +
+                                              (int64_t)s.b * p.mask_bstride + rid.node)
+                                      : 1ull;
+      float m_run = -INFINITY, l = 0.f;
+      const int n_seg = s.e - s.a;
+      int mine = 0;  // tiles of this unit this warpgroup computed
+      for (int k = x; k < n_seg; k += 2) {
+        const int t = s.a + k;
+        ok = mbar_wait_warp(&bars.s_full[x], uses & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        float sv[kBlk];
+        {
+          uint32_t r[32];
+          tmem_ld32(tS, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(r[c]);
+          tmem_ld32(tS + 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_leader(&bars.s_free[x], rank);  // the next S_X may be computed now
+        if (t == s.n - 1) {
+#pragma unroll
+          for (int c = 0; c < kBlk; ++c)
+            if (!(c < p.N && ((mrow >> c) & 1ull))) sv[c] = -INFINITY;
+        } else {
+          const int lim = s.L - t * kBlk;
+          if (lim < kBlk) {
+#pragma unroll
+            for (int c = 0; c < kBlk; ++c)
+              if (c >= lim) sv[c] = -INFINITY;
+          }
+        }
+        float mx = row_max64(sv);
+        mx *= p.scale_log2;
+        const float m_new = fmaxf(m_run, mx);
+        const bool grow = m_new > m_run + kRescaleThreshold;
+        const float m_use = grow ? m_new : ((m_run == -INFINITY) ? 0.f : m_run);
+        const uint64_t sc2 = pack_f32x2(p.scale_log2, p.scale_log2), negm2 = pack_f32x2(-m_use, -m_use);
+        uint64_t acc0 = 0, acc1 = 0;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < kBlk / 2; ++c) {
+          float e0, e1;
+          exp2_pair(sv[2 * c], sv[2 * c + 1], sc2, negm2, e0, e1);
+          if (c & 1) acc1 = add_f32x2(acc1, pack_f32x2(e0, e1)); else acc0 = add_f32x2(acc0, pack_f32x2(e0, e1));
+          pk[c] = pack_bf16(e0, e1);
+        }
+        const float sum = sum_f32x2(add_f32x2(acc0, acc1));
+        if (mine > 0) {
+          // P_X of this warpgroup's previous tile consumed; O_X holds it
+          ok = mbar_wait_warp(&bars.o_done[x], (uses - 1) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          if (__any_sync(0xffffffffu, grow)) {
+            const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 32) {
+              uint32_t r[32];
+              tmem_ld32(tO + c, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+              tmem_st32(tO + c, r);
+            }
+          }
+        }
+        if (grow) {
+          l *= exp2f(m_run - m_new);
+          m_run = m_new;
+        }
+        l += sum;
+        tmem_st32(tP, pk);
+        tmem_st_wait();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_leader(&bars.p_full[x], rank);
+        ++uses;
+        ++mine;
+      }
+      if (!ok) break;
+      g += n_seg;
+      Segment s_next;
+      const bool have_next = walk.next(p, s_next);
+      if (x == 1) {
+        // warpgroup B: post (max, sum) once its last P V has completed; its
+        // accumulator stays until warpgroup A has merged it
+        if (mine > 0) {
+          ok = mbar_wait_warp(&bars.o_done[1], (uses - 1) & 1, &bars, status);
+          if (!ok) break;
+        }
+        s_sh[rl] = m_run;
+        s_sh[128 + rl] = mine > 0 ? l : 0.f;
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.sh_stat);
+        ok = mbar_wait_warp(&bars.sh_read, useg & 1, &bars, status);
+        if (!ok) break;
+      } else {
+        ok = mbar_wait_warp(&bars.o_done[0], (uses - 1) & 1, &bars, status);
+        if (ok) ok = mbar_wait_warp(&bars.sh_stat, useg & 1, &bars, status);
+        if (!ok) break;
+        fence_after();
+        // every S product of this unit has been read (ours, and B's before
+        // it posted): the next unit's Q goes in, so its S products run
+        // during this epilogue
+        if (have_next) place_q(s_next);
+        // O = O_A 2^(m_A - m) + O_B 2^(m_B - m), l likewise (a part without
+        // keys adds nothing)
+        const float m1v = s_sh[rl], l1v = s_sh[128 + rl];
+        const bool h0 = l > 0.f, h1 = l1v > 0.f;
+        if (h1) {
+          const float mm = h0 ? fmaxf(m_run, m1v) : m1v;
+          const float a0 = h0 ? exp2f(m_run - mm) : 0.f, a1 = exp2f(m1v - mm);
+          const uint32_t tO1 = lane_addr + C::col_o(1);
+#pragma unroll 1
+          for (int c = 0; c < kD; c += 32) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tO + c, r0);
+            tmem_ld32(tO1 + c, r1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              r0[j] = __float_as_uint((h0 ? __uint_as_float(r0[j]) * a0 : 0.f) + __uint_as_float(r1[j]) * a1);
+            tmem_st32(tO + c, r0);
+          }
+          tmem_st_wait();
+          l = (h0 ? l * a0 : 0.f) + l1v * a1;
+          m_run = mm;
+        } else {
+          // B had no key: its columns are not read (warp-uniform skip of the loads only)
+          __syncwarp();
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.sh_read);  // O_B may be overwritten now
+        // after the slice's last tile the ring goes idle once the last P V
+        // product has completed: a direct merge stages through the K ring
+        uint8_t* stage = nullptr;
+        if (!have_next) {
+          ok = mbar_wait_warp(&bars.kv_empty[(g - 1) % C::kStages], ((g - 1) / C::kStages) & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          stage = smem_raw + (base - raw) + C::kOffK;
+        }
+        finish_row<2>(p, sp, s, row, rid.valid, rid.orow, tO, m_run, l, stage);
+        fence_before();
+      }
+      ++useg;
+      s = s_next;
+      have = have_next;
+    }
+  }
+
+  fence_before();
+  // no CTA of the pair leaves (or frees TMEM) while the other's MMAs may read it
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (warp == C::kAllocWarp) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -2221,7 +2813,47 @@ int launch_pair(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaSt
   return TV_OK;
 }
 
+template <bool kRope>
+int launch_duo(const AttnParams& p, const DuoMaps& maps, int32_t* status, cudaStream_t stream) {
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_tc_duo_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize, DuoCfg::kSmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_duo_kernel)");
+  attn_tc_duo_kernel<kRope><<<2 * p.P, DuoCfg::kThreads, DuoCfg::kSmem, stream>>>(p, maps, status);
+  TV_LAUNCH_CHECK("attn_tc_duo_kernel");
+  return TV_OK;
+}
+
 }  // namespace
+
+int tc_duo_pairs(const DeviceInfo& dev) {
+  // CTA pairs resident at once (one per SM pair the GPCs can place), cached per device
+  static std::mutex mu;
+  static int cached[64] = {};
+  if (dev.device < 0 || dev.device >= 64) return dev.sm_count / 2;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev.device]) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+    cfg.blockDim = dim3(DuoCfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = DuoCfg::kSmem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(attn_tc_duo_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DuoCfg::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, attn_tc_duo_kernel<false>, &cfg) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = dev.sm_count / 2;
+    }
+    cached[dev.device] = n;
+  }
+  return cached[dev.device];
+}
 
 const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim, int rows, int G, int block_size,
                                   bool rope) {
@@ -2278,7 +2910,7 @@ extern "C" int tv_debug_cta_times(void* dst, size_t bytes) {
 }
 #endif
 
-int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
+int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bool duo) {
   EncodeTiled fn;
   int st = get_encoder(&fn);
   if (st) return st;
@@ -2301,6 +2933,26 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream) {
   }
   if (p.RPG <= 128)
     return p.rope_cs ? launch_m<1, true>(p, maps, status, stream) : launch_m<1, false>(p, maps, status, stream);
+  if (duo) {
+    // one unit of up to 256 rows on a CTA pair: half of every K/V tile per SM
+    DuoMaps dm;
+    const int brk = p.block_size < 32 ? p.block_size : 32, brv = p.block_size < kBlk ? p.block_size : kBlk;
+    {
+      cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.num_blocks * p.Hkv * p.block_size};
+      cuuint64_t strides[1] = {row_bytes};
+      cuuint32_t bk[2] = {64, (cuuint32_t)brk}, bv[2] = {64, (cuuint32_t)brv};
+      if ((st = encode(fn, &dm.kc, p.k_cache, 2, dims, strides, bk, "k_cache"))) return st;
+      if ((st = encode(fn, &dm.vc, p.v_cache, 2, dims, strides, bv, "v_cache"))) return st;
+    }
+    {
+      cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.Hkv, (cuuint64_t)p.N, (cuuint64_t)p.B};
+      cuuint64_t strides[3] = {row_bytes, row_bytes * p.Hkv, row_bytes * p.Hkv * p.N};
+      cuuint32_t bk[4] = {64, 1, 32, 1}, bv[4] = {64, 1, (cuuint32_t)kBlk, 1};
+      if ((st = encode(fn, &dm.kt, p.k_tree, 4, dims, strides, bk, "k_tree"))) return st;
+      if ((st = encode(fn, &dm.vt, p.v_tree, 4, dims, strides, bv, "v_tree"))) return st;
+    }
+    return p.rope_cs ? launch_duo<true>(p, dm, status, stream) : launch_duo<false>(p, dm, status, stream);
+  }
   // rows past the two M tiles computed beside them (tc_rows_per_unit gave the unit all R rows)
   if (p.RPG > kTcMaxRows)
     return p.rope_cs ? launch_pair<true, false, true>(p, maps, status, stream)

@@ -30,7 +30,11 @@ int tc_ctas_per_sm(int rows);
 // Virtual tiles the plan charges per unit for this kernel (see AttnParams).
 int tc_unit_cost(int rows_per_unit);
 
-// Launches the persistent tensor-core kernel (plan already enqueued).
-int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream);
+// CTA pairs the CTA-pair kernel keeps resident at once on this device.
+int tc_duo_pairs(const DeviceInfo& dev);
+
+// Launches the persistent tensor-core kernel; with `duo`, units of 129-256
+// rows run on CTA pairs (p.P = pairs).
+int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bool duo);
 
 }  // namespace tv

@@ -97,14 +97,15 @@ def test_prefix_edges(L, dtype):
 @pytest.mark.parametrize("N", [1, 2, 3, 8, 16, 31, 32, 33, 47, 63, 64])
 def test_node_count_sweep(N):
     """Every node count from a single root to 64 nodes (hard-coded sizes were
-    the failure mode of the DDTree post-mortem's mask corruption)."""
+    the failure mode of the DDTree post-mortem's mask corruption); 4 heads per
+    KV head, so 33 nodes and more (129-256 rows) also run on CTA pairs."""
     rng = np.random.default_rng(80 + N)
     paths = W.random_rank_paths(N, 6, rng)
     for dtype, tol in (("f32", F32_TOL), ("bf16", BF16_TOL)):
         w = _workload(3, 4, 1, 128, dtype, 16, N, 90 + N)
         inp = W.attention_inputs(w, device="cuda", seq_lens=[0, 17, 200])
-        for flags in KERNELS:
-            if flags == capi.TV_ATTN_TCGEN05 and (dtype == "f32" or not tc_available(4, 1, N)):
+        for flags in KERNELS + ([capi.TV_ATTN_TCGEN05 | capi.TV_ATTN_CTA_PAIRS] if 4 * N > 128 else []):
+            if (flags & 3) == capi.TV_ATTN_TCGEN05 and (dtype == "f32" or not tc_available(4, 1, N)):
                 continue
             _check_all(inp, paths, tol, flags)
 
@@ -213,6 +214,7 @@ def test_split_unit_merge_routes(G, N):
         pytest.skip("tensor-core kernel unavailable for this shape")
     rng = np.random.default_rng(140 + G + N)
     paths = W.random_rank_paths(N, 6, rng)
+    kinds = [0, capi.TV_ATTN_CTA_PAIRS] if 128 < G * N <= 256 else [0]
     for lens, grids in (([3000, 70, 1500], (2, 7, 40, 152)), ([70, 0, 10], (300,))):
         w = _workload(3, 2 * G, 2, 128, "bf16", 16, N, 141 + N)
         inp = W.attention_inputs(w, device="cuda", seq_lens=lens)
@@ -221,9 +223,9 @@ def test_split_unit_merge_routes(G, N):
         ref = oracle_rows(inp, paths, pairs)
         ref_k = oracle_rows(rot, paths, pairs, rotate=False)
         bound = lse_pipeline_bound(inp, pairs)
-        for num_ctas in grids:
+        for num_ctas, kind in [(c, k) for c in grids for k in kinds]:
             res = []
-            for extra in (0, capi.TV_ATTN_PUBLISH_ALL):
+            for extra in (kind, kind | capi.TV_ATTN_PUBLISH_ALL):
                 flags = capi.TV_ATTN_TCGEN05 | extra
                 out, lse = gpu_pipeline(inp, paths, flags=flags, num_ctas=num_ctas, want_lse=True)
                 assert max_err(out, ref, pairs) <= BF16_TOL, (lens, num_ctas, extra)
@@ -236,8 +238,9 @@ def test_split_unit_merge_routes(G, N):
                 assert torch.equal(a, b), (lens, num_ctas)
 
 
-@pytest.mark.parametrize("G,N,grids", [(8, 33, (2, 3, 7)), (4, 64, (2, 5)), (4, 26, (3,))])
-def test_repeated_calls_bit_identical(G, N, grids):
+@pytest.mark.parametrize("G,N,grids,kind", [(8, 33, (2, 3, 7), 0), (4, 64, (2, 5), 0), (4, 26, (3,), 0),
+                                             (4, 64, (2, 5), 16)])
+def test_repeated_calls_bit_identical(G, N, grids, kind):
     """The same call forty times gives the same bits: every stage of the K/V
     ring is released only after all of its readers are done with it (a tail
     row read through the generic proxy without a proxy fence before the
@@ -251,7 +254,7 @@ def test_repeated_calls_bit_identical(G, N, grids):
     for num_ctas in grids:
         first = None
         for _ in range(40):
-            out, lse = gpu_attention(inp, paths, flags=capi.TV_ATTN_TCGEN05, num_ctas=num_ctas)
+            out, lse = gpu_attention(inp, paths, flags=capi.TV_ATTN_TCGEN05 | kind, num_ctas=num_ctas)
             if first is None:
                 first = (out, lse)
             else:
@@ -332,3 +335,5 @@ def test_full_size_all_nodes_of_sampled_requests(name):
         assert any(b in split for b in bs), "no request with a split unit sampled"
     pairs = [(b, i) for b in sorted(bs) for i in range(w.n_nodes)]
     _check_all(inp, paths, BF16_TOL, capi.TV_ATTN_AUTO, pairs=pairs)
+    if 128 < rows <= 256:  # the same shape on CTA pairs (every node of the same requests)
+        _check_all(inp, paths, BF16_TOL, capi.TV_ATTN_AUTO | capi.TV_ATTN_CTA_PAIRS, pairs=pairs)

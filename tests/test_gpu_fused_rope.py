@@ -64,12 +64,13 @@ CASES = {
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
-@pytest.mark.parametrize("flags", [capi.TV_ATTN_AUTO, capi.TV_ATTN_SIMT, capi.TV_ATTN_TCGEN05])
+@pytest.mark.parametrize("flags", [capi.TV_ATTN_AUTO, capi.TV_ATTN_SIMT, capi.TV_ATTN_TCGEN05,
+                                   capi.TV_ATTN_TCGEN05 | capi.TV_ATTN_CTA_PAIRS])
 def test_fused_equals_separate(name, flags):
     Hq, Hkv, N, lens = CASES[name]
     w, par, inp, _ = _case(Hq, Hkv, N, lens, 300 + N)
     table = capi.tv_rope_table(max(lens) + N + 1, 128, device="cuda")
-    if flags == capi.TV_ATTN_TCGEN05 and Hq // Hkv not in (4, 8, 16):
+    if (flags & 3) == capi.TV_ATTN_TCGEN05 and Hq // Hkv not in (4, 8, 16):
         with pytest.raises(capi.TVError, match="UNSUPPORTED"):
             _fused(inp, par, table, None, flags)
         return
