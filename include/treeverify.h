@@ -414,6 +414,32 @@ int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,
                           int32_t flags, int32_t* status, void* stream);
 
 /*
+ * tv_chain_accept_sample -- device, asynchronous.  The verifier page's own
+ * call shape, "Implement the lossless speculative sampling verifier ...",
+ * "A strong answer" (verify(draft, q, p, num_draft, u, u_final): ragged draft
+ * chains, first rejection stops the chain, replacement from the residual,
+ * bonus after a fully accepted chain).  The same walk, arithmetic and kernels
+ * as tv_tree_accept_sample on the chain whose node j + 1 is draft j (node 0
+ * the last accepted token), bit for bit; the arrays are read where they are
+ * (nothing is copied or allocated).
+ *
+ * p         device float32 [B, K + 1, V]: the target after each prefix (row K:
+ *           after the whole chain, the bonus row).
+ * q         device float32 [B, K, V]: draft j was drawn from q[b, j].
+ * draft     device int32 [B, K]; num_draft device int32 [B] (nullable = K;
+ *           clamped to [0, K]): request b's drafts are draft[b, 0 .. num_draft).
+ * u         device float32 [B, K]: uniform of the test of draft j.
+ * u_final   device float32 [B]: uniform of the replacement / bonus draw.
+ * out       device int32 [B, out_cols] out: emitted tokens, -1 padded;
+ * n_out     device int32 [B] out: accepted drafts + 1.
+ * K in [0, TV_MAX_NODES - 1]; flags, status as in tv_tree_accept_sample.
+ */
+int tv_chain_accept_sample(const float* p, const float* q, const int32_t* draft,
+                           const int32_t* num_draft, const float* u, const float* u_final,
+                           int32_t B, int32_t K, int32_t V, int32_t* out, int32_t* n_out,
+                           int32_t out_cols, int32_t flags, int32_t* status, void* stream);
+
+/*
  * tv_kv_commit -- device, asynchronous.  Copies the accepted path's tree K/V
  * into the paged cache.  "Build the tree attention mask ...", "What it
  * costs." (tree K/V in scratch, the accepted path copied into the cache);

@@ -53,6 +53,8 @@ SIGNATURES = {
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
                                              _I32, _P, _P]),
+    "tv_chain_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P,
+                                              _P]),
     "tv_kv_commit": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
                                     _I32, _I32, _P, _P]),
 }
@@ -68,12 +70,15 @@ _lib = None
 
 
 def lib():
-    """The loaded library (raises if it was not built)."""
+    """The loaded library (raises if it was not built).  The environment
+    variable TREEVERIFY_LIB names another build to load instead (the
+    development build with test hooks)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with speculative_decoding_tree_attn_gb300.build")
-        h = ctypes.CDLL(LIB_PATH)
+        path = os.environ.get("TREEVERIFY_LIB") or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with speculative_decoding_tree_attn_gb300.build")
+        h = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
             f = getattr(h, name)
             f.restype, f.argtypes = res, args
@@ -370,30 +375,44 @@ def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=No
     return out, n_out, path
 
 
-def verify_chain(draft, q, p, num_draft, u, u_final, *, flags=0, status=None, stream=None):
-    """The verifier page's chain interface on top of tv_tree_accept_sample.
+def tv_chain_accept_sample(p, q, draft, u, u_final, *, num_draft=None, out_cols=None, out=None, n_out=None,
+                           flags=0, status=None, stream=None):
+    """The verifier page's chain walk, read in place: p float32 [B, K + 1, V],
+    q float32 [B, K, V], draft int32 [B, K], u float32 [B, K], u_final float32
+    [B], num_draft int32 [B] (optional).  Returns (out [B, out_cols] -1
+    padded, n_out [B] = accepted + 1); allocates nothing when out and n_out
+    are given."""
+    _dev(p, "p", (torch.float32,))
+    _dev(q, "q", (torch.float32,))
+    _dev(draft, "draft", (torch.int32,))
+    _dev(u, "u", (torch.float32,))
+    _dev(u_final, "u_final", (torch.float32,))
+    if num_draft is not None:
+        _dev(num_draft, "num_draft", (torch.int32,))
+    B, K1, V = p.shape
+    K = K1 - 1
+    if tuple(q.shape) != (B, K, V) or tuple(draft.shape) != (B, K) or tuple(u.shape) != (B, K):
+        raise ValueError("tv_chain_accept_sample: q [B, K, V], draft and u [B, K] with p [B, K + 1, V]")
+    out_cols = K1 if out_cols is None else out_cols
+    out, n_out, _ = _accept_outputs(B, out_cols, p.device, out, n_out, False)
+    _check("tv_chain_accept_sample",
+           lib().tv_chain_accept_sample(_ptr(p), _ptr(q), _ptr(draft), _ptr(num_draft), _ptr(u), _ptr(u_final), B,
+                                        K, V, _ptr(out), _ptr(n_out), out_cols, int(flags), _ptr(status),
+                                        _stream(stream)))
+    return out, n_out
 
+
+def verify_chain(draft, q, p, num_draft, u, u_final, *, flags=0, out=None, n_out=None, status=None, stream=None):
+    """The verifier page's verify(draft, q, p, num_draft, u, u_final) call:
     draft int32 [B, K] (draft j drawn from q[:, j]); q float32 [B, K, V]; p
     float32 [B, K + 1, V] (the target after each prefix, the last row for the
     bonus); num_draft int32 [B] (ragged); u float32 [B, K] (one uniform per
     test); u_final float32 [B].  Returns (out int32 [B, K + 1] -1 padded,
-    n_out int32 [B] = accepted + 1).  Only marshalling: the chain is a tree
-    whose node j + 1 is draft j (node 0 the last accepted token), node j's q
-    row is q[:, j] (a zero row for the last node, which has no children)."""
-    B, K = draft.shape
-    V = p.shape[-1]
-    dev = p.device
-    tokens = torch.zeros(B, K + 1, dtype=torch.int32, device=dev)
-    tokens[:, 1:] = draft.to(torch.int32)
-    q_nodes = torch.zeros(B, K + 1, V, dtype=torch.float32, device=dev)
-    q_nodes[:, :K] = q
-    u_nodes = torch.zeros(B, K + 1, dtype=torch.float32, device=dev)
-    u_nodes[:, 1:] = u
-    parent = torch.arange(-1, K, dtype=torch.int32, device=dev)
-    n_nodes = (num_draft.to(torch.int32) + 1).contiguous()
-    out, n_out, _ = tv_tree_accept_sample(p.contiguous(), q_nodes, tokens, parent, u_nodes, u_final.contiguous(),
-                                          n_nodes=n_nodes, flags=flags, status=status, stream=stream)
-    return out, n_out
+    n_out int32 [B] = accepted + 1).  Marshalling only, through
+    tv_chain_accept_sample: the arrays are read in place, and with out and
+    n_out given nothing is allocated."""
+    return tv_chain_accept_sample(p, q, draft, u, u_final, num_draft=num_draft, out=out, n_out=n_out, flags=flags,
+                                  status=status, stream=stream)
 
 
 def accept_greedy(parent, tokens, target_argmax, *, n_nodes=None, status=None, stream=None):

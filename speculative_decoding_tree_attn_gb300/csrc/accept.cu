@@ -94,6 +94,34 @@ __device__ __forceinline__ void load_tree(const int32_t* parent, int64_t pstride
   }
 }
 
+// Where request b's per-node inputs of the stochastic walk live.  The tree
+// call keeps them at entry b * N + c (tokens, u_accept, rows of q); the
+// chain call (the verifier page's verify shape: draft j is node j + 1) reads
+// its own arrays in place: tokens and u of node c >= 1 at entry b * K + c - 1,
+// q of node c at row b * K + c (the last node has no children, so its q row
+// is never read), and num_draft[b] + 1 nodes.
+struct NodeIdx {
+  int64_t bs;  // entries (rows of q) between requests: N (tree) or K (chain)
+  int shift;   // tokens / u of node c: entry b * bs + c - shift
+  int n_add;   // request b has n_nodes[b] + n_add nodes
+  __device__ __forceinline__ int64_t tu(int b, int c) const { return (int64_t)b * bs + c - shift; }
+  __device__ __forceinline__ int64_t qrow(int b, int c) const { return (int64_t)b * bs + c; }
+  __device__ __forceinline__ int nodes(const int32_t* n_nodes, int b, int N) const {
+    if (!n_nodes) return N;
+    const int n = n_nodes[b] + n_add;
+    return n < 1 ? 1 : (n > N ? N : n);
+  }
+};
+
+// load_tree for the stochastic walk (node 0's token is never used).
+__device__ __forceinline__ void load_tree_ix(const int32_t* parent, int64_t pstride, const int32_t* tokens,
+                                             const NodeIdx& ix, int b, int N, int32_t* s_par, int32_t* s_tok) {
+  for (int c = threadIdx.x; c < N; c += blockDim.x) {
+    s_par[c] = parent[(int64_t)b * pstride + c];
+    s_tok[c] = c >= ix.shift ? tokens[ix.tu(b, c)] : -1;
+  }
+}
+
 // Lowest-index valid child of `node` with token `tok` (all threads get it).
 __device__ int find_child(const int32_t* s_par, const int32_t* s_tok, int node, int n, int tok, int* s_best) {
   if (threadIdx.x == 0) *s_best = INT_MAX;
@@ -749,7 +777,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
                                                           const int32_t* __restrict__ n_nodes,
                                                           const float* __restrict__ u_accept,
                                                           const float* __restrict__ u_final, int N, int V,
-                                                          AcceptOut o) {
+                                                          NodeIdx ix, AcceptOut o) {
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
   __shared__ uint64_t S[TV_MAX_NODES + 1];
   __shared__ uint64_t s_red[kSampleWarps], s_base;
@@ -759,10 +787,10 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
   __shared__ int s_flag, s_idx, s_chunk;
   const int b = blockIdx.x;
   TV_SAMPLE_T(0);
-  load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
+  load_tree_ix(parent, pstride, tokens, ix, b, N, s_par, s_tok);
   __syncthreads();
   TV_SAMPLE_T(1);
-  const int n = clamp_nodes(n_nodes, b, N);
+  const int n = ix.nodes(n_nodes, b, N);
   const bool vec = (V % 4 == 0) && (((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q)) & 15) == 0);
   const int groups = (V + 127) / 128;
   int kk = (groups + kMaxChunks - 1) / kMaxChunks;
@@ -774,7 +802,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
   };
   int node = 0, k = 0;
   while (true) {
-    RowView row{p + ((int64_t)b * N + node) * V, q + ((int64_t)b * N + node) * V, V, kk, nc, vec};
+    RowView row{p + ((int64_t)b * N + node) * V, q + ix.qrow(b, node) * V, V, kk, nc, vec};
     int m = 0;
     uint64_t Wm = 0;     // total of the current level (valid for m >= 1)
     if (threadIdx.x == 0) S[0] = 1ull << 40;
@@ -789,7 +817,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
       }
       if (threadIdx.x == 0) {
         const float px = row.p[x], qx = row.q[x];
-        const double uq = __dmul_rn((double)u_accept[(int64_t)b * N + c], (double)qx);
+        const double uq = __dmul_rn((double)u_accept[ix.tu(b, c)], (double)qx);
         bool ok;
         if (m == 0) ok = uq < (double)px;
         else ok = __dmul_rn(uq, (double)Wm) < (double)level_weight(px, qx, S, m);
@@ -1029,7 +1057,7 @@ __global__ void __launch_bounds__(kScThreads, 4)
     sample_cluster_kernel(const float* __restrict__ p, const float* __restrict__ q,
                           const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent, int64_t pstride,
                           const int32_t* __restrict__ n_nodes, const float* __restrict__ u_accept,
-                          const float* __restrict__ u_final, int N, int V, int Ls, AcceptOut o) {
+                          const float* __restrict__ u_final, int N, int V, int Ls, NodeIdx ix, AcceptOut o) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
@@ -1048,10 +1076,10 @@ __global__ void __launch_bounds__(kScThreads, 4)
   const int rank = (int)cl.block_rank();
   const int nct = (int)cl.num_blocks();
   const int b = blockIdx.x / nct;
-  load_tree(parent, pstride, tokens, b, N, s_par, s_tok);
+  load_tree_ix(parent, pstride, tokens, ix, b, N, s_par, s_tok);
   if (threadIdx.x == 0) s_x = V - 1;  // read by rank 0 after the draw's barrier
   __syncthreads();
-  const int n = clamp_nodes(n_nodes, b, N);
+  const int n = ix.nodes(n_nodes, b, N);
   const int lo = min(rank * Ls, V), len = min(V - lo, Ls);
   const int nch = (len + kScChunk - 1) / kScChunk;
   const bool vec = (V % 4 == 0) && (((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q)) & 15) == 0);
@@ -1061,7 +1089,7 @@ __global__ void __launch_bounds__(kScThreads, 4)
   TV_SC_SET(0, sc_t0);
   while (true) {
     const float* prow = p + ((int64_t)b * N + node) * V;
-    const float* qrow = q + ((int64_t)b * N + node) * V;
+    const float* qrow = q + ix.qrow(b, node) * V;
     int m = 0;
     uint64_t Wm = 0;  // total of the current level (valid for m >= 1)
     TV_SC_MARK();
@@ -1083,7 +1111,7 @@ __global__ void __launch_bounds__(kScThreads, 4)
           s_kid[j] = c;
           s_kp[j] = in_v ? prow[x] : 0.f;
           s_kq[j] = in_v ? qrow[x] : 0.f;
-          s_ku[j] = u_accept[(int64_t)b * N + c];
+          s_ku[j] = u_accept[ix.tu(b, c)];
         }
         cnt += __popc(bal);
       }
@@ -1304,21 +1332,27 @@ extern "C" int tv_tree_accept_greedy(const float* logits, const int32_t* target_
   return TV_OK;
 }
 
-extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens, const int32_t* parent,
-                                     int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept,
-                                     const float* u_final, int32_t B, int32_t N, int32_t V, int32_t* out,
-                                     int32_t* n_out, int32_t* path, int32_t out_cols, int32_t flags,
-                                     int32_t* status, void* stream) {
-  tv::clear_error();
-  int st = check_accept_args(B, N, V, tokens, parent, parent_bstride, out, n_out, out_cols);
-  if (st) return st;
-  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_STREAM)
-    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: unknown flags %d", flags);
-  if (B == 0) return TV_OK;
-  if (!p || !q || !u_accept || !u_final) return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: null pointer");
-  AcceptOut o{out, n_out, path, out_cols, status};
+namespace {
+
+// Parent array of a chain (node c's parent is c - 1), shared by every request
+// of the chain call (parent batch stride 0).
+struct ChainParent {
+  int32_t v[TV_MAX_NODES];
+};
+constexpr ChainParent make_chain_parent() {
+  ChainParent c{};
+  for (int i = 0; i < TV_MAX_NODES; ++i) c.v[i] = i - 1;
+  return c;
+}
+__device__ const ChainParent g_chain_parent = make_chain_parent();
+
+// Kernel choice and launch of the stochastic walk (both entry points).
+int launch_sample(const float* p, const float* q, const int32_t* tokens, const int32_t* parent,
+                  int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept, const float* u_final,
+                  int32_t B, int32_t N, int32_t V, NodeIdx ix, AcceptOut o, int32_t flags, void* stream) {
+  int st = TV_OK;
   if (B > INT_MAX / kScCtas && flags != TV_SAMPLE_SINGLE_CTA)
-    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: B=%d too large", B);
+    return tv::fail(TV_ERR_INVALID_ARG, "tree accept sample: B=%d too large", B);
   // 1. one 8-CTA cluster per request keeping the level weights on chip, when
   //    every request's cluster is resident at once (or when asked for)
   const int Ls8 = sc_slice(V, kScCtas);
@@ -1331,12 +1365,12 @@ extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32
     if (flags == TV_SAMPLE_CLUSTER || B <= capacity) {
       L.cfg.gridDim = dim3((unsigned)(B * kScCtas));
       cudaError_t e = cudaLaunchKernelEx(&L.cfg, sample_cluster_kernel<true>, p, q, tokens, parent, parent_bstride,
-                                         n_nodes, u_accept, u_final, (int)N, (int)V, Ls8, o);
+                                         n_nodes, u_accept, u_final, (int)N, (int)V, Ls8, ix, o);
       if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel<state>");
       return TV_OK;
     }
   } else if (flags == TV_SAMPLE_CLUSTER) {
-    return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_accept_sample: the cluster kernel needs V <= %d (V=%d)",
+    return tv::fail(TV_ERR_UNSUPPORTED, "tree accept sample: the cluster kernel needs V <= %d (V=%d)",
                     kScCtas * (int)(kScMaxDyn / 12 / 4 * 4), V);
   }
   // 2. streaming clusters: the largest cluster (8, 4, 2 or 1 CTAs) with which
@@ -1358,12 +1392,12 @@ extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32
       ScLaunch L(pick, dyn, stream);
       L.cfg.gridDim = dim3((unsigned)(B * pick));
       cudaError_t e = cudaLaunchKernelEx(&L.cfg, sample_cluster_kernel<false>, p, q, tokens, parent, parent_bstride,
-                                         n_nodes, u_accept, u_final, (int)N, (int)V, sc_slice(V, pick), o);
+                                         n_nodes, u_accept, u_final, (int)N, (int)V, sc_slice(V, pick), ix, o);
       if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel<stream>");
       return TV_OK;
     }
     if (flags == TV_SAMPLE_STREAM)
-      return tv::fail(TV_ERR_UNSUPPORTED, "tv_tree_accept_sample: V=%d too large for the streaming clusters", V);
+      return tv::fail(TV_ERR_UNSUPPORTED, "tree accept sample: V=%d too large for the streaming clusters", V);
   }
   // one CTA per request, rows streamed and w_m recomputed per pass
   constexpr size_t kDyn = sizeof(float4) * 2 * kStreamStages * (kStageElems / 4) + sizeof(uint64_t) * kMaxChunks;
@@ -1371,7 +1405,49 @@ extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32
   cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDyn);
   if (e != cudaSuccess) return tv::cuda_fail(e, "cudaFuncSetAttribute(sample_kernel)");
   sample_kernel<<<B, kSampleThreads, kDyn, (cudaStream_t)stream>>>(p, q, tokens, parent, parent_bstride, n_nodes, u_accept,
-                                                           u_final, N, V, o);
+                                                           u_final, N, V, ix, o);
   TV_LAUNCH_CHECK("sample_kernel");
   return TV_OK;
+}
+
+}  // namespace
+
+extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens, const int32_t* parent,
+                                     int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept,
+                                     const float* u_final, int32_t B, int32_t N, int32_t V, int32_t* out,
+                                     int32_t* n_out, int32_t* path, int32_t out_cols, int32_t flags,
+                                     int32_t* status, void* stream) {
+  tv::clear_error();
+  int st = check_accept_args(B, N, V, tokens, parent, parent_bstride, out, n_out, out_cols);
+  if (st) return st;
+  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_STREAM)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: unknown flags %d", flags);
+  if (B == 0) return TV_OK;
+  if (!p || !q || !u_accept || !u_final) return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: null pointer");
+  return launch_sample(p, q, tokens, parent, parent_bstride, n_nodes, u_accept, u_final, B, N, V, NodeIdx{N, 0, 0},
+                       AcceptOut{out, n_out, path, out_cols, status}, flags, stream);
+}
+
+extern "C" int tv_chain_accept_sample(const float* p, const float* q, const int32_t* draft, const int32_t* num_draft,
+                                      const float* u, const float* u_final, int32_t B, int32_t K, int32_t V,
+                                      int32_t* out, int32_t* n_out, int32_t out_cols, int32_t flags, int32_t* status,
+                                      void* stream) {
+  tv::clear_error();
+  if (B < 0 || K < 0 || K + 1 > TV_MAX_NODES || V < 1 || out_cols < 1)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_chain_accept_sample: bad sizes B=%d K=%d V=%d out_cols=%d", B, K, V,
+                    out_cols);
+  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_STREAM)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_chain_accept_sample: unknown flags %d", flags);
+  if (B == 0) return TV_OK;
+  if (!p || !u_final || !out || !n_out || (K > 0 && (!q || !draft || !u)))
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_chain_accept_sample: null pointer");
+  const int32_t* parent = nullptr;
+  cudaError_t e = cudaGetSymbolAddress((void**)&parent, g_chain_parent);
+  if (e != cudaSuccess) return tv::cuda_fail(e, "cudaGetSymbolAddress(chain parent)");
+  // K = 0: no node is read but the root; any valid address stands in
+  const float* qq = K > 0 ? q : p;
+  const int32_t* tok = K > 0 ? draft : parent;
+  const float* uu = K > 0 ? u : u_final;
+  return launch_sample(p, qq, tok, parent, 0, num_draft, uu, u_final, B, K + 1, V, NodeIdx{K, 1, 1},
+                       AcceptOut{out, n_out, nullptr, out_cols, status}, flags, stream);
 }

@@ -116,6 +116,7 @@ struct Bars {
   uint64_t q_full;
   uint64_t sh_stat, sh_read;  // shared units (two-M-tile kernel): M tile 1's part posted / read
   uint64_t tail_sync;         // tail rows (two-M-tile kernel): the four producer warps' end-of-unit exchange
+  uint64_t drain[4];          // one per MMA-issuing thread: its products have completed (after an abort)
   uint32_t tmem_base;
   int abort;
 };
@@ -131,6 +132,22 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+#ifdef TV_TEST_HOOKS
+// Development builds only (-DTV_TEST_HOOKS; the product library has neither
+// variable): a test shortens the wait limit and has CTA 0's TMA producers
+// skip the loads (and the arrival) of one ring tile, so that the bounded
+// waits run out and the timeout exit is exercised without a fault.
+__device__ unsigned long long g_test_timeout_ns = kTimeoutNs;
+__device__ int g_test_withhold = -1;  // ring index of CTA 0 left without loads
+__device__ __forceinline__ unsigned long long timeout_ns() { return *(volatile unsigned long long*)&g_test_timeout_ns; }
+__device__ __forceinline__ bool test_withhold(uint32_t g) {
+  return blockIdx.x == 0 && (int)g == *(volatile int*)&g_test_withhold;
+}
+#else
+__device__ __forceinline__ unsigned long long timeout_ns() { return kTimeoutNs; }
+__device__ __forceinline__ bool test_withhold(uint32_t) { return false; }
+#endif
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -165,7 +182,7 @@ __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, Bars* bars, int32_t* s
     if (mbar_test(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (honor_abort && *(volatile int*)&bars->abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > timeout_ns()) {
         *(volatile int*)&bars->abort = 1;
         if (status) atomicOr(status, TV_DEV_TIMEOUT);
         return false;
@@ -184,7 +201,7 @@ __device__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, Bars* bars, int32
     if (!done) done = mbar_test(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     if ((it & 255u) == 0) {
-      bool stop = *(volatile int*)&bars->abort != 0 || globaltimer() - t0 > kTimeoutNs;
+      bool stop = *(volatile int*)&bars->abort != 0 || globaltimer() - t0 > timeout_ns();
       if (__any_sync(0xffffffffu, stop)) {
         if ((threadIdx.x & 31) == 0 && !*(volatile int*)&bars->abort) {
           *(volatile int*)&bars->abort = 1;
@@ -269,6 +286,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint32_t b_lo, ui
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// After an abort: the issuing thread waits (bounded) until every MMA it has
+// issued has completed, so that no product still writes TMEM or reads a
+// stage when the CTA frees TMEM and exits.
+__device__ __forceinline__ void mma_drain(Bars& bars, int i) {
+  mma_commit(&bars.drain[i]);
+  mbar_wait(&bars.drain[i], 0, &bars, nullptr, false);
 }
 
 #define TV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
@@ -1020,6 +1045,7 @@ __device__ __forceinline__ void run_producer(const AttnParams& p, const SlicePla
         const int64_t blk = rel < 32 ? from_cur : from_nxt;
         if (use > 0) ok = mbar_wait_warp(&bars.kv_empty[stage], (use - 1) & 1, &bars, status);
         if (!ok) break;
+        if (test_withhold(g)) continue;  // development builds only
         if (prod == 0 && lane == 0) { TV_TRACE(0, g); mbar_expect_tx(&bars.kv_full[stage], 2 * kKVTileBytes); }
         __syncwarp();
         const uint32_t dst = dst_base + stage * kKVTileBytes;
@@ -1090,6 +1116,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
       mbar_init(&bars.o_done[m], 1);
     }
     mbar_init(&bars.q_full, 128 * M);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.drain[i], 1);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1169,6 +1196,7 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
         TV_TRACE(4 + m, g - 1);
         ++seg_i;
       }
+      if (!ok) mma_drain(bars, m);
     }
     __syncwarp();
   } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + 4 * M) {
@@ -1792,6 +1820,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     mbar_init(&bars.sh_stat, 128);
     mbar_init(&bars.sh_read, 128);
     mbar_init(&bars.tail_sync, 32 * kTailWarps);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.drain[i], 1);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1868,6 +1897,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         }
         ++seg_i;
       }
+      if (!ok) mma_drain(bars, m);
     }
     __syncwarp();
   } else if (warp == 6 || warp == 7) {
@@ -1908,6 +1938,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           if (m == 0) TV_TRACE(4, g);
         }
       }
+      if (!ok) mma_drain(bars, 2 + m);
     }
     __syncwarp();
   } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + 8) {
@@ -2272,7 +2303,7 @@ __device__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, Bars* bars, int32_t
     if (mbar_test_cluster(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*(volatile int*)&bars->abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > timeout_ns()) {
         *(volatile int*)&bars->abort = 1;
         if (status) atomicOr(status, TV_DEV_TIMEOUT);
         return false;
@@ -2298,6 +2329,13 @@ __device__ __forceinline__ void mma_commit2(uint64_t* bar) {
           smem_u32(bar)),
       "h"((uint16_t)3)
       : "memory");
+}
+
+// mma_drain for the pair's MMA issuer (the commit arrives on both CTAs'
+// copies of the barrier; the issuer waits on its own).
+__device__ __forceinline__ void mma_drain2(Bars& bars, int i) {
+  mma_commit2(&bars.drain[i]);
+  mbar_wait(&bars.drain[i], 0, &bars, nullptr, false);
 }
 
 struct DuoMaps {
@@ -2436,6 +2474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoCfg::kThreads, 1)
     mbar_init(&bars.q_full, 8);
     mbar_init(&bars.sh_stat, 4);
     mbar_init(&bars.sh_read, 4);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.drain[i], 1);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -2505,6 +2544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoCfg::kThreads, 1)
         }
         ++seg_i;
       }
+      if (!ok) mma_drain2(bars, x);
     }
     __syncwarp();
   } else if (warp == 6) {
@@ -2532,6 +2572,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoCfg::kThreads, 1)
           ++uses[x];
         }
       }
+      if (!ok) mma_drain2(bars, 2);
     }
     __syncwarp();
   } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + 8) {
@@ -2965,3 +3006,14 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bo
 }
 
 }  // namespace tv
+
+#ifdef TV_TEST_HOOKS
+// Development builds only: sets the wait limit of the tensor-core kernels and
+// the ring tile of CTA 0 whose TMA loads are withheld (-1: none).  Not part of
+// the product library's interface.
+extern "C" int tv_test_set_hooks(unsigned long long timeout_ns, int withhold_tile) {
+  if (cudaMemcpyToSymbol(tv::g_test_timeout_ns, &timeout_ns, sizeof(timeout_ns)) != cudaSuccess) return -6;
+  if (cudaMemcpyToSymbol(tv::g_test_withhold, &withhold_tile, sizeof(withhold_tile)) != cudaSuccess) return -6;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -6;
+}
+#endif

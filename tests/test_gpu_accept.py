@@ -95,6 +95,12 @@ def test_sample_full_workload_bit_exact(kernel):
     out_c, n_c = OA.verify_chain(c["tokens"][:, 1:], c["q"][:, :K], c["p"], c["n_nodes"] - 1, c["u_accept"][:, 1:],
                                  c["u_final"])
     np.testing.assert_array_equal(res[1].cpu().numpy(), n_c)
+    # the chain call reads the page's arrays in place: the same bits
+    out2, n2 = capi.tv_chain_accept_sample(s["p"], s["q"][:, :K].contiguous(), s["tokens"][:, 1:].contiguous(),
+                                           s["u_accept"][:, 1:].contiguous(), s["u_final"],
+                                           num_draft=(s["n_nodes"] - 1).contiguous(), flags=KERNELS[kernel])
+    np.testing.assert_array_equal(n2.cpu().numpy(), n_c)
+    np.testing.assert_array_equal(out2.cpu().numpy(), out_c)
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -290,3 +296,36 @@ def test_page_interfaces():
     am = rng.integers(0, 4, size=(B, parent.size)).astype(np.int32)
     res = capi.accept_greedy(t(parent.astype(np.int32)), t(tokens), t(am))
     _cmp(res, *OA.tree_accept_greedy(am, tokens, parent))
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_chain_call_allocates_nothing(kernel):
+    """verify_chain with its outputs passed in allocates no device memory
+    (neither through PyTorch nor behind it) and matches the oracle bit for
+    bit, with num_draft given or not and for K = 0 (bonus draw only)."""
+    rng = np.random.default_rng(143)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    for B, K, V, give_nd in ((64, 7, 5000, True), (64, 7, 5000, False), (9, 0, 333, True)):
+        p = rng.dirichlet(np.ones(V) * 0.3, size=(B, K + 1)).astype(np.float32)
+        q = rng.dirichlet(np.ones(V) * 0.3, size=(B, K)).astype(np.float32)
+        q[:B // 4] = p[:B // 4, :K]
+        draft = np.stack([[rng.choice(V, p=q[b, j] / q[b, j].sum()) for j in range(K)] for b in range(B)]
+                         ).astype(np.int32).reshape(B, K)
+        nd = rng.integers(0, K + 1, size=B).astype(np.int32) if give_nd else np.full(B, K, np.int32)
+        u = rng.random((B, K), dtype=np.float32)
+        uf = rng.random(B, dtype=np.float32)
+        args = [t(draft), t(q), t(p), t(nd) if give_nd else None, t(u), t(uf)]
+        out = torch.empty(B, K + 1, dtype=torch.int32, device="cuda")
+        n_out = torch.empty(B, dtype=torch.int32, device="cuda")
+        capi.verify_chain(*args, out=out, n_out=n_out, flags=KERNELS[kernel])  # first call: one-time set-up
+        r = None  # drop the previous case's outputs before counting
+        torch.cuda.synchronize()
+        alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+        for _ in range(3):
+            r = capi.verify_chain(*args, out=out, n_out=n_out, flags=KERNELS[kernel])
+        torch.cuda.synchronize()
+        assert r[0] is out and r[1] is n_out
+        assert torch.cuda.memory_allocated() == alloc0 and torch.cuda.mem_get_info()[0] == free0
+        r_out, r_n = OA.verify_chain(draft, q, p, nd, u, uf)
+        np.testing.assert_array_equal(n_out.cpu().numpy(), r_n)
+        np.testing.assert_array_equal(out.cpu().numpy(), r_out)
