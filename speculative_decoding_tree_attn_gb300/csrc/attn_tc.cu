@@ -1361,29 +1361,33 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
 // second row group would stream the unit's whole K/V a second time for a few
 // rows, and a third M tile costs as much tensor time as a full one and does
 // not fit in TMEM.  The rows 256 .. R - 1 (at most kTailRows) are instead
-// computed from the K/V tiles already in the stage ring by two warps of
-// their own (the kernel's producer warps 2 and 3; warps 0 and 1 issue all
-// TMA boxes), with warp-level bf16 MMAs (mma.sync m16n8k16, fp32
+// computed from the K/V tiles already in the stage ring by warps of their
+// own (kTW tail warps), with warp-level bf16 MMAs (mma.sync m16n8k16, fp32
 // accumulation) in transposed form, so that the tail rows sit on the MMA's
 // 8-wide N side and nothing is padded:
 //   S^T [16 keys x 8 rows]  = K[16 keys x 128] Q_tail^T
 //   O_w^T [128 x 8 rows]   += V[16 keys x 128]^T P^T
-// Tail warp w takes keys 32w .. 32w + 31 of every tile (two 16-key blocks)
-// and keeps its own running maximum and sum over them; the two parts are
-// merged once per unit, in warp order, and the rows are written (or, for a
-// split unit, published and merged) with the same arithmetic as the other
-// rows' memory merge.  A tail warp frees a stage with its own arrival on the
+// Tail warp w takes keys (64 / kTW) w .. (64 / kTW)(w + 1) - 1 of every tile
+// and keeps its own running maximum and sum over them; the parts are merged
+// once per unit, in warp order, and the rows are written (or, for a split
+// unit, published and merged) with the same arithmetic as the other rows'
+// memory merge.  A tail warp frees a stage with its own arrival on the
 // stage's empty barrier once its reads of the stage are done, so the ring
 // waits for the tail as it waits for the P V products; the tail warps lag the
 // TMA stream by at most the ring's depth and never hold up a TMA issue.
+//
+// These MMAs share the SM's tensor pipe with the tcgen05 products: while
+// those run, one sub-partition completes a warp-level MMA only every 40-70
+// cycles (measured), so the tail is spread over as many sub-partitions as
+// the launch allows -- four tail warps, one per sub-partition, when one TMA
+// warp can issue a tile's boxes (block size >= 32: at most 8 boxes), else two.
 constexpr int kTailRows = 8;
-constexpr int kTailWarps = 2;
-constexpr int kTailKeys = kBlk / kTailWarps;  // keys of a tile per tail warp (two 16-key blocks)
 
+template <int kTW>
 struct TailSmem {
-  float m[kTailWarps][kTailRows];                      // per warp at the unit's end: running maximum (log2)
-  float l[kTailWarps][kTailRows];                      //   ... and the sum of its keys' weights
-  float o[kTailWarps][kTailRows][kD];                  //   ... and its unnormalised rows
+  float m[kTW][kTailRows];                      // per warp at the unit's end: running maximum (log2)
+  float l[kTW][kTailRows];                      //   ... and the sum of its keys' weights
+  float o[kTW][kTailRows][kD];                  //   ... and its unnormalised rows
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -1491,19 +1495,23 @@ __device__ __forceinline__ void tail_begin(const AttnParams& p, const Segment& s
 }
 
 // Tile t of the segment from the stage at kb (K) / vb (V): S^T of this
-// warp's 32 keys, online softmax over them, O^T += V^T P^T.
+// warp's 64 / kTW keys, online softmax over them, O^T += V^T P^T.
+template <int kTW>
 __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s, int t, uint32_t kb, uint32_t vb,
                                           TailRowsState& ts, int w, int lane) {
+  constexpr int kTailKeys = kBlk / kTW;  // keys of a tile per tail warp
+  constexpr int kNB = kTailKeys / 16;    // 16-key blocks per tail warp
+  static_assert(kNB >= 1 && kNB * 16 * kTW == kBlk, "whole 16-key blocks per tail warp");
   const int g = lane >> 2, tq = lane & 3, i8 = lane >> 3;
   // S^T per 16-key block: A = K rows x 16 head dims per step, by ldmatrix:
   // matrices (keys 0-7 | 8-15) x (dims 0-7 | 8-15) of the step, lane
   // i8 * 8 + r addressing row r of matrix i8; four accumulators per block
   // (steps ks, ks + 4 chained) so that MMA latency overlaps
-  float sv[2][4];
+  float sv[kNB][4];
   {
-    float acc[2][4][4];
+    float acc[kNB][4][4];
 #pragma unroll
-    for (int kb2 = 0; kb2 < 2; ++kb2)
+    for (int kb2 = 0; kb2 < kNB; ++kb2)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -1511,7 +1519,7 @@ __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s,
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-      for (int kb2 = 0; kb2 < 2; ++kb2) {
+      for (int kb2 = 0; kb2 < kNB; ++kb2) {
         const int key = kTailKeys * w + 16 * kb2 + (lane & 7) + 8 * (i8 & 1);
         uint32_t a[4];
         ldsm_x4(kb + key * 128 + (ks >> 2) * kKVHalfBytes + (((2 * (ks & 3) + (i8 >> 1)) ^ (key & 7)) << 4), a);
@@ -1519,14 +1527,14 @@ __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s,
       }
     }
 #pragma unroll
-    for (int kb2 = 0; kb2 < 2; ++kb2)
+    for (int kb2 = 0; kb2 < kNB; ++kb2)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         sv[kb2][e] = (acc[kb2][0][e] + acc[kb2][1][e]) + (acc[kb2][2][e] + acc[kb2][3][e]);
   }
   // sv[kb2]: (key k, row 2t), (k, 2t + 1), (k + 8, 2t), (k + 8, 2t + 1), k = 32w + 16 kb2 + g
 #pragma unroll
-  for (int kb2 = 0; kb2 < 2; ++kb2) {
+  for (int kb2 = 0; kb2 < kNB; ++kb2) {
     const int k0 = kTailKeys * w + 16 * kb2 + g, k1 = k0 + 8;
     if (t == s.n - 1) {
       if (!(k0 < p.N && ((ts.mr[0] >> k0) & 1ull))) sv[kb2][0] = -INFINITY;
@@ -1539,8 +1547,12 @@ __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s,
       if (k1 >= lim) sv[kb2][2] = sv[kb2][3] = -INFINITY;
     }
   }
-  float mx[2] = {fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2])),
-                 fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]))};
+  float mx[2] = {fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[0][1], sv[0][3])};
+#pragma unroll
+  for (int kb2 = 1; kb2 < kNB; ++kb2) {
+    mx[0] = fmaxf(mx[0], fmaxf(sv[kb2][0], sv[kb2][2]));
+    mx[1] = fmaxf(mx[1], fmaxf(sv[kb2][1], sv[kb2][3]));
+  }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
 #pragma unroll
@@ -1563,27 +1575,35 @@ __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s,
     }
     m_use[j] = ts.m_run[j] == -INFINITY ? 0.f : ts.m_run[j];
   }
-  float pv[2][4];
+  float pv[kNB][4];
 #pragma unroll
-  for (int kb2 = 0; kb2 < 2; ++kb2)
+  for (int kb2 = 0; kb2 < kNB; ++kb2)
 #pragma unroll
     for (int e = 0; e < 4; ++e) pv[kb2][e] = fast_exp2(fmaf(sv[kb2][e], p.scale_log2, -m_use[e & 1]));
-  ts.l[0] += (pv[0][0] + pv[0][2]) + (pv[1][0] + pv[1][2]);
-  ts.l[1] += (pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]);
+  {
+    float l0 = pv[0][0] + pv[0][2], l1 = pv[0][1] + pv[0][3];
+#pragma unroll
+    for (int kb2 = 1; kb2 < kNB; ++kb2) {
+      l0 += pv[kb2][0] + pv[kb2][2];
+      l1 += pv[kb2][1] + pv[kb2][3];
+    }
+    ts.l[0] += l0;
+    ts.l[1] += l1;
+  }
   // P^T as the B operand of O^T: the weights of (key g | g + 8, rows 2t,
   // 2t + 1), packed as bf16 pairs, are 8x8 fragments of P[key][row];
   // movmatrix transposes them in registers to P[row g][keys 2t, 2t + 1]
   // (resp. 8 + 2t, 9 + 2t), the B fragment layout
-  uint32_t bp[2][2];
+  uint32_t bp[kNB][2];
 #pragma unroll
-  for (int kb2 = 0; kb2 < 2; ++kb2) {
+  for (int kb2 = 0; kb2 < kNB; ++kb2) {
     bp[kb2][0] = movmatrix_trans(pack_bf16(pv[kb2][0], pv[kb2][1]));
     bp[kb2][1] = movmatrix_trans(pack_bf16(pv[kb2][2], pv[kb2][3]));
   }
   // O^T: A = V^T (16 head dims x 16 keys) by transposing ldmatrix of the V
   // rows: matrices (dims 0-7 | 8-15) x (keys 0-7 | 8-15)
 #pragma unroll
-  for (int kb2 = 0; kb2 < 2; ++kb2) {
+  for (int kb2 = 0; kb2 < kNB; ++kb2) {
     const int key = kTailKeys * w + 16 * kb2 + (lane & 7) + 8 * (i8 >> 1);
     const uint32_t row = vb + key * 128;
     const int sw = key & 7;
@@ -1601,11 +1621,13 @@ __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s,
 // completes the rows' arrival counts merges them from memory, with the
 // arithmetic of the other rows' memory merge.  Collective over the tail
 // warps (two passes of the tail_sync barrier).
+template <int kTW>
 __device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& sp, const Segment& s, TailRowsState& ts,
-                                         TailSmem* sm, Bars& bars, uint32_t& tb, int w, int lane, int32_t* status) {
+                                         TailSmem<kTW>* sm, Bars& bars, uint32_t& tb, int w, int lane,
+                                         int32_t* status) {
   constexpr float kLn2 = 0.69314718055994530942f;
-  constexpr int kThreadsPerRow = 32 * kTailWarps / kTailRows;
-  constexpr int kCols = kD / kThreadsPerRow;  // head dims per thread in the merge
+  constexpr int kThreadsPerRow = 64 / kTailRows;  // the merge runs on tail warps 0 and 1
+  constexpr int kCols = kD / kThreadsPerRow;      // head dims per thread in the merge
   static_assert(kCols == 16, "the merge below handles 16 head dims per thread");
   const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
@@ -1626,16 +1648,22 @@ __device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& s
   mbar_arrive(&bars.tail_sync);
   if (!mbar_wait_warp(&bars.tail_sync, tb & 1, &bars, status)) return false;
   ++tb;
-  // thread i of the tail warps: tail row i / 8, head dims (i % 8) * 16 .. + 15
+  if (w >= 2) {  // the scratch is read by tail warps 0 and 1 only
+    mbar_arrive(&bars.tail_sync);
+    const bool ok = mbar_wait_warp(&bars.tail_sync, tb & 1, &bars, status);
+    ++tb;
+    return ok;
+  }
+  // thread i of tail warps 0 and 1: tail row i / 8, head dims (i % 8) * 16 .. + 15
   const int i = w * 32 + lane;
   const int r = i / kThreadsPerRow, d0 = (i % kThreadsPerRow) * kCols;
   const int ur = kTcMaxRows + r;
   float M = -INFINITY;
 #pragma unroll
-  for (int q = 0; q < kTailWarps; ++q) M = fmaxf(M, sm->m[q][r]);
-  float a[kTailWarps], l = 0.f;
+  for (int q = 0; q < kTW; ++q) M = fmaxf(M, sm->m[q][r]);
+  float a[kTW], l = 0.f;
 #pragma unroll
-  for (int q = 0; q < kTailWarps; ++q) {
+  for (int q = 0; q < kTW; ++q) {
     a[q] = M == -INFINITY ? 0.f : exp2f(sm->m[q][r] - M);
     l = fmaf(a[q], sm->l[q][r], l);
   }
@@ -1644,7 +1672,7 @@ __device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& s
   for (int j = 0; j < kCols; ++j) {
     float acc = 0.f;
 #pragma unroll
-    for (int q = 0; q < kTailWarps; ++q) acc = fmaf(a[q], sm->o[q][r][d0 + j], acc);
+    for (int q = 0; q < kTW; ++q) acc = fmaf(a[q], sm->o[q][r][d0 + j], acc);
     v[j] = acc;
   }
   // the scratch may be reused once every tail thread has read it
@@ -1697,9 +1725,9 @@ __device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& s
 
 // A tail warp's loop: every tile of the CTA's slice, in ring order, after
 // the TMA producers' loads land; the stage is freed after the warp's reads.
-template <int kStages, bool kRope>
+template <int kStages, bool kRope, int kTW>
 __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& sp, Bars& bars, uint32_t sK, uint32_t sV,
-                                         TailSmem* tsm, int w, int lane, int32_t* status) {
+                                         TailSmem<kTW>* tsm, int w, int lane, int32_t* status) {
   uint32_t g = 0, tb = 0;
   bool ok = true;
   Walk walk(sp);
@@ -1711,7 +1739,7 @@ __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& s
       const int stage = g % kStages;
       ok = mbar_wait_warp(&bars.kv_full[stage], (g / kStages) & 1, &bars, status);
       if (!ok) break;
-      tail_tile(p, s, t, sK + stage * kKVTileBytes, sV + stage * kKVTileBytes, ts, w, lane);
+      tail_tile<kTW>(p, s, t, sK + stage * kKVTileBytes, sV + stage * kKVTileBytes, ts, w, lane);
       // the stage was read through the generic proxy (ldmatrix) and the next
       // TMA load writes it through the async proxy: order the reads first
       fence_proxy_async();
@@ -1719,7 +1747,7 @@ __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& s
       if (lane == 0) mbar_arrive(&bars.kv_empty[stage]);
     }
     if (!ok) break;
-    ok = tail_end(p, sp, s, ts, tsm, bars, tb, w, lane, status);
+    ok = tail_end<kTW>(p, sp, s, ts, tsm, bars, tb, w, lane, status);
   }
 }
 
@@ -1734,17 +1762,20 @@ __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& s
 //  * TMEM (512 columns) holds S_0 S_1 P_0 P_1 Q_0 O_0 O_1 = 64+64+32+32+64+128+128;
 //    Q_1 therefore stays in shared memory (S_1 = Q_1 K^T reads both operands
 //    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
-template <bool kTail>
+template <int kTailW>
 struct PairCfgT {
   // Five K/V stages (measured 1-3 % faster than six on the 64-request and
   // long-context shapes); the shared memory left holds the tail rows'
   // end-of-unit scratch.
   static constexpr int kStages = 5;
-  // Warps 0-3 issue TMA (and, with tail rows, compute them), 4-7 issue MMAs
-  // (S_0, S_1, PV_0, PV_1), 8-15 are the two softmax warpgroups: warp w runs
-  // on sub-partition w % 4, so each sub-partition carries one producer, one
-  // issuer and two softmax warps.
-  static constexpr int kProducers = 4;
+  // Warps 0-3 issue TMA, 4-7 issue MMAs (S_0, S_1, PV_0, PV_1), 8-15 are the
+  // two softmax warpgroups: warp w runs on sub-partition w % 4, so each
+  // sub-partition carries one producer, one issuer and two softmax warps.
+  // With two tail warps (kTailW = 2), warps 0-1 issue TMA and 2-3 compute the
+  // tail rows; with four, warps 0-3 compute the tail rows, warp 6 issues both
+  // P V products and warp 7 issues TMA.
+  static_assert(kTailW == 0 || kTailW == 2 || kTailW == 4, "0, 2 or 4 tail warps");
+  static constexpr int kProducers = kTailW == 4 ? 1 : 4 - kTailW;
   static constexpr int kThreads = 32 * 16;
   static constexpr int kAllocWarp = 4;
   static constexpr uint32_t kTmemCols = 512;
@@ -1752,7 +1783,7 @@ struct PairCfgT {
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
   static constexpr int kOffQ1 = kOffV + kStages * kKVTileBytes;  // 2 halves x 128 rows x 128 B
   static constexpr int kOffTail = kOffQ1 + 2 * 128 * 128;
-  static constexpr int kBytes = kOffTail + (kTail ? (int)sizeof(TailSmem) : 0);
+  static constexpr int kBytes = kOffTail + (kTailW ? (int)sizeof(TailSmem<kTailW>) : 0);
   static constexpr int kSmem = kBytes + 1024;
   static constexpr uint32_t col_s(int m) { return m * 64; }
   static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
@@ -1760,9 +1791,9 @@ struct PairCfgT {
   static constexpr uint32_t col_o(int m) { return 256 + m * 128; }
   static constexpr int kSoftmaxWarp0 = 8;
 };
-using PairCfg = PairCfgT<false>;
-static_assert(PairCfgT<true>::kSmem <= 227 * 1024 - 1024, "the tail variant fits the opt-in shared memory");
-static_assert(PairCfgT<true>::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
+using PairCfg = PairCfgT<0>;
+static_assert(PairCfgT<4>::kSmem <= 227 * 1024 - 1024, "the tail variant fits the opt-in shared memory");
+static_assert(PairCfgT<4>::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 static_assert(PairCfg::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 
 // The unit is the last row group of a (request, KV head) with at most 128
@@ -1786,11 +1817,11 @@ __device__ __forceinline__ bool shared_unit(const AttnParams& p, const Segment& 
 // shared units alone and M tile 1's part is empty.
 constexpr bool kSplitKeys = false;
 __device__ __forceinline__ int sh_owner(int t) { return kSplitKeys ? (t & 1) : 0; }
-template <bool kRope, bool kSkip, bool kTail>
+template <bool kRope, bool kSkip, int kTailW>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
-  using C = PairCfgT<kTail>;
-  static_assert(!(kSkip && kTail), "tail rows replace the second row group");
+  using C = PairCfgT<kTailW>;
+  static_assert(!(kSkip && kTailW), "tail rows replace the second row group");
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   __shared__ float s_sh[kSkip ? 256 : 1];  // shared units: M tile 1's running max and sum per row
@@ -1808,7 +1839,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], kTail ? 2 + kTailWarps : 2);  // one commit from each O issuer (+ the tail warps)
+      mbar_init(&bars.kv_empty[s], 2 + kTailW);  // one commit per P V product (+ one arrival per tail warp)
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(&bars.s_full[m], 1);
@@ -1819,7 +1850,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     mbar_init(&bars.q_full, 256);
     mbar_init(&bars.sh_stat, 128);
     mbar_init(&bars.sh_read, 128);
-    mbar_init(&bars.tail_sync, 32 * kTailWarps);
+    mbar_init(&bars.tail_sync, 32 * (kTailW ? kTailW : 1));
     for (int i = 0; i < 4; ++i) mbar_init(&bars.drain[i], 1);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1836,18 +1867,52 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   constexpr uint32_t hi = desc_hi(1024);
 
-  if (warp < C::kProducers) {
-    if constexpr (kTail) {
-      // warps 0-1 issue every TMA box; warps 2-3 compute the tail rows
-      if (warp < C::kProducers - kTailWarps) {
-        run_producer<C::kStages, C::kProducers - kTailWarps>(p, sp, maps, bars, sK, sV, lane, status, warp);
+  if (warp < 4) {
+    if constexpr (kTailW > 0) {
+      // the first 4 - kTailW warps issue every TMA box (none with four tail
+      // warps: warp 7 does), the others compute the tail rows
+      if (warp < 4 - kTailW) {
+        run_producer<C::kStages, C::kProducers>(p, sp, maps, bars, sK, sV, lane, status, warp);
       } else {
-        TailSmem* tsm = reinterpret_cast<TailSmem*>(smem_raw + (base - raw) + C::kOffTail);
-        run_tail<C::kStages, kRope>(p, sp, bars, sK, sV, tsm, warp - (C::kProducers - kTailWarps), lane, status);
+        auto* tsm = reinterpret_cast<TailSmem<kTailW>*>(smem_raw + (base - raw) + C::kOffTail);
+        run_tail<C::kStages, kRope, kTailW>(p, sp, bars, sK, sV, tsm, warp - (4 - kTailW), lane, status);
       }
     } else {
       run_producer<C::kStages, C::kProducers>(p, sp, maps, bars, sK, sV, lane, status, warp);
     }
+  } else if (kTailW == 4 && warp == 7) {
+    run_producer<C::kStages, 1>(p, sp, maps, bars, sK, sV, lane, status, 0);
+  } else if (kTailW == 4 && warp == 6) {
+    // ------------------------------------------------------------ O_0 += P_0 V, then O_1 += P_1 V
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_bf16(128, kD, true);
+      uint32_t g = 0;
+      bool ok = true;
+      Walk walk(sp);
+      Segment s;
+      while (ok && walk.next(p, s)) {
+        for (int t = s.a; t < s.e && ok; ++t, ++g) {
+          const int stage = g % C::kStages;
+          ok = mbar_wait(&bars.kv_full[stage], (g / C::kStages) & 1, &bars, status);
+          const uint32_t vlo = desc_lo(sV + stage * kKVTileBytes, kKVHalfBytes);
+          for (int m = 0; m < 2 && ok; ++m) {
+            ok = mbar_wait(&bars.p_full[m], g & 1, &bars, status);
+            if (!ok) break;
+            fence_after();
+            const uint32_t dO = tmem + C::col_o(m), aP = tmem + C::col_p(m);
+            if (t > s.a) mma_ts<true>(dO, aP, vlo, hi, idO);
+            else mma_ts<false>(dO, aP, vlo, hi, idO);
+#pragma unroll
+            for (int kk = 1; kk < kBlk / 16; ++kk) mma_ts<true>(dO, aP + kk * 8, vlo + kk * (2048 >> 4), hi, idO);
+            mma_commit(&bars.o_done[m]);
+            mma_commit(&bars.kv_empty[stage]);
+          }
+          if (ok) TV_TRACE(4, g);
+        }
+      }
+      if (!ok) mma_drain(bars, 2);
+    }
+    __syncwarp();
   } else if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ S_m = Q_m K^T issuer
     const int m = warp - 4;
@@ -2843,13 +2908,13 @@ int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStrea
   return TV_OK;
 }
 
-template <bool kRope, bool kSkip, bool kTail>
+template <bool kRope, bool kSkip, int kTailW>
 int launch_pair(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
-  constexpr int smem = PairCfgT<kTail>::kSmem;
+  constexpr int smem = PairCfgT<kTailW>::kSmem;
   cudaError_t e =
-      cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip, kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip, kTailW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
-  attn_tc_pair_kernel<kRope, kSkip, kTail><<<p.P, PairCfg::kThreads, smem, stream>>>(p, maps, status);
+  attn_tc_pair_kernel<kRope, kSkip, kTailW><<<p.P, PairCfg::kThreads, smem, stream>>>(p, maps, status);
   TV_LAUNCH_CHECK("attn_tc_pair_kernel");
   return TV_OK;
 }
@@ -2907,7 +2972,7 @@ const char* tc_unsupported_reason(const DeviceInfo& dev, int dtype, int head_dim
   if (block_size % 16 || !(kBlk % block_size == 0 || block_size % kBlk == 0))
     return "block_size is not a multiple of 16 that divides or is divisible by 64";
   // dynamic ring + barriers + the shared-unit statistics + the slice plan
-  if (dev.max_smem_optin < (size_t)PairCfgT<true>::kSmem + sizeof(Bars) + 256 * sizeof(float) + 64)
+  if (dev.max_smem_optin < (size_t)PairCfgT<4>::kSmem + sizeof(Bars) + 256 * sizeof(float) + 64)
     return "not enough opt-in shared memory";
   return nullptr;
 }
@@ -2995,14 +3060,18 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bo
     return p.rope_cs ? launch_duo<true>(p, dm, status, stream) : launch_duo<false>(p, dm, status, stream);
   }
   // rows past the two M tiles computed beside them (tc_rows_per_unit gave the unit all R rows)
+  // (four tail warps when one TMA warp issues a tile's boxes: at most 8)
+  if (p.RPG > kTcMaxRows && p.block_size >= 32)
+    return p.rope_cs ? launch_pair<true, false, 4>(p, maps, status, stream)
+                     : launch_pair<false, false, 4>(p, maps, status, stream);
   if (p.RPG > kTcMaxRows)
-    return p.rope_cs ? launch_pair<true, false, true>(p, maps, status, stream)
-                     : launch_pair<false, false, true>(p, maps, status, stream);
-  if (p.rope_cs) return launch_pair<true, false, false>(p, maps, status, stream);
+    return p.rope_cs ? launch_pair<true, false, 2>(p, maps, status, stream)
+                     : launch_pair<false, false, 2>(p, maps, status, stream);
+  if (p.rope_cs) return launch_pair<true, false, 0>(p, maps, status, stream);
   // a last row group of at most 128 rows leaves M tile 1 idle: skip it
   const int tail = p.R % p.RPG;
-  if (p.R > p.RPG && tail > 0 && tail <= 128) return launch_pair<false, true, false>(p, maps, status, stream);
-  return launch_pair<false, false, false>(p, maps, status, stream);
+  if (p.R > p.RPG && tail > 0 && tail <= 128) return launch_pair<false, true, 0>(p, maps, status, stream);
+  return launch_pair<false, false, 0>(p, maps, status, stream);
 }
 
 }  // namespace tv

@@ -201,22 +201,23 @@ def test_mask_sensitive_tree_keys_dominate():
         _check_all(inp, paths, BF16_TOL, flags)
 
 
-@pytest.mark.parametrize("G,N", [(4, 26), (4, 64), (8, 33)])
-def test_split_unit_merge_routes(G, N):
+@pytest.mark.parametrize("G,N,bs", [(4, 26, 16), (4, 64, 16), (8, 33, 16), (8, 33, 64)])
+def test_split_unit_merge_routes(G, N, bs):
     """Units cut into many pieces (long prefixes, wide grids, grids wider than
     the plan so that some slices are empty).  The tensor-core kernel merges a
     split row either in the last piece straight from its accumulator, or from
     every piece's published partial (forced by TV_ATTN_PUBLISH_ALL); both
     routes must match the oracle (outputs, and the log-sum-exp at the
     kernel's own error on pre-rotated rows, where a wrong merge weight would
-    show) and each other bit for bit."""
-    if not tc_available(2 * G, 2, N):
+    show) and each other bit for bit.  The 264-row shape runs with two tail
+    warps (block size 16) and with four (64)."""
+    if not tc_available(2 * G, 2, N, bs=bs):
         pytest.skip("tensor-core kernel unavailable for this shape")
     rng = np.random.default_rng(140 + G + N)
     paths = W.random_rank_paths(N, 6, rng)
     kinds = [0, capi.TV_ATTN_CTA_PAIRS] if 128 < G * N <= 256 else [0]
     for lens, grids in (([3000, 70, 1500], (2, 7, 40, 152)), ([70, 0, 10], (300,))):
-        w = _workload(3, 2 * G, 2, 128, "bf16", 16, N, 141 + N)
+        w = _workload(3, 2 * G, 2, 128, "bf16", bs, N, 141 + N)
         inp = W.attention_inputs(w, device="cuda", seq_lens=lens)
         rot = prerotated(inp, paths)
         pairs = [(b, i) for b in range(3) for i in range(N)]
@@ -238,18 +239,19 @@ def test_split_unit_merge_routes(G, N):
                 assert torch.equal(a, b), (lens, num_ctas)
 
 
-@pytest.mark.parametrize("G,N,grids,kind", [(8, 33, (2, 3, 7), 0), (4, 64, (2, 5), 0), (4, 26, (3,), 0),
-                                             (4, 64, (2, 5), 16)])
-def test_repeated_calls_bit_identical(G, N, grids, kind):
+@pytest.mark.parametrize("G,N,grids,kind,bs", [(8, 33, (2, 3, 7), 0, 16), (8, 33, (2, 3, 7), 0, 64),
+                                                (4, 64, (2, 5), 0, 16), (4, 26, (3,), 0, 16),
+                                                (4, 64, (2, 5), 16, 16)])
+def test_repeated_calls_bit_identical(G, N, grids, kind, bs):
     """The same call forty times gives the same bits: every stage of the K/V
     ring is released only after all of its readers are done with it (a tail
     row read through the generic proxy without a proxy fence before the
     release once let the next TMA load overwrite it, here 39 runs in 40)."""
-    if not tc_available(2 * G, 2, N):
+    if not tc_available(2 * G, 2, N, bs=bs):
         pytest.skip("tensor-core kernel unavailable for this shape")
     rng = np.random.default_rng(140 + G + N)
     paths = W.random_rank_paths(N, 6, rng)
-    w = _workload(3, 2 * G, 2, 128, "bf16", 16, N, 141 + N)
+    w = _workload(3, 2 * G, 2, 128, "bf16", bs, N, 141 + N)
     inp = prerotated(W.attention_inputs(w, device="cuda", seq_lens=[3000, 70, 1500]), paths)
     for num_ctas in grids:
         first = None

@@ -58,6 +58,7 @@ CASES = {
     "g4_n26_one_tile": (32, 8, 26, [0, 1, 63, 700, 1500]),
     "g4_n64_two_tiles": (32, 8, 64, [0, 5, 640, 2000]),
     "g8_n33_row_groups": (64, 8, 33, [17, 1000]),
+    "g8_n33_tail_rows_bs64": (64, 8, 33, [17, 1000], 64),
     "g16_n20_row_groups": (32, 2, 20, [0, 300, 900]),
     "g2_n40_cuda_core": (8, 4, 40, [3, 500]),
 }
@@ -67,8 +68,8 @@ CASES = {
 @pytest.mark.parametrize("flags", [capi.TV_ATTN_AUTO, capi.TV_ATTN_SIMT, capi.TV_ATTN_TCGEN05,
                                    capi.TV_ATTN_TCGEN05 | capi.TV_ATTN_CTA_PAIRS])
 def test_fused_equals_separate(name, flags):
-    Hq, Hkv, N, lens = CASES[name]
-    w, par, inp, _ = _case(Hq, Hkv, N, lens, 300 + N)
+    Hq, Hkv, N, lens, *bs = CASES[name]
+    w, par, inp, _ = _case(Hq, Hkv, N, lens, 300 + N, bs=bs[0] if bs else 16)
     table = capi.tv_rope_table(max(lens) + N + 1, 128, device="cuda")
     if (flags & 3) == capi.TV_ATTN_TCGEN05 and Hq // Hkv not in (4, 8, 16):
         with pytest.raises(capi.TVError, match="UNSUPPORTED"):
