@@ -1367,11 +1367,13 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, Cfg<M>::kCtasPerSm)
 // 8-wide N side and nothing is padded:
 //   S^T [16 keys x 8 rows]  = K[16 keys x 128] Q_tail^T
 //   O_w^T [128 x 8 rows]   += V[16 keys x 128]^T P^T
-// Tail warp w takes keys (64 / kTW) w .. (64 / kTW)(w + 1) - 1 of every tile
-// and keeps its own running maximum and sum over them; the parts are merged
-// once per unit, in warp order, and the rows are written (or, for a split
-// unit, published and merged) with the same arithmetic as the other rows'
-// memory merge.  A tail warp frees a stage with its own arrival on the
+// Two tail warps share each tile, 32 keys each; with four tail warps the two
+// pairs take alternate tiles of the ring, so that each warp pays the per-tile
+// costs (barrier wait, row maxima across lanes, proxy fence and release)
+// once per two tiles.  Every warp keeps its own running maximum and sum over
+// the keys it saw; the parts are merged once per unit, in warp order, and the
+// rows are written (or, for a split unit, published and merged) with the
+// same arithmetic as the other rows' memory merge.  A tail warp frees a stage with its own arrival on the
 // stage's empty barrier once its reads of the stage are done, so the ring
 // waits for the tail as it waits for the P V products; the tail warps lag the
 // TMA stream by at most the ring's depth and never hold up a TMA issue.
@@ -1495,13 +1497,15 @@ __device__ __forceinline__ void tail_begin(const AttnParams& p, const Segment& s
 }
 
 // Tile t of the segment from the stage at kb (K) / vb (V): S^T of this
-// warp's 64 / kTW keys, online softmax over them, O^T += V^T P^T.
-template <int kTW>
+// warp's 32 keys (half h of the tile), online softmax over them,
+// O^T += V^T P^T.
+constexpr int kTailSplit = 2;  // tail warps per tile
 __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s, int t, uint32_t kb, uint32_t vb,
-                                          TailRowsState& ts, int w, int lane) {
-  constexpr int kTailKeys = kBlk / kTW;  // keys of a tile per tail warp
-  constexpr int kNB = kTailKeys / 16;    // 16-key blocks per tail warp
-  static_assert(kNB >= 1 && kNB * 16 * kTW == kBlk, "whole 16-key blocks per tail warp");
+                                          TailRowsState& ts, int h, int lane) {
+  constexpr int kTailKeys = kBlk / kTailSplit;  // keys of a tile per tail warp
+  constexpr int kNB = kTailKeys / 16;           // 16-key blocks per tail warp
+  static_assert(kNB >= 1 && kNB * 16 * kTailSplit == kBlk, "whole 16-key blocks per tail warp");
+  const int w = h;
   const int g = lane >> 2, tq = lane & 3, i8 = lane >> 3;
   // S^T per 16-key block: A = K rows x 16 head dims per step, by ldmatrix:
   // matrices (keys 0-7 | 8-15) x (dims 0-7 | 8-15) of the step, lane
@@ -1553,33 +1557,47 @@ __device__ __forceinline__ void tail_tile(const AttnParams& p, const Segment& s,
     mx[0] = fmaxf(mx[0], fmaxf(sv[kb2][0], sv[kb2][2]));
     mx[1] = fmaxf(mx[1], fmaxf(sv[kb2][1], sv[kb2][3]));
   }
+  // The weights are first taken against the running maxima as they stand,
+  // while the tile's row maxima are reduced across lanes beside them; only
+  // when some row of the warp has no maximum yet, or its maximum grows past
+  // the rescale threshold, are they taken again after the update below --
+  // the same values as updating first, with the cross-lane reduction off
+  // the path from the scores to the P V products.
+  float pv[kNB][4];
+#pragma unroll
+  for (int kb2 = 0; kb2 < kNB; ++kb2)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pv[kb2][e] = fast_exp2(fmaf(sv[kb2][e], p.scale_log2, -ts.m_run[e & 1]));
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
     mx[j] *= p.scale_log2;
   }
-  float m_use[2];
+  const bool redo = ts.m_run[0] == -INFINITY || ts.m_run[1] == -INFINITY ||
+                    mx[0] > ts.m_run[0] + kRescaleThreshold || mx[1] > ts.m_run[1] + kRescaleThreshold;
+  if (__any_sync(0xffffffffu, redo)) {
+    float m_use[2];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const float m_new = fmaxf(ts.m_run[j], mx[j]);
-    if (m_new > ts.m_run[j] + kRescaleThreshold) {
-      const float al = exp2f(ts.m_run[j] - m_new);
-      ts.l[j] *= al;
+    for (int j = 0; j < 2; ++j) {
+      const float m_new = fmaxf(ts.m_run[j], mx[j]);
+      if (m_new > ts.m_run[j] + kRescaleThreshold) {
+        const float al = exp2f(ts.m_run[j] - m_new);
+        ts.l[j] *= al;
 #pragma unroll
-      for (int mb = 0; mb < 8; ++mb) {
-        ts.o[mb][j] *= al;
-        ts.o[mb][2 + j] *= al;
+        for (int mb = 0; mb < 8; ++mb) {
+          ts.o[mb][j] *= al;
+          ts.o[mb][2 + j] *= al;
+        }
+        ts.m_run[j] = m_new;
       }
-      ts.m_run[j] = m_new;
+      m_use[j] = ts.m_run[j] == -INFINITY ? 0.f : ts.m_run[j];
     }
-    m_use[j] = ts.m_run[j] == -INFINITY ? 0.f : ts.m_run[j];
+#pragma unroll
+    for (int kb2 = 0; kb2 < kNB; ++kb2)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pv[kb2][e] = fast_exp2(fmaf(sv[kb2][e], p.scale_log2, -m_use[e & 1]));
   }
-  float pv[kNB][4];
-#pragma unroll
-  for (int kb2 = 0; kb2 < kNB; ++kb2)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pv[kb2][e] = fast_exp2(fmaf(sv[kb2][e], p.scale_log2, -m_use[e & 1]));
   {
     float l0 = pv[0][0] + pv[0][2], l1 = pv[0][1] + pv[0][3];
 #pragma unroll
@@ -1733,13 +1751,16 @@ __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& s
   Walk walk(sp);
   Segment s;
   TailRowsState ts;
+  constexpr int kRR = kTW / kTailSplit;  // tail warp pairs, taking tiles in turn
+  const int pair = w / kTailSplit;
   while (ok && walk.next(p, s)) {
     tail_begin<kRope>(p, s, ts, lane, status);
     for (int t = s.a; t < s.e; ++t, ++g) {
+      if ((int)(g % kRR) != pair) continue;  // the other pair's tile
       const int stage = g % kStages;
       ok = mbar_wait_warp(&bars.kv_full[stage], (g / kStages) & 1, &bars, status);
       if (!ok) break;
-      tail_tile<kTW>(p, s, t, sK + stage * kKVTileBytes, sV + stage * kKVTileBytes, ts, w, lane);
+      tail_tile(p, s, t, sK + stage * kKVTileBytes, sV + stage * kKVTileBytes, ts, w % kTailSplit, lane);
       // the stage was read through the generic proxy (ldmatrix) and the next
       // TMA load writes it through the async proxy: order the reads first
       fence_proxy_async();
@@ -1839,7 +1860,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 2 + kTailW);  // one commit per P V product (+ one arrival per tail warp)
+      mbar_init(&bars.kv_empty[s], kTailW ? 2 + kTailSplit : 2);  // one commit per P V product (+ the tile's tail warps)
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(&bars.s_full[m], 1);
