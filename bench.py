@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flags", type=int, default=0, help="tree attention kernel selection (0 auto, 1 CUDA-core, 2 tcgen05)")
     ap.add_argument("--num-ctas", type=int, default=0)
+    ap.add_argument("--requests", type=int, default=0,
+                    help="run the workload's shapes with this many requests (a small case for profiler captures; "
+                         "0: the workload's own batch)")
     ap.add_argument("--rope", default="auto", choices=["auto", "fused", "separate"],
                     help="fused: tree-key RoPE inside the mask kernel and Q RoPE inside the attention kernel's Q load; "
                          "separate: tv_tree_prepare rotating Q and the tree keys, then tv_tree_attn_verify; auto: fused where it "
@@ -542,7 +545,10 @@ def measure_config(name, args, dev):
 
 
 def run_ours(args, world, rank, local):
-    w = rank_workload(W.WORKLOADS[args.workload], rank)
+    base = W.WORKLOADS[args.workload]
+    if args.requests:
+        base = dataclasses.replace(base, B=args.requests)
+    w = rank_workload(base, rank)
     dev = torch.device("cuda", torch.cuda.current_device())
     st = Step(w, dev, args.flags, args.num_ctas, args.rope)
     flush, ws_bytes = l2_flush_buffer(st, dev)
