@@ -80,6 +80,16 @@ extern "C" {
  * instead of one SM per unit.  Same results up to rounding; slower than the
  * one-SM kernel on the shapes measured so far. */
 #define TV_ATTN_CTA_PAIRS 16
+/* Flag bit, tcgen05 kernels: the workspace's arrival counters are already
+ * zero, so the call does not clear them first (one memset fewer per call;
+ * about 4 us of a 0.28 ms step measured).  Every call that completes leaves
+ * them zero again (the piece that merges a split row resets its counter), so
+ * the flag holds on a workspace that was zeroed once when allocated and has
+ * since been used only by completed calls.  After a call that reported
+ * TV_DEV_TIMEOUT, or when the memory held anything else, zero the workspace
+ * again (or call without the flag).  Ignored by the CUDA-core kernel and by
+ * tv_tree_attn_verify_static, which always clears its counters. */
+#define TV_ATTN_WORKSPACE_ZEROED 32
 
 /* Kernel selection of tv_tree_accept_sample. */
 #define TV_SAMPLE_AUTO 0        /* TV_SAMPLE_CLUSTER when every request's cluster is resident at
@@ -247,9 +257,11 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  * workspace  device buffer of at least tv_tree_attn_workspace_size bytes,
  *            256-byte aligned; its contents on entry are irrelevant (the
  *            tensor-core path clears its arrival counters in it with a
- *            cudaMemsetAsync on `stream`).
+ *            cudaMemsetAsync on `stream`), except with
+ *            TV_ATTN_WORKSPACE_ZEROED, which asks for zero counters and
+ *            skips the clearing.
  * flags      TV_ATTN_* kernel selection, optionally | TV_ATTN_PUBLISH_ALL
- *            | TV_ATTN_CTA_PAIRS.
+ *            | TV_ATTN_CTA_PAIRS | TV_ATTN_WORKSPACE_ZEROED.
  * num_ctas   persistent grid size (0 = one wave of the current device);
  *            must equal the value given to tv_tree_attn_workspace_size.
  * status     device int32 (nullable): TV_DEV_TIMEOUT if a pipeline wait of

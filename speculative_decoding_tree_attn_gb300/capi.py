@@ -24,6 +24,7 @@ TV_ATTN_AUTO, TV_ATTN_SIMT, TV_ATTN_TCGEN05 = 0, 1, 2
 TV_ATTN_PUBLISH_ALL = 4
 TV_ATTN_ROPE_Q = 8
 TV_ATTN_CTA_PAIRS = 16
+TV_ATTN_WORKSPACE_ZEROED = 32
 TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA, TV_SAMPLE_STREAM = 0, 1, 2, 3
 TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 TV_DEV_BAD_BLOCK = 32
@@ -191,8 +192,9 @@ def tv_tree_attn_workspace_size(B, N, Hq, Hkv, head_dim, dtype, block_size, num_
 
 
 def alloc_workspace(nbytes, device="cuda"):
-    """A 256-byte aligned workspace tensor of at least nbytes."""
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    """A 256-byte aligned workspace tensor of at least nbytes, zeroed (so it
+    can be passed with TV_ATTN_WORKSPACE_ZEROED until a call times out)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def tv_tree_attn_verify(q, k_cache, v_cache, block_table, seq_lens, k_tree, v_tree, mask, *, scale=None,

@@ -407,7 +407,7 @@ int attn_config(int B, int N, int Hq, int Hkv, int D, int dtype, int block_size,
                 AttnConfig* cfg) {
   const bool rope = (flags & TV_ATTN_ROPE_Q) != 0;
   const bool pairs = (flags & TV_ATTN_CTA_PAIRS) != 0;
-  flags &= ~(TV_ATTN_ROPE_Q | TV_ATTN_CTA_PAIRS);
+  flags &= ~(TV_ATTN_ROPE_Q | TV_ATTN_CTA_PAIRS | TV_ATTN_WORKSPACE_ZEROED);
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Hq % Hkv)
     return fail(TV_ERR_INVALID_ARG, "tree attention: bad sizes B=%d N=%d Hq=%d Hkv=%d", B, N, Hq, Hkv);
   if (D != 64 && D != 128 && D != 256)
@@ -526,9 +526,11 @@ int verify_impl(const void* q, const void* k_cache, const void* v_cache, int64_t
   cudaStream_t s = (cudaStream_t)stream;
   if (cfg.tc) {
     // the tcgen05 kernel plans its own slice and merges split units itself;
-    // it only needs the arrival counters at zero
-    cudaError_t e = cudaMemsetAsync(p.arrive, 0, (size_t)p.P * p.RPG * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(arrival counters)");
+    // it only needs the arrival counters at zero, and leaves them so
+    if (!(flags & TV_ATTN_WORKSPACE_ZEROED)) {
+      cudaError_t e = cudaMemsetAsync(p.arrive, 0, (size_t)p.P * p.RPG * sizeof(uint32_t), s);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(arrival counters)");
+    }
     return launch_attn_tc(p, status, s, cfg.duo);
   }
   if ((st = launch_plan(p, s))) return st;
@@ -679,5 +681,5 @@ extern "C" int tv_tree_attn_verify_static(const void* q, const void* k_cache, co
   if ((st = static_workspace_ptr(&ws))) return st;
   return tv_tree_attn_verify(q, k_cache, v_cache, num_blocks, block_size, block_table, max_blocks, seq_lens, k_tree,
                              v_tree, mask, mask_bstride, B, N, Hq, Hkv, head_dim, dtype, scale, out, lse, ws,
-                             kStaticWorkspaceBytes, num_ctas, flags, status, stream);
+                             kStaticWorkspaceBytes, num_ctas, flags & ~TV_ATTN_WORKSPACE_ZEROED, status, stream);
 }

@@ -861,6 +861,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   if constexpr (kStage == 1) {
     if (staged && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
       staged_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
+      if (valid_row) *ctr = 0;  // every other piece has arrived: leave the counter at zero
       return 1;
     }
   }
@@ -868,6 +869,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
     const bool pair = stage != nullptr && pc.c1 - pc.c0 == 1 && pc.T >= pc.P;
     if (pair && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
       staged_pair_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
+      if (valid_row) *ctr = 0;
       return 1;
     }
   }
@@ -902,6 +904,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   __syncwarp();
   if (complete || direct) {
     if (valid_row && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+    if (direct && valid_row) *ctr = 0;
     return complete ? 0 : 1;
   }
   if constexpr (kStage == 1) {
@@ -913,6 +916,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
       }
       if (__any_sync(0xffffffffu, last)) {
         staged_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, last);
+        if (last) *ctr = 0;
         return last ? 3 : 2;
       }
       return 2;
@@ -933,6 +937,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
     store_bf16_16(out + orow * kD + c, acc);
   }
   if (p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+  *ctr = 0;
   return 3;
 }
 
@@ -1722,7 +1727,8 @@ __device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& s
     __threadfence();
     __syncwarp();
     bool last = false;
-    if (valid && lead) last = atom_add_acq_rel(p.arrive + (int64_t)pc.c0 * p.RPG + ur, mine) + mine == (uint32_t)s.n;
+    uint32_t* ctr = p.arrive + (int64_t)pc.c0 * p.RPG + ur;
+    if (valid && lead) last = atom_add_acq_rel(ctr, mine) + mine == (uint32_t)s.n;
     last = __shfl_sync(0xffffffffu, last, lane & ~(kThreadsPerRow - 1));
     if (last) {
       __threadfence();
@@ -1734,6 +1740,7 @@ __device__ __forceinline__ bool tail_end(const AttnParams& p, const SlicePlan& s
       accum_pieces<false>(acc, p, pc, -1, acc, 0.f, ur, d0, mx, 1.f / z);
       store_bf16_16(out + orow * kD + d0, acc);
       if (lead && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
+      if (lead) *ctr = 0;  // every piece has arrived: leave the counter at zero
     }
   }
   const bool ok = mbar_wait_warp(&bars.tail_sync, tb & 1, &bars, status);

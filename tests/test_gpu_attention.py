@@ -339,3 +339,39 @@ def test_full_size_all_nodes_of_sampled_requests(name):
     _check_all(inp, paths, BF16_TOL, capi.TV_ATTN_AUTO, pairs=pairs)
     if 128 < rows <= 256:  # the same shape on CTA pairs (every node of the same requests)
         _check_all(inp, paths, BF16_TOL, capi.TV_ATTN_AUTO | capi.TV_ATTN_CTA_PAIRS, pairs=pairs)
+
+
+@pytest.mark.parametrize("G,N,bs,kind", [(4, 26, 16, 0), (4, 64, 16, 0), (8, 33, 16, 0), (8, 33, 64, 0),
+                                         (4, 64, 16, 16)])
+def test_workspace_zeroed_flag(G, N, bs, kind):
+    """Every completed call leaves the workspace's arrival counters at zero
+    (the piece that merges a split row resets its counter), so calls with
+    TV_ATTN_WORKSPACE_ZEROED on one workspace -- which skip clearing the
+    counters -- give the same bits as calls that clear them, call after call,
+    on both merge routes and grids that split every unit."""
+    if not tc_available(2 * G, 2, N, bs=bs):
+        pytest.skip("tensor-core kernel unavailable for this shape")
+    rng = np.random.default_rng(160 + G + N + bs)
+    paths = W.random_rank_paths(N, 6, rng)
+    w = _workload(3, 2 * G, 2, 128, "bf16", bs, N, 161 + N)
+    inp = prerotated(W.attention_inputs(w, device="cuda", seq_lens=[3000, 70, 1500]), paths)
+    parent, *_ = capi.tv_tree_build(paths)
+    mask, _, _ = capi.tv_tree_mask(torch.from_numpy(parent).cuda(), inp["seq_lens"])
+    args = (inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"], inp["k_tree"],
+            inp["v_tree"], mask)
+    for num_ctas in (2, 7, 40):
+        for extra in (kind, kind | capi.TV_ATTN_PUBLISH_ALL):
+            flags = capi.TV_ATTN_TCGEN05 | extra
+            ws = capi.alloc_workspace(capi.tv_tree_attn_workspace_size(3, N, 2 * G, 2, 128, torch.bfloat16, bs,
+                                                                       num_ctas, flags))
+            ref_lse = torch.empty(inp["q"].shape[:3], dtype=torch.float32, device="cuda")
+            ref = capi.tv_tree_attn_verify(*args, lse=ref_lse, workspace=ws, num_ctas=num_ctas, flags=flags)
+            for _ in range(3):
+                out = torch.full_like(inp["q"], float("nan"))
+                lse = torch.full_like(ref_lse, float("nan"))
+                status = torch.zeros(1, dtype=torch.int32, device="cuda")
+                capi.tv_tree_attn_verify(*args, out=out, lse=lse, workspace=ws, num_ctas=num_ctas,
+                                         flags=flags | capi.TV_ATTN_WORKSPACE_ZEROED, status=status)
+                torch.cuda.synchronize()
+                assert int(status.item()) == 0
+                assert torch.equal(out, ref) and torch.equal(lse, ref_lse), (num_ctas, extra)
