@@ -527,6 +527,47 @@ def roofline_of(st, w, attn_ms):
 PER_CONFIG = ["gqa_b8_l512_2048_n26", "b64_l1k_8k_n64_greedy", "long_b16_l32k_n33", "b256_l2k_4k_n10_sample"]
 
 
+def measure_accept(st, w, args, flush, dev):
+    """The acceptance call alone (graph replays, L2 flushed before each):
+    time per call, tokens emitted and the row bytes the walk reads -- the
+    lazy greedy walk one logits row per emitted token; the chain sampler the
+    p row of its stop node, plus its q row when the stop was a rejection."""
+    if st.greedy is None and st.sample is None:
+        return None
+    g_acc = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_acc):
+        st.run_accept()
+    fl = flush if flush is not None else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    evc = []
+    for k in range(args.warmup + args.steps):
+        fl.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g_acc.replay()
+        b.record()
+        if k >= args.warmup:
+            evc.append((a, b))
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) for a, b in evc) * 1e3
+    emitted = int(st.acc_n.sum().item())
+    accept = {"call": "tv_tree_accept_greedy" if st.greedy is not None else "tv_tree_accept_sample",
+              "us_per_call": round(us, 2), "tokens_out": emitted}
+    rows_b = None
+    if st.greedy is not None:
+        rows_b = emitted * w.vocab * 4
+        accept["all_rows_bytes"] = w.B * st.N * w.vocab * 4
+    elif not w.sample_tree:
+        n_out = st.acc_n.cpu().numpy().astype(np.int64)
+        n_nodes = st.sample["n_nodes"].cpu().numpy().astype(np.int64)
+        V = st.sample["p"].shape[-1]
+        rejected = n_out < n_nodes  # the stop node still had its child to test
+        rows_b = int(np.sum(np.where(rejected, 2, 1))) * V * 4
+    if rows_b is not None:
+        accept.update(bytes_read=rows_b, gbs=round(rows_b / (us * 1e-6) / 1e9, 1))
+    del g_acc
+    return accept
+
+
 def measure_config(name, args, dev):
     """One workload's attention call and step, measured as the headline is."""
     w = W.WORKLOADS[name]
@@ -542,6 +583,11 @@ def measure_config(name, args, dev):
            "accept": w.accept, "rope": "fused" if st.fused_rope else "separate",
            "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
            "clocks": clocks}
+    acc = measure_accept(st, w, args, flush, dev) if graphs else None
+    if acc is not None:
+        res["accept_us_per_call"] = acc["us_per_call"]
+        if "gbs" in acc:
+            res["accept_bytes_read"], res["accept_gbs"] = acc["bytes_read"], acc["gbs"]
     del st, graphs, flush
     torch.cuda.empty_cache()
     return res
@@ -628,32 +674,7 @@ def run_ours(args, world, rank, local):
         moved = rows * w.Hkv * w.D * st.esize * 2 * 2  # K and V rows, read and written
         commit = {"us_per_call": round(us, 2), "rows": rows, "bytes": moved, "gbs": round(moved / (us * 1e-6) / 1e9, 1)}
 
-    # the acceptance call alone (graph replays, L2 flushed before each): the
-    # lazy greedy walk reads one logits row per emitted token
-    accept = None
-    if graphs and (st.greedy is not None or st.sample is not None):
-        g_acc = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_acc):
-            st.run_accept()
-        fl = flush if flush is not None else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-        evc = []
-        for k in range(args.warmup + args.steps):
-            fl.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            g_acc.replay()
-            b.record()
-            if k >= args.warmup:
-                evc.append((a, b))
-        torch.cuda.synchronize()
-        us = statistics.mean(a.elapsed_time(b) for a, b in evc) * 1e3
-        emitted = int(st.acc_n.sum().item())
-        accept = {"call": "tv_tree_accept_greedy" if st.greedy is not None else "tv_tree_accept_sample",
-                  "us_per_call": round(us, 2), "tokens_out": emitted}
-        if st.greedy is not None:
-            rows_b = emitted * w.vocab * 4
-            accept.update(bytes_read=rows_b, all_rows_bytes=w.B * st.N * w.vocab * 4,
-                          gbs=round(rows_b / (us * 1e-6) / 1e9, 1))
+    accept = measure_accept(st, w, args, flush, dev) if graphs else None
 
     roofline = roofline_of(st, w, attn_ms)
     achieved, peak = roofline["achieved"], roofline["peak"]
