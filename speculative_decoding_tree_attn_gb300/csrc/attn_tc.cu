@@ -117,6 +117,8 @@ struct Bars {
   uint64_t sh_stat, sh_read;  // shared units (two-M-tile kernel): M tile 1's part posted / read
   uint64_t tail_sync;         // tail rows (two-M-tile kernel): the four producer warps' end-of-unit exchange
   uint64_t drain[4];          // one per MMA-issuing thread: its products have completed (after an abort)
+  uint64_t q0s_full, cp_done;  // staged Q (two-M-tile kernel): the next unit's Q_0 has landed / been copied to TMEM
+  uint64_t q1_free, q1_full;   //   ... this unit's last S_1 has completed / the next unit's Q_1 has landed
   uint32_t tmem_base;
   int abort;
 };
@@ -235,6 +237,14 @@ __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, int
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -969,6 +979,7 @@ __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan&
 
 struct TcMaps {
   CUtensorMap kc, vc, kt, vt;
+  CUtensorMap qm;  // Q [B * N][Hq][D] in boxes of 64 columns x G heads x 128 / G nodes (128 rows of a unit)
 };
 
 // TMA producer (warp 0): streams every tile of the CTA's slice into the
@@ -1790,7 +1801,7 @@ __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& s
 //  * TMEM (512 columns) holds S_0 S_1 P_0 P_1 Q_0 O_0 O_1 = 64+64+32+32+64+128+128;
 //    Q_1 therefore stays in shared memory (S_1 = Q_1 K^T reads both operands
 //    from shared memory), which keeps shared-memory traffic near 128 KB per tile.
-template <int kTailW>
+template <int kTailW, bool kQS = false>
 struct PairCfgT {
   // Five K/V stages (measured 1-3 % faster than six on the 64-request and
   // long-context shapes); the shared memory left holds the tail rows'
@@ -1811,7 +1822,9 @@ struct PairCfgT {
   static constexpr int kOffV = kOffK + kStages * kKVTileBytes;
   static constexpr int kOffQ1 = kOffV + kStages * kKVTileBytes;  // 2 halves x 128 rows x 128 B
   static constexpr int kOffTail = kOffQ1 + 2 * 128 * 128;
-  static constexpr int kBytes = kOffTail + (kTailW ? (int)sizeof(TailSmem<kTailW>) : 0);
+  // kQS: the next unit's Q_0 is staged here by TMA (32 KB, 128B-swizzled)
+  static constexpr int kOffQ0S = kOffTail + (kTailW ? (int)sizeof(TailSmem<kTailW>) : 0);
+  static constexpr int kBytes = kOffQ0S + (kQS ? 128 * kD * 2 : 0);
   static constexpr int kSmem = kBytes + 1024;
   static constexpr uint32_t col_s(int m) { return m * 64; }
   static constexpr uint32_t col_p(int m) { return 128 + m * 32; }
@@ -1821,6 +1834,8 @@ struct PairCfgT {
 };
 using PairCfg = PairCfgT<0>;
 static_assert(PairCfgT<4>::kSmem <= 227 * 1024 - 1024, "the tail variant fits the opt-in shared memory");
+static_assert(PairCfgT<0, true>::kSmem <= 227 * 1024 - 1024, "the staged-Q variant fits the opt-in shared memory");
+static_assert(PairCfgT<0, true>::kOffQ0S % 1024 == 0, "the Q_0 staging tile is 1024-byte aligned (128B swizzle)");
 static_assert(PairCfgT<4>::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 static_assert(PairCfg::kStages * kKVTileBytes >= 128 * kD * 4, "each half of the pair ring holds one M tile's rows");
 
@@ -1848,7 +1863,16 @@ __device__ __forceinline__ int sh_owner(int t) { return kSplitKeys ? (t & 1) : 0
 template <bool kRope, bool kSkip, int kTailW>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
-  using C = PairCfgT<kTailW>;
+  // kQS: after a CTA's first unit, each unit's Q reaches its operand slots
+  // through the S issuers instead of the softmax warps: Q_0 is staged in
+  // shared memory by TMA during the previous unit and copied into TMEM with
+  // tcgen05.cp just before the unit's first S_0 products (the same thread
+  // issued the previous unit's S_0, so the copy follows them in the pipe);
+  // Q_1 is loaded by TMA into its tile once the previous unit's last S_1 has
+  // completed.  The softmax warps then only write the finished unit's rows at
+  // a boundary.
+  constexpr bool kQS = !kRope && !kSkip && kTailW == 0;
+  using C = PairCfgT<kTailW, kQS>;
   static_assert(!(kSkip && kTailW), "tail rows replace the second row group");
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
@@ -1880,6 +1904,10 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     mbar_init(&bars.sh_read, 128);
     mbar_init(&bars.tail_sync, 32 * (kTailW ? kTailW : 1));
     for (int i = 0; i < 4; ++i) mbar_init(&bars.drain[i], 1);
+    mbar_init(&bars.q0s_full, 1);
+    mbar_init(&bars.cp_done, 1);
+    mbar_init(&bars.q1_free, 1);
+    mbar_init(&bars.q1_full, 1);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1953,10 +1981,36 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       bool ok = true;
       Walk walk(sp);
       Segment s;
+      // kQS: Q loads this thread issued (and whether the last is still in flight)
+      uint32_t nq = 0;
+      bool q_pending = false;
+      const uint32_t sQ0S = base + C::kOffQ0S;
+      // the Q rows of M tile m of unit sg by TMA: two boxes of 64 columns
+      auto load_q = [&](const Segment& sg, uint32_t dst, uint64_t* bar) {
+        mbar_expect_tx(bar, 128 * kD * 2);
+        const int y = sg.kvh * p.G, z = sg.b * p.N + (sg.rg * p.RPG + m * 128) / p.G;
+        tma_3d(dst, &maps.qm, 0, y, z, bar);
+        tma_3d(dst + 16384, &maps.qm, 64, y, z, bar);
+        ++nq;
+        q_pending = true;
+      };
       while (ok && walk.next(p, s)) {
-        ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
-        if (!ok) break;
-        fence_after();
+        Segment sn;
+        bool hn = false;
+        if constexpr (kQS) {
+          Walk wn = walk;
+          hn = wn.next(p, sn);
+        }
+        if (!kQS || seg_i == 0) {
+          ok = mbar_wait(&bars.q_full, seg_i & 1, &bars, status);
+          if (!ok) break;
+          fence_after();
+          if (kQS && m == 0 && hn) load_q(sn, sQ0S, &bars.q0s_full);  // the staging tile is free
+        } else if (m == 1) {
+          ok = mbar_wait(&bars.q1_full, (seg_i - 1) & 1, &bars, status);
+          if (!ok) break;
+          q_pending = false;
+        }
         const bool sh = kSkip && shared_unit(p, s);
         if (m == 0) TV_TRACE(3, g);
         for (int t = s.a; t < s.e && ok; ++t, ++g) {
@@ -1969,6 +2023,22 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           fence_after();
           if (m == 0) TV_TRACE(30, g);
           const uint32_t blo = desc_lo(sK + stage * kKVTileBytes, 0);
+          if (kQS && m == 0 && seg_i > 0 && t == s.a) {
+            // the previous unit's S_0 products have completed (its last S_0
+            // was read): copy this unit's staged Q_0 into TMEM; the S_0
+            // products below follow the copies in this thread's pipe order
+            ok = mbar_wait(&bars.q0s_full, (seg_i - 1) & 1, &bars, status);
+            if (!ok) break;
+            q_pending = false;
+            const uint32_t qlo = desc_lo(sQ0S, 0);
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {
+              const uint64_t d = ((uint64_t)hi << 32) | (qlo + (k / 4) * (16384 >> 4) + (k % 4) * 2);
+              asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(tmem + C::kColQ0 + k * 8), "l"(d)
+                           : "memory");
+            }
+            mma_commit(&bars.cp_done);
+          }
           if (m == 0) {
             const uint32_t aQ = tmem + C::kColQ0;
             mma_ts<false>(dS, aQ, blo, hi, idS);
@@ -1987,10 +2057,24 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           mma_commit(&bars.s_full[m]);
           if constexpr (kSkip) ++g1;
           if (m == 0) TV_TRACE(2, g);
+          if (kQS && m == 0 && seg_i > 0 && t == s.a && hn) {
+            // once the copies have read the staging tile, stage the next unit's Q_0
+            ok = mbar_wait(&bars.cp_done, (seg_i - 1) & 1, &bars, status);
+            if (!ok) break;
+            load_q(sn, sQ0S, &bars.q0s_full);
+          }
+        }
+        if (ok && kQS && m == 1 && hn) {
+          // the Q_1 tile is free once this unit's last S_1 has completed
+          mma_commit(&bars.q1_free);
+          ok = mbar_wait(&bars.q1_free, seg_i & 1, &bars, status);
+          if (ok) load_q(sn, sQ1, &bars.q1_full);
         }
         ++seg_i;
       }
       if (!ok) mma_drain(bars, m);
+      // a Q load still in flight lands before the CTA exits
+      if (q_pending) mbar_wait(m == 0 ? &bars.q0s_full : &bars.q1_full, (nq - 1) & 1, &bars, nullptr, false);
     }
     __syncwarp();
   } else if (warp == 6 || warp == 7) {
@@ -2218,8 +2302,16 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       Segment s_next;
       const bool have_next = walk.next(p, s_next);
       if (have_next) {
-        fetch_q(s_next);
-        place_q();
+        if constexpr (kQS) {
+          // the S issuers bring the next unit's Q in; only its ancestor row here
+          const RowOf r = row_of(s_next);
+          mrow_next = r.valid ? __ldg(reinterpret_cast<const unsigned long long*>(p.mask) +
+                                      (int64_t)s_next.b * p.mask_bstride + r.node)
+                              : 1ull;
+        } else {
+          fetch_q(s_next);
+          place_q();
+        }
       }
       if (m == 0 && rl == 0) TV_TRACE(15, g - 1);
       if (!sh || kk > 0) {
@@ -2938,7 +3030,7 @@ int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStrea
 
 template <bool kRope, bool kSkip, int kTailW>
 int launch_pair(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
-  constexpr int smem = PairCfgT<kTailW>::kSmem;
+  constexpr int smem = PairCfgT<kTailW, !kRope && !kSkip && kTailW == 0>::kSmem;
   cudaError_t e =
       cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip, kTailW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
@@ -3067,6 +3159,14 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bo
   }
   if (p.RPG <= 128)
     return p.rope_cs ? launch_m<1, true>(p, maps, status, stream) : launch_m<1, false>(p, maps, status, stream);
+  {
+    // Q as [B * N][Hq][D]: one box is 128 consecutive rows (node, head) of a
+    // unit's M tile, 64 columns wide (G divides 128)
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.Hq, (cuuint64_t)p.B * p.N};
+    cuuint64_t strides[2] = {row_bytes, row_bytes * p.Hq};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)(128 / p.G)};
+    if ((st = encode(fn, &maps.qm, p.q, 3, dims, strides, box, "q"))) return st;
+  }
   if (duo) {
     // one unit of up to 256 rows on a CTA pair: half of every K/V tile per SM
     DuoMaps dm;
