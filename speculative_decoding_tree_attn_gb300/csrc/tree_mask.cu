@@ -17,6 +17,7 @@
 // are absent -- mask row 0, depth 0, position -1 -- and their parents are not
 // read.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.h"
 #include "rope_math.cuh"
@@ -137,11 +138,94 @@ __global__ void __launch_bounds__(256) tree_prepare_kernel(
   }
 }
 
+// The same for bf16 rows of D = 128, a node per warp: the warp reads the
+// node's cos/sin table row once (each lane the 8 frequencies of its 16-byte
+// chunk) and rotates the node's Hq + Hkv rows four at a time (8 lanes per
+// row, one 16-byte load from each half), requesting kBatch rows' loads per
+// lane before the first rotation.  Same arithmetic and rounding as
+// tv_rope_apply, element by element.
+constexpr int kPrepWarps = 8;
+template <int D>
+__global__ void __launch_bounds__(32 * kPrepWarps) tree_prepare_nodes_kernel(
+    const int32_t* __restrict__ parent, int64_t pstride, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ n_nodes, int N, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
+    int32_t* __restrict__ pos, __nv_bfloat16* __restrict__ q, int Hq, __nv_bfloat16* __restrict__ kt, int Hkv,
+    const float* __restrict__ cs, int max_pos, int32_t* __restrict__ status) {
+  constexpr int half = D / 2;
+  constexpr int chunks = half / 8;           // lanes per row
+  constexpr int rows_per_it = 32 / chunks;   // rows a warp rotates at once
+  constexpr int kBatch = 5;                  // loads in flight per lane and half
+  static_assert(32 % chunks == 0, "whole rows per warp");
+  __shared__ int32_t s_par[TV_MAX_NODES], s_pos[TV_MAX_NODES];
+  const int b = blockIdx.x;
+  if (threadIdx.x < 32)
+    request_rows(parent, pstride, seq_lens, n_nodes, b, N, s_par, blockIdx.y == 0 ? mask : nullptr, depth, pos,
+                 s_pos, status);
+  __syncthreads();
+  const int hq = q ? Hq : 0, hk = kt ? Hkv : 0, heads = hq + hk;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = lane % chunks, sub = lane / chunks;
+  for (int i = blockIdx.y * kPrepWarps + warp; i < N; i += gridDim.y * kPrepWarps) {
+    const int32_t p = s_pos[i];
+    if (p < 0 || p >= max_pos) {  // -1: an absent node (or a bad tree), left as it is
+      if (status && lane == 0 && p != -1) atomicOr(status, TV_DEV_BAD_POSITION);
+      continue;
+    }
+    float co[8], si[8];
+    Vec8<float>::load(cs + (int64_t)p * D + c * 8, co);
+    Vec8<float>::load(cs + (int64_t)p * D + half + c * 8, si);
+    for (int h0 = 0; h0 < heads; h0 += rows_per_it * kBatch) {
+      uint4 x1[kBatch], x2[kBatch];
+      __nv_bfloat16* rows[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int h = h0 + j * rows_per_it + sub;
+        rows[j] = nullptr;
+        if (h < heads) {
+          rows[j] = h < hq ? q + (((int64_t)b * N + i) * Hq + h) * D : kt + (((int64_t)b * N + i) * Hkv + (h - hq)) * D;
+          x1[j] = *reinterpret_cast<const uint4*>(rows[j] + c * 8);
+          x2[j] = *reinterpret_cast<const uint4*>(rows[j] + half + c * 8);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (!rows[j]) continue;
+        const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&x1[j]);
+        const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(&x2[j]);
+        uint4 y1, y2;
+        __nv_bfloat162* o1 = reinterpret_cast<__nv_bfloat162*>(&y1);
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&y2);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 u = __bfloat1622float2(a[e]), v = __bfloat1622float2(bb[e]);
+          float r1a, r2a, r1b, r2b;
+          rope_pair(u.x, v.x, co[2 * e], si[2 * e], r1a, r2a);
+          rope_pair(u.y, v.y, co[2 * e + 1], si[2 * e + 1], r1b, r2b);
+          o1[e] = __floats2bfloat162_rn(r1a, r1b);
+          o2[e] = __floats2bfloat162_rn(r2a, r2b);
+        }
+        *reinterpret_cast<uint4*>(rows[j] + c * 8) = y1;
+        *reinterpret_cast<uint4*>(rows[j] + half + c * 8) = y2;
+      }
+    }
+  }
+}
+
 template <typename T, int D>
 int launch_prepare(const int32_t* parent, int64_t pstride, const int32_t* seq_lens, const int32_t* n_nodes, int B,
                    int N, uint64_t* mask, int32_t* depth, int32_t* pos, void* q, int Hq, void* kt, int Hkv,
                    const float* cs, int max_pos, int32_t* status, cudaStream_t stream) {
   const int heads = (q ? Hq : 0) + (kt ? Hkv : 0);
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+    if (heads) {
+      const int ys = (int)std::min<int64_t>(tv::ceil_div(N, kPrepWarps), 32);
+      tree_prepare_nodes_kernel<D><<<dim3(B, ys), 32 * kPrepWarps, 0, stream>>>(
+          parent, pstride, seq_lens, n_nodes, N, mask, depth, pos, static_cast<__nv_bfloat16*>(q), Hq,
+          static_cast<__nv_bfloat16*>(kt), Hkv, cs, max_pos, status);
+      TV_LAUNCH_CHECK("tree_prepare_nodes_kernel");
+      return TV_OK;
+    }
+  }
   const int items = N * heads * (D / 16);
   const int ys = heads ? (int)std::min<int64_t>(tv::ceil_div(items, 256 * 4), 32) : 1;
   tree_prepare_kernel<T, D><<<dim3(B, ys), 256, 0, stream>>>(parent, pstride, seq_lens, n_nodes, N, mask, depth,
