@@ -251,7 +251,9 @@ int tv_tree_attn_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
  * mask       device uint64 [B, N] with row stride mask_bstride elements
  *            (0 = shared); bit j of mask[b, i] <=> node i may see node j.
  * scale      softmax scale (e.g. 1/sqrt(D)).
- * out        device [B, N, Hq, D] (dtype) out.
+ * out        device [B, N, Hq, D] (dtype) out; 32-byte aligned (and q
+ *            16-byte aligned) on the tensor-core path, else
+ *            TV_ERR_INVALID_ARG.
  * lse        device float32 [B, N, Hq] out (nullable): natural-log softmax
  *            normaliser of each row.
  * workspace  device buffer of at least tv_tree_attn_workspace_size bytes,

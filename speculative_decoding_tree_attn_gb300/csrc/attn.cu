@@ -498,6 +498,10 @@ int verify_impl(const void* q, const void* k_cache, const void* v_cache, int64_t
     return fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify: bad num_blocks/max_blocks/mask stride");
   if (cfg.tc && num_blocks * Hkv * block_size >= (int64_t(1) << 31))
     return fail(TV_ERR_UNSUPPORTED, "tv_tree_attn_verify: KV cache rows exceed the tensor-map range");
+  // the tensor-core kernels write output rows in 32-byte pieces and read Q
+  // rows in 16-byte pieces (and by TMA)
+  if (cfg.tc && ((reinterpret_cast<uintptr_t>(out) & 31) || (reinterpret_cast<uintptr_t>(q) & 15)))
+    return fail(TV_ERR_INVALID_ARG, "tv_tree_attn_verify: out must be 32-byte and q 16-byte aligned");
   if (!workspace || workspace_bytes < (size_t)cfg.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(TV_ERR_WORKSPACE, "tv_tree_attn_verify: workspace needs %lld bytes, 256-byte aligned",
                 (long long)cfg.bytes);

@@ -650,16 +650,24 @@ __device__ __forceinline__ void accum_pieces(float (&acc)[16], const AttnParams&
   }
 }
 
+// 16 columns of an output row (dst 32-byte aligned: a row is 256 bytes and
+// the columns start at a multiple of 16).  kWide: one 32-byte store, which
+// halves the store transactions of a warp writing 32 rows at once (measured
+// faster in the two-M-tile kernel without tail rows, slower in the others,
+// whose code it changes); else two 16-byte stores.
+template <bool kWide = false>
 __device__ __forceinline__ void store_bf16_16(__nv_bfloat16* dst, const float (&acc)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  uint32_t w[8];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    uint4 v;
-    v.x = pack_bf16(acc[8 * j + 0], acc[8 * j + 1]);
-    v.y = pack_bf16(acc[8 * j + 2], acc[8 * j + 3]);
-    v.z = pack_bf16(acc[8 * j + 4], acc[8 * j + 5]);
-    v.w = pack_bf16(acc[8 * j + 6], acc[8 * j + 7]);
-    d[j] = v;
+  for (int j = 0; j < 8; ++j) w[j] = pack_bf16(acc[2 * j], acc[2 * j + 1]);
+  if constexpr (kWide) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -794,6 +802,7 @@ __device__ __forceinline__ void staged_merge(const AttnParams& p, const Pieces& 
 // piece order with the arithmetic of piece_stats / accum_pieces, so the row
 // matches the other merge routes bit for bit.  Warp-collective (TMEM reads);
 // `active` lanes merge their row.
+template <bool kWide>
 __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pieces& pc, float lse2, float inv,
                                                   int row, int rl, int64_t orow, uint32_t tO, uint8_t* stage,
                                                   bool active) {
@@ -841,7 +850,7 @@ __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pie
         acc[4 * j + e] = fmaf(w1, self_first ? ov[e] : mine, a);
       }
     }
-    store_bf16_16(out + orow * kD + c, acc);
+    store_bf16_16<kWide>(out + orow * kD + c, acc);
   }
   __syncwarp();
   if (active && p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
@@ -850,7 +859,7 @@ __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pie
 // kStage: 0 no staging; 1 merges at the slice's last segment may stage
 // through `stage` (staged_merge); 2 only a direct merge with one other piece
 // stages (staged_pair_merge).
-template <int kStage>
+template <int kStage, bool kWide = false>
 __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
                                                bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
                                                uint8_t* stage) {
@@ -878,7 +887,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   if constexpr (kStage == 2) {
     const bool pair = stage != nullptr && pc.c1 - pc.c0 == 1 && pc.T >= pc.P;
     if (pair && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
-      staged_pair_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
+      staged_pair_merge<kWide>(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
       if (valid_row) *ctr = 0;
       return 1;
     }
@@ -898,13 +907,13 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) * inv;
     if (complete) {
-      store_bf16_16(out + orow * kD + c, v);
+      store_bf16_16<kWide>(out + orow * kD + c, v);
     } else if (direct) {
       float acc[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = 0.f;
       accum_pieces<true>(acc, p, pc, self, v, lse2, row, c, mx, zinv);
-      store_bf16_16(out + orow * kD + c, acc);
+      store_bf16_16<kWide>(out + orow * kD + c, acc);
     } else {
       float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kD + c);
 #pragma unroll
@@ -944,7 +953,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
     accum_pieces<false>(acc, p, pc, -1, acc, 0.f, row, c, mx, zinv2);
-    store_bf16_16(out + orow * kD + c, acc);
+    store_bf16_16<kWide>(out + orow * kD + c, acc);
   }
   if (p.lse) p.lse[orow] = (mx + log2f(z)) * kLn2;
   *ctr = 0;
@@ -953,7 +962,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
 
 // kStage (as in finish_row_impl): how merges at the slice's last segment may
 // stage through `stage`.
-template <int kStage>
+template <int kStage, bool kWide = false>
 __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
                                            bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
                                            uint8_t* stage) {
@@ -964,7 +973,7 @@ __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan&
 #ifdef TV_TC_TRACE
   const int route =
 #endif
-  finish_row_impl<kStage>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
+  finish_row_impl<kStage, kWide>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
 #ifdef TV_TC_TRACE
   const unsigned long long t_out = globaltimer();
   TV_TRACE_ROW0(5, t_out);
@@ -2379,7 +2388,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         stage = smem_raw + (base - raw) + (m == 0 ? C::kOffK : C::kOffV);
       }
       if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
-      finish_row<2>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
+      finish_row<2, kQS>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
       fence_before();
       if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       if constexpr (kSkip) ++useg;

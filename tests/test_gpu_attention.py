@@ -375,3 +375,26 @@ def test_workspace_zeroed_flag(G, N, bs, kind):
                 torch.cuda.synchronize()
                 assert int(status.item()) == 0
                 assert torch.equal(out, ref) and torch.equal(lse, ref_lse), (num_ctas, extra)
+
+
+def test_misaligned_output_is_refused():
+    """The tensor-core path writes output rows in 32-byte pieces: an output
+    pointer off a 32-byte boundary is refused with TV_ERR_INVALID_ARG (and a
+    32-byte aligned one that is not 256-byte aligned works)."""
+    if not tc_available(8, 2, 10):
+        pytest.skip("tensor-core kernel unavailable")
+    w = _workload(2, 8, 2, 128, "bf16", 16, 10, 171)
+    inp = W.attention_inputs(w, device="cuda", seq_lens=[100, 300])
+    parent, *_ = capi.tv_tree_build(W.PAGE_TREE_PATHS)
+    mask, _, _ = capi.tv_tree_mask(torch.from_numpy(parent).cuda(), inp["seq_lens"])
+    args = (inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"], inp["k_tree"],
+            inp["v_tree"], mask)
+    ref = capi.tv_tree_attn_verify(*args, flags=capi.TV_ATTN_TCGEN05)
+    big = torch.empty(ref.numel() + 64, dtype=ref.dtype, device="cuda")
+    with pytest.raises(capi.TVError) as e:
+        capi.tv_tree_attn_verify(*args, out=big[8:8 + ref.numel()].view(ref.shape), flags=capi.TV_ATTN_TCGEN05)
+    assert e.value.code == -1
+    out32 = big[16:16 + ref.numel()].view(ref.shape)  # 32 bytes past a 256-byte boundary
+    capi.tv_tree_attn_verify(*args, out=out32, flags=capi.TV_ATTN_TCGEN05)
+    torch.cuda.synchronize()
+    assert torch.equal(out32, ref)
