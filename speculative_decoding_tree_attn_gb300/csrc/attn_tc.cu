@@ -119,6 +119,7 @@ struct Bars {
   uint64_t drain[4];          // one per MMA-issuing thread: its products have completed (after an abort)
   uint64_t q0s_full, cp_done;  // staged Q (two-M-tile kernel): the next unit's Q_0 has landed / been copied to TMEM
   uint64_t q1_free, q1_full;   //   ... this unit's last S_1 has completed / the next unit's Q_1 has landed
+  uint64_t merge_full[2];      //   ... the other piece's rows of M tile m have landed (end-of-slice merge)
   uint32_t tmem_base;
   int abort;
 };
@@ -245,6 +246,14 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
           dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -802,23 +811,38 @@ __device__ __forceinline__ void staged_merge(const AttnParams& p, const Pieces& 
 // piece order with the arithmetic of piece_stats / accum_pieces, so the row
 // matches the other merge routes bit for bit.  Warp-collective (TMEM reads);
 // `active` lanes merge their row.
+// kWide (the staged-Q two-M-tile kernel): the other piece's 128 rows of
+// this M tile come by TMA (pm: four 16 KB boxes of 32 columns, 128B-swizzled,
+// on mbar) instead of 32 16-byte cp.async requests per thread, which the
+// load/store unit took about 9,000 cycles to issue; rows are then read
+// swizzled (4 wavefronts per warp access, the minimum for 512 bytes).
 template <bool kWide>
 __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pieces& pc, float lse2, float inv,
                                                   int row, int rl, int64_t orow, uint32_t tO, uint8_t* stage,
-                                                  bool active) {
+                                                  bool active, const CUtensorMap* pm, uint64_t* mbar) {
   constexpr float kLn2 = 0.69314718055994530942f;
   const bool self_first = pc.self == pc.c0;
   const int64_t so = pc.slot(self_first ? pc.c1 : pc.c0) * p.RPG + row;
   const uint32_t dst = smem_u32(stage) + rl * 16;
   float lo = 0.f;
-  if (active) {
-    const float* src = p.part_o + so * kD;
+  if constexpr (kWide) {
+    if (rl == 0) {
+      const int y = (int)(so - rl);  // the M tile's first row in the partials
+      mbar_expect_tx(mbar, 128 * kD * 4);
 #pragma unroll
-    for (int j = 0; j < kD / 4; ++j)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + j * 2048), "l"(src + 4 * j) : "memory");
-    lo = __ldcg(p.part_lse + so);
+      for (int k = 0; k < kD / 32; ++k) tma_2d(smem_u32(stage) + k * 16384, pm, 32 * k, y, mbar);
+    }
+    if (active) lo = __ldcg(p.part_lse + so);
+  } else {
+    if (active) {
+      const float* src = p.part_o + so * kD;
+#pragma unroll
+      for (int j = 0; j < kD / 4; ++j)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + j * 2048), "l"(src + 4 * j) : "memory");
+      lo = __ldcg(p.part_lse + so);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
   const float l0 = self_first ? lse2 : lo, l1 = self_first ? lo : lse2;
   float mx = -INFINITY;
   mx = fmaxf(mx, l0);
@@ -828,7 +852,21 @@ __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pie
   z += exp2f(l1 - mx);
   const float zinv = 1.f / z;
   const float w0 = exp2f(l0 - mx) * zinv, w1 = exp2f(l1 - mx) * zinv;
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if constexpr (kWide) {
+    // bounded; the copy is waited for even after another role's abort, so
+    // that it has landed before the CTA exits
+    const unsigned long long t0 = globaltimer();
+    bool landed = mbar_test(mbar, 0);
+    while (!landed) {
+      landed = mbar_test(mbar, 0);
+      if (!landed && globaltimer() - t0 > timeout_ns()) {
+        if (p.status) atomicOr(p.status, TV_DEV_TIMEOUT);
+        break;
+      }
+    }
+  } else {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   const uint8_t* srow = stage + rl * 16;
 #pragma unroll 1
@@ -841,7 +879,10 @@ __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pie
     float acc[16];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float4 o = *reinterpret_cast<const float4*>(srow + ((c >> 2) + j) * 2048);
+      const int q4 = (c >> 2) + j;  // float4 chunk of the row
+      const float4 o = kWide ? *reinterpret_cast<const float4*>(stage + (q4 >> 3) * 16384 + rl * 128 +
+                                                                 (((q4 & 7) ^ (rl & 7)) << 4))
+                             : *reinterpret_cast<const float4*>(srow + q4 * 2048);
       const float ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -862,7 +903,8 @@ __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pie
 template <int kStage, bool kWide = false>
 __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
                                                bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
-                                               uint8_t* stage) {
+                                               uint8_t* stage, const CUtensorMap* pm = nullptr,
+                                               uint64_t* mbar = nullptr) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   constexpr float kLn2 = 0.69314718055994530942f;
   const float inv = l > 0.f ? 1.f / l : 0.f;  // no key at all (empty prefix, absent node): zero row
@@ -887,7 +929,7 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   if constexpr (kStage == 2) {
     const bool pair = stage != nullptr && pc.c1 - pc.c0 == 1 && pc.T >= pc.P;
     if (pair && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
-      staged_pair_merge<kWide>(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
+      staged_pair_merge<kWide>(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row, pm, mbar);
       if (valid_row) *ctr = 0;
       return 1;
     }
@@ -965,7 +1007,8 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
 template <int kStage, bool kWide = false>
 __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan& sp, const Segment& s, int row,
                                            bool valid_row, int64_t orow, uint32_t tO, float m_run, float l,
-                                           uint8_t* stage) {
+                                           uint8_t* stage, const CUtensorMap* pm = nullptr,
+                                           uint64_t* mbar = nullptr) {
 #ifdef TV_TC_TRACE
   const unsigned long long t_in = globaltimer();
   TV_TRACE_ROW0(4, t_in);
@@ -973,7 +1016,7 @@ __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan&
 #ifdef TV_TC_TRACE
   const int route =
 #endif
-  finish_row_impl<kStage, kWide>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
+  finish_row_impl<kStage, kWide>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage, pm, mbar);
 #ifdef TV_TC_TRACE
   const unsigned long long t_out = globaltimer();
   TV_TRACE_ROW0(5, t_out);
@@ -989,6 +1032,7 @@ __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan&
 struct TcMaps {
   CUtensorMap kc, vc, kt, vt;
   CUtensorMap qm;  // Q [B * N][Hq][D] in boxes of 64 columns x G heads x 128 / G nodes (128 rows of a unit)
+  CUtensorMap pm;  // float32 partials [2 P RPG][D] in boxes of 32 columns x 128 rows (one M tile's rows)
 };
 
 // TMA producer (warp 0): streams every tile of the CTA's slice into the
@@ -1917,6 +1961,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     mbar_init(&bars.cp_done, 1);
     mbar_init(&bars.q1_free, 1);
     mbar_init(&bars.q1_full, 1);
+    mbar_init(&bars.merge_full[0], 1);
+    mbar_init(&bars.merge_full[1], 1);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -2388,7 +2434,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         stage = smem_raw + (base - raw) + (m == 0 ? C::kOffK : C::kOffV);
       }
       if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
-      finish_row<2, kQS>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage);
+      finish_row<2, kQS>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage, &maps.pm, &bars.merge_full[m]);
       fence_before();
       if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       if constexpr (kSkip) ++useg;
@@ -3017,9 +3063,10 @@ int get_encoder(EncodeTiled* fn) {
 }
 
 int encode(EncodeTiled fn, CUtensorMap* map, const void* ptr, int rank, const cuuint64_t* dims,
-           const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+           const cuuint64_t* strides, const cuuint32_t* box, const char* what,
+           CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+  CUresult r = fn(map, type, rank, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
@@ -3121,13 +3168,18 @@ int tc_ctas_per_sm(int rows) { return rows <= 128 ? Cfg<1>::kCtasPerSm : 1; }
 
 // Virtual tiles charged per unit: measured cost of finishing one unit and
 // starting the next, in units of one 64-key tile of the steady state (chosen
-// by sweeping: 3 for one M tile, 8 for two on the 64-request workload).
+// by sweeping: 3 for one M tile; 6 for two -- 3 to 8 swept on the 64-request,
+// dynamic and ragged workloads once Q reached the operand slots through the
+// S issuers, 6 best on all three; every two-M-tile variant takes the same
+// value, so that the fused-RoPE and separate paths split units alike and give
+// the same bits).
 #ifndef TV_UNIT_COST_M1
 #define TV_UNIT_COST_M1 3
 #endif
 #ifndef TV_UNIT_COST_M2
-#define TV_UNIT_COST_M2 8
+#define TV_UNIT_COST_M2 6
 #endif
+
 int tc_unit_cost(int rows_per_unit) { return rows_per_unit <= 128 ? TV_UNIT_COST_M1 : TV_UNIT_COST_M2; }
 
 #ifdef TV_TC_TRACE
@@ -3175,6 +3227,14 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bo
     cuuint64_t strides[2] = {row_bytes, row_bytes * p.Hq};
     cuuint32_t box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)(128 / p.G)};
     if ((st = encode(fn, &maps.qm, p.q, 3, dims, strides, box, "q"))) return st;
+  }
+  {
+    // the float32 partials [2 P RPG][D]: one box is 128 rows x 32 columns
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)2 * p.P * p.RPG};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 4};
+    cuuint32_t box[2] = {32, 128};
+    if ((st = encode(fn, &maps.pm, p.part_o, 2, dims, strides, box, "partials", CU_TENSOR_MAP_DATA_TYPE_FLOAT32)))
+      return st;
   }
   if (duo) {
     // one unit of up to 256 rows on a CTA pair: half of every K/V tile per SM
