@@ -119,7 +119,7 @@ struct Bars {
   uint64_t drain[4];          // one per MMA-issuing thread: its products have completed (after an abort)
   uint64_t q0s_full, cp_done;  // staged Q (two-M-tile kernel): the next unit's Q_0 has landed / been copied to TMEM
   uint64_t q1_free, q1_full;   //   ... this unit's last S_1 has completed / the next unit's Q_1 has landed
-  uint64_t merge_full[2];      //   ... the other piece's rows of M tile m have landed (end-of-slice merge)
+  uint64_t merge_full[2][4];   //   ... the other piece's rows of warp q of M tile m have landed (end-of-slice merge)
   uint32_t tmem_base;
   int abort;
 };
@@ -137,19 +137,26 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 }
 
 #ifdef TV_TEST_HOOKS
-// Development builds only (-DTV_TEST_HOOKS; the product library has neither
-// variable): a test shortens the wait limit and has CTA 0's TMA producers
-// skip the loads (and the arrival) of one ring tile, so that the bounded
-// waits run out and the timeout exit is exercised without a fault.
+// Development builds only (-DTV_TEST_HOOKS; the product library has none of
+// these variables): a test shortens the wait limit and has CTA 0's TMA
+// producers skip the loads (and the arrival) of one ring tile, so that the
+// bounded waits run out and the timeout exit is exercised without a fault;
+// or it keeps the epilogue warps of some TMEM quarters off the direct merge,
+// so that the warps of one M tile take different merge routes.
 __device__ unsigned long long g_test_timeout_ns = kTimeoutNs;
-__device__ int g_test_withhold = -1;  // ring index of CTA 0 left without loads
+__device__ int g_test_withhold = -1;      // ring index of CTA 0 left without loads
+__device__ int g_test_publish_warps = 0;  // bit q: warps of TMEM quarter q never merge directly
 __device__ __forceinline__ unsigned long long timeout_ns() { return *(volatile unsigned long long*)&g_test_timeout_ns; }
 __device__ __forceinline__ bool test_withhold(uint32_t g) {
   return blockIdx.x == 0 && (int)g == *(volatile int*)&g_test_withhold;
 }
+__device__ __forceinline__ bool test_no_direct(int rl) {
+  return (*(volatile int*)&g_test_publish_warps >> (rl >> 5)) & 1;
+}
 #else
 __device__ __forceinline__ unsigned long long timeout_ns() { return kTimeoutNs; }
 __device__ __forceinline__ bool test_withhold(uint32_t) { return false; }
+__device__ __forceinline__ bool test_no_direct(int) { return false; }
 #endif
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -811,11 +818,13 @@ __device__ __forceinline__ void staged_merge(const AttnParams& p, const Pieces& 
 // piece order with the arithmetic of piece_stats / accum_pieces, so the row
 // matches the other merge routes bit for bit.  Warp-collective (TMEM reads);
 // `active` lanes merge their row.
-// kWide (the staged-Q two-M-tile kernel): the other piece's 128 rows of
-// this M tile come by TMA (pm: four 16 KB boxes of 32 columns, 128B-swizzled,
-// on mbar) instead of 32 16-byte cp.async requests per thread, which the
-// load/store unit took about 9,000 cycles to issue; rows are then read
-// swizzled (4 wavefronts per warp access, the minimum for 512 bytes).
+// kWide (the staged-Q two-M-tile kernel): each warp's 32 rows of the other
+// piece come by TMA (pm: four 4 KB boxes of 32 columns x 32 rows,
+// 128B-swizzled, on the warp's own barrier `mbar`) instead of 32 16-byte
+// cp.async requests per thread, which the load/store unit took about 9,000
+// cycles to issue; rows are then read swizzled (4 wavefronts per warp access,
+// the minimum for 512 bytes).  Each warp takes this route on its own rows'
+// arrival counts, so no warp waits for a copy another warp issues.
 template <bool kWide>
 __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pieces& pc, float lse2, float inv,
                                                   int row, int rl, int64_t orow, uint32_t tO, uint8_t* stage,
@@ -826,11 +835,11 @@ __device__ __forceinline__ void staged_pair_merge(const AttnParams& p, const Pie
   const uint32_t dst = smem_u32(stage) + rl * 16;
   float lo = 0.f;
   if constexpr (kWide) {
-    if (rl == 0) {
-      const int y = (int)(so - rl);  // the M tile's first row in the partials
-      mbar_expect_tx(mbar, 128 * kD * 4);
+    if ((rl & 31) == 0) {
+      const int y = (int)so;  // the warp's first row in the partials
+      mbar_expect_tx(mbar, 32 * kD * 4);
 #pragma unroll
-      for (int k = 0; k < kD / 32; ++k) tma_2d(smem_u32(stage) + k * 16384, pm, 32 * k, y, mbar);
+      for (int k = 0; k < kD / 32; ++k) tma_2d(smem_u32(stage) + k * 16384 + rl * 128, pm, 32 * k, y, mbar);
     }
     if (active) lo = __ldcg(p.part_lse + so);
   } else {
@@ -918,7 +927,8 @@ __device__ __forceinline__ int finish_row_impl(const AttnParams& p, const SliceP
   float mx = lse2, z = 1.f;
   const int rl = row & 127;
   const bool staged = kStage == 1 && stage != nullptr && !complete && pc.c1 - pc.c0 < kStagePieces && pc.T >= pc.P;
-  if (!complete && valid_row && p.direct_merge) direct = ld_acquire_u32(ctr) + mine == (uint32_t)s.n;
+  if (!complete && valid_row && p.direct_merge && !test_no_direct(rl))
+    direct = ld_acquire_u32(ctr) + mine == (uint32_t)s.n;
   if constexpr (kStage == 1) {
     if (staged && __all_sync(0xffffffffu, direct || !valid_row) && __any_sync(0xffffffffu, direct)) {
       staged_merge(p, pc, lse2, inv, row, rl, orow, tO, stage, valid_row);
@@ -1032,7 +1042,7 @@ __device__ __forceinline__ void finish_row(const AttnParams& p, const SlicePlan&
 struct TcMaps {
   CUtensorMap kc, vc, kt, vt;
   CUtensorMap qm;  // Q [B * N][Hq][D] in boxes of 64 columns x G heads x 128 / G nodes (128 rows of a unit)
-  CUtensorMap pm;  // float32 partials [2 P RPG][D] in boxes of 32 columns x 128 rows (one M tile's rows)
+  CUtensorMap pm;  // float32 partials [2 P RPG][D] in boxes of 32 columns x 32 rows (one warp's rows)
 };
 
 // TMA producer (warp 0): streams every tile of the CTA's slice into the
@@ -1961,8 +1971,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     mbar_init(&bars.cp_done, 1);
     mbar_init(&bars.q1_free, 1);
     mbar_init(&bars.q1_full, 1);
-    mbar_init(&bars.merge_full[0], 1);
-    mbar_init(&bars.merge_full[1], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&bars.merge_full[i / 4][i % 4], 1);
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -2434,7 +2443,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         stage = smem_raw + (base - raw) + (m == 0 ? C::kOffK : C::kOffV);
       }
       if (m == 0 && rl == 0) TV_TRACE(14, g - 1);
-      finish_row<2, kQS>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage, &maps.pm, &bars.merge_full[m]);
+      finish_row<2, kQS>(p, sp, s, row, valid_row, orow, tO, m_run, l, stage, &maps.pm,
+                         &bars.merge_full[m][rl >> 5]);
       fence_before();
       if (m == 0 && rl == 0) TV_TRACE(5, g - 1);
       if constexpr (kSkip) ++useg;
@@ -3229,10 +3239,10 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bo
     if ((st = encode(fn, &maps.qm, p.q, 3, dims, strides, box, "q"))) return st;
   }
   {
-    // the float32 partials [2 P RPG][D]: one box is 128 rows x 32 columns
+    // the float32 partials [2 P RPG][D]: one box is 32 rows x 32 columns
     cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)2 * p.P * p.RPG};
     cuuint64_t strides[1] = {(cuuint64_t)kD * 4};
-    cuuint32_t box[2] = {32, 128};
+    cuuint32_t box[2] = {32, 32};
     if ((st = encode(fn, &maps.pm, p.part_o, 2, dims, strides, box, "partials", CU_TENSOR_MAP_DATA_TYPE_FLOAT32)))
       return st;
   }
@@ -3280,6 +3290,14 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bo
 extern "C" int tv_test_set_hooks(unsigned long long timeout_ns, int withhold_tile) {
   if (cudaMemcpyToSymbol(tv::g_test_timeout_ns, &timeout_ns, sizeof(timeout_ns)) != cudaSuccess) return -6;
   if (cudaMemcpyToSymbol(tv::g_test_withhold, &withhold_tile, sizeof(withhold_tile)) != cudaSuccess) return -6;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -6;
+}
+
+// Development builds only: warps of the TMEM quarters in `mask` (bit q for
+// lanes 32 q .. 32 q + 31 of every M tile) publish their rows of a split unit
+// instead of merging them directly; 0 restores the normal routes.
+extern "C" int tv_test_set_publish_warps(int mask) {
+  if (cudaMemcpyToSymbol(tv::g_test_publish_warps, &mask, sizeof(mask)) != cudaSuccess) return -6;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -6;
 }
 #endif
