@@ -339,6 +339,15 @@ class Step:
             self.sample = (W.sample_tree_inputs(w, parent, device=dev) if w.sample_tree
                            else W.sample_chain_inputs(w, device=dev))
         cols = n if self.sample is None else self.sample["p"].shape[1]
+        # the sampler's workspace: with it TV_SAMPLE_AUTO may take the grid
+        # sampler (walk, pass and draw kernels, then the single-launch walk
+        # of the requests they leave)
+        self.sample_ws, acc_launches = None, 1
+        if self.sample is not None:
+            sB, sN, sV = self.sample["p"].shape
+            ws_bytes = capi.tv_accept_sample_workspace_size(sB, sN, sV)
+            self.sample_ws = capi.alloc_workspace(ws_bytes, dev)
+            acc_launches = 4 if capi.tv_accept_sample_uses_grid(sB, sN, sV, 0, ws_bytes) else 1
         self.acc_out = torch.empty(B, cols, dtype=torch.int32, device=dev)
         self.acc_n = torch.empty(B, dtype=torch.int32, device=dev)
         self.acc_path = torch.empty(B, cols, dtype=torch.int32, device=dev)
@@ -358,7 +367,7 @@ class Step:
             except capi.TVError:
                 uses_tc = False
         # mask + rope, the attention kernel(s), the acceptance kernel
-        self.launches = 1 + (1 if uses_tc else 3) + (1 if w.accept != "none" else 0)
+        self.launches = 1 + (1 if uses_tc else 3) + (acc_launches if w.accept != "none" else 0)
 
     def run_attn(self):
         i = self.inp
@@ -395,7 +404,8 @@ class Step:
         elif self.sample is not None:
             s = self.sample
             c.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
-                                    n_nodes=s["n_nodes"], out=self.acc_out, n_out=self.acc_n, path=self.acc_path)
+                                    n_nodes=s["n_nodes"], out=self.acc_out, n_out=self.acc_n, path=self.acc_path,
+                                    workspace=self.sample_ws)
 
     def commit_path(self):
         """The accepted path of the last step (the deepest chain when the

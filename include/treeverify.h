@@ -91,15 +91,23 @@ extern "C" {
  * tv_tree_attn_verify_static, which always clears its counters. */
 #define TV_ATTN_WORKSPACE_ZEROED 32
 
-/* Kernel selection of tv_tree_accept_sample. */
+/* Kernel selection of tv_tree_accept_sample and tv_chain_accept_sample. */
 #define TV_SAMPLE_AUTO 0        /* TV_SAMPLE_CLUSTER when every request's cluster is resident at
-                                   once, else TV_SAMPLE_STREAM with the largest cluster size that
-                                   keeps them all resident, else TV_SAMPLE_SINGLE_CTA            */
+                                   once; else TV_SAMPLE_GRID when a workspace is given and
+                                   V <= 1,048,576; else TV_SAMPLE_STREAM with the largest cluster
+                                   size that keeps them all resident, else TV_SAMPLE_SINGLE_CTA  */
 #define TV_SAMPLE_CLUSTER 1     /* one 8-CTA cluster per request, level weights in shared memory;
                                    TV_ERR_UNSUPPORTED when V > 136,512                            */
 #define TV_SAMPLE_SINGLE_CTA 2  /* one CTA per request, rows streamed, weights recomputed per pass */
 #define TV_SAMPLE_STREAM 3      /* clusters of 1-8 CTAs per request streaming their row slices, only
                                    chunk totals kept; TV_ERR_UNSUPPORTED when V > 1,048,576         */
+#define TV_SAMPLE_GRID 4        /* three kernels over a workspace: a warp per request walks to its
+                                   first rejection or leaf, the stop rows' pass runs as uniform
+                                   4096-entry items over the whole GPU, a CTA per request draws;
+                                   a request whose rejected child has a later valid sibling is
+                                   walked again by the TV_SAMPLE_AUTO kernel (the others return at
+                                   once).  TV_ERR_INVALID_ARG without a large enough workspace,
+                                   TV_ERR_UNSUPPORTED when V > 1,048,576                         */
 
 /* Description of the last failure on this thread ("" if none). */
 const char* tv_last_error(void);
@@ -417,15 +425,42 @@ int tv_tree_accept_greedy(const float* logits, const int32_t* target_argmax,
  *           entry), so repeated rejections at a node cost one shared-memory
  *           pass each.  The streaming clusters re-read their slice from
  *           memory at every pass and keep only 256-element chunk totals, so
- *           large batches stay resident.  Unknown flags give
+ *           large batches stay resident.  The grid sampler spreads the stop
+ *           rows' pass evenly over the GPU (a request that rejected reads
+ *           two rows, one that reached a leaf one).  Unknown flags give
  *           TV_ERR_INVALID_ARG.
+ * workspace device scratch (nullable), 16-byte aligned, of workspace_bytes
+ *           >= tv_accept_sample_workspace_size(B, N, V) for the grid
+ *           sampler; its contents need no initialisation and are not read
+ *           after the call.  NULL (or a smaller size) keeps TV_SAMPLE_AUTO
+ *           to the single-launch kernels.  Calls that overlap on the GPU
+ *           need their own workspaces.
  */
 int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,
                           const int32_t* parent, int64_t parent_bstride,
                           const int32_t* n_nodes, const float* u_accept,
                           const float* u_final, int32_t B, int32_t N, int32_t V,
                           int32_t* out, int32_t* n_out, int32_t* path, int32_t out_cols,
-                          int32_t flags, int32_t* status, void* stream);
+                          int32_t flags, void* workspace, size_t workspace_bytes,
+                          int32_t* status, void* stream);
+
+/*
+ * tv_accept_sample_workspace_size -- host.  Bytes of the grid sampler's
+ * workspace for B requests of N nodes over V vocabulary entries: 16 per
+ * request, and 16 per request and 4096-entry chunk of a row; 0 when B <= 0
+ * or V <= 0.
+ */
+size_t tv_accept_sample_workspace_size(int32_t B, int32_t N, int32_t V);
+
+/*
+ * tv_accept_sample_uses_grid -- host (queries the current device).  Sets
+ * *grid to 1 when a sampler call with these sizes, flags and a workspace of
+ * workspace_bytes (0: none) takes the grid sampler (its three kernels plus a
+ * walk of the requests they leave), else 0.  TV_ERR_INVALID_ARG for unknown
+ * flags or bad sizes.
+ */
+int tv_accept_sample_uses_grid(int32_t B, int32_t N, int32_t V, int32_t flags,
+                               size_t workspace_bytes, int32_t* grid);
 
 /*
  * tv_chain_accept_sample -- device, asynchronous.  The verifier page's own
@@ -446,12 +481,14 @@ int tv_tree_accept_sample(const float* p, const float* q, const int32_t* tokens,
  * u_final   device float32 [B]: uniform of the replacement / bonus draw.
  * out       device int32 [B, out_cols] out: emitted tokens, -1 padded;
  * n_out     device int32 [B] out: accepted drafts + 1.
- * K in [0, TV_MAX_NODES - 1]; flags, status as in tv_tree_accept_sample.
+ * K in [0, TV_MAX_NODES - 1]; flags, workspace (size for N = K + 1) and
+ * status as in tv_tree_accept_sample.
  */
 int tv_chain_accept_sample(const float* p, const float* q, const int32_t* draft,
                            const int32_t* num_draft, const float* u, const float* u_final,
                            int32_t B, int32_t K, int32_t V, int32_t* out, int32_t* n_out,
-                           int32_t out_cols, int32_t flags, int32_t* status, void* stream);
+                           int32_t out_cols, int32_t flags, void* workspace,
+                           size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
  * tv_kv_commit -- device, asynchronous.  Copies the accepted path's tree K/V

@@ -25,7 +25,7 @@ TV_ATTN_PUBLISH_ALL = 4
 TV_ATTN_ROPE_Q = 8
 TV_ATTN_CTA_PAIRS = 16
 TV_ATTN_WORKSPACE_ZEROED = 32
-TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA, TV_SAMPLE_STREAM = 0, 1, 2, 3
+TV_SAMPLE_AUTO, TV_SAMPLE_CLUSTER, TV_SAMPLE_SINGLE_CTA, TV_SAMPLE_STREAM, TV_SAMPLE_GRID = 0, 1, 2, 3, 4
 TV_DEV_BAD_TOPOLOGY, TV_DEV_BAD_TOKEN, TV_DEV_OUT_OVERFLOW, TV_DEV_BAD_POSITION, TV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 TV_DEV_BAD_BLOCK = 32
 STATUS_NAMES = {0: "TV_OK", -1: "TV_ERR_INVALID_ARG", -2: "TV_ERR_MISSING_PARENT", -3: "TV_ERR_TOO_MANY_NODES",
@@ -53,9 +53,11 @@ SIGNATURES = {
                                        _P, _I32, _P, _P]),
     "tv_tree_accept_greedy": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P]),
     "tv_tree_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32,
-                                             _I32, _P, _P]),
-    "tv_chain_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P,
-                                              _P]),
+                                             _I32, _P, _SZ, _P, _P]),
+    "tv_accept_sample_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32]),
+    "tv_accept_sample_uses_grid": (ctypes.c_int, [_I32, _I32, _I32, _I32, _SZ, _P]),
+    "tv_chain_accept_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _SZ,
+                                              _P, _P]),
     "tv_kv_commit": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
                                     _I32, _I32, _P, _P]),
 }
@@ -356,10 +358,34 @@ def tv_tree_accept_greedy(tokens, parent, *, logits=None, target_argmax=None, n_
     return out, n_out, path
 
 
+def tv_accept_sample_workspace_size(B, N, V):
+    """Bytes of the grid sampler's workspace (tv_tree_accept_sample and
+    tv_chain_accept_sample with N = K + 1)."""
+    return int(lib().tv_accept_sample_workspace_size(B, N, V))
+
+
+def tv_accept_sample_uses_grid(B, N, V, flags=0, workspace_bytes=0):
+    """Whether a sampler call with these sizes, flags and workspace size takes
+    the grid sampler (queries the current device)."""
+    g = ctypes.c_int32(0)
+    _check("tv_accept_sample_uses_grid",
+           lib().tv_accept_sample_uses_grid(B, N, V, int(flags), int(workspace_bytes), ctypes.addressof(g)))
+    return bool(g.value)
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    _dev(workspace, "workspace", (torch.uint8,))
+    return workspace, workspace.numel()
+
+
 def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=None, out_cols=None, out=None,
-                          n_out=None, path=None, flags=0, status=None, stream=None):
+                          n_out=None, path=None, flags=0, workspace=None, status=None, stream=None):
     """Stochastic walk; returns (out [B, out_cols], n_out [B], path [B, out_cols]).
-    flags: TV_SAMPLE_AUTO / TV_SAMPLE_CLUSTER / TV_SAMPLE_SINGLE_CTA / TV_SAMPLE_STREAM."""
+    flags: TV_SAMPLE_AUTO / TV_SAMPLE_CLUSTER / TV_SAMPLE_SINGLE_CTA / TV_SAMPLE_STREAM /
+    TV_SAMPLE_GRID; workspace: uint8 device tensor of
+    tv_accept_sample_workspace_size(B, N, V) bytes (alloc_workspace), or None."""
     _dev(p, "p", (torch.float32,))
     _dev(q, "q", (torch.float32,))
     _dev(tokens, "tokens", (torch.int32,))
@@ -370,20 +396,21 @@ def tv_tree_accept_sample(p, q, tokens, parent, u_accept, u_final, *, n_nodes=No
     out_cols = N if out_cols is None else out_cols
     out, n_out, path = _accept_outputs(B, out_cols, p.device, out, n_out, path)
     bstride = 0 if parent.dim() == 1 else parent.stride(0)
+    ws, ws_bytes = _ws(workspace)
     _check("tv_tree_accept_sample",
            lib().tv_tree_accept_sample(_ptr(p), _ptr(q), _ptr(tokens), _ptr(parent), bstride, _ptr(n_nodes),
                                        _ptr(u_accept), _ptr(u_final), B, N, V, _ptr(out), _ptr(n_out), _ptr(path),
-                                       out_cols, int(flags), _ptr(status), _stream(stream)))
+                                       out_cols, int(flags), _ptr(ws), ws_bytes, _ptr(status), _stream(stream)))
     return out, n_out, path
 
 
 def tv_chain_accept_sample(p, q, draft, u, u_final, *, num_draft=None, out_cols=None, out=None, n_out=None,
-                           flags=0, status=None, stream=None):
+                           flags=0, workspace=None, status=None, stream=None):
     """The verifier page's chain walk, read in place: p float32 [B, K + 1, V],
     q float32 [B, K, V], draft int32 [B, K], u float32 [B, K], u_final float32
-    [B], num_draft int32 [B] (optional).  Returns (out [B, out_cols] -1
-    padded, n_out [B] = accepted + 1); allocates nothing when out and n_out
-    are given."""
+    [B], num_draft int32 [B] (optional), workspace as in tv_tree_accept_sample
+    (N = K + 1).  Returns (out [B, out_cols] -1 padded, n_out [B] =
+    accepted + 1); allocates nothing when out and n_out are given."""
     _dev(p, "p", (torch.float32,))
     _dev(q, "q", (torch.float32,))
     _dev(draft, "draft", (torch.int32,))
@@ -397,14 +424,16 @@ def tv_chain_accept_sample(p, q, draft, u, u_final, *, num_draft=None, out_cols=
         raise ValueError("tv_chain_accept_sample: q [B, K, V], draft and u [B, K] with p [B, K + 1, V]")
     out_cols = K1 if out_cols is None else out_cols
     out, n_out, _ = _accept_outputs(B, out_cols, p.device, out, n_out, False)
+    ws, ws_bytes = _ws(workspace)
     _check("tv_chain_accept_sample",
            lib().tv_chain_accept_sample(_ptr(p), _ptr(q), _ptr(draft), _ptr(num_draft), _ptr(u), _ptr(u_final), B,
-                                        K, V, _ptr(out), _ptr(n_out), out_cols, int(flags), _ptr(status),
-                                        _stream(stream)))
+                                        K, V, _ptr(out), _ptr(n_out), out_cols, int(flags), _ptr(ws), ws_bytes,
+                                        _ptr(status), _stream(stream)))
     return out, n_out
 
 
-def verify_chain(draft, q, p, num_draft, u, u_final, *, flags=0, out=None, n_out=None, status=None, stream=None):
+def verify_chain(draft, q, p, num_draft, u, u_final, *, flags=0, out=None, n_out=None, workspace=None, status=None,
+                 stream=None):
     """The verifier page's verify(draft, q, p, num_draft, u, u_final) call:
     draft int32 [B, K] (draft j drawn from q[:, j]); q float32 [B, K, V]; p
     float32 [B, K + 1, V] (the target after each prefix, the last row for the
@@ -414,7 +443,7 @@ def verify_chain(draft, q, p, num_draft, u, u_final, *, flags=0, out=None, n_out
     tv_chain_accept_sample: the arrays are read in place, and with out and
     n_out given nothing is allocated."""
     return tv_chain_accept_sample(p, q, draft, u, u_final, num_draft=num_draft, out=out, n_out=n_out, flags=flags,
-                                  status=status, stream=stream)
+                                  workspace=workspace, status=status, stream=stream)
 
 
 def accept_greedy(parent, tokens, target_argmax, *, n_nodes=None, status=None, stream=None):

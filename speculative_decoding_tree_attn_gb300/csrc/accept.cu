@@ -113,12 +113,34 @@ struct NodeIdx {
   }
 };
 
-// load_tree for the stochastic walk (node 0's token is never used).
-__device__ __forceinline__ void load_tree_ix(const int32_t* parent, int64_t pstride, const int32_t* tokens,
-                                             const NodeIdx& ix, int b, int N, int32_t* s_par, int32_t* s_tok) {
+// A request's state after the grid sampler's walk (see gc_walk_kernel): its
+// stop node is drawn from, its walk was truncated, or it needs another
+// kernel's walk.  The other kernels take an optional state array and walk
+// only the requests marked kGcOther.
+enum : int { kGcDraw = 0, kGcDone = 1, kGcOther = 2 };
+
+// The tree of request b for the stochastic walk (node 0's token is never
+// used), with every node's acceptance-test inputs: p(x) and q(x) from its
+// parent's rows at its token x, and its uniform (a test after rejections at
+// the parent computes the residual's weight from the same p(x) and q(x)).
+// They depend on the tree alone (the walk only chooses which it reads), so
+// all of them are requested at once: one memory round trip for the whole
+// walk instead of one per level.  Nodes whose parent does not precede them,
+// or whose token is outside the vocabulary, are never tested and load
+// nothing.
+__device__ __forceinline__ void load_walk(const float* p, const float* q, const float* u_accept,
+                                          const int32_t* parent, int64_t pstride, const int32_t* tokens,
+                                          const NodeIdx& ix, int b, int N, int V, int32_t* s_par, int32_t* s_tok,
+                                          float* s_tp, float* s_tq, float* s_tu) {
   for (int c = threadIdx.x; c < N; c += blockDim.x) {
-    s_par[c] = parent[(int64_t)b * pstride + c];
-    s_tok[c] = c >= ix.shift ? tokens[ix.tu(b, c)] : -1;
+    const int par = parent[(int64_t)b * pstride + c];
+    const int x = c >= ix.shift ? tokens[ix.tu(b, c)] : -1;
+    s_par[c] = par;
+    s_tok[c] = x;
+    const bool test = c >= 1 && par >= 0 && par < c && x >= 0 && x < V;
+    s_tu[c] = c >= 1 && c >= ix.shift ? u_accept[ix.tu(b, c)] : 0.f;
+    s_tp[c] = test ? p[((int64_t)b * N + par) * V + x] : 0.f;
+    s_tq[c] = test ? q[ix.qrow(b, par) * V + x] : 0.f;
   }
 }
 
@@ -777,8 +799,10 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
                                                           const int32_t* __restrict__ n_nodes,
                                                           const float* __restrict__ u_accept,
                                                           const float* __restrict__ u_final, int N, int V,
-                                                          NodeIdx ix, AcceptOut o) {
+                                                          NodeIdx ix, AcceptOut o, const int4* __restrict__ only) {
+  if (only && only[blockIdx.x].x != kGcOther) return;  // walked by the grid sampler
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
+  __shared__ float s_tp[TV_MAX_NODES], s_tq[TV_MAX_NODES], s_tu[TV_MAX_NODES];  // acceptance-test inputs by node
   __shared__ uint64_t S[TV_MAX_NODES + 1];
   __shared__ uint64_t s_red[kSampleWarps], s_base;
   extern __shared__ float4 dsm[];  // stream ring, then the chunk totals of the current level
@@ -787,7 +811,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
   __shared__ int s_flag, s_idx, s_chunk;
   const int b = blockIdx.x;
   TV_SAMPLE_T(0);
-  load_tree_ix(parent, pstride, tokens, ix, b, N, s_par, s_tok);
+  load_walk(p, q, u_accept, parent, pstride, tokens, ix, b, N, V, s_par, s_tok, s_tp, s_tq, s_tu);
   __syncthreads();
   TV_SAMPLE_T(1);
   const int n = ix.nodes(n_nodes, b, N);
@@ -816,8 +840,8 @@ __global__ void __launch_bounds__(kSampleThreads, 2) sample_kernel(const float* 
         continue;
       }
       if (threadIdx.x == 0) {
-        const float px = row.p[x], qx = row.q[x];
-        const double uq = __dmul_rn((double)u_accept[ix.tu(b, c)], (double)qx);
+        const float px = s_tp[c], qx = s_tq[c];
+        const double uq = __dmul_rn((double)s_tu[c], (double)qx);
         bool ok;
         if (m == 0) ok = uq < (double)px;
         else ok = __dmul_rn(uq, (double)Wm) < (double)level_weight(px, qx, S, m);
@@ -1057,16 +1081,19 @@ __global__ void __launch_bounds__(kScThreads, 4)
     sample_cluster_kernel(const float* __restrict__ p, const float* __restrict__ q,
                           const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent, int64_t pstride,
                           const int32_t* __restrict__ n_nodes, const float* __restrict__ u_accept,
-                          const float* __restrict__ u_final, int N, int V, int Ls, NodeIdx ix, AcceptOut o) {
+                          const float* __restrict__ u_final, int N, int V, int Ls, NodeIdx ix, AcceptOut o,
+                          const int4* __restrict__ only) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
+  // walked by the grid sampler: the whole cluster returns before its first barrier
+  if (only && only[blockIdx.x / cl.num_blocks()].x != kGcOther) return;
   __shared__ int32_t s_par[TV_MAX_NODES], s_tok[TV_MAX_NODES];
   __shared__ uint64_t S[TV_MAX_NODES + 1];
   __shared__ uint64_t s_tot[2][kScCtas];
   __shared__ uint64_t s_lev[kScCtas];  // slice totals of the current level
   __shared__ uint64_t s_red[kScWarps];
   __shared__ int s_kid[TV_MAX_NODES];  // the current node's children in index order
-  __shared__ float s_kp[TV_MAX_NODES], s_kq[TV_MAX_NODES], s_ku[TV_MAX_NODES];  // their p(x), q(x), u
+  __shared__ float s_tp[TV_MAX_NODES], s_tq[TV_MAX_NODES], s_tu[TV_MAX_NODES];  // acceptance-test inputs by node
   __shared__ int s_nk, s_x, s_flag, s_chunk, s_idx;
   __shared__ uint64_t s_thr, s_base;
   extern __shared__ __align__(16) uint64_t sc_dyn[];
@@ -1076,7 +1103,7 @@ __global__ void __launch_bounds__(kScThreads, 4)
   const int rank = (int)cl.block_rank();
   const int nct = (int)cl.num_blocks();
   const int b = blockIdx.x / nct;
-  load_tree_ix(parent, pstride, tokens, ix, b, N, s_par, s_tok);
+  load_walk(p, q, u_accept, parent, pstride, tokens, ix, b, N, V, s_par, s_tok, s_tp, s_tq, s_tu);
   if (threadIdx.x == 0) s_x = V - 1;  // read by rank 0 after the draw's barrier
   __syncthreads();
   const int n = ix.nodes(n_nodes, b, N);
@@ -1096,23 +1123,14 @@ __global__ void __launch_bounds__(kScThreads, 4)
     TV_SC_SET(7, sc_tr[7] + 1);
     if (threadIdx.x == 0) S[0] = 1ull << 40;
     if (threadIdx.x < 32) {
-      // list the node's children with the row values their tests read, all
-      // loads in flight together
+      // list the node's children in index order
       const int lane = threadIdx.x;
       int cnt = 0;
       for (int base = node + 1; base < n; base += 32) {
         const int c = base + lane;
         const bool is = c < n && s_par[c] == node;
         const unsigned bal = __ballot_sync(0xffffffffu, is);
-        if (is) {
-          const int j = cnt + __popc(bal & ((1u << lane) - 1u));
-          const int x = s_tok[c];
-          const bool in_v = x >= 0 && x < V;
-          s_kid[j] = c;
-          s_kp[j] = in_v ? prow[x] : 0.f;
-          s_kq[j] = in_v ? qrow[x] : 0.f;
-          s_ku[j] = u_accept[ix.tu(b, c)];
-        }
+        if (is) s_kid[cnt + __popc(bal & ((1u << lane) - 1u))] = c;
         cnt += __popc(bal);
       }
       if (lane == 0) s_nk = cnt;
@@ -1130,8 +1148,8 @@ __global__ void __launch_bounds__(kScThreads, 4)
       // one thread decides (double precision is slow here) and shares it;
       // the pass after a rejection synchronises before s_flag is written again
       if (threadIdx.x == 0) {
-        const float px = s_kp[j], qx = s_kq[j];
-        const double uq = __dmul_rn((double)s_ku[j], (double)qx);
+        const float px = s_tp[c], qx = s_tq[c];
+        const double uq = __dmul_rn((double)s_tu[c], (double)qx);
         s_flag = m == 0 ? uq < (double)px : __dmul_rn(uq, (double)Wm) < (double)level_weight(px, qx, S, m);
       }
       __syncthreads();
@@ -1243,6 +1261,288 @@ __global__ void __launch_bounds__(kScThreads, 4)
   TV_SC_STORE(b);
 }
 
+// ------------------------------------------------------- stochastic, grid
+
+// The walk as three kernels over a caller's workspace, for large batches:
+// (1) one warp per request walks from the root with the gathered test inputs
+// (as load_walk does) until its first rejection or a leaf; (2) the pass that
+// the stop node needs -- the residual max(0, P - Q) after a rejection, or P
+// for a bonus -- runs over uniform (request, 4096-element chunk) items spread
+// over the whole GPU, each leaving its chunk's level-0 and level-1 totals;
+// (3) one CTA per request draws from those totals, re-reading the one chunk
+// that holds the crossing.  (Drawing in the pass kernel, by the last item of
+// a request to finish, measured slower: the last requests' draws then run
+// one after another at the end of the pass.)  The same arithmetic as the
+// other kernels, so the results match them bit for bit.  A request whose rejected child has a later valid sibling
+// needs the next level's total before that sibling's test: the walk marks
+// it, and one of the other kernels walks it again (every other request
+// returns at once there).
+constexpr int kGcChunk = 4096;                     // elements of one pass item
+constexpr int kGcThreads = 256;                    // = kScThreads: sc_block_sum serves these kernels too
+constexpr int kGcPer = kGcChunk / kGcThreads;      // 16 elements per thread
+constexpr int kGcMaxChunks = kGcThreads;           // chunk totals one draw CTA scans (V <= 2^20)
+constexpr int kGcWalkWarps = kGcThreads / 32;      // requests per walk CTA
+static_assert(kGcThreads == kScThreads, "sc_block_sum");
+
+// per request: {state, stop node, level of the draw (0 bonus, 1 residual), tokens emitted}
+struct GcWs {
+  int4* state;     // [B]
+  uint64_t* tot;   // [B][nch][2]: level-1 and level-0 totals of each chunk
+  int nch;
+};
+
+__global__ void __launch_bounds__(kGcThreads) gc_walk_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                                                            const int32_t* __restrict__ tokens,
+                                                            const int32_t* __restrict__ parent, int64_t pstride,
+                                                            const int32_t* __restrict__ n_nodes,
+                                                            const float* __restrict__ u_accept, int B, int N, int V,
+                                                            NodeIdx ix, AcceptOut o, GcWs ws) {
+  const int lane = threadIdx.x % 32;
+  const int b = blockIdx.x * kGcWalkWarps + threadIdx.x / 32;
+  if (b >= B) return;
+  const int n = ix.nodes(n_nodes, b, N);
+  // nodes lane and lane + 32: parent, token and the test's p(x), q(x), u
+  int par[2], tok[2];
+  float tp[2], tq[2], tu[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = lane + 32 * h;
+    par[h] = -1;
+    tok[h] = -1;
+    tp[h] = tq[h] = tu[h] = 0.f;
+    if (c < N) {
+      par[h] = parent[(int64_t)b * pstride + c];
+      tok[h] = c >= ix.shift ? tokens[ix.tu(b, c)] : -1;
+      if (c >= 1 && c >= ix.shift) tu[h] = u_accept[ix.tu(b, c)];
+      if (c >= 1 && par[h] >= 0 && par[h] < c && tok[h] >= 0 && tok[h] < V) {
+        tp[h] = p[((int64_t)b * N + par[h]) * V + tok[h]];
+        tq[h] = q[ix.qrow(b, par[h]) * V + tok[h]];
+      }
+    }
+  }
+  int node = 0, k = 0, state = kGcDraw, level = 0;
+  while (true) {
+    // the node's children in index order, as bit masks over the two windows
+    unsigned kids[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = lane + 32 * h;
+      kids[h] = __ballot_sync(0xffffffffu, c > node && c < n && par[h] == node);
+    }
+    int taken = -1;
+    bool rejected = false;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      unsigned m = kids[h];
+      const int tk = h ? tok[1] : tok[0];
+      const float pk = h ? tp[1] : tp[0], qk = h ? tq[1] : tq[0], uk = h ? tu[1] : tu[0];
+      while (m && taken < 0 && state == kGcDraw) {
+        const int l = __ffs(m) - 1;
+        m &= m - 1;
+        const int x = __shfl_sync(0xffffffffu, tk, l);
+        const float px = __shfl_sync(0xffffffffu, pk, l), qx = __shfl_sync(0xffffffffu, qk, l);
+        const float u = __shfl_sync(0xffffffffu, uk, l);
+        if (x < 0 || x >= V) {
+          if (lane == 0 && o.status) atomicOr(o.status, TV_DEV_BAD_TOKEN);
+          continue;
+        }
+        if (rejected) {
+          state = kGcOther;  // a later sibling is tested at the next level: another kernel's walk
+        } else if (__dmul_rn((double)u, (double)qx) < (double)px) {
+          taken = l + 32 * h;
+          if (lane == 0) {
+            o.out[(int64_t)b * o.out_cols + k] = x;
+            if (o.path) o.path[(int64_t)b * o.out_cols + k] = node;
+          }
+        } else {
+          rejected = true;
+        }
+      }
+    }
+    if (state != kGcDraw) break;
+    if (taken >= 0) {
+      ++k;
+      if (k == o.out_cols) {
+        if (lane == 0 && o.status) atomicOr(o.status, TV_DEV_OUT_OVERFLOW);
+        state = kGcDone;
+        break;
+      }
+      node = taken;
+      continue;
+    }
+    level = rejected ? 1 : 0;  // the residual after the rejection, else a bonus from p
+    break;
+  }
+  if (lane == 0) ws.state[b] = make_int4(state, node, level, k);
+  if (state == kGcDone) {  // truncated: no draw
+    for (int j = k + lane; j < o.out_cols; j += 32) {
+      o.out[(int64_t)b * o.out_cols + j] = -1;
+      if (o.path) o.path[(int64_t)b * o.out_cols + j] = -1;
+    }
+    if (lane == 0) o.n_out[b] = k;
+  }
+}
+
+// The draw of request b after its pass: level 1 when W_1 > 0 after a
+// rejection, else level 0; the crossing's chunk from an exclusive scan of
+// the chunk totals, then its element from a scan of that chunk re-read
+// (thread t: 16 consecutive elements; the one thread holding the crossing
+// reads its elements again to find it).
+__device__ void gc_draw(const float* __restrict__ p, const float* __restrict__ q, const float* __restrict__ u_final,
+                        int N, int V, const NodeIdx& ix, const AcceptOut& o, const GcWs& ws, int b, int4 st,
+                        uint64_t* s_red, int* s_chunk, int* s_x, uint64_t* s_base) {
+  const int node = st.y, k = st.w;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int t = threadIdx.x;
+  const uint64_t* tot = ws.tot + (int64_t)b * ws.nch * 2;
+  uint64_t v1 = t < ws.nch ? tot[2 * t] : 0, v0 = t < ws.nch ? tot[2 * t + 1] : 0;
+  const uint64_t W1 = sc_block_sum(v1, s_red);
+  const int m = st.z == 1 && W1 > 0 ? 1 : 0;
+  const uint64_t v = m ? v1 : v0;
+  const uint64_t W = m ? W1 : sc_block_sum(v0, s_red);
+  const uint64_t thr = (uint64_t)ceil(__dmul_rn((double)u_final[b], (double)W));
+  if (t == 0) {
+    *s_chunk = -1;
+    *s_x = thr == 0 ? 0 : V - 1;
+  }
+  // exclusive scan of the chosen totals over the chunks (thread t: chunk t)
+  uint64_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) s_red[warp] = incl;
+  __syncthreads();
+  uint64_t ex = incl - v;
+  for (int i = 0; i < warp; ++i) ex += s_red[i];
+  if (thr > 0 && v > 0 && ex < thr && thr <= ex + v) {
+    *s_chunk = t;
+    *s_base = ex;
+  }
+  __syncthreads();
+  const int cc = *s_chunk;
+  if (cc >= 0) {
+    const float* prow = p + ((int64_t)b * N + node) * V;
+    const float* qrow = q + ix.qrow(b, node) * V;
+    const int e0 = cc * kGcChunk + kGcPer * t;
+    // level-m weight of element e (0 past the end of the row)
+    auto weight = [&](int e) -> uint64_t {
+      if (e >= V) return 0;
+      const int64_t P = fix40(__ldg(prow + e));
+      if (m == 0) return (uint64_t)P;
+      const int64_t Q = fix40(__ldg(qrow + e));
+      return P > Q ? (uint64_t)(P - Q) : 0;
+    };
+    uint64_t mine = 0;
+#pragma unroll
+    for (int j = 0; j < kGcPer; ++j) mine += weight(e0 + j);
+    uint64_t inc = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    __syncthreads();  // s_red's chunk-scan values are no longer read
+    if (lane == 31) s_red[warp] = inc;
+    __syncthreads();
+    uint64_t run = *s_base + inc - mine;
+    for (int i = 0; i < warp; ++i) run += s_red[i];
+    if (mine > 0 && run < thr && thr <= run + mine) {
+      for (int j = 0; j < kGcPer; ++j) {  // the one thread holding the crossing re-reads its elements
+        run += weight(e0 + j);
+        if (run >= thr) {
+          *s_x = e0 + j;
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (t == 0) {
+    int x = *s_x;
+    if (x > V - 1) x = V - 1;
+    o.out[(int64_t)b * o.out_cols + k] = x;
+    if (o.path) o.path[(int64_t)b * o.out_cols + k] = node;
+  }
+  finish_walk(o, b, k + 1);
+}
+
+// One pass item: chunk c of request b's stop-node row at its level; the
+// chunk's level-1 total (w_1 = max(0, P - Q), summed only after a rejection)
+// and level-0 total (P: the bonus, or the draw's row when W_1 = 0).
+__global__ void __launch_bounds__(kGcThreads) gc_pass_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                                                            int N, int V, NodeIdx ix, GcWs ws) {
+  __shared__ uint64_t s_red[kScWarps];
+  const int b = blockIdx.x / ws.nch, c = blockIdx.x % ws.nch;
+  const int4 st = ws.state[b];
+  if (st.x != kGcDraw) return;
+  const int node = st.y, level = st.z;
+  const float* prow = p + ((int64_t)b * N + node) * V;
+  const float* qrow = q + ix.qrow(b, node) * V;
+  const bool vec = (V % 4 == 0) && (((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q)) & 15) == 0);
+  const int e0 = c * kGcChunk;
+  float pv[kGcPer], qv[kGcPer];
+  if (vec) {
+    // float4 j of the thread: elements e0 + 4 (j * kGcThreads + t) .. + 3
+#pragma unroll
+    for (int j = 0; j < kGcPer / 4; ++j) {
+      const int e = e0 + 4 * (j * kGcThreads + (int)threadIdx.x);
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), d = a;
+      if (e < V) {
+        a = __ldg(reinterpret_cast<const float4*>(prow + e));
+        if (level) d = __ldg(reinterpret_cast<const float4*>(qrow + e));
+      }
+      pv[4 * j] = a.x; pv[4 * j + 1] = a.y; pv[4 * j + 2] = a.z; pv[4 * j + 3] = a.w;
+      qv[4 * j] = d.x; qv[4 * j + 1] = d.y; qv[4 * j + 2] = d.z; qv[4 * j + 3] = d.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kGcPer; ++j) {
+      const int e = e0 + j * kGcThreads + (int)threadIdx.x;
+      pv[j] = e < V ? __ldg(prow + e) : 0.f;
+      qv[j] = e < V && level ? __ldg(qrow + e) : 0.f;
+    }
+  }
+  // sums as h * 2^20 + l in 32-bit parts (16 elements of at most 2 each: no overflow)
+  int32_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+#pragma unroll
+  for (int j = 0; j < kGcPer; ++j) {
+    int32_t Hp, Lp;
+    fix40_parts(pv[j], Hp, Lp);
+    h0 += Hp;
+    l0 += Lp;
+    if (level) {
+      int32_t Hq, Lq;
+      fix40_parts(qv[j], Hq, Lq);
+      const int32_t dH = Hp - Hq, dL = Lp - Lq;
+      const bool pos = dH > 0 || (dH == 0 && dL > 0);
+      h1 += pos ? dH : 0;
+      l1 += pos ? dL : 0;
+    }
+  }
+  const uint64_t t1 = sc_block_sum((uint64_t)(((int64_t)h1 << 20) + l1), s_red);
+  const uint64_t t0 = sc_block_sum((uint64_t)(((int64_t)h0 << 20) + l0), s_red);
+  if (threadIdx.x == 0) {
+    uint64_t* t = ws.tot + ((int64_t)b * ws.nch + c) * 2;
+    t[0] = t1;
+    t[1] = t0;
+  }
+}
+
+// One CTA per request: the draw of a request whose walk stopped.
+__global__ void __launch_bounds__(kGcThreads) gc_draw_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                                                            const float* __restrict__ u_final, int N, int V,
+                                                            NodeIdx ix, AcceptOut o, GcWs ws) {
+  __shared__ uint64_t s_red[kScWarps];
+  __shared__ int s_chunk, s_x;
+  __shared__ uint64_t s_base;
+  const int4 st = ws.state[blockIdx.x];
+  if (st.x != kGcDraw) return;
+  gc_draw(p, q, u_final, N, V, ix, o, ws, blockIdx.x, st, s_red, &s_chunk, &s_x, &s_base);
+}
+
+
 // Clusters of a sampler kernel resident on the current device at once for a
 // launch configuration (cached per device, kernel, cluster size and shared
 // memory).  Also raises the kernel's dynamic shared-memory limit.
@@ -1346,10 +1646,13 @@ constexpr ChainParent make_chain_parent() {
 }
 __device__ const ChainParent g_chain_parent = make_chain_parent();
 
-// Kernel choice and launch of the stochastic walk (both entry points).
-int launch_sample(const float* p, const float* q, const int32_t* tokens, const int32_t* parent,
-                  int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept, const float* u_final,
-                  int32_t B, int32_t N, int32_t V, NodeIdx ix, AcceptOut o, int32_t flags, void* stream) {
+// Kernel choice and launch of the single-launch walks; `only` (nullable):
+// the grid sampler's request states, of which only kGcOther requests are
+// walked.
+int launch_walk(const float* p, const float* q, const int32_t* tokens, const int32_t* parent,
+                int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept, const float* u_final,
+                int32_t B, int32_t N, int32_t V, NodeIdx ix, AcceptOut o, int32_t flags, const int4* only,
+                void* stream) {
   int st = TV_OK;
   if (B > INT_MAX / kScCtas && flags != TV_SAMPLE_SINGLE_CTA)
     return tv::fail(TV_ERR_INVALID_ARG, "tree accept sample: B=%d too large", B);
@@ -1365,7 +1668,7 @@ int launch_sample(const float* p, const float* q, const int32_t* tokens, const i
     if (flags == TV_SAMPLE_CLUSTER || B <= capacity) {
       L.cfg.gridDim = dim3((unsigned)(B * kScCtas));
       cudaError_t e = cudaLaunchKernelEx(&L.cfg, sample_cluster_kernel<true>, p, q, tokens, parent, parent_bstride,
-                                         n_nodes, u_accept, u_final, (int)N, (int)V, Ls8, ix, o);
+                                         n_nodes, u_accept, u_final, (int)N, (int)V, Ls8, ix, o, only);
       if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel<state>");
       return TV_OK;
     }
@@ -1392,7 +1695,8 @@ int launch_sample(const float* p, const float* q, const int32_t* tokens, const i
       ScLaunch L(pick, dyn, stream);
       L.cfg.gridDim = dim3((unsigned)(B * pick));
       cudaError_t e = cudaLaunchKernelEx(&L.cfg, sample_cluster_kernel<false>, p, q, tokens, parent, parent_bstride,
-                                         n_nodes, u_accept, u_final, (int)N, (int)V, sc_slice(V, pick), ix, o);
+                                         n_nodes, u_accept, u_final, (int)N, (int)V, sc_slice(V, pick), ix, o,
+                                         only);
       if (e != cudaSuccess) return tv::cuda_fail(e, "sample_cluster_kernel<stream>");
       return TV_OK;
     }
@@ -1404,10 +1708,73 @@ int launch_sample(const float* p, const float* q, const int32_t* tokens, const i
   static_assert(2 * (kDyn + 2048 + 1024) <= 228 * 1024, "two CTAs per SM");
   cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDyn);
   if (e != cudaSuccess) return tv::cuda_fail(e, "cudaFuncSetAttribute(sample_kernel)");
-  sample_kernel<<<B, kSampleThreads, kDyn, (cudaStream_t)stream>>>(p, q, tokens, parent, parent_bstride, n_nodes, u_accept,
-                                                           u_final, N, V, ix, o);
+  sample_kernel<<<B, kSampleThreads, kDyn, (cudaStream_t)stream>>>(p, q, tokens, parent, parent_bstride, n_nodes,
+                                                                   u_accept, u_final, N, V, ix, o, only);
   TV_LAUNCH_CHECK("sample_kernel");
   return TV_OK;
+}
+
+// Chunks of a row in the grid sampler, and its workspace: request states
+// (16 bytes each), then two totals per (request, chunk).
+int gc_chunks(int V) { return (V + kGcChunk - 1) / kGcChunk; }
+size_t gc_workspace_bytes(int64_t B, int V) { return (size_t)B * 16u * (1u + (size_t)gc_chunks(V)); }
+
+// Whether a call takes the grid sampler: when asked for, or under
+// TV_SAMPLE_AUTO when the workspace is large enough and the on-chip-state
+// cluster kernel cannot hold every request at once.
+int takes_grid(int B, int V, int flags, bool ws_ok, void* stream, bool* grid) {
+  *grid = flags == TV_SAMPLE_GRID;
+  if (flags == TV_SAMPLE_AUTO && ws_ok && gc_chunks(V) <= kGcMaxChunks) {
+    const size_t dyn_state = (size_t)sc_slice(V, kScCtas) * (sizeof(uint64_t) + sizeof(float));
+    *grid = dyn_state > kScMaxDyn;
+    if (!*grid) {
+      ScLaunch L(kScCtas, dyn_state, stream);
+      int capacity = 0;
+      const int st = sc_capacity<true>(L.cfg, &capacity);
+      if (st) return st;
+      *grid = B > capacity;
+    }
+  }
+  return TV_OK;
+}
+
+// The stochastic walk, both entry points: the grid sampler (three kernels,
+// then the single-launch walk of the requests it leaves) when asked for, or
+// under TV_SAMPLE_AUTO when a workspace is given and the cluster kernel
+// cannot hold every request at once; else one single-launch walk.
+int launch_sample(const float* p, const float* q, const int32_t* tokens, const int32_t* parent,
+                  int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept, const float* u_final,
+                  int32_t B, int32_t N, int32_t V, NodeIdx ix, AcceptOut o, int32_t flags, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  const bool ws_ok = workspace != nullptr && workspace_bytes >= gc_workspace_bytes(B, V) &&
+                     (int64_t)B * gc_chunks(V) <= INT_MAX;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return tv::fail(TV_ERR_INVALID_ARG, "tree accept sample: workspace not 16-byte aligned");
+  if (flags == TV_SAMPLE_GRID) {
+    if (!ws_ok)
+      return tv::fail(TV_ERR_INVALID_ARG, "tree accept sample: TV_SAMPLE_GRID needs a workspace of %zu bytes (%zu)",
+                      gc_workspace_bytes(B, V), workspace ? workspace_bytes : (size_t)0);
+    if (gc_chunks(V) > kGcMaxChunks)
+      return tv::fail(TV_ERR_UNSUPPORTED, "tree accept sample: V=%d too large for the grid sampler", V);
+  }
+  bool grid = false;
+  const int st = takes_grid(B, V, flags, ws_ok, stream, &grid);
+  if (st) return st;
+  if (!grid)
+    return launch_walk(p, q, tokens, parent, parent_bstride, n_nodes, u_accept, u_final, B, N, V, ix, o, flags,
+                       nullptr, stream);
+  const cudaStream_t s = (cudaStream_t)stream;
+  char* base = static_cast<char*>(workspace);
+  const GcWs ws{reinterpret_cast<int4*>(base), reinterpret_cast<uint64_t*>(base + (size_t)B * 16u), gc_chunks(V)};
+  gc_walk_kernel<<<(B + kGcWalkWarps - 1) / kGcWalkWarps, kGcThreads, 0, s>>>(p, q, tokens, parent, parent_bstride,
+                                                                             n_nodes, u_accept, B, N, V, ix, o, ws);
+  TV_LAUNCH_CHECK("gc_walk_kernel");
+  gc_pass_kernel<<<(unsigned)((int64_t)B * ws.nch), kGcThreads, 0, s>>>(p, q, N, V, ix, ws);
+  TV_LAUNCH_CHECK("gc_pass_kernel");
+  gc_draw_kernel<<<B, kGcThreads, 0, s>>>(p, q, u_final, N, V, ix, o, ws);
+  TV_LAUNCH_CHECK("gc_draw_kernel");
+  return launch_walk(p, q, tokens, parent, parent_bstride, n_nodes, u_accept, u_final, B, N, V, ix, o,
+                     TV_SAMPLE_AUTO, ws.state, stream);
 }
 
 }  // namespace
@@ -1416,27 +1783,27 @@ extern "C" int tv_tree_accept_sample(const float* p, const float* q, const int32
                                      int64_t parent_bstride, const int32_t* n_nodes, const float* u_accept,
                                      const float* u_final, int32_t B, int32_t N, int32_t V, int32_t* out,
                                      int32_t* n_out, int32_t* path, int32_t out_cols, int32_t flags,
-                                     int32_t* status, void* stream) {
+                                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   tv::clear_error();
   int st = check_accept_args(B, N, V, tokens, parent, parent_bstride, out, n_out, out_cols);
   if (st) return st;
-  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_STREAM)
+  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_GRID)
     return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: unknown flags %d", flags);
   if (B == 0) return TV_OK;
   if (!p || !q || !u_accept || !u_final) return tv::fail(TV_ERR_INVALID_ARG, "tv_tree_accept_sample: null pointer");
   return launch_sample(p, q, tokens, parent, parent_bstride, n_nodes, u_accept, u_final, B, N, V, NodeIdx{N, 0, 0},
-                       AcceptOut{out, n_out, path, out_cols, status}, flags, stream);
+                       AcceptOut{out, n_out, path, out_cols, status}, flags, workspace, workspace_bytes, stream);
 }
 
 extern "C" int tv_chain_accept_sample(const float* p, const float* q, const int32_t* draft, const int32_t* num_draft,
                                       const float* u, const float* u_final, int32_t B, int32_t K, int32_t V,
-                                      int32_t* out, int32_t* n_out, int32_t out_cols, int32_t flags, int32_t* status,
-                                      void* stream) {
+                                      int32_t* out, int32_t* n_out, int32_t out_cols, int32_t flags, void* workspace,
+                                      size_t workspace_bytes, int32_t* status, void* stream) {
   tv::clear_error();
   if (B < 0 || K < 0 || K + 1 > TV_MAX_NODES || V < 1 || out_cols < 1)
     return tv::fail(TV_ERR_INVALID_ARG, "tv_chain_accept_sample: bad sizes B=%d K=%d V=%d out_cols=%d", B, K, V,
                     out_cols);
-  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_STREAM)
+  if (flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_GRID)
     return tv::fail(TV_ERR_INVALID_ARG, "tv_chain_accept_sample: unknown flags %d", flags);
   if (B == 0) return TV_OK;
   if (!p || !u_final || !out || !n_out || (K > 0 && (!q || !draft || !u)))
@@ -1449,5 +1816,25 @@ extern "C" int tv_chain_accept_sample(const float* p, const float* q, const int3
   const int32_t* tok = K > 0 ? draft : parent;
   const float* uu = K > 0 ? u : u_final;
   return launch_sample(p, qq, tok, parent, 0, num_draft, uu, u_final, B, K + 1, V, NodeIdx{K, 1, 1},
-                       AcceptOut{out, n_out, nullptr, out_cols, status}, flags, stream);
+                       AcceptOut{out, n_out, nullptr, out_cols, status}, flags, workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t tv_accept_sample_workspace_size(int32_t B, int32_t N, int32_t V) {
+  (void)N;
+  return B > 0 && V > 0 ? gc_workspace_bytes(B, V) : 0;
+}
+
+extern "C" int tv_accept_sample_uses_grid(int32_t B, int32_t N, int32_t V, int32_t flags, size_t workspace_bytes,
+                                          int32_t* grid) {
+  tv::clear_error();
+  (void)N;
+  if (!grid || B < 0 || V < 1 || flags < TV_SAMPLE_AUTO || flags > TV_SAMPLE_GRID)
+    return tv::fail(TV_ERR_INVALID_ARG, "tv_accept_sample_uses_grid: bad arguments");
+  const bool ws_ok = workspace_bytes > 0 && workspace_bytes >= gc_workspace_bytes(B, V) &&
+                     (int64_t)B * gc_chunks(V) <= INT_MAX;
+  bool g = false;
+  const int st = takes_grid(B, V, flags, ws_ok, nullptr, &g);
+  if (st) return st;
+  *grid = g ? 1 : 0;
+  return TV_OK;
 }

@@ -78,7 +78,16 @@ def test_greedy_overflow_flag():
     assert status.item() == capi.TV_DEV_OUT_OVERFLOW and n_out.item() == 3
 
 
-KERNELS = {"auto": 0, "cluster": 1, "single_cta": 2, "stream": 3}
+KERNELS = {"auto": 0, "cluster": 1, "single_cta": 2, "stream": 3, "grid": 4, "auto_ws": 0}
+
+
+def _kw(kernel, B, N, V):
+    """flags of one kernel choice, with a workspace for the grid sampler and
+    for TV_SAMPLE_AUTO allowed to pick it ("auto_ws")."""
+    kw = {"flags": KERNELS[kernel]}
+    if kernel in ("grid", "auto_ws"):
+        kw["workspace"] = capi.alloc_workspace(capi.tv_accept_sample_workspace_size(B, N, V))
+    return kw
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -86,8 +95,9 @@ def test_sample_full_workload_bit_exact(kernel):
     """B=256 chains over a 128000-token vocabulary, ragged num_draft ~ U{0..4}."""
     w = W.WORKLOADS["b256_l2k_4k_n10_sample"]
     s = W.sample_chain_inputs(w, device="cuda")
+    kw = _kw(kernel, *s["p"].shape)
     res = capi.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
-                                     n_nodes=s["n_nodes"], flags=KERNELS[kernel])
+                                     n_nodes=s["n_nodes"], **kw)
     c = {k: v.cpu().numpy() for k, v in s.items()}
     ref = OA.tree_accept_sample(c["p"], c["q"], c["tokens"], c["parent"], c["n_nodes"], c["u_accept"], c["u_final"])
     _cmp(res, *ref)
@@ -98,7 +108,7 @@ def test_sample_full_workload_bit_exact(kernel):
     # the chain call reads the page's arrays in place: the same bits
     out2, n2 = capi.tv_chain_accept_sample(s["p"], s["q"][:, :K].contiguous(), s["tokens"][:, 1:].contiguous(),
                                            s["u_accept"][:, 1:].contiguous(), s["u_final"],
-                                           num_draft=(s["n_nodes"] - 1).contiguous(), flags=KERNELS[kernel])
+                                           num_draft=(s["n_nodes"] - 1).contiguous(), **kw)
     np.testing.assert_array_equal(n2.cpu().numpy(), n_c)
     np.testing.assert_array_equal(out2.cpu().numpy(), out_c)
 
@@ -111,7 +121,7 @@ def test_sample_tree_full_workload_bit_exact(kernel):
     parent, *_ = OT.build_tree(w.paths())
     s = W.sample_tree_inputs(w, parent, device="cuda")
     res = capi.tv_tree_accept_sample(s["p"], s["q"], s["tokens"], s["parent"], s["u_accept"], s["u_final"],
-                                     n_nodes=s["n_nodes"], flags=KERNELS[kernel])
+                                     n_nodes=s["n_nodes"], **_kw(kernel, *s["p"].shape))
     c = {k: v.cpu().numpy() for k, v in s.items()}
     ref = OA.tree_accept_sample(c["p"], c["q"], c["tokens"], c["parent"], c["n_nodes"], c["u_accept"], c["u_final"])
     _cmp(res, *ref)
@@ -121,8 +131,8 @@ def test_sample_tree_full_workload_bit_exact(kernel):
 
 
 @pytest.mark.parametrize("V,B,kernel",
-                         [(V, 200, k) for V in (4, 33, 1000, 4096) for k in ("cluster", "single_cta", "stream")]
-                         + [(V, 12, k) for V in (160000, 160001) for k in ("auto", "single_cta")])
+                         [(V, 200, k) for V in (4, 33, 1000, 4096) for k in ("cluster", "single_cta", "stream", "grid")]
+                         + [(V, 12, k) for V in (160000, 160001) for k in ("auto", "single_cta", "grid")])
 def test_sample_trees_with_sibling_levels(V, B, kernel):
     """Trees with up to 5 siblings per node: several residual levels per node,
     on every kernel.  Vocabularies above 136,512 have no on-chip-state
@@ -145,7 +155,7 @@ def test_sample_trees_with_sibling_levels(V, B, kernel):
     uf = rng.random(B, dtype=np.float32)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     res = capi.tv_tree_accept_sample(t(p), t(q), t(tokens), t(parent.astype(np.int32)), t(ua), t(uf),
-                                     n_nodes=t(n_nodes), flags=KERNELS[kernel])
+                                     n_nodes=t(n_nodes), **_kw(kernel, B, N, V))
     _cmp(res, *OA.tree_accept_sample(p, q, tokens, parent, n_nodes, ua, uf))
     if V > 136512:
         with pytest.raises(capi.TVError, match="UNSUPPORTED"):
@@ -153,8 +163,8 @@ def test_sample_trees_with_sibling_levels(V, B, kernel):
                                        flags=capi.TV_SAMPLE_CLUSTER)
 
 
-@pytest.mark.parametrize("V,kernel", [(4096, "cluster"), (4096, "single_cta"), (4096, "stream"), (160000, "auto"),
-                                      (160000, "single_cta")])
+@pytest.mark.parametrize("V,kernel", [(4096, "cluster"), (4096, "single_cta"), (4096, "stream"), (4096, "grid"),
+                                      (160000, "auto"), (160000, "single_cta"), (160000, "grid")])
 def test_sample_kept_level_after_empty_residual(V, kernel):
     """A rejection whose residual pass leaves no mass keeps the level (the
     p = q guard) and the final draw still uses that level's weights: q is
@@ -174,10 +184,94 @@ def test_sample_kept_level_after_empty_residual(V, kernel):
     n_nodes = np.full(B, N, dtype=np.int32)
     tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     res = capi.tv_tree_accept_sample(tt(p), tt(q), tt(tokens), tt(parent), tt(ua), tt(uf), n_nodes=tt(n_nodes),
-                                     flags=KERNELS[kernel])
+                                     **_kw(kernel, B, N, V))
     ref = OA.tree_accept_sample(p, q, tokens, parent, n_nodes, ua, uf)
     _cmp(res, *ref)
     assert (ref[1] == 1).all() and (ref[0][:, 0] == t).all()
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_sample_chain_empty_residual_draws_from_p(kernel):
+    """A chain whose only child is rejected with an empty residual: p = q
+    rows and a draft token both give probability 0 (u q(x) < p(x) fails at
+    0 < 0), so max(0, P - Q) sums to 0, the level is kept and the
+    replacement is drawn from p itself; the other requests accept every
+    draft (u < 1 with p(x) = q(x) > 0) and draw the bonus."""
+    rng = np.random.default_rng(150)
+    B, N, V = 40, 4, 3000
+    parent = np.arange(-1, N - 1, dtype=np.int32)
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, N)).astype(np.float32)
+    p[:, :, 17] = 0.0
+    q = p.copy()
+    tokens = rng.integers(18, V, size=(B, N)).astype(np.int32)
+    tokens[: B // 2, 2] = 17  # the second draft is rejected with nothing left
+    ua = rng.random((B, N), dtype=np.float32)
+    uf = rng.random(B, dtype=np.float32)
+    n_nodes = np.full(B, N, dtype=np.int32)
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    res = capi.tv_tree_accept_sample(tt(p), tt(q), tt(tokens), tt(parent), tt(ua), tt(uf), n_nodes=tt(n_nodes),
+                                     **_kw(kernel, B, N, V))
+    ref = OA.tree_accept_sample(p, q, tokens, parent, n_nodes, ua, uf)
+    _cmp(res, *ref)
+    assert (ref[1][: B // 2] == 2).all() and (ref[1][B // 2:] == N).all()
+
+
+def test_sample_truncated_walk_same_on_every_kernel():
+    """out_cols shorter than the accepted chain: every kernel flags
+    TV_DEV_OUT_OVERFLOW and returns the same first out_cols tokens as the
+    oracle's walk, without the final draw."""
+    rng = np.random.default_rng(151)
+    B, N, V, cols = 30, 6, 2000, 3
+    parent = np.arange(-1, N - 1, dtype=np.int32)
+    p = rng.dirichlet(np.ones(V), size=(B, N)).astype(np.float32)
+    rows = p.astype(np.float64)
+    rows /= rows.sum(axis=2, keepdims=True)
+    tokens = np.stack([[rng.choice(V, p=rows[b, max(c - 1, 0)]) for c in range(N)] for b in range(B)]).astype(np.int32)
+    ua = rng.random((B, N), dtype=np.float32)
+    uf = rng.random(B, dtype=np.float32)
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    ref = OA.tree_accept_sample(p, p, tokens, parent, np.full(B, N, np.int32), ua, uf)
+    assert (ref[1] == N).all()  # q = p: every draft is accepted
+    for kernel in sorted(KERNELS):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, n_out, path = capi.tv_tree_accept_sample(tt(p), tt(p), tt(tokens), tt(parent), tt(ua), tt(uf),
+                                                      out_cols=cols, status=status, **_kw(kernel, B, N, V))
+        assert status.item() == capi.TV_DEV_OUT_OVERFLOW, kernel
+        assert (n_out.cpu().numpy() == cols).all(), kernel
+        np.testing.assert_array_equal(out.cpu().numpy(), ref[0][:, :cols])
+        np.testing.assert_array_equal(path.cpu().numpy(), ref[2][:, :cols])
+
+
+def test_grid_sampler_arguments():
+    """The grid sampler needs a large enough, 16-byte aligned workspace and
+    V <= 2^20; TV_SAMPLE_AUTO without one keeps to the single-launch
+    kernels."""
+    B, N, V = 3, 2, 500
+    p = torch.full((B, N, V), 1.0 / V, device="cuda")
+    tokens = torch.zeros(B, N, dtype=torch.int32, device="cuda")
+    parent = torch.tensor([-1, 0], dtype=torch.int32, device="cuda")
+    ua, uf = torch.zeros(B, N, device="cuda"), torch.full((B,), 0.5, device="cuda")
+    need = capi.tv_accept_sample_workspace_size(B, N, V)
+    assert need == 16 * B + 16 * B * 1
+    call = lambda **kw: capi.tv_tree_accept_sample(p, p, tokens, parent, ua, uf, **kw)
+    with pytest.raises(capi.TVError, match="INVALID_ARG"):
+        call(flags=capi.TV_SAMPLE_GRID)
+    with pytest.raises(capi.TVError, match="INVALID_ARG"):
+        call(flags=capi.TV_SAMPLE_GRID, workspace=capi.alloc_workspace(need)[: need - 16])
+    with pytest.raises(capi.TVError, match="INVALID_ARG"):
+        call(flags=capi.TV_SAMPLE_GRID, workspace=capi.alloc_workspace(need + 64)[8: need + 8])
+    with pytest.raises(capi.TVError, match="INVALID_ARG"):
+        call(flags=5, workspace=capi.alloc_workspace(need))
+    big = torch.full((1, 1, (1 << 20) + 1), 0.5 ** 20, device="cuda")
+    z = torch.zeros(1, 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(capi.TVError, match="UNSUPPORTED"):
+        capi.tv_tree_accept_sample(big, big, z, parent[:1], torch.zeros(1, 1, device="cuda"), uf[:1],
+                                   flags=capi.TV_SAMPLE_GRID,
+                                   workspace=capi.alloc_workspace(capi.tv_accept_sample_workspace_size(1, 1, big.shape[2])))
+    ref = call(flags=capi.TV_SAMPLE_SINGLE_CTA)
+    for kw in ({}, {"flags": capi.TV_SAMPLE_GRID, "workspace": capi.alloc_workspace(need)}):
+        for a, b in zip(call(**kw), ref):
+            assert torch.equal(a, b)
 
 
 def test_sample_bad_token_flag():
@@ -190,10 +284,11 @@ def test_sample_bad_token_flag():
     assert status.item() == capi.TV_DEV_BAD_TOKEN and n_out.item() == 1
 
 
-def _gpu_verify(p, q, tokens, parent, n_nodes, ua, uf, flags=0):
+def _gpu_verify(p, q, tokens, parent, n_nodes, ua, uf, kernel="auto"):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     out, n_out, _ = capi.tv_tree_accept_sample(t(p), t(q), t(tokens.astype(np.int32)), t(parent.astype(np.int32)),
-                                               t(ua), t(uf), n_nodes=t(n_nodes.astype(np.int32)), flags=flags)
+                                               t(ua), t(uf), n_nodes=t(n_nodes.astype(np.int32)),
+                                               **_kw(kernel, *p.shape))
     return out.cpu().numpy(), n_out.cpu().numpy()
 
 
@@ -206,13 +301,13 @@ def test_gpu_chain_lossless_chi_square(verifier_facts):
     assert chi_square(seqs, pt) < thr
 
 
-@pytest.mark.parametrize("kernel", ["cluster", "single_cta", "stream"])
+@pytest.mark.parametrize("kernel", ["cluster", "single_cta", "stream", "grid"])
 def test_gpu_tree_lossless_chi_square(verifier_facts, kernel):
     f = verifier_facts
     V, n_tok, thr = int(f["chi2_vocab"][0][0]), int(f["chi2_tokens"][0][0]), float(f["chi2_threshold"][0][0])
     parent, *_ = OT.build_tree([(0,), (1,), (2,), (0, 0), (2, 0)])
     pt, qt = W.markov_tables(V, 22)
-    verify = lambda *a: _gpu_verify(*a, flags=KERNELS[kernel])
+    verify = lambda *a: _gpu_verify(*a, kernel=kernel)
     seqs = generate(verify, pt, qt, parent, 200_000, n_tok, 131)
     assert chi_square(seqs, pt) < thr
 
@@ -255,7 +350,7 @@ def test_sample_edge_shapes(kernel):
         ua = rng.random((B, N), dtype=np.float32)
         uf = rng.random(B, dtype=np.float32)
         res = capi.tv_tree_accept_sample(t(p), t(q), t(tok), t(par), t(ua), t(uf), n_nodes=t(n_nodes),
-                                         flags=KERNELS[kernel])
+                                         **_kw(kernel, B, N, V))
         _cmp(res, *OA.tree_accept_sample(p, q, tok, par, n_nodes, ua, uf))
         if V == 1:
             assert (res[0].cpu().numpy()[:, 0] == 0).all()
@@ -317,12 +412,13 @@ def test_chain_call_allocates_nothing(kernel):
         args = [t(draft), t(q), t(p), t(nd) if give_nd else None, t(u), t(uf)]
         out = torch.empty(B, K + 1, dtype=torch.int32, device="cuda")
         n_out = torch.empty(B, dtype=torch.int32, device="cuda")
-        capi.verify_chain(*args, out=out, n_out=n_out, flags=KERNELS[kernel])  # first call: one-time set-up
+        kw = _kw(kernel, B, K + 1, V)
+        capi.verify_chain(*args, out=out, n_out=n_out, **kw)  # first call: one-time set-up
         r = None  # drop the previous case's outputs before counting
         torch.cuda.synchronize()
         alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
         for _ in range(3):
-            r = capi.verify_chain(*args, out=out, n_out=n_out, flags=KERNELS[kernel])
+            r = capi.verify_chain(*args, out=out, n_out=n_out, **kw)
         torch.cuda.synchronize()
         assert r[0] is out and r[1] is n_out
         assert torch.cuda.memory_allocated() == alloc0 and torch.cuda.mem_get_info()[0] == free0

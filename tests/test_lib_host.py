@@ -82,11 +82,19 @@ def test_device_entry_points_reject_bad_sizes_on_host():
     assert h.tv_rope_apply(None, None, None, None, 10, 1, 1, 1, 1, 60, 1, None, None) == -1
     assert h.tv_tree_accept_greedy(None, None, None, None, 0, None, 1, 65, 10, None, None, None, 4, None, None) == -1
     assert h.tv_tree_accept_sample(None, None, None, None, 0, None, None, None, 0, 10, 10, None, None, None, 4,
-                                   0, None, None) == 0
+                                   0, None, 0, None, None) == 0
     assert b"bad sizes" in h.tv_last_error() or h.tv_last_error() == b""
     assert h.tv_tree_accept_sample(None, None, None, None, 0, None, None, None, 0, 10, 10, None, None, None, 4,
-                                   4, None, None) == -1
+                                   5, None, 0, None, None) == -1
     assert b"unknown flags" in h.tv_last_error()
+    assert h.tv_chain_accept_sample(None, None, None, None, None, None, 0, 3, 10, None, None, 4, 5, None, 0, None,
+                                    None) == -1
+    assert b"unknown flags" in h.tv_last_error()
+    # the grid sampler's workspace: a 16-byte state per request, and 16 bytes per request and
+    # 4096-entry chunk
+    assert h.tv_accept_sample_workspace_size(256, 10, 128000) == 16 * 256 + 16 * 256 * 32
+    assert h.tv_accept_sample_workspace_size(3, 2, 4097) == 16 * 3 + 16 * 3 * 2
+    assert h.tv_accept_sample_workspace_size(0, 2, 100) == 0
 
 
 def test_tree_prepare_rejects_bad_arguments_on_host():
