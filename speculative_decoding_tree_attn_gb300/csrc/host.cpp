@@ -66,7 +66,7 @@ int current_device_info(DeviceInfo* info) {
 
 extern "C" const char* tv_last_error(void) { return tv::g_last_error.c_str(); }
 
-extern "C" int tv_version(void) { return 201; }
+extern "C" int tv_version(void) { return 202; }
 
 extern "C" int tv_tree_build(const int32_t* ranks, const int32_t* offsets, int32_t n_paths,
                              int32_t max_nodes, int32_t* parent, int32_t* depth, uint64_t* mask,
