@@ -142,10 +142,13 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 // producers skip the loads (and the arrival) of one ring tile, so that the
 // bounded waits run out and the timeout exit is exercised without a fault;
 // or it keeps the epilogue warps of some TMEM quarters off the direct merge,
-// so that the warps of one M tile take different merge routes.
+// so that the warps of one M tile take different merge routes; or it makes
+// the first pair of tail warps sleep before each of its tiles, so that it
+// falls behind the other pair.
 __device__ unsigned long long g_test_timeout_ns = kTimeoutNs;
 __device__ int g_test_withhold = -1;      // ring index of CTA 0 left without loads
 __device__ int g_test_publish_warps = 0;  // bit q: warps of TMEM quarter q never merge directly
+__device__ unsigned long long g_test_tail_delay_ns = 0;  // sleep of tail pair 0 before each tile
 __device__ __forceinline__ unsigned long long timeout_ns() { return *(volatile unsigned long long*)&g_test_timeout_ns; }
 __device__ __forceinline__ bool test_withhold(uint32_t g) {
   return blockIdx.x == 0 && (int)g == *(volatile int*)&g_test_withhold;
@@ -153,10 +156,21 @@ __device__ __forceinline__ bool test_withhold(uint32_t g) {
 __device__ __forceinline__ bool test_no_direct(int rl) {
   return (*(volatile int*)&g_test_publish_warps >> (rl >> 5)) & 1;
 }
+__device__ __forceinline__ void test_tail_delay(int pair) {
+  const unsigned long long d = *(volatile unsigned long long*)&g_test_tail_delay_ns;
+  if (pair != 0 || d == 0) return;
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  do {
+    __nanosleep(1000);
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  } while (t - t0 < d);
+}
 #else
 __device__ __forceinline__ unsigned long long timeout_ns() { return kTimeoutNs; }
 __device__ __forceinline__ bool test_withhold(uint32_t) { return false; }
 __device__ __forceinline__ bool test_no_direct(int) { return false; }
+__device__ __forceinline__ void test_tail_delay(int) {}
 #endif
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -1841,6 +1855,7 @@ __device__ __forceinline__ void run_tail(const AttnParams& p, const SlicePlan& s
       const int stage = g % kStages;
       ok = mbar_wait_warp(&bars.kv_full[stage], (g / kStages) & 1, &bars, status);
       if (!ok) break;
+      test_tail_delay(pair);
       tail_tile(p, s, t, sK + stage * kKVTileBytes, sV + stage * kKVTileBytes, ts, w % kTailSplit, lane);
       // the stage was read through the generic proxy (ldmatrix) and the next
       // TMA load writes it through the async proxy: order the reads first
@@ -2432,12 +2447,19 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       // last P.V products have completed (the last stage's empty barrier
       // counts one commit from each O issuer, and each commit covers that
       // issuer's earlier products; the S products completed before their
-      // softmax).  A direct merge with one other piece then stages that
-      // piece's rows through it, M tile m in its own 64 KB (the K half of the
-      // ring for m = 0, the V half for 1).
+      // softmax) and the tail warps have read their last tiles: with four
+      // tail warps the two pairs take tiles in turn, so the other pair's last
+      // tile is the one before, whose stage may still be read after the last
+      // tile's is released (no stage is loaded again, so each of these
+      // barriers has completed at most the phase waited for).  A direct
+      // merge with one other piece then stages that piece's rows through the
+      // ring, M tile m in its own 64 KB (the K half of the ring for m = 0,
+      // the V half for 1).
       uint8_t* stage = nullptr;
       if (!have_next) {
-        ok = mbar_wait_warp(&bars.kv_empty[(g - 1) % C::kStages], ((g - 1) / C::kStages) & 1, &bars, status);
+        constexpr int kLastTiles = kTailW ? kTailW / kTailSplit : 1;  // tail warp pairs taking tiles in turn
+        for (int j = 1; j <= kLastTiles && j <= (int)g && ok; ++j)
+          ok = mbar_wait_warp(&bars.kv_empty[(g - j) % C::kStages], ((g - j) / C::kStages) & 1, &bars, status);
         if (!ok) break;
         fence_after();
         stage = smem_raw + (base - raw) + (m == 0 ? C::kOffK : C::kOffV);
@@ -3298,6 +3320,14 @@ extern "C" int tv_test_set_hooks(unsigned long long timeout_ns, int withhold_til
 // instead of merging them directly; 0 restores the normal routes.
 extern "C" int tv_test_set_publish_warps(int mask) {
   if (cudaMemcpyToSymbol(tv::g_test_publish_warps, &mask, sizeof(mask)) != cudaSuccess) return -6;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -6;
+}
+
+// Development builds only: the first pair of tail warps sleeps delay_ns
+// (about; 0: not at all) after each of its tiles has landed and before it
+// reads the tile.
+extern "C" int tv_test_set_tail_delay(unsigned long long delay_ns) {
+  if (cudaMemcpyToSymbol(tv::g_test_tail_delay_ns, &delay_ns, sizeof(delay_ns)) != cudaSuccess) return -6;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -6;
 }
 #endif
