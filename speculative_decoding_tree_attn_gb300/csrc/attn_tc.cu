@@ -1938,10 +1938,11 @@ __device__ __forceinline__ bool shared_unit(const AttnParams& p, const Segment& 
 // shared units alone and M tile 1's part is empty.
 constexpr bool kSplitKeys = false;
 __device__ __forceinline__ int sh_owner(int t) { return kSplitKeys ? (t & 1) : 0; }
-template <bool kRope, bool kSkip, int kTailW>
+template <bool kRope, bool kSkip, int kTailW, bool kStagedQ>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     attn_tc_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps, int32_t* status) {
-  // kQS: after a CTA's first unit, each unit's Q reaches its operand slots
+  // kQS (kStagedQ, where the variant allows it): after a CTA's first unit,
+  // each unit's Q reaches its operand slots
   // through the S issuers instead of the softmax warps: Q_0 is staged in
   // shared memory by TMA during the previous unit and copied into TMEM with
   // tcgen05.cp just before the unit's first S_0 products (the same thread
@@ -1949,7 +1950,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   // Q_1 is loaded by TMA into its tile once the previous unit's last S_1 has
   // completed.  The softmax warps then only write the finished unit's rows at
   // a boundary.
-  constexpr bool kQS = !kRope && !kSkip && kTailW == 0;
+  constexpr bool kQS = kStagedQ && !kRope && !kSkip && kTailW == 0;
   using C = PairCfgT<kTailW, kQS>;
   static_assert(!(kSkip && kTailW), "tail rows replace the second row group");
   extern __shared__ uint8_t smem_raw[];
@@ -3116,13 +3117,13 @@ int launch_m(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStrea
   return TV_OK;
 }
 
-template <bool kRope, bool kSkip, int kTailW>
+template <bool kRope, bool kSkip, int kTailW, bool kStagedQ = false>
 int launch_pair(const AttnParams& p, const TcMaps& maps, int32_t* status, cudaStream_t stream) {
-  constexpr int smem = PairCfgT<kTailW, !kRope && !kSkip && kTailW == 0>::kSmem;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip, kTailW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = PairCfgT<kTailW, kStagedQ && !kRope && !kSkip && kTailW == 0>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<kRope, kSkip, kTailW, kStagedQ>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_pair_kernel)");
-  attn_tc_pair_kernel<kRope, kSkip, kTailW><<<p.P, PairCfg::kThreads, smem, stream>>>(p, maps, status);
+  attn_tc_pair_kernel<kRope, kSkip, kTailW, kStagedQ><<<p.P, PairCfg::kThreads, smem, stream>>>(p, maps, status);
   TV_LAUNCH_CHECK("attn_tc_pair_kernel");
   return TV_OK;
 }
@@ -3300,7 +3301,13 @@ int launch_attn_tc(const AttnParams& p, int32_t* status, cudaStream_t stream, bo
   // a last row group of at most 128 rows leaves M tile 1 idle: skip it
   const int tail = p.R % p.RPG;
   if (p.R > p.RPG && tail > 0 && tail <= 128) return launch_pair<false, true, 0>(p, maps, status, stream);
-  return launch_pair<false, false, 0>(p, maps, status, stream);
+  // Q staged by the S issuers pays off at unit boundaries: with no more units
+  // than CTAs every slice holds one or two segments, and the variant with the
+  // softmax warps placing Q measured faster there (16 requests of the 64-node
+  // tree: 0.119 against 0.104 ms; 32 requests: 0.137 against 0.142 ms; the
+  // two give the same bits)
+  return p.U > p.P ? launch_pair<false, false, 0, true>(p, maps, status, stream)
+                   : launch_pair<false, false, 0, false>(p, maps, status, stream);
 }
 
 }  // namespace tv
